@@ -1,0 +1,504 @@
+#!/usr/bin/env python3
+"""Throughput of the projected-and-quantized KV cache hot path on GB300.
+
+One step = for K and for V: empty the layer (kvc_trim), append the whole
+context in one call (project + quantise + bit-pack), fetch it back
+(unpack + dequantise + reconstruct to fp16 [B, H, S, D]).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama3-8b|palu-group|turboquant|sweep] [--path auto|generic]
+
+Prints one JSON line (rank 0).  ``value`` is KV tokens per second over all
+ranks, a KV token being one (batch, kv-head, position): its key row and its
+value row are each appended and fetched once per step.  Inputs are resident
+in HBM; L2 is flushed (a 256 MiB write) between timed steps.  ``e2e`` times
+the same step through the public API with the inputs copied from pinned host
+memory and the fetched rows copied back, every step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV tokens/s for fetch (unpack+reconstruct) and append; % of HBM/tensor roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+WORKLOADS = {
+    # Llama-3-8B-like decode layer: KVTC-style uniform mode, local PCA per (b, h)
+    "llama3-8b": dict(B=8, H=8, D=128, S=4096, fit=512, r=32, choices=(0, 2, 4, 8),
+                      budget=128, mode="uniform", dtype="bf16"),
+    # PALU-style group-head mode: 4 groups of 8 heads (D_in = 1024 -> r = 256)
+    "palu-group": dict(B=4, H=32, D=128, S=8192, hpg=8, r=256, mode="group", dtype="bf16"),
+    # TurboQuant-MSE-style: rotation + 3-bit codebook keys, int8 values
+    "turboquant": dict(B=16, H=8, D=128, S=16384, mode="codebook", dtype="f16"),
+    # Llama-3-70B-like KV shape, uniform all-b allocation (one sweep point)
+    "sweep": dict(B=8, H=8, D=128, S=8192, r=32, bits=4, mode="uniform", dtype="bf16"),
+}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.idx = gpu_index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.p = None
+        return self
+
+    def stop(self):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(", ") for r in self.f.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def build_layers(wl, dev):
+    """Synthetic inputs (seeded, generated on the GPU) and fitted layers for K and V."""
+    import torch
+
+    import rank_quantized_kv_gb300 as kvc
+    import synth
+    from rank_quantized_kv_gb300 import calib
+
+    B, H, D, S = wl["B"], wl["H"], wl["D"], wl["S"]
+    layers, inputs = [], []
+    f32 = torch.float32
+    for tensor in (0, 1):
+        if wl["mode"] == "group":
+            x = synth.group_spectral(B, H, S, D, wl["hpg"], alpha=1.0, seed=3000, tensor=tensor,
+                                     n_outliers=20, dtype="bf16", device=dev, work_dtype=f32)
+            params = calib.fit_group(x, wl["hpg"], wl["r"])
+            L = kvc.KVCacheLayer("group", B, H, D, in_dtype="bf16", capacity=S, device=dev,
+                                 **params)
+        elif wl["mode"] == "codebook":
+            if tensor == 0:
+                x = synth.heavy_tailed_keys(B, H, S, D, seed=4000, dtype="f16", device=dev)
+                L = kvc.KVCacheLayer("codebook", B, H, D, in_dtype="f16", capacity=S, device=dev,
+                                     V=calib.rotation(D, 1234),
+                                     codebook=calib.gaussian_codebook(3, 1 / math.sqrt(D)))
+            else:
+                x = synth.kv_spectral(B, H, S, D, alpha=1.0, seed=4100, tensor=1, dtype="f16",
+                                      device=dev, work_dtype=f32)
+                L = kvc.KVCacheLayer("int8", B, H, D, in_dtype="f16", capacity=S, device=dev)
+        else:
+            x = synth.kv_spectral(B, H, S, D, alpha=1.0, seed=2000 if "fit" in wl else 5000,
+                                  tensor=tensor, n_outliers=3 if "fit" in wl else 0,
+                                  dtype="bf16", device=dev, work_dtype=f32)
+            if "fit" in wl:
+                params = calib.fit_uniform(x[:, :, :wl["fit"]], wl["r"], wl["choices"],
+                                           wl["budget"])
+            else:
+                params = calib.fit_uniform_shared(x[:, :, :min(S, 4096)], wl["r"], wl["bits"])
+            L = kvc.KVCacheLayer("uniform", B, H, D, in_dtype="bf16", capacity=S, device=dev,
+                                 **params)
+        layers.append(L)
+        inputs.append(x.contiguous())
+    return layers, inputs
+
+
+def algorithmic(wl, layers):
+    """Per tensor: (fetch bytes, append bytes, flops) per full-context launch."""
+    out = []
+    B, H, D, S = wl["B"], wl["H"], wl["D"], wl["S"]
+    for L in layers:
+        n_slots = L.n_slots
+        P = np.mean([L.slot_layout(s)["row_bytes"] for s in range(n_slots)])
+        side = L.slot_layout(0)["side_bytes"]
+        in_b = {"bf16": 2, "f16": 2, "f32": 4}[L.in_dtype]
+        rows = n_slots * S
+        d_in = L.hpg * D
+        coded = rows * (P + side)
+        fetch_b = coded + B * H * S * D * 2
+        append_b = B * H * S * D * in_b + coded
+        r = 0 if L.mode == "int8" else (D if L.mode == "codebook" else wl["r"])
+        flops = 2.0 * rows * d_in * r
+        out.append((fetch_b, append_b, flops))
+    return out
+
+
+def gpu_arm(args, rank, world):
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl = WORKLOADS[args.workload]
+    B, H, D, S = wl["B"], wl["H"], wl["D"], wl["S"]
+    layers, inputs = build_layers(wl, dev)
+    for L in layers:
+        L.set_path(args.path)
+    outs = [torch.empty(B, H, S, D, dtype=torch.float16, device=dev) for _ in layers]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    alg = algorithmic(wl, layers)
+
+    def step(ev=None):
+        for i, (L, x, o) in enumerate(zip(layers, inputs, outs)):
+            L.trim(len(L))
+            if ev is not None:
+                ev[i][0].record()
+            L.append(x)
+            if ev is not None:
+                ev[i][1].record()
+            L.fetch(out=o)
+            if ev is not None:
+                ev[i][2].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for L in layers:
+        if L.sync_status() != 0:
+            raise RuntimeError("device error during warm-up")
+        L.counters(reset=True)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    sampler = ClockSampler(dev.index).start() if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    nten = len(layers)
+    step_ms, app_ms, fet_ms = [], np.zeros(nten), np.zeros(nten)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        flush.fill_(1)                       # L2 flush, outside the timed events
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nten)]
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record()
+        step(ev)
+        s1.record()
+        s1.synchronize()
+        step_ms.append(s0.elapsed_time(s1))
+        for i in range(nten):
+            app_ms[i] += ev[i][0].elapsed_time(ev[i][1])
+            fet_ms[i] += ev[i][1].elapsed_time(ev[i][2])
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if sampler else None
+    total_ms = float(np.sum(step_ms))
+    counters = [L.counters() for L in layers]
+    for L in layers:
+        if L.sync_status() != 0:
+            raise RuntimeError("device error in the timed region")
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    units = B * H * S                                   # KV tokens per step per rank
+    value = world * units / (ms_per_step / 1e3)
+
+    # e2e: pinned host inputs in, fetched rows out, every step
+    hosts_in = [x.cpu().pin_memory() for x in inputs]
+    hosts_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(h.numel() * h.element_size() for h in hosts_in)
+    d2h = sum(h.numel() * h.element_size() for h in hosts_out)
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        for L, xh, x, o, oh in zip(layers, hosts_in, inputs, outs, hosts_out):
+            x.copy_(xh, non_blocking=True)
+            L.trim(len(L))
+            L.append(x)
+            L.fetch(out=o)
+            oh.copy_(o, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for _ in range(e2e_steps):
+        e0.record()
+        for L, xh, x, o, oh in zip(layers, hosts_in, inputs, outs, hosts_out):
+            x.copy_(xh, non_blocking=True)
+            L.trim(len(L))
+            L.append(x)
+            L.fetch(out=o)
+            oh.copy_(o, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_ms /= e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if rank != 0:
+        return None
+
+    peaks = load_peaks()
+    hbm = peaks["hbm_gbs"] * 1e9
+    tflops = peaks["bf16_tflops"] * 1e12
+    ops = {}
+    for i, L in enumerate(layers):
+        name = ("keys" if i == 0 else "values") + f"/{L.mode}"
+        fb, ab, fl = alg[i]
+        ta, tf = app_ms[i] / args.steps / 1e3, fet_ms[i] / args.steps / 1e3
+        ops[name] = {
+            "append_us": ta * 1e6, "fetch_us": tf * 1e6,
+            "append_tokens_per_s": B * H * S / ta, "fetch_tokens_per_s": B * H * S / tf,
+            "append_roofline_frac": max(ab / hbm, fl / tflops) / ta,
+            "fetch_roofline_frac": max(fb / hbm, fl / tflops) / tf,
+            "append_bytes": ab, "fetch_bytes": fb, "flops": fl,
+        }
+    # dominant kernel: the op with the largest time per launch
+    cand = []
+    for i, L in enumerate(layers):
+        fb, ab, fl = alg[i]
+        cand.append((fet_ms[i], "fetch", i, fb, fl))
+        cand.append((app_ms[i], "append", i, ab, fl))
+    t_ms, kind, i, nbytes, fl = max(cand)
+    t = t_ms / args.steps / 1e3
+    tensor_bound = fl / tflops > nbytes / hbm
+    roof = {
+        "kernel": f"{kind} ({'keys' if i == 0 else 'values'}, {layers[i].mode})",
+        "bound": "tensor" if tensor_bound else "hbm",
+        "achieved": (fl / t / 1e12) if tensor_bound else (nbytes / t / 1e9),
+        "peak": peaks["bf16_tflops"] if tensor_bound else peaks["hbm_gbs"],
+        "unit": "TFLOP/s" if tensor_bound else "GB/s",
+        "peak_source": peaks["source"],
+        "traffic": None,
+        "algorithmic_bytes_per_launch": nbytes,
+    }
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    launches = sum(c["launches"] for c in counters)
+    line = {
+        "metric": METRIC, "value": value, "unit": "KV tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, **{k: v for k, v in wl.items() if k != "choices"},
+                   "choices": list(wl.get("choices", [])), "path": args.path,
+                   "parallelism": f"replicas{world}", "l2": "flushed between timed steps",
+                   "step": "per tensor (K, V): trim all, append S tokens, fetch S tokens"},
+        "e2e": {"value": world * units / (e2e_ms / 1e3), "unit": "KV tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "roofline": roof,
+        "ops": ops,
+        "refined": {f"{'keys' if i == 0 else 'values'}": c for i, c in enumerate(counters)},
+        "clocks": clocks,
+        "wall_s_timed": wall,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+    return line
+
+
+# ----------------------------------------------------------------------------- oracle legs
+
+def _oracle_sample(wl, n_slots_sample):
+    """Fitted oracle layers for K and V on a few slots of the workload (CPU, float64)."""
+    import torch
+
+    import synth
+    from oracle import codec, fit
+    from oracle.layer import OracleLayer
+
+    D, S = wl["D"], wl["S"]
+    jobs = []
+    for tensor in (0, 1):
+        if wl["mode"] == "group":
+            hpg = wl["hpg"]
+            x = synth.group_spectral(1, hpg, S, D, hpg, alpha=1.0, seed=3000, tensor=tensor,
+                                     n_outliers=20, dtype="bf16")
+            x64 = x.double().numpy()
+            rows = np.concatenate(list(x64[0]), axis=1)
+            mean, lam, U = fit.pca_fit(rows)
+            bits = fit.palu_bits(wl["r"], 4, 2, 0.25)
+            L = OracleLayer("group", 1, hpg, D, heads_per_group=hpg, V=U[:, :wl["r"]].astype(
+                np.float32).astype(np.float64), mean=mean.astype(np.float32).astype(np.float64),
+                bits=bits, group_size=32)
+        elif wl["mode"] == "codebook":
+            if tensor == 0:
+                x = synth.heavy_tailed_keys(1, n_slots_sample, S, D, seed=4000, dtype="f16")
+                L = OracleLayer("codebook", 1, n_slots_sample, D,
+                                V=fit.seeded_rotation(D, 1234).astype(np.float32),
+                                codebook=fit.lloyd_max_gaussian(8, 1 / math.sqrt(D)).astype(
+                                    np.float32))
+            else:
+                x = synth.kv_spectral(1, n_slots_sample, S, D, alpha=1.0, seed=4100, tensor=1,
+                                      dtype="f16")
+                L = OracleLayer("int8", 1, n_slots_sample, D)
+            x64 = x.double().numpy()
+        else:
+            fit_len = wl.get("fit", min(S, 4096))
+            x = synth.kv_spectral(1, n_slots_sample, S, D, alpha=1.0, seed=2000, tensor=tensor,
+                                  n_outliers=3 if "fit" in wl else 0, dtype="bf16")
+            x64 = x.double().numpy()
+            Vs, ms, bs, los, sts = [], [], [], [], []
+            for h in range(n_slots_sample):
+                mean, lam, U = fit.pca_fit(x64[0, h, :fit_len])
+                V32 = U[:, :wl["r"]].astype(np.float32)
+                m32 = mean.astype(np.float32)
+                bits = (fit.dp_allocate(lam[:wl["r"]], wl["choices"], wl["budget"])
+                        if "fit" in wl else np.full(wl["r"], wl["bits"]))
+                lo, st = fit.uniform_params(codec.project(x64[0, h, :fit_len], m32, V32), bits)
+                Vs.append(V32), ms.append(m32), bs.append(bits)
+                los.append(lo.astype(np.float32)), sts.append(st.astype(np.float32))
+            L = OracleLayer("uniform", 1, n_slots_sample, D, V=np.stack(Vs), mean=np.stack(ms),
+                            bits=np.stack(bs), qmin=np.stack(los), qstep=np.stack(sts),
+                            basis_of=np.arange(n_slots_sample))
+        jobs.append((L, x64))
+    return jobs
+
+
+def _cores_used():
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def _oracle_once(jobs):
+    """Append then fetch every job's tokens; returns the KV tokens processed."""
+    for L, x64 in jobs:
+        L.trim(L.len)
+        L.append(x64)
+        L.fetch()
+    x0 = jobs[0][1]
+    return x0.shape[0] * x0.shape[1] * x0.shape[2]
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    """The float64 oracle, as it stands, on a bounded sample of the workload."""
+    n_sample = 2 if wl["mode"] != "group" else wl["hpg"]
+    jobs = _oracle_sample(wl, n_sample)
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        done += _oracle_once(jobs)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    sample = (f"{n_sample} of the workload's KV heads x {wl['S']} tokens (K and V), "
+              f"appended and fetched repeatedly for {dt:.1f} s")
+    return {"value": done / dt, "unit": "KV tokens/s", "cores": _cores_used(), "kind": "oracle",
+            "sample": sample}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    wl = WORKLOADS[args.workload]
+    n_sample = 2 if wl["mode"] != "group" else wl["hpg"]
+    jobs = _oracle_sample(wl, n_sample)
+    for _ in range(args.warmup):
+        _oracle_once(jobs)
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(args.steps):
+        done += _oracle_once(jobs)
+    dt = time.perf_counter() - t0
+    value = done / dt
+    sample = f"{n_sample} KV heads x {wl['S']} tokens (K and V) per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "KV tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, **{k: v for k, v in wl.items() if k != "choices"},
+                   "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "KV tokens/s", "cores": _cores_used(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "KV tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="llama3-8b")
+    ap.add_argument("--path", choices=["auto", "generic"], default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", args.gpus))
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    line = reference_arm(args, rank, world) if args.impl == "reference" else gpu_arm(args, rank,
+                                                                                     world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,233 @@
+/*
+ * kvc.h -- C ABI of the projected-and-quantized KV cache hot path (GB300, sm_103a).
+ *
+ * A layer holds one tensor (keys or values) of one attention layer.  Its
+ * parameters are frozen at init: a basis V (rank r) with a mean, a per
+ * component bit width b_k in {0,1,2,3,4,8} (0 drops the component) and the
+ * quantiser's parameters.  The hot path is two calls:
+ *
+ *   kvc_append  z = (x - mean) V ; quantise each kept component ; bit-pack
+ *               the codes into a growing store (one row of P bytes per token);
+ *   kvc_fetch   unpack ; dequantise ; x_hat = z_hat V^T + mean, written as
+ *               fp16 (or bf16) [B, H, S, D] for attention.
+ *
+ * Sources (VeloxQuant-MLX documentation pages): the kvtc_cache page (module
+ * docstring "Design" and "NOT PATH-DEPENDENT"; _TensorKVTC._requantize;
+ * KVTCKVCache.trim and its byte accounting), the turboquant_cache page
+ * (TurboQuantKVCache: bit-packed indices, append_key, append_value,
+ * _unpack_indices_block, memory_bytes, reset) and the palu_cache page
+ * (PALUKVCache "Design" and "Byte accounting", trim).
+ *
+ * Memory: every pointer named "device" is CUDA device memory on the layer's
+ * device; every pointer named "host" is ordinary host memory read during the
+ * call only.  The caller owns the store, the inputs and the outputs.  The
+ * library owns one small block of device memory per layer (its frozen
+ * parameters in kernel layouts, plus an error word and counters), allocated
+ * in kvc_init_layer and freed in kvc_destroy; no other call allocates.
+ *
+ * Errors: every call returns a kvc_status.  Arguments are checked on the host
+ * before any launch; on error nothing is launched and the layer is unchanged.
+ * kvc_last_error() returns a message for the last failure on this thread.
+ * Work is asynchronous on the given stream (a cudaStream_t passed as void*;
+ * NULL is the legacy default stream); device-side conditions surface through
+ * kvc_sync_status.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVC_ABI_VERSION 1
+
+typedef struct kvc_layer kvc_layer; /* opaque, host-owned */
+
+typedef enum {
+  KVC_OK = 0,
+  KVC_EINVAL = -1,    /* bad argument or descriptor field */
+  KVC_ESTATE = -2,    /* call not valid for this layer (NULL or destroyed layer) */
+  KVC_ECAPACITY = -3, /* the append would exceed the capacity; nothing was written */
+  KVC_ECUDA = -4,     /* a CUDA runtime call failed (no device, bad stream, launch error) */
+  KVC_ETIMEOUT = -5,  /* a bounded device-side wait gave up (read by kvc_sync_status) */
+  KVC_EDEVICE = -6    /* a kernel met data it cannot encode exactly (e.g. |x| > 65504
+                         on the tensor-core path); read by kvc_sync_status */
+} kvc_status;
+
+enum {
+  KVC_MODE_UNIFORM = 0,  /* KVTC-style: code = clip(rint((z - lo)/step), 0, 2^b - 1) */
+  KVC_MODE_GROUP = 1,    /* PALU-style: symmetric per-token scale per group of components */
+  KVC_MODE_CODEBOOK = 2, /* TurboQuant-MSE-style: rotation + scalar codebook + fp16 norm */
+  KVC_MODE_INT8 = 3      /* per-token int8 with an fp16 scale (values) */
+};
+
+enum { KVC_F32 = 0, KVC_F16 = 1, KVC_BF16 = 2 };
+
+/* Kernel path selection (kvc_set_path). */
+enum {
+  KVC_PATH_AUTO = 0,    /* tensor-core kernels where the shape allows, else CUDA cores */
+  KVC_PATH_GENERIC = 1  /* CUDA-core kernels only (any shape) */
+};
+
+/*
+ * Layer descriptor.  Slots: the layer has B * (H / heads_per_group) slots;
+ * slot (b, g) holds head group g of batch entry b and uses basis
+ * basis_of[b * (H / heads_per_group) + g].  Its token row is the
+ * concatenation of the group's heads: D_in = heads_per_group * D values.
+ *
+ *  mode             KVC_MODE_*.
+ *  B, H, D          batch, KV heads, head dimension (> 0).
+ *  heads_per_group  heads sharing one projection (palu_cache page: contiguous
+ *                   head groups); must be 1 unless mode == GROUP.  Divides H.
+ *  r                rank (columns of V).  CODEBOOK: r == D.  INT8: ignored.
+ *  n_bases          number of distinct bases (>= 1; ignored for INT8).
+ *  basis_of         host int32 [n_slots]; NULL means every slot uses basis 0.
+ *  V                host fp32 [n_bases][D_in][r], row-major (column k = basis
+ *                   vector k).  CODEBOOK: the D x D rotation.
+ *  mean             host fp32 [n_bases][D_in] or NULL (zero).  CODEBOOK: must be NULL.
+ *  bits             host uint8 [n_bases][r], each in {0,1,2,3,4,8}.  GROUP: widths
+ *                   in {0,2,3,4,8}, non-increasing in k and equal for every basis.
+ *                   CODEBOOK: ignored (every component has cb_bits).
+ *  qmin, qstep      host fp32 [n_bases][r] (UNIFORM only): frozen minimum and step
+ *                   (step > 0 for kept components).
+ *  group_size       GROUP only: components per scale group, 1..32 (palu_group_size).
+ *  codebook         host fp32 [1 << cb_bits], strictly ascending (CODEBOOK only).
+ *  cb_bits          CODEBOOK only: 1, 2, 3, 4 or 8.
+ *  in_dtype         dtype of appended rows: KVC_F32, KVC_F16 or KVC_BF16.
+ *  out_dtype        dtype of fetched rows: KVC_F16 or KVC_BF16.
+ *  capacity         tokens each slot can hold (>= 1).
+ *  store            device, caller-owned, at least kvc_store_bytes() bytes,
+ *                   256-byte aligned; borrowed for the layer's lifetime.
+ *  store_bytes      size of store in bytes.
+ */
+typedef struct {
+  int32_t mode;
+  int32_t B, H, D;
+  int32_t heads_per_group;
+  int32_t r;
+  int32_t n_bases;
+  const int32_t *basis_of;
+  const float *V;
+  const float *mean;
+  const uint8_t *bits;
+  const float *qmin;
+  const float *qstep;
+  int32_t group_size;
+  const float *codebook;
+  int32_t cb_bits;
+  int32_t in_dtype;
+  int32_t out_dtype;
+  int64_t capacity;
+  void *store;
+  size_t store_bytes;
+} kvc_layer_desc;
+
+/* Byte accounting (kvtc_cache page "Byte accounting"; turboquant_cache page
+ * memory_bytes; palu_cache page "Byte accounting").
+ *  payload     packed code bytes: sum over slots of length * P(slot),
+ *              P = sum over widths b of ceil(r_b * b / 8) (INT8: D).
+ *  side        per-token fp16 side words: GROUP 2 * n_groups, CODEBOOK 2 (norm),
+ *              INT8 2 (scale), UNIFORM 0 -- times length, summed over slots.
+ *  fixed       frozen parameters a decoder needs, counted as fp32 values and
+ *              1-byte widths: UNIFORM n_bases * (4 D_in r + 4 D_in + 8 r + r);
+ *              GROUP n_bases * (4 D_in r + 4 D_in + r); CODEBOOK 4 D r + 4 * 2^cb_bits;
+ *              INT8 0.
+ *  fp16_equiv  B * H * length * D * 2, the uncompressed fp16 size. */
+typedef struct {
+  int64_t payload;
+  int64_t side;
+  int64_t fixed;
+  int64_t fp16_equiv;
+} kvc_bytes;
+
+/* Where slot s lives inside the store: token t's packed row is the row_bytes
+ * bytes at store + payload_offset + t * row_bytes; its side words are the
+ * side_bytes bytes at store + side_offset + t * side_bytes (GROUP: fp16
+ * scales in group order; CODEBOOK: fp16 norm; INT8: fp16 scale). */
+typedef struct {
+  int64_t payload_offset;
+  int64_t row_bytes;
+  int64_t side_offset;
+  int64_t side_bytes;
+} kvc_slot_layout;
+
+/* ABI version of the loaded library (KVC_ABI_VERSION). */
+int32_t kvc_abi_version(void);
+
+/* Message for the last failing call on this thread ("" if none). */
+const char *kvc_last_error(void);
+
+/* Bytes of device store the descriptor needs (host-only; desc->store unused).
+ * KVC_EINVAL on a bad descriptor. */
+kvc_status kvc_store_bytes(const kvc_layer_desc *desc, size_t *out);
+
+/* Validate the descriptor, copy the frozen parameters to the device in the
+ * kernels' layouts and return a layer of length 0 (kvtc_cache page "Design":
+ * basis and allocation fit once at prefill, then reused unchanged).  Runs on
+ * the current CUDA device and synchronises with it.  Host arrays are only read
+ * during the call.  KVC_EINVAL on a bad descriptor, KVC_ECUDA on a CUDA error. */
+kvc_status kvc_init_layer(const kvc_layer_desc *desc, kvc_layer **out);
+
+/* Append T tokens: x is device memory, [B, H, T, D] contiguous in in_dtype.
+ * Equivalent to kvc_append_strided with strides (H*T*D, T*D, D). */
+kvc_status kvc_append(kvc_layer *layer, const void *x, int64_t T, void *stream);
+
+/* Append T tokens from x (device) with element strides: token t of head h of
+ * batch b starts at x + b*stride_b + h*stride_h + t*stride_t (elements of
+ * in_dtype); the D values of a token are contiguous.  Each token is
+ * projected, quantised and packed independently (kvtc_cache page, "Design",
+ * decode step 1; turboquant_cache page, append_key / append_value), so T
+ * tokens in one call store exactly what T calls of one token store.
+ * KVC_ECAPACITY if length + T > capacity (nothing written); T == 0 is a no-op. */
+kvc_status kvc_append_strided(kvc_layer *layer, const void *x, int64_t T, int64_t stride_b,
+                              int64_t stride_h, int64_t stride_t, void *stream);
+
+/* Reconstruct every stored token: out is device memory [B, H, ld_s, D] in
+ * out_dtype; rows 0..length-1 of each (b, h) are written, rows length..ld_s-1
+ * are left untouched.  *S_out (may be NULL) receives length.  (kvtc_cache page,
+ * "Design": every call returns reconstructed [B, H, S_total, D] for SDPA;
+ * palu_cache page: latent -> dequant -> reconstruct.)  KVC_EINVAL if
+ * ld_s < length or out is not device memory. */
+kvc_status kvc_fetch(kvc_layer *layer, void *out, int64_t ld_s, int64_t *S_out, void *stream);
+
+/* Drop the n most recent tokens (kvtc_cache page KVTCKVCache.trim; palu_cache
+ * page trim): n is clamped to the length, n <= 0 drops nothing; *dropped (may
+ * be NULL) receives the count.  Host-only, O(1).  The frozen parameters stay,
+ * also at length 0 (as turboquant_cache page reset keeps its quantiser). */
+kvc_status kvc_trim(kvc_layer *layer, int64_t n, int64_t *dropped);
+
+/* Current length (tokens per slot). */
+kvc_status kvc_length(const kvc_layer *layer, int64_t *out);
+
+/* Byte accounting, see kvc_bytes.  Host-only. */
+kvc_status kvc_nbytes(const kvc_layer *layer, kvc_bytes *out);
+
+/* Store layout of one slot (0 <= slot < n_slots).  Host-only. */
+kvc_status kvc_get_slot_layout(const kvc_layer *layer, int32_t slot, kvc_slot_layout *out);
+
+/* Choose the kernels used by later calls (KVC_PATH_*).  Host-only. */
+kvc_status kvc_set_path(kvc_layer *layer, int32_t path);
+
+/* Synchronise `stream`, then read and clear the layer's device error word:
+ * KVC_OK, KVC_ETIMEOUT (a bounded wait gave up) or KVC_EDEVICE (data the kernel
+ * cannot encode exactly).  KVC_ECUDA if the synchronisation itself failed. */
+kvc_status kvc_sync_status(kvc_layer *layer, void *stream);
+
+/* Synchronise `stream` and copy the layer's device counters to host out[4]:
+ * [0] components whose code was re-decided in double precision (near a rounding
+ * boundary), [1] per-token fp16 side words re-decided, [2] appended tokens,
+ * [3] kernels this layer has launched (counted on the host).  With reset != 0
+ * the counters are then zeroed. */
+kvc_status kvc_counters(kvc_layer *layer, int64_t out[4], int32_t reset, void *stream);
+
+/* Free the layer's parameter block (synchronises the device first).  NULL is a no-op. */
+void kvc_destroy(kvc_layer *layer);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

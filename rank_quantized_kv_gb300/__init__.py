@@ -1,0 +1,342 @@
+"""GB300-native projected-and-quantized KV cache: Python binding of libkvc.
+
+The binding only marshals arguments: every step of append and fetch runs in
+the library's CUDA kernels.  PyTorch provides device memory and streams.
+If libkvc.so is missing or cannot be loaded, every entry point raises; there
+is no CPU fallback.
+
+    layer = KVCacheLayer("uniform", B, H, D, V=V, mean=mean, bits=bits,
+                         qmin=lo, qstep=step, in_dtype="bf16", capacity=S)
+    layer.append(x)            # x: [B, H, T, D] on the layer's device
+    k_hat = layer.fetch()      # [B, H, S, D] fp16
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from ctypes import POINTER, byref, c_float, c_int32, c_int64, c_size_t, c_uint8, c_void_p
+
+import numpy as np
+
+__all__ = ["KVCacheLayer", "load_library", "library_path", "KvcError", "MODES", "DTYPES",
+           "EXPORTED_SYMBOLS", "store_bytes"]
+
+MODES = {"uniform": 0, "group": 1, "codebook": 2, "int8": 3}
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
+PATHS = {"auto": 0, "generic": 1}
+STATUS = {0: "KVC_OK", -1: "KVC_EINVAL", -2: "KVC_ESTATE", -3: "KVC_ECAPACITY",
+          -4: "KVC_ECUDA", -5: "KVC_ETIMEOUT", -6: "KVC_EDEVICE"}
+
+# Every function include/kvc.h declares.
+EXPORTED_SYMBOLS = (
+    "kvc_abi_version", "kvc_last_error", "kvc_store_bytes", "kvc_init_layer", "kvc_append",
+    "kvc_append_strided", "kvc_fetch", "kvc_trim", "kvc_length", "kvc_nbytes",
+    "kvc_get_slot_layout", "kvc_set_path", "kvc_sync_status", "kvc_counters", "kvc_destroy",
+)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def library_path() -> str:
+    return os.environ.get("KVC_LIBRARY", os.path.join(_HERE, "_lib", "libkvc.so"))
+
+
+class KvcError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [
+        ("mode", c_int32), ("B", c_int32), ("H", c_int32), ("D", c_int32),
+        ("heads_per_group", c_int32), ("r", c_int32), ("n_bases", c_int32),
+        ("basis_of", POINTER(c_int32)), ("V", POINTER(c_float)), ("mean", POINTER(c_float)),
+        ("bits", POINTER(c_uint8)), ("qmin", POINTER(c_float)), ("qstep", POINTER(c_float)),
+        ("group_size", c_int32), ("codebook", POINTER(c_float)), ("cb_bits", c_int32),
+        ("in_dtype", c_int32), ("out_dtype", c_int32), ("capacity", c_int64),
+        ("store", c_void_p), ("store_bytes", c_size_t),
+    ]
+
+
+class _Bytes(ctypes.Structure):
+    _fields_ = [("payload", c_int64), ("side", c_int64), ("fixed", c_int64),
+                ("fp16_equiv", c_int64)]
+
+
+class _SlotLayout(ctypes.Structure):
+    _fields_ = [("payload_offset", c_int64), ("row_bytes", c_int64),
+                ("side_offset", c_int64), ("side_bytes", c_int64)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library():
+    """Load libkvc.so once; raises if it is missing (no fallback exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(f"libkvc.so not found at {path}; build it with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        # Bind to the CUDA runtime torch already loaded (same libcudart.so.13),
+        # so that torch's streams and allocations are this library's too.
+        import torch  # noqa: F401
+
+        lib = ctypes.CDLL(path)
+        P = c_void_p
+        sig = {
+            "kvc_abi_version": (c_int32, []),
+            "kvc_last_error": (ctypes.c_char_p, []),
+            "kvc_store_bytes": (c_int32, [POINTER(_Desc), POINTER(c_size_t)]),
+            "kvc_init_layer": (c_int32, [POINTER(_Desc), POINTER(c_void_p)]),
+            "kvc_append": (c_int32, [P, P, c_int64, P]),
+            "kvc_append_strided": (c_int32, [P, P, c_int64, c_int64, c_int64, c_int64, P]),
+            "kvc_fetch": (c_int32, [P, P, c_int64, POINTER(c_int64), P]),
+            "kvc_trim": (c_int32, [P, c_int64, POINTER(c_int64)]),
+            "kvc_length": (c_int32, [P, POINTER(c_int64)]),
+            "kvc_nbytes": (c_int32, [P, POINTER(_Bytes)]),
+            "kvc_get_slot_layout": (c_int32, [P, c_int32, POINTER(_SlotLayout)]),
+            "kvc_set_path": (c_int32, [P, c_int32]),
+            "kvc_sync_status": (c_int32, [P, P]),
+            "kvc_counters": (c_int32, [P, POINTER(c_int64), c_int32, P]),
+            "kvc_destroy": (None, [P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if lib.kvc_abi_version() != 1:
+            raise ImportError("libkvc ABI version mismatch")
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise KvcError(status, _lib.kvc_last_error().decode())
+
+
+def _f32(a, shape=None):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    if shape is not None:
+        a = a.reshape(shape)
+    return a
+
+
+def _ptr(a, ctype):
+    return None if a is None else a.ctypes.data_as(POINTER(ctype))
+
+
+def _build_desc(mode, B, H, D, r, V, mean, bits, qmin, qstep, basis_of, heads_per_group,
+                group_size, codebook, in_dtype, out_dtype, capacity):
+    """Marshal arguments into a descriptor; returns (desc, keepalive arrays)."""
+    if mode not in MODES:
+        raise ValueError(f"mode must be one of {list(MODES)}")
+    d_in = heads_per_group * D
+    keep = {}
+    desc = _Desc()
+    desc.mode = MODES[mode]
+    desc.B, desc.H, desc.D = B, H, D
+    desc.heads_per_group = heads_per_group
+    desc.in_dtype = DTYPES[in_dtype]
+    desc.out_dtype = DTYPES[out_dtype]
+    desc.capacity = int(capacity)
+    desc.group_size = int(group_size)
+    if mode != "int8":
+        Vn = np.asarray(V, dtype=np.float32)
+        if Vn.ndim == 2:
+            Vn = Vn[None]
+        nb, rows, rr = Vn.shape
+        if r is not None and r != rr:
+            raise ValueError("r disagrees with V")
+        keep["V"] = np.ascontiguousarray(Vn)
+        desc.r, desc.n_bases = rr, nb
+        desc.V = _ptr(keep["V"], c_float)
+        if mean is not None:
+            keep["mean"] = _f32(mean, (nb, d_in))
+            desc.mean = _ptr(keep["mean"], c_float)
+        if bits is not None:
+            keep["bits"] = np.ascontiguousarray(np.asarray(bits, dtype=np.uint8).reshape(nb, rr))
+            desc.bits = _ptr(keep["bits"], c_uint8)
+        if qmin is not None:
+            keep["qmin"] = _f32(qmin, (nb, rr))
+            keep["qstep"] = _f32(qstep, (nb, rr))
+            desc.qmin = _ptr(keep["qmin"], c_float)
+            desc.qstep = _ptr(keep["qstep"], c_float)
+        if basis_of is not None:
+            keep["basis_of"] = np.ascontiguousarray(np.asarray(basis_of, dtype=np.int32))
+            desc.basis_of = _ptr(keep["basis_of"], c_int32)
+        if codebook is not None:
+            keep["codebook"] = _f32(codebook)
+            desc.codebook = _ptr(keep["codebook"], c_float)
+            desc.cb_bits = int(round(np.log2(keep["codebook"].shape[0])))
+    return desc, keep
+
+
+def store_bytes(mode, B, H, D, *, capacity, r=None, V=None, bits=None, qmin=None, qstep=None,
+                basis_of=None, heads_per_group=1, group_size=32, codebook=None,
+                in_dtype="bf16", out_dtype="f16", mean=None) -> int:
+    """Bytes of device store a layer with these parameters needs."""
+    lib = load_library()
+    desc, keep = _build_desc(mode, B, H, D, r, V, mean, bits, qmin, qstep, basis_of,
+                             heads_per_group, group_size, codebook, in_dtype, out_dtype, capacity)
+    n = c_size_t()
+    _check(lib.kvc_store_bytes(byref(desc), byref(n)))
+    return int(n.value)
+
+
+def _stream_ptr(stream, device):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return c_void_p(stream.cuda_stream)
+
+
+_TORCH_DT = None
+
+
+def _torch_dtypes():
+    global _TORCH_DT
+    if _TORCH_DT is None:
+        import torch
+
+        _TORCH_DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+    return _TORCH_DT
+
+
+class KVCacheLayer:
+    """One K or V tensor of one attention layer, stored projected and quantised.
+
+    mode: "uniform" (KVTC-style), "group" (PALU-style), "codebook"
+    (TurboQuant-MSE-style) or "int8" (per-token int8 values).  Parameters are
+    host arrays (numpy or CPU tensors) with the shapes of include/kvc.h; the
+    store is a torch uint8 tensor on ``device`` owned by this object.
+    """
+
+    def __init__(self, mode, B, H, D, *, capacity, r=None, V=None, mean=None, bits=None,
+                 qmin=None, qstep=None, basis_of=None, heads_per_group=1, group_size=32,
+                 codebook=None, in_dtype="bf16", out_dtype="f16", device=None, path="auto"):
+        import torch
+
+        lib = load_library()
+        self.mode, self.B, self.H, self.D = mode, B, H, D
+        self.hpg = heads_per_group
+        self.Hg = H // heads_per_group
+        self.n_slots = B * self.Hg
+        self.in_dtype, self.out_dtype = in_dtype, out_dtype
+        self.device = torch.device(device if device is not None else "cuda")
+        if self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
+        self.capacity = int(capacity)
+        desc, keep = _build_desc(mode, B, H, D, r, V, mean, bits, qmin, qstep, basis_of,
+                                 heads_per_group, group_size, codebook, in_dtype, out_dtype,
+                                 capacity)
+        n = c_size_t()
+        _check(lib.kvc_store_bytes(byref(desc), byref(n)))
+        self.store = torch.zeros(int(n.value), dtype=torch.uint8, device=self.device)
+        desc.store = c_void_p(self.store.data_ptr())
+        desc.store_bytes = n.value
+        handle = c_void_p()
+        with torch.cuda.device(self.device):
+            _check(lib.kvc_init_layer(byref(desc), byref(handle)))
+        self._h = handle
+        self._lib = lib
+        self.set_path(path)
+
+    # -- hot path ------------------------------------------------------------------------
+    def append(self, x, stream=None):
+        """Append x [B, H, T, D] (device tensor of in_dtype; last dim contiguous)."""
+        if x.dim() != 4 or x.shape[0] != self.B or x.shape[1] != self.H or x.shape[3] != self.D:
+            raise ValueError(f"x must be [{self.B}, {self.H}, T, {self.D}], got {tuple(x.shape)}")
+        if x.dtype != _torch_dtypes()[self.in_dtype]:
+            raise TypeError(f"x must be {self.in_dtype}")
+        if x.shape[2] and x.stride(3) != 1:
+            raise ValueError("the head dimension of x must be contiguous")
+        sb, sh, st, _ = x.stride()
+        _check(self._lib.kvc_append_strided(self._h, c_void_p(x.data_ptr()), x.shape[2], sb, sh,
+                                            st, _stream_ptr(stream, self.device)))
+
+    def fetch(self, out=None, stream=None):
+        """Reconstruct everything stored into out [B, H, ld_s, D] (allocated if None)."""
+        import torch
+
+        S = len(self)
+        if out is None:
+            out = torch.empty(self.B, self.H, S, self.D, dtype=_torch_dtypes()[self.out_dtype],
+                              device=self.device)
+        if out.dtype != _torch_dtypes()[self.out_dtype] or not out.is_contiguous():
+            raise ValueError("out must be a contiguous tensor of out_dtype")
+        if out.shape[0] != self.B or out.shape[1] != self.H or out.shape[3] != self.D:
+            raise ValueError("out must be [B, H, ld_s, D]")
+        s_out = c_int64()
+        _check(self._lib.kvc_fetch(self._h, c_void_p(out.data_ptr()), out.shape[2], byref(s_out),
+                                   _stream_ptr(stream, self.device)))
+        return out
+
+    # -- state -----------------------------------------------------------------------------
+    def trim(self, n: int) -> int:
+        d = c_int64()
+        _check(self._lib.kvc_trim(self._h, int(n), byref(d)))
+        return int(d.value)
+
+    def __len__(self) -> int:
+        n = c_int64()
+        _check(self._lib.kvc_length(self._h, byref(n)))
+        return int(n.value)
+
+    def nbytes(self) -> dict:
+        b = _Bytes()
+        _check(self._lib.kvc_nbytes(self._h, byref(b)))
+        return {"payload": b.payload, "side": b.side, "fixed": b.fixed, "fp16_equiv": b.fp16_equiv}
+
+    def slot_layout(self, slot: int) -> dict:
+        s = _SlotLayout()
+        _check(self._lib.kvc_get_slot_layout(self._h, int(slot), byref(s)))
+        return {"payload_offset": s.payload_offset, "row_bytes": s.row_bytes,
+                "side_offset": s.side_offset, "side_bytes": s.side_bytes}
+
+    def slot_rows(self, slot: int):
+        """Views into the store: (packed rows [len, P] uint8, side words [len, side_bytes] or None)."""
+        lay = self.slot_layout(slot)
+        n = len(self)
+        P, o = lay["row_bytes"], lay["payload_offset"]
+        rows = self.store[o:o + n * P].view(n, P)
+        side = None
+        if lay["side_bytes"]:
+            so, sb = lay["side_offset"], lay["side_bytes"]
+            side = self.store[so:so + n * sb].view(n, sb)
+        return rows, side
+
+    def set_path(self, path: str):
+        _check(self._lib.kvc_set_path(self._h, PATHS[path]))
+
+    def sync_status(self, stream=None) -> int:
+        """Synchronise and return the device status (0 = ok); clears it."""
+        return int(self._lib.kvc_sync_status(self._h, _stream_ptr(stream, self.device)))
+
+    def counters(self, reset=False, stream=None):
+        out = (c_int64 * 4)()
+        _check(self._lib.kvc_counters(self._h, out, int(bool(reset)),
+                                      _stream_ptr(stream, self.device)))
+        return {"refined_codes": out[0], "refined_side": out[1], "appended": out[2],
+                "launches": out[3]}
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.kvc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

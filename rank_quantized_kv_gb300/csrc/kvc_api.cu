@@ -1,0 +1,595 @@
+// Host side of libkvc: descriptor validation, store layout, the frozen
+// parameter block in kernel layouts, and the kvc_* C entry points.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kvc_internal.h"
+#include "kvc_tc.h"
+
+using kvc::Params;
+
+struct kvc_layer {
+  Params p{};
+  void* block = nullptr;  // device parameter block (owned)
+  int device = 0;
+  int64_t len = 0;
+  int64_t capacity = 0;
+  int32_t path = KVC_PATH_AUTO;
+  int64_t launches = 0;              // kernels launched by this layer (host count)
+  int mode = 0, B = 0, H = 0, D = 0, hpg = 1, r = 0, n_bases = 0, n_slots = 0;
+  int side_bytes = 0;
+  int64_t fixed_bytes = 0;
+  std::vector<int32_t> P_host;       // per basis
+  std::vector<int32_t> basis_host;   // per slot
+  std::vector<int64_t> pay_host, side_host;
+  kvc::TcPlan tc{};                  // tensor-core path tables (kvc_tc.cu)
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+kvc_status fail(kvc_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+kvc_status succeed() {
+  g_err.clear();
+  return KVC_OK;
+}
+
+kvc_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(KVC_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+bool valid_width(int b) { return b == 0 || b == 1 || b == 2 || b == 3 || b == 4 || b == 8; }
+
+// Everything derived from a descriptor, on the host.
+struct Geo {
+  int d_in = 0, Hg = 0, n_slots = 0, nb = 0, r = 0;
+  int cb_levels = 0, n_groups = 0, side_bytes = 0;
+  std::vector<uint8_t> bits;     // [nb][r]
+  std::vector<int32_t> P, n_kept, seg, groups, basis;
+  std::vector<int16_t> order;
+  std::vector<int64_t> pay_off, side_off;
+  int64_t store_total = 0;
+  int64_t fixed = 0;
+};
+
+kvc_status build_geo(const kvc_layer_desc* d, Geo& g) {
+  if (!d) return fail(KVC_EINVAL, "descriptor is NULL");
+  if (d->mode < KVC_MODE_UNIFORM || d->mode > KVC_MODE_INT8)
+    return fail(KVC_EINVAL, "mode %d is not a KVC_MODE_*", d->mode);
+  if (d->B <= 0 || d->H <= 0 || d->D <= 0) return fail(KVC_EINVAL, "B, H, D must be > 0");
+  if (d->heads_per_group <= 0 || d->H % d->heads_per_group)
+    return fail(KVC_EINVAL, "heads_per_group must be >= 1 and divide H");
+  if (d->heads_per_group != 1 && d->mode != KVC_MODE_GROUP)
+    return fail(KVC_EINVAL, "heads_per_group != 1 needs KVC_MODE_GROUP");
+  if (d->in_dtype != KVC_F32 && d->in_dtype != KVC_F16 && d->in_dtype != KVC_BF16)
+    return fail(KVC_EINVAL, "in_dtype must be KVC_F32, KVC_F16 or KVC_BF16");
+  if (d->out_dtype != KVC_F16 && d->out_dtype != KVC_BF16)
+    return fail(KVC_EINVAL, "out_dtype must be KVC_F16 or KVC_BF16");
+  if (d->capacity < 1) return fail(KVC_EINVAL, "capacity must be >= 1");
+  g.Hg = d->H / d->heads_per_group;
+  g.d_in = d->heads_per_group * d->D;
+  g.n_slots = d->B * g.Hg;
+  if ((int64_t)d->B * g.Hg > (1 << 30)) return fail(KVC_EINVAL, "too many slots");
+
+  if (d->mode == KVC_MODE_INT8) {
+    g.nb = 0;
+    g.r = 0;
+    g.side_bytes = 2;
+    g.basis.assign(g.n_slots, 0);
+    g.P.assign(1, d->D);
+  } else {
+    if (d->r < 1 || d->r > kvc::kMaxRank || d->r > g.d_in)
+      return fail(KVC_EINVAL, "r must be in [1, min(D_in, %d)]", kvc::kMaxRank);
+    if (d->n_bases < 1) return fail(KVC_EINVAL, "n_bases must be >= 1");
+    if (!d->V) return fail(KVC_EINVAL, "V is NULL");
+    g.r = d->r;
+    g.nb = d->n_bases;
+    g.basis.assign(g.n_slots, 0);
+    if (d->basis_of) {
+      for (int s = 0; s < g.n_slots; ++s) {
+        if (d->basis_of[s] < 0 || d->basis_of[s] >= g.nb)
+          return fail(KVC_EINVAL, "basis_of[%d] = %d outside [0, %d)", s, d->basis_of[s], g.nb);
+        g.basis[s] = d->basis_of[s];
+      }
+    }
+    g.bits.assign((size_t)g.nb * g.r, 0);
+    if (d->mode == KVC_MODE_CODEBOOK) {
+      if (d->r != g.d_in) return fail(KVC_EINVAL, "codebook mode needs r == D");
+      if (d->mean) return fail(KVC_EINVAL, "codebook mode takes no mean");
+      const int cb = d->cb_bits;
+      if (!(cb == 1 || cb == 2 || cb == 3 || cb == 4 || cb == 8))
+        return fail(KVC_EINVAL, "cb_bits must be 1, 2, 3, 4 or 8");
+      if (!d->codebook) return fail(KVC_EINVAL, "codebook is NULL");
+      g.cb_levels = 1 << cb;
+      for (int j = 0; j < g.cb_levels; ++j) {
+        if (!std::isfinite(d->codebook[j])) return fail(KVC_EINVAL, "codebook has a non-finite entry");
+        if (j && !(d->codebook[j] > d->codebook[j - 1]))
+          return fail(KVC_EINVAL, "codebook must be strictly ascending");
+      }
+      std::fill(g.bits.begin(), g.bits.end(), (uint8_t)cb);
+      g.side_bytes = 2;
+    } else {
+      if (!d->bits) return fail(KVC_EINVAL, "bits is NULL");
+      for (size_t i = 0; i < g.bits.size(); ++i) {
+        if (!valid_width(d->bits[i]))
+          return fail(KVC_EINVAL, "bits[%zu] = %d is not in {0,1,2,3,4,8}", i, (int)d->bits[i]);
+        g.bits[i] = d->bits[i];
+      }
+    }
+    if (d->mode == KVC_MODE_UNIFORM) {
+      if (!d->qmin || !d->qstep) return fail(KVC_EINVAL, "uniform mode needs qmin and qstep");
+      for (size_t i = 0; i < g.bits.size(); ++i) {
+        if (!g.bits[i]) continue;
+        if (!std::isfinite(d->qmin[i]) || !std::isfinite(d->qstep[i]) || !(d->qstep[i] > 0.f))
+          return fail(KVC_EINVAL, "qmin/qstep[%zu] must be finite with qstep > 0", i);
+      }
+    }
+    if (d->mode == KVC_MODE_GROUP) {
+      if (d->group_size < 1 || d->group_size > kvc::kMaxGroupSize)
+        return fail(KVC_EINVAL, "group_size must be in [1, %d]", kvc::kMaxGroupSize);
+      for (int b = 0; b < g.nb; ++b)
+        for (int k = 0; k < g.r; ++k) {
+          const int w = g.bits[(size_t)b * g.r + k];
+          if (w == 1) return fail(KVC_EINVAL, "group mode needs widths >= 2 (or 0)");
+          if (k && w > g.bits[(size_t)b * g.r + k - 1])
+            return fail(KVC_EINVAL, "group mode needs non-increasing widths");
+          if (w != g.bits[k]) return fail(KVC_EINVAL, "group mode needs the same widths for every basis");
+        }
+    }
+    for (size_t i = 0; i < (size_t)g.nb * g.d_in * g.r; ++i)
+      if (!std::isfinite(d->V[i])) return fail(KVC_EINVAL, "V has a non-finite entry");
+    if (d->mean)
+      for (size_t i = 0; i < (size_t)g.nb * g.d_in; ++i)
+        if (!std::isfinite(d->mean[i])) return fail(KVC_EINVAL, "mean has a non-finite entry");
+
+    // packed order and segments: widths descending, components ascending within a width
+    g.P.assign(g.nb, 0);
+    g.n_kept.assign(g.nb, 0);
+    g.seg.assign((size_t)g.nb * kvc::kMaxSeg * 4, 0);
+    g.order.assign((size_t)g.nb * g.r, (int16_t)-1);
+    static const int kWidths[kvc::kMaxSeg] = {8, 4, 3, 2, 1};
+    for (int b = 0; b < g.nb; ++b) {
+      int m = 0, byte = 0, s = 0;
+      for (int wi = 0; wi < kvc::kMaxSeg; ++wi) {
+        const int w = kWidths[wi];
+        int cnt = 0;
+        for (int k = 0; k < g.r; ++k)
+          if (g.bits[(size_t)b * g.r + k] == w) g.order[(size_t)b * g.r + m + cnt++] = (int16_t)k;
+        if (!cnt) continue;
+        int32_t* e = &g.seg[((size_t)b * kvc::kMaxSeg + s) * 4];
+        e[0] = byte;
+        e[1] = w;
+        e[2] = m;
+        e[3] = cnt;
+        ++s;
+        m += cnt;
+        byte += (cnt * w + 7) / 8;
+      }
+      g.P[b] = byte;
+      g.n_kept[b] = m;
+    }
+    if (d->mode == KVC_MODE_GROUP) {
+      for (int s = 0; s < kvc::kMaxSeg; ++s) {
+        const int32_t* e = &g.seg[(size_t)s * 4];
+        if (!e[3]) break;
+        const int first = g.order[e[2]];
+        for (int o = 0; o < e[3]; o += d->group_size) {
+          g.groups.push_back(first + o);
+          g.groups.push_back(std::min(d->group_size, e[3] - o));
+          g.groups.push_back(e[1]);
+        }
+      }
+      g.n_groups = (int)g.groups.size() / 3;
+      g.side_bytes = 2 * g.n_groups;
+    }
+  }
+
+  // store layout: per slot, payload rows then side words, 256-byte aligned,
+  // each region with 16 bytes of slack for vector over-reads
+  g.pay_off.assign(g.n_slots, 0);
+  g.side_off.assign(g.n_slots, 0);
+  int64_t cur = 0;
+  for (int s = 0; s < g.n_slots; ++s) {
+    const int64_t P = d->mode == KVC_MODE_INT8 ? d->D : g.P[g.basis[s]];
+    cur = align_up(cur, 256);
+    g.pay_off[s] = cur;
+    cur += d->capacity * P + 16;
+    cur = align_up(cur, 256);
+    g.side_off[s] = cur;
+    cur += d->capacity * g.side_bytes + 16;
+  }
+  g.store_total = align_up(cur, 256);
+
+  const int64_t din = g.d_in, r = g.r, nb = g.nb;
+  switch (d->mode) {
+    case KVC_MODE_UNIFORM: g.fixed = nb * (4 * din * r + 4 * din + 8 * r + r); break;
+    case KVC_MODE_GROUP: g.fixed = nb * (4 * din * r + 4 * din + r); break;
+    case KVC_MODE_CODEBOOK: g.fixed = nb * 4 * din * r + 4 * (int64_t)g.cb_levels; break;
+    default: g.fixed = 0;
+  }
+  return KVC_OK;
+}
+
+// Host image of the parameter block: arrays appended at 256-byte alignment.
+struct Image {
+  std::vector<uint8_t> bytes;
+  template <class T>
+  size_t put(const T* src, size_t n) {
+    const size_t off = (size_t)align_up((int64_t)bytes.size(), 256);
+    bytes.resize(off + sizeof(T) * std::max<size_t>(n, 1), 0);
+    if (n) std::memcpy(bytes.data() + off, src, sizeof(T) * n);
+    return off;
+  }
+  size_t zeros(size_t nbytes) {
+    const size_t off = (size_t)align_up((int64_t)bytes.size(), 256);
+    bytes.resize(off + std::max<size_t>(nbytes, 1), 0);
+    return off;
+  }
+};
+
+bool is_device_ptr(const void* ptr, int dev) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == dev;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+int32_t kvc_abi_version(void) { return KVC_ABI_VERSION; }
+
+const char* kvc_last_error(void) { return g_err.c_str(); }
+
+kvc_status kvc_store_bytes(const kvc_layer_desc* desc, size_t* out) {
+  if (!out) return fail(KVC_EINVAL, "out is NULL");
+  Geo g;
+  kvc_status st = build_geo(desc, g);
+  if (st) return st;
+  *out = (size_t)g.store_total;
+  return succeed();
+}
+
+kvc_status kvc_init_layer(const kvc_layer_desc* d, kvc_layer** out) {
+  if (!out) return fail(KVC_EINVAL, "out is NULL");
+  *out = nullptr;
+  Geo g;
+  kvc_status st = build_geo(d, g);
+  if (st) return st;
+  if (!d->store) return fail(KVC_EINVAL, "store is NULL");
+  if ((uintptr_t)d->store % 256) return fail(KVC_EINVAL, "store must be 256-byte aligned");
+  if (d->store_bytes < (size_t)g.store_total)
+    return fail(KVC_EINVAL, "store_bytes %zu < required %lld", d->store_bytes,
+                (long long)g.store_total);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (!is_device_ptr(d->store, dev)) return fail(KVC_EINVAL, "store is not device memory of the current device");
+
+  const int nb = g.nb, r = g.r, din = g.d_in;
+  const bool coded = d->mode != KVC_MODE_INT8;
+  std::vector<float> V, Vt, mean, lo, step, inv, vnorm, cb, mids;
+  if (coded) {
+    V.assign(d->V, d->V + (size_t)nb * din * r);
+    Vt.assign((size_t)nb * r * din, 0.f);
+    vnorm.assign((size_t)nb * r, 0.f);
+    for (int b = 0; b < nb; ++b)
+      for (int k = 0; k < r; ++k) {
+        double ss = 0.0;
+        for (int i = 0; i < din; ++i) {
+          const float v = V[((size_t)b * din + i) * r + k];
+          Vt[((size_t)b * r + k) * din + i] = v;
+          ss += (double)v * v;
+        }
+        vnorm[(size_t)b * r + k] = std::nextafter((float)std::sqrt(ss), INFINITY);
+      }
+    mean.assign((size_t)nb * din, 0.f);
+    if (d->mean) std::copy(d->mean, d->mean + (size_t)nb * din, mean.begin());
+    lo.assign((size_t)nb * r, 0.f);
+    step.assign((size_t)nb * r, 0.f);
+    inv.assign((size_t)nb * r, 0.f);
+    if (d->mode == KVC_MODE_UNIFORM)
+      for (size_t i = 0; i < lo.size(); ++i) {
+        if (!g.bits[i]) continue;
+        lo[i] = d->qmin[i];
+        step[i] = d->qstep[i];
+        inv[i] = (float)(1.0 / (double)d->qstep[i]);
+      }
+    if (d->mode == KVC_MODE_CODEBOOK) {
+      cb.assign(d->codebook, d->codebook + g.cb_levels);
+      for (int j = 0; j + 1 < g.cb_levels; ++j)
+        mids.push_back((float)(0.5 * ((double)cb[j] + (double)cb[j + 1])));
+    }
+  }
+
+  Image im;
+  const size_t oV = im.put(V.data(), V.size());
+  const size_t oVt = im.put(Vt.data(), Vt.size());
+  const size_t oMean = im.put(mean.data(), mean.size());
+  const size_t oLo = im.put(lo.data(), lo.size());
+  const size_t oStep = im.put(step.data(), step.size());
+  const size_t oInv = im.put(inv.data(), inv.size());
+  const size_t oVn = im.put(vnorm.data(), vnorm.size());
+  const size_t oBits = im.put(g.bits.data(), g.bits.size());
+  const size_t oOrder = im.put(g.order.data(), g.order.size());
+  const size_t oSeg = im.put(g.seg.data(), g.seg.size());
+  const size_t oP = im.put(g.P.data(), g.P.size());
+  const size_t oKept = im.put(g.n_kept.data(), g.n_kept.size());
+  const size_t oGroups = im.put(g.groups.data(), g.groups.size());
+  const size_t oCb = im.put(cb.data(), cb.size());
+  const size_t oMids = im.put(mids.data(), mids.size());
+  const size_t oBasis = im.put(g.basis.data(), g.basis.size());
+  const size_t oPay = im.put(g.pay_off.data(), g.pay_off.size());
+  const size_t oSide = im.put(g.side_off.data(), g.side_off.size());
+  const size_t oErr = im.zeros(sizeof(int));
+  const size_t oCnt = im.zeros(4 * sizeof(unsigned long long));
+
+  kvc_layer* L = new kvc_layer();
+  L->tc = kvc::TcPlan{};
+  st = kvc::tc_prepare(*d, din, g.Hg, nb, r, g.bits, g.order, g.n_kept, im.bytes, L->tc);
+  if (st) {
+    delete L;
+    return st;
+  }
+
+  void* block = nullptr;
+  e = cudaMalloc(&block, im.bytes.size());
+  if (e != cudaSuccess) {
+    delete L;
+    return cuda_fail(e, "cudaMalloc(parameter block)");
+  }
+  e = cudaMemcpy(block, im.bytes.data(), im.bytes.size(), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(block);
+    delete L;
+    return cuda_fail(e, "cudaMemcpy(parameter block)");
+  }
+  auto* base = static_cast<uint8_t*>(block);
+  Params& p = L->p;
+  p.mode = d->mode;
+  p.B = d->B;
+  p.H = d->H;
+  p.D = d->D;
+  p.hpg = d->heads_per_group;
+  p.Hg = g.Hg;
+  p.d_in = din;
+  p.r = r;
+  p.n_bases = nb;
+  p.n_slots = g.n_slots;
+  p.in_dtype = d->in_dtype;
+  p.out_dtype = d->out_dtype;
+  p.group_size = d->group_size;
+  p.n_groups = g.n_groups;
+  p.cb_levels = g.cb_levels;
+  p.cb_bits = d->cb_bits;
+  p.side_bytes = g.side_bytes;
+  p.V = reinterpret_cast<const float*>(base + oV);
+  p.Vt = reinterpret_cast<const float*>(base + oVt);
+  p.mean = reinterpret_cast<const float*>(base + oMean);
+  p.lo = reinterpret_cast<const float*>(base + oLo);
+  p.step = reinterpret_cast<const float*>(base + oStep);
+  p.inv_step = reinterpret_cast<const float*>(base + oInv);
+  p.vnorm = reinterpret_cast<const float*>(base + oVn);
+  p.bits = base + oBits;
+  p.order = reinterpret_cast<const int16_t*>(base + oOrder);
+  p.seg = reinterpret_cast<const int32_t*>(base + oSeg);
+  p.P = reinterpret_cast<const int32_t*>(base + oP);
+  p.n_kept = reinterpret_cast<const int32_t*>(base + oKept);
+  p.groups = reinterpret_cast<const int32_t*>(base + oGroups);
+  p.codebook = reinterpret_cast<const float*>(base + oCb);
+  p.mids = reinterpret_cast<const float*>(base + oMids);
+  p.basis_of = reinterpret_cast<const int32_t*>(base + oBasis);
+  p.store = static_cast<uint8_t*>(d->store);
+  p.pay_off = reinterpret_cast<const int64_t*>(base + oPay);
+  p.side_off = reinterpret_cast<const int64_t*>(base + oSide);
+  p.err = reinterpret_cast<int*>(base + oErr);
+  p.counters = reinterpret_cast<unsigned long long*>(base + oCnt);
+  kvc::tc_bind(L->tc, base);
+
+  L->block = block;
+  L->device = dev;
+  L->capacity = d->capacity;
+  L->mode = d->mode;
+  L->B = d->B;
+  L->H = d->H;
+  L->D = d->D;
+  L->hpg = d->heads_per_group;
+  L->r = r;
+  L->n_bases = nb;
+  L->n_slots = g.n_slots;
+  L->side_bytes = g.side_bytes;
+  L->fixed_bytes = g.fixed;
+  L->P_host = g.P;
+  L->basis_host = g.basis;
+  L->pay_host = g.pay_off;
+  L->side_host = g.side_off;
+  *out = L;
+  return succeed();
+}
+
+kvc_status kvc_append_strided(kvc_layer* L, const void* x, int64_t T, int64_t sb, int64_t sh,
+                              int64_t st, void* stream) {
+  if (!L) return fail(KVC_ESTATE, "layer is NULL");
+  if (T < 0) return fail(KVC_EINVAL, "T must be >= 0");
+  if (T == 0) return succeed();
+  if (T > L->capacity - L->len)
+    return fail(KVC_ECAPACITY, "append of %lld tokens exceeds capacity %lld (length %lld)",
+                (long long)T, (long long)L->capacity, (long long)L->len);
+  if (!x) return fail(KVC_EINVAL, "x is NULL");
+  if (sb < 0 || sh < 0 || st < 0) return fail(KVC_EINVAL, "strides must be >= 0");
+  DeviceGuard dg(L->device);
+  if (!dg.ok) return fail(KVC_ECUDA, "cannot select the layer's device");
+  if (!is_device_ptr(x, L->device)) return fail(KVC_EINVAL, "x is not device memory of the layer's device");
+  kvc::AppendArgs a{x, sb, sh, st, T, L->len};
+  auto s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  int nk = 0;
+  if (L->mode == KVC_MODE_INT8)
+    e = kvc::launch_append_int8(L->p, a, s, &nk);
+  else if (L->path == KVC_PATH_AUTO && kvc::tc_append_ok(L->tc, L->p, a))
+    e = kvc::launch_append_tc(L->tc, L->p, a, s, &nk);
+  else
+    e = kvc::launch_append_generic(L->p, a, s, &nk);
+  L->launches += nk;
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  L->len += T;
+  return succeed();
+}
+
+kvc_status kvc_append(kvc_layer* L, const void* x, int64_t T, void* stream) {
+  if (!L) return fail(KVC_ESTATE, "layer is NULL");
+  return kvc_append_strided(L, x, T, (int64_t)L->H * T * L->D, T * (int64_t)L->D, L->D, stream);
+}
+
+kvc_status kvc_fetch(kvc_layer* L, void* out, int64_t ld_s, int64_t* S_out, void* stream) {
+  if (!L) return fail(KVC_ESTATE, "layer is NULL");
+  if (ld_s < L->len) return fail(KVC_EINVAL, "ld_s %lld < length %lld", (long long)ld_s, (long long)L->len);
+  if (S_out) *S_out = L->len;
+  if (L->len == 0) return succeed();
+  if (!out) return fail(KVC_EINVAL, "out is NULL");
+  DeviceGuard dg(L->device);
+  if (!dg.ok) return fail(KVC_ECUDA, "cannot select the layer's device");
+  if (!is_device_ptr(out, L->device)) return fail(KVC_EINVAL, "out is not device memory of the layer's device");
+  kvc::FetchArgs f{out, ld_s, L->len};
+  auto s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  int nk = 0;
+  if (L->mode == KVC_MODE_INT8)
+    e = kvc::launch_fetch_int8(L->p, f, s, &nk);
+  else if (L->path == KVC_PATH_AUTO && kvc::tc_fetch_ok(L->tc, L->p, f))
+    e = kvc::launch_fetch_tc(L->tc, L->p, f, s, &nk);
+  else
+    e = kvc::launch_fetch_generic(L->p, f, s, &nk);
+  L->launches += nk;
+  if (e != cudaSuccess) return cuda_fail(e, "fetch launch");
+  return succeed();
+}
+
+kvc_status kvc_trim(kvc_layer* L, int64_t n, int64_t* dropped) {
+  if (!L) return fail(KVC_ESTATE, "layer is NULL");
+  int64_t k = std::min(L->len, n);
+  if (k < 0) k = 0;
+  L->len -= k;
+  if (dropped) *dropped = k;
+  return succeed();
+}
+
+kvc_status kvc_length(const kvc_layer* L, int64_t* out) {
+  if (!L) return fail(KVC_ESTATE, "layer is NULL");
+  if (!out) return fail(KVC_EINVAL, "out is NULL");
+  *out = L->len;
+  return succeed();
+}
+
+kvc_status kvc_nbytes(const kvc_layer* L, kvc_bytes* out) {
+  if (!L) return fail(KVC_ESTATE, "layer is NULL");
+  if (!out) return fail(KVC_EINVAL, "out is NULL");
+  int64_t payload = 0;
+  for (int s = 0; s < L->n_slots; ++s)
+    payload += L->len * (L->mode == KVC_MODE_INT8 ? L->D : L->P_host[L->basis_host[s]]);
+  out->payload = payload;
+  out->side = (int64_t)L->n_slots * L->len * L->side_bytes;
+  out->fixed = L->fixed_bytes;
+  out->fp16_equiv = (int64_t)L->B * L->H * L->len * L->D * 2;
+  return succeed();
+}
+
+kvc_status kvc_get_slot_layout(const kvc_layer* L, int32_t slot, kvc_slot_layout* out) {
+  if (!L) return fail(KVC_ESTATE, "layer is NULL");
+  if (!out) return fail(KVC_EINVAL, "out is NULL");
+  if (slot < 0 || slot >= L->n_slots) return fail(KVC_EINVAL, "slot %d outside [0, %d)", slot, L->n_slots);
+  out->payload_offset = L->pay_host[slot];
+  out->row_bytes = L->mode == KVC_MODE_INT8 ? L->D : L->P_host[L->basis_host[slot]];
+  out->side_offset = L->side_host[slot];
+  out->side_bytes = L->side_bytes;
+  return succeed();
+}
+
+kvc_status kvc_set_path(kvc_layer* L, int32_t path) {
+  if (!L) return fail(KVC_ESTATE, "layer is NULL");
+  if (path != KVC_PATH_AUTO && path != KVC_PATH_GENERIC) return fail(KVC_EINVAL, "unknown path %d", path);
+  L->path = path;
+  return succeed();
+}
+
+kvc_status kvc_sync_status(kvc_layer* L, void* stream) {
+  if (!L) return fail(KVC_ESTATE, "layer is NULL");
+  DeviceGuard dg(L->device);
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int err = 0;
+  e = cudaMemcpy(&err, L->p.err, sizeof err, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (err) {
+    e = cudaMemset(L->p.err, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  }
+  if (err == kvc::kErrTimeout) return fail(KVC_ETIMEOUT, "a bounded device wait gave up");
+  if (err == kvc::kErrRange) return fail(KVC_EDEVICE, "input outside the exactly encodable range");
+  if (err) return fail(KVC_EDEVICE, "device error %d", err);
+  return succeed();
+}
+
+kvc_status kvc_counters(kvc_layer* L, int64_t out[4], int32_t reset, void* stream) {
+  if (!L) return fail(KVC_ESTATE, "layer is NULL");
+  if (!out) return fail(KVC_EINVAL, "out is NULL");
+  DeviceGuard dg(L->device);
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned long long c[4];
+  e = cudaMemcpy(c, L->p.counters, sizeof c, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read counters");
+  for (int i = 0; i < 3; ++i) out[i] = (int64_t)c[i];
+  out[3] = L->launches;
+  if (reset) {
+    L->launches = 0;
+    e = cudaMemset(L->p.counters, 0, sizeof c);
+    if (e != cudaSuccess) return cuda_fail(e, "clear counters");
+  }
+  return succeed();
+}
+
+void kvc_destroy(kvc_layer* L) {
+  if (!L) return;
+  {
+    DeviceGuard dg(L->device);
+    if (L->block) cudaFree(L->block);
+    kvc::tc_release(L->tc);
+  }
+  delete L;
+}
+
+}  // extern "C"

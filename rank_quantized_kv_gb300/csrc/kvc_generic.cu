@@ -1,0 +1,554 @@
+// CUDA-core kernels of the KV cache hot path: any shape, any input dtype.
+//
+// Append: each CTA takes TT tokens of one slot.  The projection runs in fp32
+// on the CUDA cores (sequential FMA over the input dimension, so the
+// textbook bound |z32 - z| <= gamma_{n} * sum_i |x_i - m_i| |V_ik| holds with
+// gamma_n = n u / (1 - n u), u = 2^-24).  Every code whose fp32 value lies
+// within that bound (carried through the quantiser's own roundings) of a
+// rounding boundary is re-decided in double precision by one warp, so the
+// stored codes are the ones exact arithmetic gives (and float64 with it,
+// except at ties closer than float64's own error).
+//
+// Fetch: each CTA takes TT tokens of one slot, unpacks and dequantises into
+// shared memory, then reconstructs x_hat = z_hat V^T + mean in fp32.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kU = 5.9604644775390625e-08f;  // 2^-24
+
+__device__ __forceinline__ float load_in(const void* x, int dt, int64_t off) {
+  if (dt == KVC_F32) return static_cast<const float*>(x)[off];
+  if (dt == KVC_F16) return __half2float(static_cast<const __half*>(x)[off]);
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(x)[off]);
+}
+
+__device__ __forceinline__ void store_out(void* out, int dt, int64_t off, float v) {
+  if (dt == KVC_F16)
+    static_cast<__half*>(out)[off] = __float2half_rn(v);
+  else
+    static_cast<__nv_bfloat16*>(out)[off] = __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_sumf(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_maxf(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+__device__ __forceinline__ double warp_maxd(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+// gamma_n = n u / (1 - n u)
+__device__ __forceinline__ float gamma_n(int n) {
+  const float nu = n * kU;
+  return nu / (1.f - nu);
+}
+
+// sum_i (x_i - m_i) * w_i in double precision, one warp, result on every lane.
+__device__ __forceinline__ double dot64(const float* x, const float* m, const float* w, int n,
+                                        int lane) {
+  double acc = 0.0;
+  for (int i = lane; i < n; i += 32) acc = fma((double)x[i] - (double)m[i], (double)w[i], acc);
+  return warp_sum(acc);
+}
+
+// sum_i x_i^2 in double precision, one warp.
+__device__ __forceinline__ double sumsq64(const float* x, int n, int lane) {
+  double acc = 0.0;
+  for (int i = lane; i < n; i += 32) acc = fma((double)x[i], (double)x[i], acc);
+  return warp_sum(acc);
+}
+
+// True when every value in [lo, hi] rounds to the same fp16.
+__device__ __forceinline__ bool same_half(float lo, float hi) {
+  return __half_as_ushort(__float2half_rn(lo)) == __half_as_ushort(__float2half_rn(hi));
+}
+
+// ---------------------------------------------------------------------------
+// Quantisers: one warp per item, lane = component.
+// ---------------------------------------------------------------------------
+
+struct RowCtx {
+  const float* xs;    // token row (fp32 copy of the input), d_in values
+  const float* mean;  // basis mean, d_in values
+  const float* zs;    // fp32 latents, r values
+  float nrm;          // fp32 ||x - mean|| (||x|| in codebook mode)
+  uint8_t* codes;     // r codes out
+  __half* side;       // side words out
+};
+
+// Uniform: code = clip(rint((z - lo) / step), 0, 2^b - 1).
+__device__ void quant_uniform(const Params& p, int beta, const float* vnorm, const RowCtx& c,
+                              int chunk, int lane, unsigned* nref) {
+  const int k = chunk * 32 + lane;
+  const bool valid = k < p.r;
+  const int w = valid ? p.bits[beta * p.r + k] : 0;
+  const float gam = gamma_n(p.d_in + 2);
+  int code = 0;
+  bool near = false;
+  float lo = 0.f, step = 1.f;
+  int qmax = 0;
+  if (w > 0) {
+    lo = p.lo[beta * p.r + k];
+    step = p.step[beta * p.r + k];
+    const float inv = p.inv_step[beta * p.r + k];
+    const float z = c.zs[k];
+    const float u = (z - lo) * inv;
+    const float tau_z = gam * c.nrm * vnorm[k] * (1.f + 1e-3f);
+    const float tau_u = tau_z * inv * (1.f + 1e-6f) + 4.f * kU * (fabsf(u) + 1.f);
+    qmax = (1 << w) - 1;
+    const float hb = floorf(u) + 0.5f;
+    near = (hb >= 0.5f) && (hb <= (float)qmax - 0.5f) && (fabsf(u - hb) <= tau_u);
+    code = (int)fminf(fmaxf(rintf(u), 0.f), (float)qmax);
+  }
+  unsigned m = __ballot_sync(kFull, near);
+  if (lane == 0 && m) atomicAdd(nref, (unsigned)__popc(m));
+  while (m) {
+    const int f = __ffs(m) - 1;
+    m &= m - 1;
+    const int kf = chunk * 32 + f;
+    const double z64 =
+        dot64(c.xs, c.mean, p.Vt + ((int64_t)beta * p.r + kf) * p.d_in, p.d_in, lane);
+    if (lane == f) {
+      const double u64 = (z64 - (double)lo) / (double)step;
+      code = (int)fmin(fmax(rint(u64), 0.0), (double)qmax);
+    }
+  }
+  if (valid && w > 0) c.codes[k] = (uint8_t)code;
+}
+
+// Group: per token and group, s = max(absmax / qmax, 1e-8); q = clip(rint(z / s)).
+__device__ void quant_group(const Params& p, int beta, const float* vnorm, const RowCtx& c,
+                            int gi, int lane, unsigned* nref, unsigned* nside) {
+  const int first = p.groups[gi * 3 + 0];
+  const int cnt = p.groups[gi * 3 + 1];
+  const int w = p.groups[gi * 3 + 2];
+  const int qmax = (1 << (w - 1)) - 1;
+  const int off = 1 << (w - 1);
+  const int k = first + lane;
+  const bool valid = lane < cnt;
+  const float gam = gamma_n(p.d_in + 2);
+  const float z = valid ? c.zs[k] : 0.f;
+  const float az = fabsf(z);
+  const float tz = valid ? gam * c.nrm * vnorm[k] * (1.f + 1e-3f) : 0.f;
+  const float a32 = warp_maxf(valid ? az : 0.f);
+  const float tzm = warp_maxf(tz);
+  // Too close to zero (or to the 1e-8 floor) to trust the fp32 maximum.
+  const bool full = a32 <= 2.f * tzm + (float)qmax * 4e-8f;
+  const float s32 = a32 / (float)qmax;
+  const float eps = full ? 0.f : tzm / a32 + 4.f * kU;
+  const bool s_unsure = !full && !same_half(s32 * (1.f - eps), s32 * (1.f + eps));
+  float u = full ? 0.f : z / s32;
+  const float au = fabsf(u);
+  const float tau_u = full ? 0.f : (tz / s32 + au * eps) * (1.f + 1e-6f) + 4.f * kU * (au + 1.f);
+  const float hb = floorf(au) + 0.5f;
+  const bool near = valid && !full && (hb <= (float)qmax - 0.5f) && (fabsf(au - hb) <= tau_u);
+  int q = (int)fminf(fmaxf(rintf(u), -(float)qmax), (float)qmax);
+  __half s16 = __float2half_rn(s32);
+
+  const unsigned vmask = __ballot_sync(kFull, valid);
+  const unsigned nmask = full ? vmask : __ballot_sync(kFull, near);
+  if (full || s_unsure || nmask) {
+    // The scale needs the exact maximum: recompute every component that could hold it.
+    const bool cand = valid && (full || az + tz >= a32 - tzm);
+    unsigned todo = __ballot_sync(kFull, cand) | nmask;
+    if (lane == 0) {
+      atomicAdd(nref, (unsigned)__popc(nmask));
+      atomicAdd(nside, 1u);
+    }
+    double zmine = 0.0;
+    while (todo) {
+      const int f = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const double z64 =
+          dot64(c.xs, c.mean, p.Vt + ((int64_t)beta * p.r + first + f) * p.d_in, p.d_in, lane);
+      if (lane == f) zmine = z64;
+    }
+    const double a64 = warp_maxd(cand ? fabs(zmine) : 0.0);
+    const double s64 = fmax(a64 / (double)qmax, 1e-8);
+    s16 = __double2half(s64);
+    if ((nmask >> lane) & 1u) q = (int)fmin(fmax(rint(zmine / s64), -(double)qmax), (double)qmax);
+  }
+  if (valid) c.codes[k] = (uint8_t)(q + off);
+  if (lane == 0) c.side[gi] = s16;
+}
+
+// Codebook: u = (x R) / ||x||; idx = argmin_j |u - c_j| (first on ties); norm fp16.
+__device__ void quant_codebook(const Params& p, int beta, const float* vnorm, const RowCtx& c,
+                               int chunk, int lane, unsigned* nref, unsigned* nside) {
+  const int k = chunk * 32 + lane;
+  const bool valid = k < p.r;
+  const int L = p.cb_levels;
+  const float nrm = c.nrm;
+  const bool tiny = nrm < 1e-18f;
+  const float z = valid ? c.zs[k] : 0.f;
+  const float u = tiny ? 0.f : z / nrm;
+  // idx = number of midpoints strictly below u
+  int lo_i = 0, hi_i = L - 1;
+  while (lo_i < hi_i) {
+    const int mid = (lo_i + hi_i) >> 1;
+    if (p.mids[mid] < u) lo_i = mid + 1; else hi_i = mid;
+  }
+  int idx = lo_i;
+  float dmin = 3.4e38f;
+  if (idx > 0) dmin = fminf(dmin, fabsf(u - p.mids[idx - 1]));
+  if (idx < L - 1) dmin = fminf(dmin, fabsf(u - p.mids[idx]));
+  const float gam = gamma_n(p.d_in + 2);
+  const float eps_n = 0.5f * gam + 2.f * kU;
+  const float cmax = fmaxf(fabsf(p.codebook[0]), fabsf(p.codebook[L - 1]));
+  const float tau_u = tiny ? 0.f
+                           : (gam * vnorm[valid ? k : 0] * (1.f + 1e-3f) + fabsf(u) * eps_n) *
+                                     (1.f + 1e-6f) +
+                                 4.f * kU * (fabsf(u) + cmax);
+  const bool near = valid && (tiny || dmin <= tau_u);
+  const bool norm_unsure =
+      chunk == 0 && (tiny || !same_half(nrm * (1.f - eps_n), nrm * (1.f + eps_n)));
+  unsigned m = __ballot_sync(kFull, near);
+  double n64 = -1.0;
+  if (m || norm_unsure) n64 = sqrt(sumsq64(c.xs, p.d_in, lane));
+  if (lane == 0 && m) atomicAdd(nref, (unsigned)__popc(m));
+  while (m) {
+    const int f = __ffs(m) - 1;
+    m &= m - 1;
+    const int kf = chunk * 32 + f;
+    const double z64 =
+        dot64(c.xs, c.mean, p.Vt + ((int64_t)beta * p.r + kf) * p.d_in, p.d_in, lane);
+    if (lane == f) {
+      const double u64 = n64 > 0.0 ? z64 / n64 : 0.0;
+      double best = fabs(u64 - (double)p.codebook[0]);
+      int bi = 0;
+      for (int j = 1; j < L; ++j) {
+        const double d = fabs(u64 - (double)p.codebook[j]);
+        if (d < best) { best = d; bi = j; }
+      }
+      idx = bi;
+    }
+  }
+  if (valid) c.codes[k] = (uint8_t)idx;
+  if (chunk == 0 && lane == 0) {
+    if (norm_unsure) {
+      c.side[0] = __double2half(n64);
+      atomicAdd(nside, 1u);
+    } else {
+      c.side[0] = __float2half_rn(nrm);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Append
+// ---------------------------------------------------------------------------
+
+constexpr int kAppTT = 8;
+constexpr int kAppThreads = 256;
+
+__global__ void __launch_bounds__(kAppThreads)
+append_generic_kernel(Params p, AppendArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int slot = blockIdx.y;
+  const int64_t t0 = (int64_t)blockIdx.x * kAppTT;
+  const int n = (int)min((int64_t)kAppTT, a.T - t0);
+  const int beta = p.basis_of[slot];
+  const int d_in = p.d_in, r = p.r;
+  const int b = slot / p.Hg, g = slot % p.Hg;
+
+  float* xs = reinterpret_cast<float*>(smem);      // [TT][d_in]
+  float* zs = xs + kAppTT * d_in;                  // [TT][r]
+  float* nrm = zs + kAppTT * r;                    // [TT]
+  __half* side = reinterpret_cast<__half*>(nrm + kAppTT);  // [TT][n_side]
+  const int n_side = p.side_bytes / 2;
+  uint8_t* codes = reinterpret_cast<uint8_t*>(side + kAppTT * (n_side > 0 ? n_side : 1));
+  __shared__ unsigned s_nref, s_nside;
+
+  const float* mean = p.mean + (int64_t)beta * d_in;
+  const float* vnorm = p.vnorm + (int64_t)beta * r;
+  if (threadIdx.x == 0) { s_nref = 0; s_nside = 0; }
+
+  // 1. token rows -> fp32 (exact for f32 / f16 / bf16 inputs)
+  for (int idx = threadIdx.x; idx < kAppTT * d_in; idx += blockDim.x) {
+    const int t = idx / d_in, i = idx - t * d_in;
+    float v = 0.f;
+    if (t < n) {
+      const int h = g * p.hpg + i / p.D, dd = i % p.D;
+      v = load_in(a.x, p.in_dtype, (int64_t)b * a.sb + (int64_t)h * a.sh + (t0 + t) * a.st + dd);
+    }
+    xs[idx] = v;
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  // 2. fp32 norms of the centred rows (the error bound's scale)
+  for (int t = warp; t < kAppTT; t += nwarps) {
+    float acc = 0.f;
+    for (int i = lane; i < d_in; i += 32) {
+      const float d = xs[t * d_in + i] - mean[i];
+      acc = fmaf(d, d, acc);
+    }
+    acc = warp_sumf(acc);
+    if (lane == 0) nrm[t] = sqrtf(acc);  // the bounds below carry their own margin
+  }
+  // 3. projection, sequential fp32 FMA per component
+  const float* V = p.V + (int64_t)beta * d_in * r;
+  for (int k = threadIdx.x; k < r; k += blockDim.x) {
+    float acc[kAppTT];
+#pragma unroll
+    for (int t = 0; t < kAppTT; ++t) acc[t] = 0.f;
+    for (int i = 0; i < d_in; ++i) {
+      const float v = V[(int64_t)i * r + k];
+      const float m = mean[i];
+#pragma unroll
+      for (int t = 0; t < kAppTT; ++t) acc[t] = fmaf(xs[t * d_in + i] - m, v, acc[t]);
+    }
+#pragma unroll
+    for (int t = 0; t < kAppTT; ++t) zs[t * r + k] = acc[t];
+  }
+  __syncthreads();
+
+  // 4. quantise (+ exact re-decision near boundaries), one warp per item
+  if (p.mode == KVC_MODE_GROUP) {
+    for (int item = warp; item < n * p.n_groups; item += nwarps) {
+      const int t = item / p.n_groups, gi = item - t * p.n_groups;
+      RowCtx c{xs + t * d_in, mean, zs + t * r, nrm[t], codes + t * r, side + t * n_side};
+      quant_group(p, beta, vnorm, c, gi, lane, &s_nref, &s_nside);
+    }
+  } else {
+    const int nchunk = (r + 31) / 32;
+    for (int item = warp; item < n * nchunk; item += nwarps) {
+      const int t = item / nchunk, ch = item - t * nchunk;
+      RowCtx c{xs + t * d_in, mean, zs + t * r, nrm[t], codes + t * r, side + t * n_side};
+      if (p.mode == KVC_MODE_UNIFORM)
+        quant_uniform(p, beta, vnorm, c, ch, lane, &s_nref);
+      else
+        quant_codebook(p, beta, vnorm, c, ch, lane, &s_nref, &s_nside);
+    }
+  }
+  __syncthreads();
+
+  // 5. pack: one thread per output byte
+  const int P = p.P[beta];
+  const int16_t* order = p.order + (int64_t)beta * r;
+  const int32_t* seg = p.seg + (int64_t)beta * kMaxSeg * 4;
+  uint8_t* dst = p.store + p.pay_off[slot] + (a.t_base + t0) * P;
+  for (int idx = threadIdx.x; idx < n * P; idx += blockDim.x) {
+    const int t = idx / P, j = idx - t * P;
+    int s = 0;
+    while (s + 1 < kMaxSeg && seg[(s + 1) * 4 + 3] > 0 && seg[(s + 1) * 4 + 0] <= j) ++s;
+    const int start = seg[s * 4 + 0], w = seg[s * 4 + 1], m0 = seg[s * 4 + 2], cntm = seg[s * 4 + 3];
+    const int q0 = 8 * (j - start);
+    int mlo = q0 / w, mhi = (q0 + 7) / w;
+    if (mhi > cntm - 1) mhi = cntm - 1;
+    unsigned v = 0;
+    for (int mm = mlo; mm <= mhi; ++mm) {
+      const unsigned code = codes[t * r + order[m0 + mm]];
+      const int sh = mm * w - q0;
+      v |= sh >= 0 ? (code << sh) : (code >> (-sh));
+    }
+    dst[idx] = (uint8_t)(v & 0xffu);
+  }
+  if (n_side > 0) {
+    __half* sdst = reinterpret_cast<__half*>(p.store + p.side_off[slot]) + (a.t_base + t0) * n_side;
+    for (int idx = threadIdx.x; idx < n * n_side; idx += blockDim.x) sdst[idx] = side[idx];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (s_nref) atomicAdd(&p.counters[0], (unsigned long long)s_nref);
+    if (s_nside) atomicAdd(&p.counters[1], (unsigned long long)s_nside);
+    if (blockIdx.y == 0) atomicAdd(&p.counters[2], (unsigned long long)n);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Fetch
+// ---------------------------------------------------------------------------
+
+constexpr int kFetTT = 16;
+constexpr int kFetThreads = 256;
+
+__global__ void __launch_bounds__(kFetThreads) fetch_generic_kernel(Params p, FetchArgs f) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int slot = blockIdx.y;
+  const int64_t t0 = (int64_t)blockIdx.x * kFetTT;
+  const int n = (int)min((int64_t)kFetTT, f.S - t0);
+  const int beta = p.basis_of[slot];
+  const int d_in = p.d_in, r = p.r;
+  const int b = slot / p.Hg, g = slot % p.Hg;
+  float* zh = reinterpret_cast<float*>(smem);  // [TT][r]
+
+  for (int idx = threadIdx.x; idx < kFetTT * r; idx += blockDim.x) zh[idx] = 0.f;
+  __syncthreads();
+
+  const int P = p.P[beta];
+  const int nk = p.n_kept[beta];
+  const int16_t* order = p.order + (int64_t)beta * r;
+  const int32_t* seg = p.seg + (int64_t)beta * kMaxSeg * 4;
+  const uint8_t* src = p.store + p.pay_off[slot] + t0 * P;
+  const int n_side = p.side_bytes / 2;
+  const __half* sside =
+      reinterpret_cast<const __half*>(p.store + p.side_off[slot]) + t0 * (int64_t)n_side;
+
+  for (int idx = threadIdx.x; idx < n * nk; idx += blockDim.x) {
+    const int t = idx / nk, m = idx - t * nk;
+    int s = 0;
+    while (s + 1 < kMaxSeg && seg[(s + 1) * 4 + 3] > 0 && seg[(s + 1) * 4 + 2] <= m) ++s;
+    const int start = seg[s * 4 + 0], w = seg[s * 4 + 1], m0 = seg[s * 4 + 2];
+    const int bit = 8 * start + (m - m0) * w;
+    const uint8_t* row = src + (int64_t)t * P;
+    unsigned v = row[bit >> 3];
+    if ((bit & 7) + w > 8) v |= (unsigned)row[(bit >> 3) + 1] << 8;
+    const int code = (int)((v >> (bit & 7)) & ((1u << w) - 1u));
+    const int k = order[m];
+    float zv;
+    if (p.mode == KVC_MODE_UNIFORM) {
+      zv = fmaf((float)code, p.step[beta * r + k], p.lo[beta * r + k]);
+    } else if (p.mode == KVC_MODE_GROUP) {
+      int gi = 0;
+      while (gi + 1 < p.n_groups && p.groups[(gi + 1) * 3] <= k) ++gi;
+      zv = (float)(code - (1 << (w - 1))) * __half2float(sside[(int64_t)t * n_side + gi]);
+    } else {
+      zv = __half2float(sside[t]) * p.codebook[code];
+    }
+    zh[t * r + k] = zv;
+  }
+  __syncthreads();
+
+  const float* Vt = p.Vt + (int64_t)beta * r * d_in;
+  const float* mean = p.mean + (int64_t)beta * d_in;
+  for (int i = threadIdx.x; i < d_in; i += blockDim.x) {
+    float acc[kFetTT];
+    const float m = mean[i];
+#pragma unroll
+    for (int t = 0; t < kFetTT; ++t) acc[t] = m;
+    for (int k = 0; k < r; ++k) {
+      const float v = Vt[(int64_t)k * d_in + i];
+#pragma unroll
+      for (int t = 0; t < kFetTT; ++t) acc[t] = fmaf(zh[t * r + k], v, acc[t]);
+    }
+    const int h = g * p.hpg + i / p.D, dd = i % p.D;
+    const int64_t base = (((int64_t)b * p.H + h) * f.ld_s + t0) * p.D + dd;
+    for (int t = 0; t < n; ++t) store_out(f.out, p.out_dtype, base + (int64_t)t * p.D, acc[t]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// int8 values: one warp per token
+// ---------------------------------------------------------------------------
+
+constexpr int kI8Warps = 8;
+
+__global__ void __launch_bounds__(kI8Warps * 32) append_int8_kernel(Params p, AppendArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t tok = (int64_t)blockIdx.x * kI8Warps + (threadIdx.x >> 5);  // over n_slots * T
+  if (tok >= (int64_t)p.n_slots * a.T) return;
+  const int slot = (int)(tok / a.T);
+  const int64_t t = tok - (int64_t)slot * a.T;
+  const int b = slot / p.H, h = slot % p.H;
+  const int64_t xoff = (int64_t)b * a.sb + (int64_t)h * a.sh + t * a.st;
+  float amax = 0.f;
+  for (int i = lane; i < p.D; i += 32) amax = fmaxf(amax, fabsf(load_in(a.x, p.in_dtype, xoff + i)));
+  amax = warp_maxf(amax);
+  // exactly the double-precision scale of the reference arithmetic
+  const double s64 = fmax((double)amax / 127.0, 1e-8);
+  const float inv = (float)(1.0 / s64);
+  int8_t* dst = reinterpret_cast<int8_t*>(p.store + p.pay_off[slot]) + (a.t_base + t) * p.D;
+  unsigned nref = 0;
+  for (int i = lane; i < p.D; i += 32) {
+    const float v = load_in(a.x, p.in_dtype, xoff + i);
+    const float u = v * inv;  // |u - v / s| <= 3 * 2^-24 * 127.5 < 2.5e-5
+    const float au = fabsf(u);
+    float q;
+    if (fabsf(au - floorf(au) - 0.5f) < 1e-4f) {
+      q = (float)rint((double)v / s64);
+      ++nref;
+    } else {
+      q = rintf(u);
+    }
+    dst[i] = (int8_t)fminf(fmaxf(q, -127.f), 127.f);
+  }
+  if (lane == 0) {
+    reinterpret_cast<__half*>(p.store + p.side_off[slot])[a.t_base + t] = __double2half(s64);
+  }
+  nref = __reduce_add_sync(kFull, nref);
+  if (lane == 0 && nref) atomicAdd(&p.counters[0], (unsigned long long)nref);
+  if (lane == 0 && slot == 0) atomicAdd(&p.counters[2], 1ull);
+}
+
+__global__ void __launch_bounds__(kI8Warps * 32) fetch_int8_kernel(Params p, FetchArgs f) {
+  const int lane = threadIdx.x & 31;
+  const int64_t tok = (int64_t)blockIdx.x * kI8Warps + (threadIdx.x >> 5);
+  if (tok >= (int64_t)p.n_slots * f.S) return;
+  const int slot = (int)(tok / f.S);
+  const int64_t t = tok - (int64_t)slot * f.S;
+  const int b = slot / p.H, h = slot % p.H;
+  const int8_t* src = reinterpret_cast<const int8_t*>(p.store + p.pay_off[slot]) + t * p.D;
+  const float s = __half2float(reinterpret_cast<const __half*>(p.store + p.side_off[slot])[t]);
+  const int64_t base = (((int64_t)b * p.H + h) * f.ld_s + t) * p.D;
+  for (int i = lane; i < p.D; i += 32) store_out(f.out, p.out_dtype, base + i, (float)src[i] * s);
+}
+
+}  // namespace
+
+cudaError_t launch_append_generic(const Params& p, const AppendArgs& a, cudaStream_t s, int* nk) {
+  if (a.T <= 0) return cudaSuccess;
+  const int n_side = p.side_bytes / 2;
+  const size_t smem = sizeof(float) * (kAppTT * p.d_in + kAppTT * p.r + kAppTT) +
+                      sizeof(__half) * kAppTT * (n_side > 0 ? n_side : 1) + kAppTT * p.r + 16;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(append_generic_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid((unsigned)((a.T + kAppTT - 1) / kAppTT), (unsigned)p.n_slots);
+  append_generic_kernel<<<grid, kAppThreads, smem, s>>>(p, a);
+  ++*nk;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fetch_generic(const Params& p, const FetchArgs& f, cudaStream_t s, int* nk) {
+  if (f.S <= 0) return cudaSuccess;
+  const size_t smem = sizeof(float) * kFetTT * p.r;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(fetch_generic_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid((unsigned)((f.S + kFetTT - 1) / kFetTT), (unsigned)p.n_slots);
+  fetch_generic_kernel<<<grid, kFetThreads, smem, s>>>(p, f);
+  ++*nk;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_int8(const Params& p, const AppendArgs& a, cudaStream_t s, int* nk) {
+  const int64_t toks = (int64_t)p.n_slots * a.T;
+  if (toks <= 0) return cudaSuccess;
+  append_int8_kernel<<<(unsigned)((toks + kI8Warps - 1) / kI8Warps), kI8Warps * 32, 0, s>>>(p, a);
+  ++*nk;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fetch_int8(const Params& p, const FetchArgs& f, cudaStream_t s, int* nk) {
+  const int64_t toks = (int64_t)p.n_slots * f.S;
+  if (toks <= 0) return cudaSuccess;
+  fetch_int8_kernel<<<(unsigned)((toks + kI8Warps - 1) / kI8Warps), kI8Warps * 32, 0, s>>>(p, f);
+  ++*nk;
+  return cudaGetLastError();
+}
+
+}  // namespace kvc

@@ -1,0 +1,117 @@
+"""The C-ABI library: it loads, exports every symbol include/kvc.h declares,
+and validates descriptors on the host (no GPU needed, no compute calls)."""
+import ctypes
+import math
+import re
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    import rank_quantized_kv_gb300 as kvc
+
+    try:
+        kvc.load_library()
+    except ImportError:
+        import __graft_entry__
+
+        __graft_entry__.build()
+        kvc.load_library()
+    return kvc
+
+
+def _declared():
+    text = (ROOT / "include" / "kvc.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(kvc_\w+)\s*\(", text))
+
+
+def test_exports_every_declared_symbol(kvc):
+    declared = _declared()
+    assert declared == set(kvc.EXPORTED_SYMBOLS)
+    lib = ctypes.CDLL(kvc.library_path())
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert lib.kvc_abi_version() == 1
+
+
+def _uniform_args(rng, nb=3, B=2, H=4, D=32, r=8):
+    V = rng.standard_normal((nb, D, r)).astype(np.float32)
+    bits = rng.choice([0, 1, 2, 3, 4, 8], size=(nb, r)).astype(np.uint8)
+    return dict(V=V, mean=rng.standard_normal((nb, D)), bits=bits,
+                qmin=-np.ones((nb, r)), qstep=np.full((nb, r), 0.1),
+                basis_of=rng.integers(0, nb, size=B * H))
+
+
+def test_store_bytes_covers_every_slot(kvc):
+    rng = np.random.default_rng(0)
+    a = _uniform_args(rng)
+    P = [sum(math.ceil(int(np.sum(bb == w)) * w / 8) for w in (8, 4, 3, 2, 1)) for bb in a["bits"]]
+    need = sum(100 * P[b] for b in a["basis_of"])
+    n100 = kvc.store_bytes("uniform", 2, 4, 32, capacity=100, **a)
+    n200 = kvc.store_bytes("uniform", 2, 4, 32, capacity=200, **a)
+    assert n100 >= need and n100 % 256 == 0
+    assert n200 >= 2 * need and n200 > n100
+    # int8: D bytes + a 2-byte scale per token
+    n = kvc.store_bytes("int8", 2, 4, 32, capacity=10)
+    assert n >= 8 * 10 * (32 + 2)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(mode="uniform", change=lambda a: a.update(bits=np.full_like(a["bits"], 5))),
+    dict(mode="uniform", change=lambda a: a.update(qstep=np.zeros_like(a["qstep"]))),
+    dict(mode="uniform", change=lambda a: a.update(basis_of=np.full(8, 7))),
+    dict(mode="uniform", change=lambda a: a.update(V=np.full_like(a["V"], np.nan))),
+    dict(mode="uniform", change=lambda a: a.update(capacity=0)),
+    dict(mode="uniform", change=lambda a: a.update(heads_per_group=2, mean=None)),
+    dict(mode="group", change=lambda a: a.update(bits=np.tile([2, 4, 4, 4, 2, 2, 2, 2], (3, 1)),
+                                                 qmin=None, qstep=None)),
+    dict(mode="group", change=lambda a: a.update(bits=np.tile([4, 4, 1, 1, 0, 0, 0, 0], (3, 1)),
+                                                 qmin=None, qstep=None)),
+    dict(mode="codebook", change=lambda a: a.update(codebook=[0.3, 0.1], mean=None, qmin=None,
+                                                    qstep=None, bits=None)),
+])
+def test_bad_descriptors_are_rejected(kvc, bad):
+    rng = np.random.default_rng(1)
+    a = _uniform_args(rng)
+    a["capacity"] = 16
+    bad["change"](a)
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.store_bytes(bad["mode"], 2, 4, 32, **a)
+    assert e.value.status == -1
+
+
+def test_null_layer_calls_fail_cleanly(kvc):
+    lib = kvc.load_library()
+    n = ctypes.c_int64()
+    assert lib.kvc_trim(None, 3, ctypes.byref(n)) == -2
+    assert lib.kvc_length(None, ctypes.byref(n)) == -2
+    assert lib.kvc_append(None, None, 1, None) == -2
+    assert lib.kvc_fetch(None, None, 1, None, None) == -2
+    lib.kvc_destroy(None)
+    assert b"NULL" in lib.kvc_last_error()
+
+
+def test_init_without_device_memory_is_an_error(kvc):
+    # A host buffer is never accepted as the store (CPU-only machines report a
+    # CUDA error; machines with a GPU reject the host pointer).
+    rng = np.random.default_rng(2)
+    a = _uniform_args(rng)
+    desc, keep = kvc._build_desc("uniform", 2, 4, 32, None, a["V"], a["mean"], a["bits"],
+                                 a["qmin"], a["qstep"], a["basis_of"], 1, 32, None, "bf16",
+                                 "f16", 16)
+    n = ctypes.c_size_t()
+    lib = kvc.load_library()
+    assert lib.kvc_store_bytes(ctypes.byref(desc), ctypes.byref(n)) == 0
+    host = (ctypes.c_uint8 * (n.value + 256))()
+    addr = (ctypes.addressof(host) + 255) // 256 * 256
+    desc.store = ctypes.c_void_p(addr)
+    desc.store_bytes = n.value
+    h = ctypes.c_void_p()
+    st = lib.kvc_init_layer(ctypes.byref(desc), ctypes.byref(h))
+    assert st in (-1, -4) and not h.value
