@@ -226,6 +226,36 @@ kvc_status kvc_counters(kvc_layer *layer, int64_t out[4], int32_t reset, void *s
 /* Free the layer's parameter block (synchronises the device first).  NULL is a no-op. */
 void kvc_destroy(kvc_layer *layer);
 
+/* Append without allocating any device memory.  The pages have no
+ * counterpart of this call: it exists for callers that are handed their
+ * device buffers and may not allocate, such as a plugin or custom operator
+ * run inside another inference engine's execution step, or a server whose
+ * device memory is all reserved by its own pool.
+ *
+ * Stores exactly what kvc_init_layer(desc) followed by kvc_append_strided(x,
+ * T, ...) on a layer of length `length` stores: rows length .. length+T-1 of
+ * every slot in desc->store (and their side words), computed by the CUDA-core
+ * kernels.  The caller keeps track of the length.  x, strides and dtypes as
+ * for kvc_append_strided; desc and its host arrays as for kvc_init_layer.
+ *
+ * Memory: the kernel's parameter tables, error word and counters live in one
+ * static device array of 8 MiB that every GPU loading this library holds
+ * until exit.  Each call uploads its tables there (cudaMemcpyAsync on
+ * `stream`, from host memory, which synchronises the stream first) and
+ * zeroes the error word and counters.  All calls share that array, so calls
+ * whose work overlaps on the GPU (other streams, other threads) race and
+ * corrupt each other's tables: order them on one stream.  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.
+ *
+ * Errors: KVC_EINVAL for a bad descriptor or pointers, or when the tables
+ * exceed 8 MiB (e.g. many bases of a large D_in x r); KVC_ECAPACITY if
+ * length + T > capacity; KVC_ECUDA on a CUDA error.  Nothing is written on
+ * error.  Calls no cudaMalloc or cudaFree. */
+kvc_status kvc_append_noalloc(const kvc_layer_desc *desc, int64_t length, const void *x,
+                              int64_t T, int64_t stride_b, int64_t stride_h, int64_t stride_t,
+                              void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -33,6 +33,7 @@ EXPORTED_SYMBOLS = (
     "kvc_abi_version", "kvc_last_error", "kvc_store_bytes", "kvc_init_layer", "kvc_append",
     "kvc_append_strided", "kvc_fetch", "kvc_trim", "kvc_length", "kvc_nbytes",
     "kvc_get_slot_layout", "kvc_set_path", "kvc_sync_status", "kvc_counters", "kvc_destroy",
+    "kvc_append_noalloc",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -106,6 +107,8 @@ def load_library():
             "kvc_sync_status": (c_int32, [P, P]),
             "kvc_counters": (c_int32, [P, POINTER(c_int64), c_int32, P]),
             "kvc_destroy": (None, [P]),
+            "kvc_append_noalloc": (c_int32, [POINTER(_Desc), c_int64, P, c_int64, c_int64,
+                                             c_int64, c_int64, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

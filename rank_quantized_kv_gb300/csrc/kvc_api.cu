@@ -57,17 +57,9 @@ int64_t align_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
 bool valid_width(int b) { return b == 0 || b == 1 || b == 2 || b == 3 || b == 4 || b == 8; }
 
-// Everything derived from a descriptor, on the host.
-struct Geo {
-  int d_in = 0, Hg = 0, n_slots = 0, nb = 0, r = 0;
-  int cb_levels = 0, n_groups = 0, side_bytes = 0;
-  std::vector<uint8_t> bits;     // [nb][r]
-  std::vector<int32_t> P, n_kept, seg, groups, basis;
-  std::vector<int16_t> order;
-  std::vector<int64_t> pay_off, side_off;
-  int64_t store_total = 0;
-  int64_t fixed = 0;
-};
+}  // namespace
+
+namespace kvc {
 
 kvc_status build_geo(const kvc_layer_desc* d, Geo& g) {
   if (!d) return fail(KVC_EINVAL, "descriptor is NULL");
@@ -227,78 +219,8 @@ kvc_status build_geo(const kvc_layer_desc* d, Geo& g) {
   return KVC_OK;
 }
 
-// Host image of the parameter block: arrays appended at 256-byte alignment.
-struct Image {
-  std::vector<uint8_t> bytes;
-  template <class T>
-  size_t put(const T* src, size_t n) {
-    const size_t off = (size_t)align_up((int64_t)bytes.size(), 256);
-    bytes.resize(off + sizeof(T) * std::max<size_t>(n, 1), 0);
-    if (n) std::memcpy(bytes.data() + off, src, sizeof(T) * n);
-    return off;
-  }
-  size_t zeros(size_t nbytes) {
-    const size_t off = (size_t)align_up((int64_t)bytes.size(), 256);
-    bytes.resize(off + std::max<size_t>(nbytes, 1), 0);
-    return off;
-  }
-};
-
-bool is_device_ptr(const void* ptr, int dev) {
-  cudaPointerAttributes at;
-  if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  return (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == dev;
-}
-
-struct DeviceGuard {
-  int prev = -1;
-  bool ok = true;
-  explicit DeviceGuard(int dev) {
-    if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
-    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
-  }
-  ~DeviceGuard() {
-    int cur = -1;
-    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
-  }
-};
-
-}  // namespace
-
-extern "C" {
-
-int32_t kvc_abi_version(void) { return KVC_ABI_VERSION; }
-
-const char* kvc_last_error(void) { return g_err.c_str(); }
-
-kvc_status kvc_store_bytes(const kvc_layer_desc* desc, size_t* out) {
-  if (!out) return fail(KVC_EINVAL, "out is NULL");
-  Geo g;
-  kvc_status st = build_geo(desc, g);
-  if (st) return st;
-  *out = (size_t)g.store_total;
-  return succeed();
-}
-
-kvc_status kvc_init_layer(const kvc_layer_desc* d, kvc_layer** out) {
-  if (!out) return fail(KVC_EINVAL, "out is NULL");
-  *out = nullptr;
-  Geo g;
-  kvc_status st = build_geo(d, g);
-  if (st) return st;
-  if (!d->store) return fail(KVC_EINVAL, "store is NULL");
-  if ((uintptr_t)d->store % 256) return fail(KVC_EINVAL, "store must be 256-byte aligned");
-  if (d->store_bytes < (size_t)g.store_total)
-    return fail(KVC_EINVAL, "store_bytes %zu < required %lld", d->store_bytes,
-                (long long)g.store_total);
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (!is_device_ptr(d->store, dev)) return fail(KVC_EINVAL, "store is not device memory of the current device");
-
+// The frozen parameters in kernel layouts (host image of the parameter block).
+void build_param_image(const kvc_layer_desc* d, const Geo& g, ParamImage& im) {
   const int nb = g.nb, r = g.r, din = g.d_in;
   const bool coded = d->mode != KVC_MODE_INT8;
   std::vector<float> V, Vt, mean, lo, step, inv, vnorm, cb, mids;
@@ -335,27 +257,142 @@ kvc_status kvc_init_layer(const kvc_layer_desc* d, kvc_layer** out) {
     }
   }
 
-  Image im;
-  const size_t oV = im.put(V.data(), V.size());
-  const size_t oVt = im.put(Vt.data(), Vt.size());
-  const size_t oMean = im.put(mean.data(), mean.size());
-  const size_t oLo = im.put(lo.data(), lo.size());
-  const size_t oStep = im.put(step.data(), step.size());
-  const size_t oInv = im.put(inv.data(), inv.size());
-  const size_t oVn = im.put(vnorm.data(), vnorm.size());
-  const size_t oBits = im.put(g.bits.data(), g.bits.size());
-  const size_t oOrder = im.put(g.order.data(), g.order.size());
-  const size_t oSeg = im.put(g.seg.data(), g.seg.size());
-  const size_t oP = im.put(g.P.data(), g.P.size());
-  const size_t oKept = im.put(g.n_kept.data(), g.n_kept.size());
-  const size_t oGroups = im.put(g.groups.data(), g.groups.size());
-  const size_t oCb = im.put(cb.data(), cb.size());
-  const size_t oMids = im.put(mids.data(), mids.size());
-  const size_t oBasis = im.put(g.basis.data(), g.basis.size());
-  const size_t oPay = im.put(g.pay_off.data(), g.pay_off.size());
-  const size_t oSide = im.put(g.side_off.data(), g.side_off.size());
-  const size_t oErr = im.zeros(sizeof(int));
-  const size_t oCnt = im.zeros(4 * sizeof(unsigned long long));
+  im.oV = im.put(V.data(), V.size());
+  im.oVt = im.put(Vt.data(), Vt.size());
+  im.oMean = im.put(mean.data(), mean.size());
+  im.oLo = im.put(lo.data(), lo.size());
+  im.oStep = im.put(step.data(), step.size());
+  im.oInv = im.put(inv.data(), inv.size());
+  im.oVn = im.put(vnorm.data(), vnorm.size());
+  im.oBits = im.put(g.bits.data(), g.bits.size());
+  im.oOrder = im.put(g.order.data(), g.order.size());
+  im.oSeg = im.put(g.seg.data(), g.seg.size());
+  im.oP = im.put(g.P.data(), g.P.size());
+  im.oKept = im.put(g.n_kept.data(), g.n_kept.size());
+  im.oGroups = im.put(g.groups.data(), g.groups.size());
+  im.oCb = im.put(cb.data(), cb.size());
+  im.oMids = im.put(mids.data(), mids.size());
+  im.oBasis = im.put(g.basis.data(), g.basis.size());
+  im.oPay = im.put(g.pay_off.data(), g.pay_off.size());
+  im.oSide = im.put(g.side_off.data(), g.side_off.size());
+  im.oErr = im.zeros(sizeof(int));
+  im.oCnt = im.zeros(4 * sizeof(unsigned long long));
+}
+
+// Device pointers of a parameter block uploaded from `im` at `base`.
+void bind_params(Params& p, const kvc_layer_desc* d, const Geo& g, const ParamImage& im,
+                 uint8_t* base) {
+  p.mode = d->mode;
+  p.B = d->B;
+  p.H = d->H;
+  p.D = d->D;
+  p.hpg = d->heads_per_group;
+  p.Hg = g.Hg;
+  p.d_in = g.d_in;
+  p.r = g.r;
+  p.n_bases = g.nb;
+  p.n_slots = g.n_slots;
+  p.in_dtype = d->in_dtype;
+  p.out_dtype = d->out_dtype;
+  p.group_size = d->group_size;
+  p.n_groups = g.n_groups;
+  p.cb_levels = g.cb_levels;
+  p.cb_bits = d->cb_bits;
+  p.side_bytes = g.side_bytes;
+  p.V = reinterpret_cast<const float*>(base + im.oV);
+  p.Vt = reinterpret_cast<const float*>(base + im.oVt);
+  p.mean = reinterpret_cast<const float*>(base + im.oMean);
+  p.lo = reinterpret_cast<const float*>(base + im.oLo);
+  p.step = reinterpret_cast<const float*>(base + im.oStep);
+  p.inv_step = reinterpret_cast<const float*>(base + im.oInv);
+  p.vnorm = reinterpret_cast<const float*>(base + im.oVn);
+  p.bits = base + im.oBits;
+  p.order = reinterpret_cast<const int16_t*>(base + im.oOrder);
+  p.seg = reinterpret_cast<const int32_t*>(base + im.oSeg);
+  p.P = reinterpret_cast<const int32_t*>(base + im.oP);
+  p.n_kept = reinterpret_cast<const int32_t*>(base + im.oKept);
+  p.groups = reinterpret_cast<const int32_t*>(base + im.oGroups);
+  p.codebook = reinterpret_cast<const float*>(base + im.oCb);
+  p.mids = reinterpret_cast<const float*>(base + im.oMids);
+  p.basis_of = reinterpret_cast<const int32_t*>(base + im.oBasis);
+  p.store = static_cast<uint8_t*>(d->store);
+  p.pay_off = reinterpret_cast<const int64_t*>(base + im.oPay);
+  p.side_off = reinterpret_cast<const int64_t*>(base + im.oSide);
+  p.err = reinterpret_cast<int*>(base + im.oErr);
+  p.counters = reinterpret_cast<unsigned long long*>(base + im.oCnt);
+}
+
+kvc_status set_error(kvc_status s, const char* msg) { return fail(s, "%s", msg); }
+
+}  // namespace kvc
+
+namespace {
+
+using kvc::Geo;
+using kvc::ParamImage;
+
+bool is_device_ptr(const void* ptr, int dev) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == dev;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+namespace kvc {
+bool device_ptr_on(const void* ptr, int dev) { return is_device_ptr(ptr, dev); }
+}  // namespace kvc
+
+extern "C" {
+
+int32_t kvc_abi_version(void) { return KVC_ABI_VERSION; }
+
+const char* kvc_last_error(void) { return g_err.c_str(); }
+
+kvc_status kvc_store_bytes(const kvc_layer_desc* desc, size_t* out) {
+  if (!out) return fail(KVC_EINVAL, "out is NULL");
+  Geo g;
+  kvc_status st = kvc::build_geo(desc, g);
+  if (st) return st;
+  *out = (size_t)g.store_total;
+  return succeed();
+}
+
+kvc_status kvc_init_layer(const kvc_layer_desc* d, kvc_layer** out) {
+  if (!out) return fail(KVC_EINVAL, "out is NULL");
+  *out = nullptr;
+  Geo g;
+  kvc_status st = kvc::build_geo(d, g);
+  if (st) return st;
+  if (!d->store) return fail(KVC_EINVAL, "store is NULL");
+  if ((uintptr_t)d->store % 256) return fail(KVC_EINVAL, "store must be 256-byte aligned");
+  if (d->store_bytes < (size_t)g.store_total)
+    return fail(KVC_EINVAL, "store_bytes %zu < required %lld", d->store_bytes,
+                (long long)g.store_total);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (!is_device_ptr(d->store, dev)) return fail(KVC_EINVAL, "store is not device memory of the current device");
+
+  const int nb = g.nb, r = g.r, din = g.d_in;
+  ParamImage im;
+  kvc::build_param_image(d, g, im);
 
   kvc_layer* L = new kvc_layer();
   L->tc = kvc::TcPlan{};
@@ -378,45 +415,7 @@ kvc_status kvc_init_layer(const kvc_layer_desc* d, kvc_layer** out) {
     return cuda_fail(e, "cudaMemcpy(parameter block)");
   }
   auto* base = static_cast<uint8_t*>(block);
-  Params& p = L->p;
-  p.mode = d->mode;
-  p.B = d->B;
-  p.H = d->H;
-  p.D = d->D;
-  p.hpg = d->heads_per_group;
-  p.Hg = g.Hg;
-  p.d_in = din;
-  p.r = r;
-  p.n_bases = nb;
-  p.n_slots = g.n_slots;
-  p.in_dtype = d->in_dtype;
-  p.out_dtype = d->out_dtype;
-  p.group_size = d->group_size;
-  p.n_groups = g.n_groups;
-  p.cb_levels = g.cb_levels;
-  p.cb_bits = d->cb_bits;
-  p.side_bytes = g.side_bytes;
-  p.V = reinterpret_cast<const float*>(base + oV);
-  p.Vt = reinterpret_cast<const float*>(base + oVt);
-  p.mean = reinterpret_cast<const float*>(base + oMean);
-  p.lo = reinterpret_cast<const float*>(base + oLo);
-  p.step = reinterpret_cast<const float*>(base + oStep);
-  p.inv_step = reinterpret_cast<const float*>(base + oInv);
-  p.vnorm = reinterpret_cast<const float*>(base + oVn);
-  p.bits = base + oBits;
-  p.order = reinterpret_cast<const int16_t*>(base + oOrder);
-  p.seg = reinterpret_cast<const int32_t*>(base + oSeg);
-  p.P = reinterpret_cast<const int32_t*>(base + oP);
-  p.n_kept = reinterpret_cast<const int32_t*>(base + oKept);
-  p.groups = reinterpret_cast<const int32_t*>(base + oGroups);
-  p.codebook = reinterpret_cast<const float*>(base + oCb);
-  p.mids = reinterpret_cast<const float*>(base + oMids);
-  p.basis_of = reinterpret_cast<const int32_t*>(base + oBasis);
-  p.store = static_cast<uint8_t*>(d->store);
-  p.pay_off = reinterpret_cast<const int64_t*>(base + oPay);
-  p.side_off = reinterpret_cast<const int64_t*>(base + oSide);
-  p.err = reinterpret_cast<int*>(base + oErr);
-  p.counters = reinterpret_cast<unsigned long long*>(base + oCnt);
+  kvc::bind_params(L->p, d, g, im, base);
   kvc::tc_bind(L->tc, base);
 
   L->block = block;

@@ -1,7 +1,11 @@
 // Internal declarations shared by the host library and the kernels.
 #pragma once
 
+#include <algorithm>
 #include <cstdint>
+#include <cstring>
+#include <vector>
+
 #include <cuda_runtime.h>
 
 #include "../../include/kvc.h"
@@ -60,6 +64,48 @@ struct FetchArgs {
   int64_t ld_s;  // rows per (b, h) in out
   int64_t S;     // tokens to reconstruct
 };
+
+// Everything derived from a descriptor, on the host (kvc_api.cu).
+struct Geo {
+  int d_in = 0, Hg = 0, n_slots = 0, nb = 0, r = 0;
+  int cb_levels = 0, n_groups = 0, side_bytes = 0;
+  std::vector<uint8_t> bits;     // [nb][r]
+  std::vector<int32_t> P, n_kept, seg, groups, basis;
+  std::vector<int16_t> order;
+  std::vector<int64_t> pay_off, side_off;
+  int64_t store_total = 0;
+  int64_t fixed = 0;
+};
+
+// Host image of a layer's parameter block: arrays appended at 256-byte
+// alignment, with each array's offset.
+struct ParamImage {
+  std::vector<uint8_t> bytes;
+  size_t oV = 0, oVt = 0, oMean = 0, oLo = 0, oStep = 0, oInv = 0, oVn = 0, oBits = 0,
+         oOrder = 0, oSeg = 0, oP = 0, oKept = 0, oGroups = 0, oCb = 0, oMids = 0, oBasis = 0,
+         oPay = 0, oSide = 0, oErr = 0, oCnt = 0;
+  template <class T>
+  size_t put(const T* src, size_t n) {
+    const size_t off = (bytes.size() + 255) / 256 * 256;
+    bytes.resize(off + sizeof(T) * std::max<size_t>(n, 1), 0);
+    if (n) std::memcpy(bytes.data() + off, src, sizeof(T) * n);
+    return off;
+  }
+  size_t zeros(size_t nbytes) {
+    const size_t off = (bytes.size() + 255) / 256 * 256;
+    bytes.resize(off + std::max<size_t>(nbytes, 1), 0);
+    return off;
+  }
+};
+
+// Validate a descriptor and derive its layout; on failure the message is
+// available from kvc_last_error().
+kvc_status build_geo(const kvc_layer_desc* d, Geo& g);
+void build_param_image(const kvc_layer_desc* d, const Geo& g, ParamImage& im);
+void bind_params(Params& p, const kvc_layer_desc* d, const Geo& g, const ParamImage& im,
+                 uint8_t* base);
+kvc_status set_error(kvc_status s, const char* msg);
+bool device_ptr_on(const void* ptr, int dev);
 
 // Kernel launchers (kvc_generic.cu).  Return the launch's cudaError_t and add
 // the number of kernels launched to *nk.
