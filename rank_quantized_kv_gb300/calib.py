@@ -28,7 +28,8 @@ def pca(rows: torch.Tensor):
     mean = X.mean(dim=1)
     Xc = X - mean[:, None, :]
     C = Xc.transpose(1, 2) @ Xc / X.shape[1]
-    lam, U = torch.linalg.eigh(C)
+    lam, U = torch.linalg.eigh(C.cpu())      # small symmetric eigenproblems, on the host
+    lam, U = lam.to(X.device), U.to(X.device)
     lam, U = lam.flip(-1), U.flip(-1)
     piv = U.abs().argmax(dim=1, keepdim=True)
     sign = torch.sign(torch.gather(U, 1, piv))

@@ -56,8 +56,8 @@ def spectral_basis(d_in: int, gen: torch.Generator, device="cpu", dtype=torch.fl
     """Draw (mu, U): mu ~ N(0, 0.5^2) and an orthogonal U from a QR factorisation."""
     mu = 0.5 * torch.randn(d_in, generator=gen, device=device, dtype=dtype)
     g = torch.randn(d_in, d_in, generator=gen, device=device, dtype=dtype)
-    q, _ = torch.linalg.qr(g)
-    return mu, q
+    q, _ = torch.linalg.qr(g.cpu())        # small factorisation on the host
+    return mu, q.to(device)
 
 
 def spectral_rows(mu, U, n: int, alpha: float, gen: torch.Generator, noise: float = 0.01):
