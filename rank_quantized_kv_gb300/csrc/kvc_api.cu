@@ -396,7 +396,7 @@ kvc_status kvc_init_layer(const kvc_layer_desc* d, kvc_layer** out) {
 
   kvc_layer* L = new kvc_layer();
   L->tc = kvc::TcPlan{};
-  st = kvc::tc_prepare(*d, din, g.Hg, nb, r, g.bits, g.order, g.n_kept, im.bytes, L->tc);
+  st = kvc::tc_prepare(*d, g, im.bytes, L->tc);
   if (st) {
     delete L;
     return st;

@@ -1,22 +1,400 @@
-// Tensor-core kernels of the hot path (sm_103a).
+// Tensor-core kernels of the hot path (sm_103a): fetch as a tcgen05 contraction.
+//
+// Fetch of one 128-token tile of one slot, one CTA of 128 threads (thread t
+// owns token t of the tile, i.e. TMEM lane t):
+//   1. copy the tile's packed rows (and fp16 side words) to shared memory;
+//   2. thread t decodes its row into the fp16 A operand (UMMA K-major, no
+//      swizzle), K = kept components in packed order:
+//        uniform   A = code - 2^(b-1)            (exact; B = fp16(step * V^T))
+//        group     A = fp16((code - 2^(b-1)) * s) (B = fp16(V^T))
+//        codebook  A = fp16(c[code])             (B = fp16(R^T), norm in the epilogue)
+//   3. one thread issues K/16 tcgen05.mma (M = 128, N = D) into TMEM;
+//   4. the epilogue reads TMEM (tcgen05.ld 32x32b), adds the per-basis bias
+//      mean + sum_k (lo_k + 2^(b_k-1) step_k) V_k (uniform), mean (group) or
+//      scales by the fp16 norm (codebook), converts to fp16/bf16 into a
+//      128-byte-swizzled staging tile and TMA-stores it to [B, H, S, D];
+//      rows past the length are clipped by the tensor map.
+// In group mode the tile is decoded once and contracted against each head's
+// slice of the group basis in turn.  Several CTAs per SM overlap the phases.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "kvc_sm100.cuh"
 #include "kvc_tc.h"
 
 namespace kvc {
 
-kvc_status tc_prepare(const kvc_layer_desc&, int, int, int, int, const std::vector<uint8_t>&,
-                      const std::vector<int16_t>&, const std::vector<int32_t>&,
-                      std::vector<uint8_t>&, TcPlan& plan) {
+using namespace sm100;
+
+namespace {
+
+constexpr int kTile = 128;
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+
+struct FetchTc {
+  const uint16_t* B;  // fp16 bits, [nb][D_in][K] UMMA order
+  const float* bias;  // [nb][D_in]
+  int K;
+  int cols;
+};
+
+__device__ __forceinline__ void set_err(int* err, int code) { atomicCAS(err, 0, code); }
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Accumulates fp16 values of one A row and stores them 8 at a time (16 bytes)
+// at the row's place in the UMMA no-swizzle K-major layout.
+struct RowWriter {
+  unsigned char* row_base;  // A + (t / 8) * sbo + (t % 8) * 16
+  uint64_t lo = 0, hi = 0;  // values 0-3 and 4-7 of the current chunk
+  int n = 0;                // values in the current chunk
+  int kc = 0;               // chunk index along K
+  __device__ __forceinline__ void push(__half v) {
+    const uint64_t bits = __half_as_ushort(v);
+    if (n < 4)
+      lo |= bits << (16 * n);
+    else
+      hi |= bits << (16 * (n - 4));
+    if (++n == 8) {
+      *reinterpret_cast<uint4*>(row_base + kc * 128) =
+          make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+      lo = hi = 0;
+      n = 0;
+      ++kc;
+    }
+  }
+  __device__ __forceinline__ void pad_to(int K) {
+    while (kc * 8 + n < K) push(__ushort_as_half(0));
+  }
+};
+
+template <int MODE, bool OUT_BF16>
+__global__ void __launch_bounds__(kTile) fetch_tc_kernel(const Params p, const FetchTc t,
+                                                         const __grid_constant__ CUtensorMap omap,
+                                                         int64_t S, int tiles_per_slot) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  const int D = p.D, K = t.K, nbox = D / 64;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int slot = blockIdx.x / tiles_per_slot;
+  const int64_t t0 = (int64_t)(blockIdx.x % tiles_per_slot) * kTile;
+  const int n = (int)min((int64_t)kTile, S - t0);
+  const int beta = p.basis_of[slot];
+  const int P = p.P[beta];
+  const int sbytes = p.side_bytes;
+  const int b = slot / p.Hg, g = slot % p.Hg;
+
+  unsigned char* stage = smem;                               // nbox x [128 rows x 128 B]
+  unsigned char* As = stage + nbox * 16384;                  // [128 x K] fp16
+  unsigned char* Bs = As + kTile * K * 2;                    // [D x K] fp16
+  float* bias_s = reinterpret_cast<float*>(Bs + D * K * 2);  // [D]
+  float* cb_s = bias_s + D;                                  // [256]
+  unsigned char* codes_s = reinterpret_cast<unsigned char*>(cb_s + 256);
+  unsigned char* side_s = codes_s + ((kTile * P + 16 + 15) & ~15);
+
+  if (warp == 0) tmem_alloc(&tmem_base, t.cols);
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  {  // packed rows and side words of the tile (16-byte aligned, over-read <= 15 bytes)
+    const uint4* src = reinterpret_cast<const uint4*>(p.store + p.pay_off[slot] + t0 * P);
+    const int nv = (n * P + 15) >> 4;
+    for (int i = tid; i < nv; i += kTile) reinterpret_cast<uint4*>(codes_s)[i] = src[i];
+    if (sbytes) {
+      const uint4* ss = reinterpret_cast<const uint4*>(p.store + p.side_off[slot] + t0 * sbytes);
+      const int ns = (n * sbytes + 15) >> 4;
+      for (int i = tid; i < ns; i += kTile) reinterpret_cast<uint4*>(side_s)[i] = ss[i];
+    }
+    if (MODE == KVC_MODE_CODEBOOK)
+      for (int j = tid; j < p.cb_levels; j += kTile) cb_s[j] = p.codebook[j];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr = tmem_base;
+
+  // ---- decode row tid into A
+  const uint32_t sbo = (uint32_t)(K / 8) * 128;
+  RowWriter w{As + (tid >> 3) * sbo + (tid & 7) * 16};
+  if (tid < n) {
+    const unsigned char* row = codes_s + tid * P;
+    const int32_t* seg = p.seg + (int64_t)beta * kMaxSeg * 4;
+    int kk = 0, gi = 0, gend = 0;
+    float gscale = 0.f;
+    if (MODE == KVC_MODE_GROUP) {
+      gend = p.groups[1];
+      gscale = __half2float(reinterpret_cast<const __half*>(side_s + tid * sbytes)[0]);
+    }
+    for (int s = 0; s < kMaxSeg; ++s) {
+      const int cnt = seg[s * 4 + 3];
+      if (!cnt) break;
+      const int start = seg[s * 4 + 0], wd = seg[s * 4 + 1];
+      const int off = 1 << (wd - 1);
+      const unsigned mask = (1u << wd) - 1u;
+      for (int m = 0; m < cnt; ++m, ++kk) {
+        const int bit = start * 8 + m * wd;
+        unsigned v = row[bit >> 3];
+        if ((bit & 7) + wd > 8) v |= (unsigned)row[(bit >> 3) + 1] << 8;
+        const int code = (int)((v >> (bit & 7)) & mask);
+        if (MODE == KVC_MODE_UNIFORM) {
+          w.push(__int2half_rn(code - off));
+        } else if (MODE == KVC_MODE_GROUP) {
+          if (kk == gend) {
+            ++gi;
+            gend += p.groups[gi * 3 + 1];
+            gscale = __half2float(reinterpret_cast<const __half*>(side_s + tid * sbytes)[gi]);
+          }
+          w.push(__float2half_rn((float)(code - off) * gscale));
+        } else {
+          w.push(__float2half_rn(cb_s[code]));
+        }
+      }
+    }
+  }
+  w.pad_to(K);
+  fence_proxy_async_smem();
+
+  float nrm = 1.f;
+  if (MODE == KVC_MODE_CODEBOOK && tid < n)
+    nrm = __half2float(reinterpret_cast<const __half*>(side_s)[tid]);
+
+  const uint32_t idesc = idesc_f16(kTile, D, 0);
+  uint32_t phase = 0;
+  for (int j = 0; j < p.hpg; ++j) {
+    {  // this head's slice of B and of the bias
+      const uint4* bsrc = reinterpret_cast<const uint4*>(
+          t.B + ((size_t)beta * p.d_in + (size_t)j * D) * (size_t)K);
+      const int nv = D * K * 2 / 16;
+      for (int i = tid; i < nv; i += kTile) reinterpret_cast<uint4*>(Bs)[i] = bsrc[i];
+      for (int c = tid; c < D; c += kTile) bias_s[c] = t.bias[(size_t)beta * p.d_in + j * D + c];
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      for (int ks = 0; ks < K / 16; ++ks) {
+        const uint64_t ad = desc_kmajor_noswizzle(smem_u32(As) + ks * 256, 128, sbo);
+        const uint64_t bd = desc_kmajor_noswizzle(smem_u32(Bs) + ks * 256, 128, sbo);
+        umma_f16(taddr, ad, bd, idesc, ks > 0 ? 1u : 0u);
+      }
+      umma_commit(&bar);
+    }
+    const bool ok = mbar_wait_bounded(&bar, phase, kWaitNs);
+    phase ^= 1;
+    tc_fence_after();
+    if (!ok) abort_flag = 1;
+    if (tid == 0) bulk_wait_read0();  // the previous head's stores have left the staging tile
+    __syncthreads();
+    if (abort_flag) {
+      if (tid == 0) set_err(p.err, kErrTimeout);
+      break;
+    }
+    // ---- epilogue: TMEM -> registers -> fp16/bf16 -> swizzled staging
+    const uint32_t lane_addr = taddr + ((uint32_t)(warp * 32) << 16);
+    for (int cc = 0; cc < D / 32; ++cc) {
+      uint32_t r[32];
+      tmem_ld32(lane_addr + cc * 32, r);
+      tmem_wait_ld();
+      unsigned char* dst = stage + (cc >> 1) * 16384 + tid * 128;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c0 = q * 8 + 2 * e;
+          float v0 = __uint_as_float(r[c0]), v1 = __uint_as_float(r[c0 + 1]);
+          if (MODE == KVC_MODE_CODEBOOK) {
+            v0 *= nrm;
+            v1 *= nrm;
+          } else {
+            v0 += bias_s[cc * 32 + c0];
+            v1 += bias_s[cc * 32 + c0 + 1];
+          }
+          h[e] = OUT_BF16 ? pack_bf162(v0, v1) : pack_half2(v0, v1);
+        }
+        const int c16 = (cc & 1) * 4 + q;
+        *reinterpret_cast<uint4*>(dst + ((c16 ^ (tid & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+      }
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      const int z = b * p.H + g * p.hpg + j;
+      for (int bx = 0; bx < nbox; ++bx) tma_store_3d(&omap, stage + bx * 16384, bx * 64, (int)t0, z);
+      bulk_commit();
+    }
+  }
+  if (tid == 0) bulk_wait0();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(taddr, t.cols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      cudaGetLastError();
+  });
+  return g_encode;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+template <class T>
+size_t put(std::vector<uint8_t>& im, const T* src, size_t n) {
+  const size_t off = align_up(im.size(), 256);
+  im.resize(off + sizeof(T) * std::max<size_t>(n, 1), 0);
+  if (n) std::memcpy(im.data() + off, src, sizeof(T) * n);
+  return off;
+}
+
+uint16_t half_bits(float v) {
+  const __half h = __float2half_rn(v);
+  return __half_as_ushort(h);
+}
+
+using FetchKernel = void (*)(const Params, const FetchTc, const CUtensorMap, int64_t, int);
+
+FetchKernel fetch_kernel_for(int mode, int out_dtype) {
+  const bool bf = out_dtype == KVC_BF16;
+  switch (mode) {
+    case KVC_MODE_UNIFORM:
+      return bf ? fetch_tc_kernel<KVC_MODE_UNIFORM, true> : fetch_tc_kernel<KVC_MODE_UNIFORM, false>;
+    case KVC_MODE_GROUP:
+      return bf ? fetch_tc_kernel<KVC_MODE_GROUP, true> : fetch_tc_kernel<KVC_MODE_GROUP, false>;
+    default:
+      return bf ? fetch_tc_kernel<KVC_MODE_CODEBOOK, true>
+                : fetch_tc_kernel<KVC_MODE_CODEBOOK, false>;
+  }
+}
+
+}  // namespace
+
+kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>& image,
+                      TcPlan& plan) {
   plan = TcPlan{};
+  if (d.mode == KVC_MODE_INT8) return KVC_OK;
+  const int D = d.D, din = g.d_in, r = g.r, nb = g.nb;
+  int kmax = 0, pmax = 0;
+  for (int b = 0; b < nb; ++b) {
+    kmax = std::max(kmax, g.n_kept[b]);
+    pmax = std::max(pmax, g.P[b]);
+  }
+  const int K = (kmax + 15) / 16 * 16;
+  const int cols = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
+  size_t smem = 1024 + (size_t)(D / 64) * 16384 + (size_t)kTile * K * 2 + (size_t)D * K * 2 +
+                (size_t)D * 4 + 256 * 4 + align_up((size_t)kTile * pmax + 16, 16) +
+                align_up((size_t)kTile * g.side_bytes + 16, 16);
+  // No more CTAs per SM than TMEM holds (512 columns), so allocation never waits.
+  smem = std::max(smem, (size_t)(228 * 1024) / (512 / cols + 1) + 1024);
+  if (!(D % 64 == 0 && D <= 256 && K >= 16 && K <= 256 && smem <= 226 * 1024 &&
+        (d.mode != KVC_MODE_GROUP || d.group_size <= 32)))
+    return KVC_OK;  // the CUDA-core kernels serve this shape
+
+  // B = coef_k * V[:, order[kk]] in UMMA order, coef = step (uniform) or 1; bias in fp64.
+  std::vector<uint16_t> Bop((size_t)nb * din * K, 0);
+  std::vector<float> bias((size_t)nb * din, 0.f);
+  for (int b = 0; b < nb; ++b) {
+    const float* V = d.V + (size_t)b * din * r;
+    const int16_t* order = g.order.data() + (size_t)b * r;
+    for (int nrow = 0; nrow < din; ++nrow) {
+      double acc = d.mean && d.mode != KVC_MODE_CODEBOOK ? (double)d.mean[(size_t)b * din + nrow] : 0.0;
+      for (int kk = 0; kk < g.n_kept[b]; ++kk) {
+        const int k = order[kk];
+        const double v = V[(size_t)nrow * r + k];
+        double coef = 1.0;
+        if (d.mode == KVC_MODE_UNIFORM) {
+          const int wdt = g.bits[(size_t)b * r + k];
+          coef = d.qstep[(size_t)b * r + k];
+          acc += ((double)d.qmin[(size_t)b * r + k] + (double)(1 << (wdt - 1)) * coef) * v;
+        }
+        const size_t idx = ((size_t)(nrow / 8) * (K / 8) + kk / 8) * 64 + (nrow % 8) * 8 + (kk % 8);
+        Bop[(size_t)b * din * K + idx] = half_bits((float)(coef * v));
+      }
+      bias[(size_t)b * din + nrow] = (float)acc;
+    }
+  }
+  plan.oFetchB = put(image, Bop.data(), Bop.size());
+  plan.oBias = put(image, bias.data(), bias.size());
+  plan.fetch_K = K;
+  plan.fetch_cols = cols;
+  plan.fetch_smem = smem;
+  plan.fetch_ready = encoder() != nullptr;
   return KVC_OK;
 }
-void tc_bind(TcPlan&, uint8_t*) {}
-void tc_release(TcPlan&) {}
-bool tc_append_ok(const TcPlan& plan, const Params&, const AppendArgs&) { return plan.append_ready; }
-bool tc_fetch_ok(const TcPlan& plan, const Params&, const FetchArgs&) { return plan.fetch_ready; }
-cudaError_t launch_append_tc(const TcPlan&, const Params&, const AppendArgs&, cudaStream_t, int*) {
-  return cudaErrorNotSupported;
+
+void tc_bind(TcPlan& plan, uint8_t* base) {
+  if (plan.fetch_ready) {
+    plan.fetchB = reinterpret_cast<const uint16_t*>(base + plan.oFetchB);
+    plan.bias = reinterpret_cast<const float*>(base + plan.oBias);
+  }
 }
-cudaError_t launch_fetch_tc(const TcPlan&, const Params&, const FetchArgs&, cudaStream_t, int*) {
+
+void tc_release(TcPlan&) {}
+
+bool tc_fetch_ok(const TcPlan& plan, const Params&, const FetchArgs& f) {
+  return plan.fetch_ready && (reinterpret_cast<uintptr_t>(f.out) % 16 == 0) && f.S > 0 &&
+         f.S < (int64_t(1) << 31);
+}
+
+cudaError_t launch_fetch_tc(const TcPlan& plan, const Params& p, const FetchArgs& f,
+                            cudaStream_t s, int* nk) {
+  CUtensorMap map;
+  const cuuint64_t dims[3] = {(cuuint64_t)p.D, (cuuint64_t)f.S, (cuuint64_t)p.B * p.H};
+  const cuuint64_t strides[2] = {(cuuint64_t)p.D * 2, (cuuint64_t)f.ld_s * p.D * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult cr = encoder()(
+      &map, p.out_dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+      3, f.out, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  FetchKernel kern = fetch_kernel_for(p.mode, p.out_dtype);
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.fetch_smem);
+  if (e != cudaSuccess) return e;
+  const int tiles = (int)((f.S + kTile - 1) / kTile);
+  const FetchTc t{plan.fetchB, plan.bias, plan.fetch_K, plan.fetch_cols};
+  kern<<<(unsigned)(tiles * p.n_slots), kTile, plan.fetch_smem, s>>>(p, t, map, f.S, tiles);
+  ++*nk;
+  return cudaGetLastError();
+}
+
+bool tc_append_ok(const TcPlan& plan, const Params&, const AppendArgs&) { return plan.append_ready; }
+
+cudaError_t launch_append_tc(const TcPlan&, const Params&, const AppendArgs&, cudaStream_t, int*) {
   return cudaErrorNotSupported;
 }
 

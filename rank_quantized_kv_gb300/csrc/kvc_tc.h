@@ -12,13 +12,19 @@ namespace kvc {
 // Tables the tensor-core kernels need, appended to the layer's parameter
 // block by tc_prepare (as offsets) and turned into device pointers by tc_bind.
 struct TcPlan {
+  // fetch: x_hat = A B^T + bias, A = decoded codes [tokens x K], B [D_in x K]
   bool fetch_ready = false;
+  int fetch_K = 0;             // K: kept components rounded up to 16
+  int fetch_cols = 0;          // TMEM columns (D, a power of two)
+  size_t fetch_smem = 0;       // dynamic shared memory per CTA
+  size_t oFetchB = 0, oBias = 0;
+  const uint16_t* fetchB = nullptr;  // fp16 [nb][D_in][K] in UMMA no-swizzle K-major order
+  const float* bias = nullptr;       // fp32 [nb][D_in]
+
   bool append_ready = false;
 };
 
-kvc_status tc_prepare(const kvc_layer_desc& d, int d_in, int Hg, int nb, int r,
-                      const std::vector<uint8_t>& bits, const std::vector<int16_t>& order,
-                      const std::vector<int32_t>& n_kept, std::vector<uint8_t>& image,
+kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>& image,
                       TcPlan& plan);
 void tc_bind(TcPlan& plan, uint8_t* block_base);
 void tc_release(TcPlan& plan);
