@@ -44,6 +44,11 @@ struct FetchTc {
 
 __device__ __forceinline__ void set_err(int* err, int code) { atomicCAS(err, 0, code); }
 
+// True when every value in [lo, hi] rounds to the same fp16.
+__device__ __forceinline__ bool same_half(float lo, float hi) {
+  return __half_as_ushort(__float2half_rn(lo)) == __half_as_ushort(__float2half_rn(hi));
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -251,6 +256,358 @@ __global__ void __launch_bounds__(kTile) fetch_tc_kernel(const Params p, const F
   }
 }
 
+// ---------------------------------------------------------------- append
+//
+// One CTA per 128-token tile of one slot (thread t = token t = TMEM lane t).
+// The x tile arrives by TMA (128-byte swizzle) and is the A operand as is
+// (bf16 or fp16 values are exact).  B holds the fp32 basis as three exact
+// 16-bit pieces, each accumulated in its own TMEM region, so z = hi + mid + lo.
+// Error bound of the tensor-core accumulation (a model of aligned, truncated
+// fp32 accumulation, per K = 16 block at most 17 ulp of the running magnitude,
+// itself <= sum_i |x_i V_ik| <= ||x|| ||V_k||):
+//   |z32 - z| <= gamma * ||x|| * ||V_k|| + 2^-21 (|z| + |mean . V_k|),
+//   gamma = (17 D/16 + 2) 2^-23 (1 + 2^-7).
+// Codes closer than that (through the quantiser's own roundings) to a rounding
+// boundary are queued and re-decided by a warp with a compensated fp32 dot
+// product (error ~ 1e-13 relative) finished in double precision.
+
+constexpr int kQueue = 1024;
+constexpr uint32_t kNormEntry = 0xFFFFu;
+
+struct AppendTc {
+  const uint16_t* B;    // [nb][3][rpad][D]
+  const double* c64;    // [nb][r]
+  int rpad, cols;
+  float inv_scale, gamma;
+};
+
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// x_t . w with x_t a row of the swizzled x tile (w == nullptr: x_t . x_t),
+// compensated fp32 (TwoProd / TwoSum) finished in double.  WARP: the 32 lanes
+// split the row and the result is on every lane; else one thread does it all.
+template <bool BF16, bool WARP>
+__device__ double dot2_row(const unsigned char* xs, int t, int D, const float* w, int lane) {
+  float S = 0.f, C = 0.f;
+  for (int i = WARP ? lane : 0; i < D; i += WARP ? 32 : 1) {
+    const unsigned char* src =
+        xs + (i >> 6) * 16384 + t * 128 + ((((i & 63) >> 3) ^ (t & 7)) << 4) + (i & 7) * 2;
+    const uint16_t raw = *reinterpret_cast<const uint16_t*>(src);
+    const float xv = BF16 ? __bfloat162float(__ushort_as_bfloat16(raw))
+                          : __half2float(__ushort_as_half(raw));
+    const float wv = w ? w[i] : xv;
+    const float pr = xv * wv;
+    const float pe = fmaf(xv, wv, -pr);
+    float s, e;
+    two_sum(S, pr, s, e);
+    S = s;
+    C += pe + e;
+  }
+  if (WARP) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float So = __shfl_xor_sync(0xffffffffu, S, o);
+      const float Co = __shfl_xor_sync(0xffffffffu, C, o);
+      float s, e;
+      two_sum(S, So, s, e);
+      S = s;
+      C = C + Co + e;
+    }
+  }
+  return (double)S + (double)C;
+}
+
+// Decide code k of token tt exactly (or, k == kNormEntry, the fp16 norm of a
+// codebook token).  Lane 0 (or the lone thread) writes the result.
+template <int MODE, bool BF16, bool WARP>
+__device__ void refine_entry(const Params& p, const AppendTc& t, int beta, const unsigned char* xs,
+                             unsigned char* codes_s, __half* side_s, unsigned* nside, int tt, int k,
+                             int lane) {
+  const int D = p.D, r = p.r;
+  const float* Vt = p.Vt + (size_t)beta * r * D;
+  if (MODE == KVC_MODE_UNIFORM) {
+    const double z64 = dot2_row<BF16, WARP>(xs, tt, D, Vt + (size_t)k * D, lane) -
+                       t.c64[(size_t)beta * r + k];
+    if (lane == 0) {
+      const int qmax = (1 << p.bits[(size_t)beta * r + k]) - 1;
+      const double u64 =
+          (z64 - (double)p.lo[(size_t)beta * r + k]) / (double)p.step[(size_t)beta * r + k];
+      codes_s[tt * r + k] = (uint8_t)(int)fmin(fmax(rint(u64), 0.0), (double)qmax);
+    }
+  } else {
+    const double n64 = sqrt(dot2_row<BF16, WARP>(xs, tt, D, nullptr, lane));
+    if (k == (int)kNormEntry) {
+      if (lane == 0) {
+        side_s[tt] = __double2half(n64);
+        atomicAdd(nside, 1u);
+      }
+    } else {
+      const double z64 = dot2_row<BF16, WARP>(xs, tt, D, Vt + (size_t)k * D, lane);
+      if (lane == 0) {
+        const double u64 = n64 > 0.0 ? z64 / n64 : 0.0;
+        double best = fabs(u64 - (double)p.codebook[0]);
+        int bi = 0;
+        for (int j = 1; j < p.cb_levels; ++j) {
+          const double d = fabs(u64 - (double)p.codebook[j]);
+          if (d < best) {
+            best = d;
+            bi = j;
+          }
+        }
+        codes_s[tt * r + k] = (uint8_t)bi;
+      }
+    }
+  }
+}
+
+template <int MODE, bool BF16>
+__global__ void __launch_bounds__(kTile) append_tc_kernel(const Params p, const AppendTc t,
+                                                          const __grid_constant__ CUtensorMap xmap,
+                                                          const AppendArgs a, int tiles_per_slot) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t tma_bar, mma_bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ unsigned qcount, nside;
+  __shared__ int abort_flag;
+
+  const int D = p.D, r = p.r, rpad = t.rpad, nbox = D / 64;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int slot = blockIdx.x / tiles_per_slot;
+  const int64_t t0 = (int64_t)(blockIdx.x % tiles_per_slot) * kTile;
+  const int n = (int)min((int64_t)kTile, a.T - t0);
+  const int beta = p.basis_of[slot];
+  const int P = p.P[beta];
+  const int Pp = ((P + 3) & ~3) + 4;
+  const int b = slot / p.H, h = slot % p.H;
+
+  unsigned char* xs = smem;                                    // nbox x 16 KB
+  unsigned char* Bs = xs + nbox * 16384;                       // 3 x rpad x D fp16/bf16
+  unsigned char* codes_s = Bs + 3 * rpad * D * 2;              // [128][r]
+  unsigned char* row_s = codes_s + ((kTile * r + 15) & ~15);   // [128][Pp]
+  uint32_t* queue = reinterpret_cast<uint32_t*>(row_s + kTile * Pp);
+  __half* side_s = reinterpret_cast<__half*>(queue + kQueue);  // [128]
+
+  if (warp == 0) tmem_alloc(&tmem_base, t.cols);
+  if (tid == 0) {
+    mbar_init(&tma_bar, 1);
+    mbar_init(&mma_bar, 1);
+    fence_mbar_init();
+    qcount = 0;
+    nside = 0;
+    abort_flag = 0;
+    mbar_arrive_expect_tx(&tma_bar, nbox * 16384);
+    for (int bx = 0; bx < nbox; ++bx) tma_load_4d(xs + bx * 16384, &xmap, &tma_bar, bx * 64, (int)t0, h, b);
+  }
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(t.B + (size_t)beta * 3 * rpad * D);
+    const int nv = 3 * rpad * D * 2 / 16;
+    for (int i = tid; i < nv; i += kTile) reinterpret_cast<uint4*>(Bs)[i] = src[i];
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr = tmem_base;
+
+  if (!mbar_wait_bounded(&tma_bar, 0, kWaitNs)) abort_flag = 1;
+  __syncthreads();
+  if (abort_flag) {
+    if (tid == 0) set_err(p.err, kErrTimeout);
+  } else if (tid == 0) {
+    const uint32_t idesc = idesc_f16(kTile, rpad, BF16 ? 1 : 0);
+    const uint32_t sbo = (uint32_t)(D / 8) * 128;
+    for (int pc = 0; pc < 3; ++pc)
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint64_t ad = desc_kmajor_sw128(smem_u32(xs) + (ks >> 2) * 16384 + (ks & 3) * 32);
+        const uint64_t bd =
+            desc_kmajor_noswizzle(smem_u32(Bs) + pc * rpad * D * 2 + ks * 256, 128, sbo);
+        umma_f16(taddr + pc * rpad, ad, bd, idesc, ks > 0 ? 1u : 0u);
+      }
+    umma_commit(&mma_bar);
+  }
+
+  // ||x_t|| in fp32 while the MMAs run (sequential over the row)
+  float nx = 0.f;
+  if (tid < n) {
+    for (int bx = 0; bx < nbox; ++bx)
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xs + bx * 16384 + tid * 128 + ((c ^ (tid & 7)) << 4));
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float lo2, hi2;
+          if (BF16) {
+            lo2 = __bfloat162float(__ushort_as_bfloat16((uint16_t)(w4[q] & 0xffff)));
+            hi2 = __bfloat162float(__ushort_as_bfloat16((uint16_t)(w4[q] >> 16)));
+          } else {
+            lo2 = __half2float(__ushort_as_half((uint16_t)(w4[q] & 0xffff)));
+            hi2 = __half2float(__ushort_as_half((uint16_t)(w4[q] >> 16)));
+          }
+          nx = fmaf(lo2, lo2, nx);
+          nx = fmaf(hi2, hi2, nx);
+        }
+      }
+    nx = sqrtf(nx);
+  }
+  if (!abort_flag && !mbar_wait_bounded(&mma_bar, 0, kWaitNs)) abort_flag = 1;
+  tc_fence_after();
+  __syncthreads();
+  if (abort_flag) {
+    if (tid == 0) set_err(p.err, kErrTimeout);
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(taddr, t.cols);
+    return;
+  }
+
+  // ---- fast-path quantisation, thread t = token t
+  const float kU = 5.9604644775390625e-08f;
+  const float nxb = nx * (1.f + 1e-3f);
+  const float* vnorm = p.vnorm + (size_t)beta * r;
+  const double* c64 = t.c64 + (size_t)beta * r;
+  const float eps_n = 0.5f * ((D + 2) * kU) / (1.f - (D + 2) * kU) + 2.f * kU;
+  float cmax = 0.f;
+  bool tiny = false;
+  if (MODE == KVC_MODE_CODEBOOK) {
+    cmax = fmaxf(fabsf(p.codebook[0]), fabsf(p.codebook[p.cb_levels - 1]));
+    tiny = nx < 1e-18f;
+  }
+  const uint32_t lane_addr = taddr + ((uint32_t)(warp * 32) << 16);
+  for (int cc = 0; cc * 32 < r; ++cc) {
+    float z[32];
+    uint32_t rr[32];
+    tmem_ld32(lane_addr + cc * 32, rr);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = __uint_as_float(rr[i]);
+    tmem_ld32(lane_addr + rpad + cc * 32, rr);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] += __uint_as_float(rr[i]);
+    tmem_ld32(lane_addr + 2 * rpad + cc * 32, rr);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] += __uint_as_float(rr[i]);
+    if (tid >= n) continue;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int k = cc * 32 + i;
+      if (k >= r) continue;
+      bool near = false;
+      int code = 0;
+      if (MODE == KVC_MODE_UNIFORM) {
+        const int w = p.bits[(size_t)beta * r + k];
+        if (w == 0) continue;
+        const float ck = (float)c64[k];
+        const float zc = z[i] * t.inv_scale - ck;
+        const float lo = p.lo[(size_t)beta * r + k], inv = p.inv_step[(size_t)beta * r + k];
+        const float u = (zc - lo) * inv;
+        const float tz = t.gamma * nxb * vnorm[k] + 4.f * kU * (fabsf(zc) + fabsf(ck));
+        const float tau = tz * inv * (1.f + 1e-6f) + 4.f * kU * (fabsf(u) + 1.f);
+        const int qmax = (1 << w) - 1;
+        const float hb = floorf(u) + 0.5f;
+        near = hb >= 0.5f && hb <= (float)qmax - 0.5f && fabsf(u - hb) <= tau;
+        code = (int)fminf(fmaxf(rintf(u), 0.f), (float)qmax);
+      } else {
+        const int L = p.cb_levels;
+        const float u = tiny ? 0.f : z[i] * t.inv_scale / nx;
+        int lo_i = 0, hi_i = L - 1;
+        while (lo_i < hi_i) {
+          const int mid = (lo_i + hi_i) >> 1;
+          if (p.mids[mid] < u) lo_i = mid + 1; else hi_i = mid;
+        }
+        code = lo_i;
+        float dmin = 3.4e38f;
+        if (code > 0) dmin = fminf(dmin, fabsf(u - p.mids[code - 1]));
+        if (code < L - 1) dmin = fminf(dmin, fabsf(u - p.mids[code]));
+        const float tau = (t.gamma * vnorm[k] * (1.f + 1e-3f) + fabsf(u) * eps_n) * (1.f + 1e-6f) +
+                          4.f * kU * (fabsf(u) + cmax);
+        near = tiny || dmin <= tau;
+      }
+      codes_s[tid * r + k] = (uint8_t)code;
+      if (near) {
+        const unsigned q = atomicAdd(&qcount, 1u);
+        if (q < kQueue)
+          queue[q] = ((uint32_t)tid << 16) | (uint32_t)k;
+        else  // queue full: decide it here, alone
+          refine_entry<MODE, BF16, false>(p, t, beta, xs, codes_s, side_s, &nside, tid, k, 0);
+      }
+    }
+  }
+  if (MODE == KVC_MODE_CODEBOOK && tid < n) {
+    if (tiny || !same_half(nx * (1.f - eps_n), nx * (1.f + eps_n))) {
+      const unsigned q = atomicAdd(&qcount, 1u);
+      if (q < kQueue)
+        queue[q] = ((uint32_t)tid << 16) | kNormEntry;
+      else
+        refine_entry<MODE, BF16, false>(p, t, beta, xs, codes_s, side_s, &nside, tid,
+                                        (int)kNormEntry, 0);
+    } else {
+      side_s[tid] = __float2half_rn(nx);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(taddr, t.cols);
+  }
+
+  // ---- exact re-decision of the queued codes, one warp per entry
+  const unsigned nq = qcount;
+  for (unsigned e = warp; e < min(nq, (unsigned)kQueue); e += kTile / 32) {
+    const uint32_t ent = queue[e];
+    refine_entry<MODE, BF16, true>(p, t, beta, xs, codes_s, side_s, &nside, (int)(ent >> 16),
+                                   (int)(ent & 0xffffu), lane);
+  }
+  __syncthreads();
+
+  // ---- bit-pack each token's row (segments widest first, LSB-first stream)
+  if (tid < n) {
+    unsigned char* row = row_s + tid * Pp;
+    const int32_t* seg = p.seg + (int64_t)beta * kMaxSeg * 4;
+    const int16_t* order = p.order + (int64_t)beta * r;
+    int pos = 0;
+    for (int s = 0; s < kMaxSeg; ++s) {
+      const int cnt = seg[s * 4 + 3];
+      if (!cnt) break;
+      const int wd = seg[s * 4 + 1], m0 = seg[s * 4 + 2];
+      uint32_t acc = 0;
+      int nb = 0;
+      for (int m = 0; m < cnt; ++m) {
+        acc |= (uint32_t)codes_s[tid * r + order[m0 + m]] << nb;
+        nb += wd;
+        while (nb >= 8) {
+          row[pos++] = (unsigned char)(acc & 0xffu);
+          acc >>= 8;
+          nb -= 8;
+        }
+      }
+      if (nb > 0) row[pos++] = (unsigned char)(acc & 0xffu);
+    }
+  }
+  __syncthreads();
+  unsigned char* dst = p.store + p.pay_off[slot] + (a.t_base + t0) * P;
+  for (int idx = tid; idx < n * P; idx += kTile) {
+    const int tt = idx / P;
+    dst[idx] = row_s[tt * Pp + (idx - tt * P)];
+  }
+  if (MODE == KVC_MODE_CODEBOOK) {
+    __half* sdst = reinterpret_cast<__half*>(p.store + p.side_off[slot]) + a.t_base + t0;
+    if (tid < n) sdst[tid] = side_s[tid];
+  }
+  if (tid == 0) {
+    if (nq > nside) atomicAdd(&p.counters[0], (unsigned long long)(nq - nside));
+    if (nside) atomicAdd(&p.counters[1], (unsigned long long)nside);
+    if (slot == 0) atomicAdd(&p.counters[2], (unsigned long long)n);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -300,12 +657,93 @@ FetchKernel fetch_kernel_for(int mode, int out_dtype) {
   }
 }
 
+uint16_t bf16_bits(float v) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  return __bfloat16_as_ushort(h);
+}
+
+// Tensor-core append tables: three exact 16-bit pieces of V (scaled by
+// 2^scale_exp for fp16 so that no piece is subnormal) and c = mean . V in double.
+void prepare_append(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>& image,
+                    TcPlan& plan) {
+  const int D = d.D, r = g.r, nb = g.nb;
+  if (!(d.mode == KVC_MODE_UNIFORM || d.mode == KVC_MODE_CODEBOOK)) return;
+  if (!(d.in_dtype == KVC_BF16 || d.in_dtype == KVC_F16) || d.heads_per_group != 1) return;
+  const int rpad = (r + 15) / 16 * 16;
+  if (!(D % 64 == 0 && D <= 256 && rpad <= 160)) return;
+  int cols = 32;
+  while (cols < 3 * rpad + 32) cols *= 2;
+  int pmax = 0;
+  for (int b = 0; b < nb; ++b) pmax = std::max(pmax, g.P[b]);
+  const int Pp = (pmax + 3) / 4 * 4 + 4;
+  size_t smem = 1024 + (size_t)(D / 64) * 16384 + (size_t)3 * rpad * D * 2 +
+                align_up((size_t)kTile * r, 16) + (size_t)kTile * Pp + (size_t)kQueue * 4 + 256;
+  smem = std::max(smem, (size_t)(228 * 1024) / (512 / cols + 1) + 1024);
+  if (smem > 226 * 1024) return;
+  const bool bf = d.in_dtype == KVC_BF16;
+  int scale_exp = 0;
+  if (!bf) {
+    float vmax = 0.f;
+    for (size_t i = 0; i < (size_t)nb * D * r; ++i) vmax = std::max(vmax, std::fabs(d.V[i]));
+    if (!(vmax > 0.f)) return;
+    scale_exp = 14 - (int)std::ceil(std::log2((double)vmax));
+  }
+  const float scale = std::ldexp(1.f, scale_exp);
+  std::vector<uint16_t> Bop((size_t)nb * 3 * rpad * D, 0);
+  std::vector<double> c64((size_t)nb * r, 0.0);
+  for (int b = 0; b < nb; ++b) {
+    const float* V = d.V + (size_t)b * D * r;
+    for (int k = 0; k < r; ++k) {
+      double c = 0.0;
+      for (int i = 0; i < D; ++i) {
+        const float v = V[(size_t)i * r + k];
+        if (d.mean) c += (double)d.mean[(size_t)b * D + i] * (double)v;
+        float rest = v * scale;  // exact
+        for (int pc = 0; pc < 3; ++pc) {
+          uint16_t bits;
+          float got;
+          if (bf) {
+            bits = bf16_bits(rest);
+            got = __bfloat162float(__ushort_as_bfloat16(bits));
+          } else {
+            bits = half_bits(rest);
+            got = __half2float(__ushort_as_half(bits));
+          }
+          rest -= got;  // exact: the rounding error of a 16-bit rounding of an fp32 value
+          const size_t idx = ((size_t)(pc * (rpad / 8) + k / 8) * (D / 8) + i / 8) * 64 +
+                             (k % 8) * 8 + (i % 8);
+          Bop[(size_t)b * 3 * rpad * D + idx] = bits;
+        }
+      }
+      c64[(size_t)b * r + k] = c;
+    }
+  }
+  plan.oAppB = put(image, Bop.data(), Bop.size());
+  plan.oC64 = put(image, c64.data(), c64.size());
+  plan.app_rpad = rpad;
+  plan.app_cols = cols;
+  plan.app_smem = smem;
+  plan.app_bf16 = bf ? 1 : 0;
+  plan.app_inv_scale = std::ldexp(1.f, -scale_exp);
+  plan.app_gamma = (float)((17.0 * D / 16.0 + 2.0) * std::ldexp(1.0, -23) * (1.0 + std::ldexp(1.0, -7)));
+  plan.append_ready = encoder() != nullptr;
+}
+
+using AppendKernel = void (*)(const Params, const AppendTc, const CUtensorMap, const AppendArgs, int);
+
+AppendKernel append_kernel_for(int mode, int bf16) {
+  if (mode == KVC_MODE_UNIFORM)
+    return bf16 ? append_tc_kernel<KVC_MODE_UNIFORM, true> : append_tc_kernel<KVC_MODE_UNIFORM, false>;
+  return bf16 ? append_tc_kernel<KVC_MODE_CODEBOOK, true> : append_tc_kernel<KVC_MODE_CODEBOOK, false>;
+}
+
 }  // namespace
 
 kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>& image,
                       TcPlan& plan) {
   plan = TcPlan{};
   if (d.mode == KVC_MODE_INT8) return KVC_OK;
+  prepare_append(d, g, image, plan);
   const int D = d.D, din = g.d_in, r = g.r, nb = g.nb;
   int kmax = 0, pmax = 0;
   for (int b = 0; b < nb; ++b) {
@@ -360,6 +798,10 @@ void tc_bind(TcPlan& plan, uint8_t* base) {
     plan.fetchB = reinterpret_cast<const uint16_t*>(base + plan.oFetchB);
     plan.bias = reinterpret_cast<const float*>(base + plan.oBias);
   }
+  if (plan.append_ready) {
+    plan.appB = reinterpret_cast<const uint16_t*>(base + plan.oAppB);
+    plan.c64 = reinterpret_cast<const double*>(base + plan.oC64);
+  }
 }
 
 void tc_release(TcPlan&) {}
@@ -392,10 +834,39 @@ cudaError_t launch_fetch_tc(const TcPlan& plan, const Params& p, const FetchArgs
   return cudaGetLastError();
 }
 
-bool tc_append_ok(const TcPlan& plan, const Params&, const AppendArgs&) { return plan.append_ready; }
+bool tc_append_ok(const TcPlan& plan, const Params& p, const AppendArgs& a) {
+  // TMA needs a 16-byte aligned base and strides that are multiples of 16 bytes
+  return plan.append_ready && (reinterpret_cast<uintptr_t>(a.x) % 16 == 0) && a.T > 0 &&
+         a.T < (int64_t(1) << 31) && a.st % 8 == 0 && a.sh % 8 == 0 && a.sb % 8 == 0 &&
+         a.st >= p.D && (p.H == 1 || a.sh > 0) && (p.B == 1 || a.sb > 0);
+}
 
-cudaError_t launch_append_tc(const TcPlan&, const Params&, const AppendArgs&, cudaStream_t, int*) {
-  return cudaErrorNotSupported;
+cudaError_t launch_append_tc(const TcPlan& plan, const Params& p, const AppendArgs& a,
+                             cudaStream_t s, int* nk) {
+  CUtensorMap map;
+  // dims: D, tokens, heads, batch (innermost first); strides of dims 1..3 in bytes
+  const cuuint64_t dims[4] = {(cuuint64_t)p.D, (cuuint64_t)a.T, (cuuint64_t)p.H, (cuuint64_t)p.B};
+  const cuuint64_t strides[3] = {(cuuint64_t)a.st * 2,
+                                 (cuuint64_t)(p.H > 1 ? a.sh : a.T * a.st) * 2,
+                                 (cuuint64_t)(p.B > 1 ? a.sb : p.H * a.T * a.st) * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)kTile, 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult cr = encoder()(
+      &map, plan.app_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+      const_cast<void*>(a.x), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  AppendKernel kern = append_kernel_for(p.mode, plan.app_bf16);
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.app_smem);
+  if (e != cudaSuccess) return e;
+  const int tiles = (int)((a.T + kTile - 1) / kTile);
+  const AppendTc t{plan.appB, plan.c64, plan.app_rpad, plan.app_cols, plan.app_inv_scale,
+                   plan.app_gamma};
+  kern<<<(unsigned)(tiles * p.n_slots), kTile, plan.app_smem, s>>>(p, t, map, a, tiles);
+  ++*nk;
+  return cudaGetLastError();
 }
 
 }  // namespace kvc

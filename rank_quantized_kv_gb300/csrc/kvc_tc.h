@@ -21,7 +21,18 @@ struct TcPlan {
   const uint16_t* fetchB = nullptr;  // fp16 [nb][D_in][K] in UMMA no-swizzle K-major order
   const float* bias = nullptr;       // fp32 [nb][D_in]
 
+  // append: z = x [V_hi | V_mid | V_lo] (three exact 16-bit pieces of the fp32
+  // basis, each in its own TMEM accumulator) * 2^-scale_exp - mean V
   bool append_ready = false;
+  int app_rpad = 0;            // r rounded up to 16 (N of each piece)
+  int app_cols = 0;            // TMEM columns
+  size_t app_smem = 0;
+  int app_bf16 = 0;            // operands bf16 (else fp16)
+  float app_inv_scale = 1.f;   // 2^-scale_exp
+  float app_gamma = 0.f;       // accumulation error bound per unit of ||x|| ||V_k||
+  size_t oAppB = 0, oC64 = 0;
+  const uint16_t* appB = nullptr;  // [nb][3][rpad][D] UMMA no-swizzle K-major order
+  const double* c64 = nullptr;     // [nb][r] mean . V_k in double
 };
 
 kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>& image,
