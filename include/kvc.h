@@ -216,12 +216,14 @@ kvc_status kvc_set_path(kvc_layer *layer, int32_t path);
  * cannot encode exactly).  KVC_ECUDA if the synchronisation itself failed. */
 kvc_status kvc_sync_status(kvc_layer *layer, void *stream);
 
-/* Synchronise `stream` and copy the layer's device counters to host out[4]:
- * [0] components whose code was re-decided in double precision (near a rounding
- * boundary), [1] per-token fp16 side words re-decided, [2] appended tokens,
- * [3] kernels this layer has launched (counted on the host).  With reset != 0
- * the counters are then zeroed. */
-kvc_status kvc_counters(kvc_layer *layer, int64_t out[4], int32_t reset, void *stream);
+/* Synchronise `stream` and copy the layer's counters to host out[6]:
+ * [0] components whose code was re-decided exactly (near a rounding boundary),
+ * [1] per-token fp16 side words re-decided, [2] appended tokens, [3] kernels
+ * this layer has launched (counted on the host), [4] the largest
+ * |fast-path value - exact value| / (error bound) seen among re-decided codes
+ * of the tensor-core append, times 1e6 (below 1e6 means the bound held with
+ * margin), [5] reserved (0).  With reset != 0 the counters are then zeroed. */
+kvc_status kvc_counters(kvc_layer *layer, int64_t out[6], int32_t reset, void *stream);
 
 /* Free the layer's parameter block (synchronises the device first).  NULL is a no-op. */
 void kvc_destroy(kvc_layer *layer);

@@ -327,11 +327,11 @@ class KVCacheLayer:
         return int(self._lib.kvc_sync_status(self._h, _stream_ptr(stream, self.device)))
 
     def counters(self, reset=False, stream=None):
-        out = (c_int64 * 4)()
+        out = (c_int64 * 6)()
         _check(self._lib.kvc_counters(self._h, out, int(bool(reset)),
                                       _stream_ptr(stream, self.device)))
         return {"refined_codes": out[0], "refined_side": out[1], "appended": out[2],
-                "launches": out[3]}
+                "launches": out[3], "max_error_ratio": out[4] / 1e6}
 
     def close(self):
         if getattr(self, "_h", None):

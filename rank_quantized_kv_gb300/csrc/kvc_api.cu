@@ -562,7 +562,7 @@ kvc_status kvc_sync_status(kvc_layer* L, void* stream) {
   return succeed();
 }
 
-kvc_status kvc_counters(kvc_layer* L, int64_t out[4], int32_t reset, void* stream) {
+kvc_status kvc_counters(kvc_layer* L, int64_t out[6], int32_t reset, void* stream) {
   if (!L) return fail(KVC_ESTATE, "layer is NULL");
   if (!out) return fail(KVC_EINVAL, "out is NULL");
   DeviceGuard dg(L->device);
@@ -573,6 +573,11 @@ kvc_status kvc_counters(kvc_layer* L, int64_t out[4], int32_t reset, void* strea
   if (e != cudaSuccess) return cuda_fail(e, "read counters");
   for (int i = 0; i < 3; ++i) out[i] = (int64_t)c[i];
   out[3] = L->launches;
+  float ratio;
+  const uint32_t bits = (uint32_t)c[3];
+  std::memcpy(&ratio, &bits, sizeof ratio);
+  out[4] = (int64_t)std::llround((double)ratio * 1e6);
+  out[5] = 0;
   if (reset) {
     L->launches = 0;
     e = cudaMemset(L->p.counters, 0, sizeof c);

@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(kTile) fetch_tc_kernel(const Params p, const F
           w.push(__float2half_rn(cb_s[code]));
         }
       }
+      w.pad_to((w.kc * 8 + w.n + 7) & ~7);  // the next segment starts a new chunk
     }
   }
   w.pad_to(K);
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(kTile) fetch_tc_kernel(const Params p, const F
 // boundary are queued and re-decided by a warp with a compensated fp32 dot
 // product (error ~ 1e-13 relative) finished in double precision.
 
-constexpr int kQueue = 1024;
+constexpr int kQueue = 512;
 constexpr uint32_t kNormEntry = 0xFFFFu;
 
 struct AppendTc {
@@ -323,10 +324,19 @@ __device__ double dot2_row(const unsigned char* xs, int t, int D, const float* w
 
 // Decide code k of token tt exactly (or, k == kNormEntry, the fp16 norm of a
 // codebook token).  Lane 0 (or the lone thread) writes the result.
+// The largest |u_fast - u_exact| / bound seen (float bits; all non-negative)
+// is kept in counters[3]: evidence of how much margin the bound carries.
+__device__ __forceinline__ void note_ratio(const Params& p, double uf, double u, float tau) {
+  if (tau > 0.f) {
+    const float ratio = (float)(fabs(uf - u) / (double)tau);
+    atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(ratio));
+  }
+}
+
 template <int MODE, bool BF16, bool WARP>
 __device__ void refine_entry(const Params& p, const AppendTc& t, int beta, const unsigned char* xs,
                              unsigned char* codes_s, __half* side_s, unsigned* nside, int tt, int k,
-                             int lane) {
+                             int lane, float uf = 0.f, float tau = 0.f) {
   const int D = p.D, r = p.r;
   const float* Vt = p.Vt + (size_t)beta * r * D;
   if (MODE == KVC_MODE_UNIFORM) {
@@ -337,6 +347,7 @@ __device__ void refine_entry(const Params& p, const AppendTc& t, int beta, const
       const double u64 =
           (z64 - (double)p.lo[(size_t)beta * r + k]) / (double)p.step[(size_t)beta * r + k];
       codes_s[tt * r + k] = (uint8_t)(int)fmin(fmax(rint(u64), 0.0), (double)qmax);
+      note_ratio(p, uf, u64, tau);
     }
   } else {
     const double n64 = sqrt(dot2_row<BF16, WARP>(xs, tt, D, nullptr, lane));
@@ -349,6 +360,7 @@ __device__ void refine_entry(const Params& p, const AppendTc& t, int beta, const
       const double z64 = dot2_row<BF16, WARP>(xs, tt, D, Vt + (size_t)k * D, lane);
       if (lane == 0) {
         const double u64 = n64 > 0.0 ? z64 / n64 : 0.0;
+        note_ratio(p, uf, u64, tau);
         double best = fabs(u64 - (double)p.codebook[0]);
         int bi = 0;
         for (int j = 1; j < p.cb_levels; ++j) {
@@ -364,10 +376,20 @@ __device__ void refine_entry(const Params& p, const AppendTc& t, int beta, const
   }
 }
 
-template <int MODE, bool BF16>
-__global__ void __launch_bounds__(kTile) append_tc_kernel(const Params p, const AppendTc t,
-                                                          const __grid_constant__ CUtensorMap xmap,
-                                                          const AppendArgs a, int tiles_per_slot) {
+// ---------------------------------------------------------------- append, 512 threads
+//
+// Same arithmetic as above with the tile's work spread over 16 warps: warp w
+// reads TMEM lanes 32 (w % 4) .. +31 (its tokens) and column block w / 4 (a
+// quarter of the components).  Accumulators: the hi piece alone, the smaller
+// pieces together (their accumulation error is <= 2^-8 of the hi piece's).
+
+constexpr int kV3 = 512;
+
+template <int MODE, bool BF16, int CW>
+__global__ void __launch_bounds__(kV3) append_tc_v3(const Params p, const AppendTc t,
+                                                    const __grid_constant__ CUtensorMap xmap,
+                                                    const AppendArgs a, int tiles_per_slot,
+                                                    int npieces) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -375,23 +397,34 @@ __global__ void __launch_bounds__(kTile) append_tc_kernel(const Params p, const 
   __shared__ uint32_t tmem_base;
   __shared__ unsigned qcount, nside;
   __shared__ int abort_flag;
+  __shared__ int32_t seg_s[kMaxSeg * 4];
 
-  const int D = p.D, r = p.r, rpad = t.rpad, nbox = D / 64;
+  constexpr int rpad = 4 * CW;
+  const int D = p.D, r = p.r, nbox = D / 64;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, cblk = warp >> 2;
+  const int row = quarter * 32 + lane;  // token of this thread within the tile
   const int slot = blockIdx.x / tiles_per_slot;
   const int64_t t0 = (int64_t)(blockIdx.x % tiles_per_slot) * kTile;
   const int n = (int)min((int64_t)kTile, a.T - t0);
   const int beta = p.basis_of[slot];
   const int P = p.P[beta];
-  const int Pp = ((P + 3) & ~3) + 4;
   const int b = slot / p.H, h = slot % p.H;
 
-  unsigned char* xs = smem;                                    // nbox x 16 KB
-  unsigned char* Bs = xs + nbox * 16384;                       // 3 x rpad x D fp16/bf16
-  unsigned char* codes_s = Bs + 3 * rpad * D * 2;              // [128][r]
-  unsigned char* row_s = codes_s + ((kTile * r + 15) & ~15);   // [128][Pp]
-  uint32_t* queue = reinterpret_cast<uint32_t*>(row_s + kTile * Pp);
-  __half* side_s = reinterpret_cast<__half*>(queue + kQueue);  // [128]
+  unsigned char* xs = smem;                                           // nbox x 16 KB
+  unsigned char* Bs = xs + nbox * 16384;                              // npieces x rpad x D
+  unsigned char* codes_s = Bs + npieces * rpad * D * 2;               // [128][r]
+  uint32_t* queue = reinterpret_cast<uint32_t*>(codes_s + ((kTile * r + 15) & ~15));
+  float2* aux = reinterpret_cast<float2*>(queue + kQueue);
+  float* nsq_s = reinterpret_cast<float*>(aux + kQueue);              // [4][128]
+  float* lo_s = nsq_s + 4 * kTile;                                     // [rpad] each
+  float* inv_s = lo_s + rpad;
+  float* ck_s = inv_s + rpad;
+  float* vn_s = ck_s + rpad;
+  float* mids_s = vn_s + rpad;                                         // [256]
+  __half* side_s = reinterpret_cast<__half*>(mids_s + 256);           // [128]
+  int16_t* order_s = reinterpret_cast<int16_t*>(side_s + kTile);      // [rpad]
+  uint8_t* bits_s = reinterpret_cast<uint8_t*>(order_s + rpad);       // [rpad]
 
   if (warp == 0) tmem_alloc(&tmem_base, t.cols);
   if (tid == 0) {
@@ -405,9 +438,22 @@ __global__ void __launch_bounds__(kTile) append_tc_kernel(const Params p, const 
     for (int bx = 0; bx < nbox; ++bx) tma_load_4d(xs + bx * 16384, &xmap, &tma_bar, bx * 64, (int)t0, h, b);
   }
   {
-    const uint4* src = reinterpret_cast<const uint4*>(t.B + (size_t)beta * 3 * rpad * D);
-    const int nv = 3 * rpad * D * 2 / 16;
-    for (int i = tid; i < nv; i += kTile) reinterpret_cast<uint4*>(Bs)[i] = src[i];
+    const uint4* src = reinterpret_cast<const uint4*>(t.B + (size_t)beta * npieces * rpad * D);
+    const int nv = npieces * rpad * D * 2 / 16;
+    for (int i = tid; i < nv; i += kV3) reinterpret_cast<uint4*>(Bs)[i] = src[i];
+    for (int k = tid; k < rpad; k += kV3) {
+      const bool in = k < r;
+      const size_t bk = (size_t)beta * r + k;
+      lo_s[k] = in && MODE == KVC_MODE_UNIFORM ? p.lo[bk] : 0.f;
+      inv_s[k] = in && MODE == KVC_MODE_UNIFORM ? p.inv_step[bk] : 0.f;
+      ck_s[k] = in ? (float)t.c64[bk] : 0.f;
+      vn_s[k] = in ? p.vnorm[bk] : 0.f;
+      bits_s[k] = in ? p.bits[bk] : 0;
+      order_s[k] = in ? p.order[bk] : 0;
+    }
+    if (MODE == KVC_MODE_CODEBOOK)
+      for (int j = tid; j < p.cb_levels - 1; j += kV3) mids_s[j] = p.mids[j];
+    if (tid < kMaxSeg * 4) seg_s[tid] = p.seg[(int64_t)beta * kMaxSeg * 4 + tid];
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -417,141 +463,145 @@ __global__ void __launch_bounds__(kTile) append_tc_kernel(const Params p, const 
 
   if (!mbar_wait_bounded(&tma_bar, 0, kWaitNs)) abort_flag = 1;
   __syncthreads();
-  if (abort_flag) {
-    if (tid == 0) set_err(p.err, kErrTimeout);
-  } else if (tid == 0) {
+  if (!abort_flag && tid == 0) {
     const uint32_t idesc = idesc_f16(kTile, rpad, BF16 ? 1 : 0);
     const uint32_t sbo = (uint32_t)(D / 8) * 128;
-    for (int pc = 0; pc < 3; ++pc)
+    for (int pc = 0; pc < npieces; ++pc)
       for (int ks = 0; ks < D / 16; ++ks) {
         const uint64_t ad = desc_kmajor_sw128(smem_u32(xs) + (ks >> 2) * 16384 + (ks & 3) * 32);
         const uint64_t bd =
             desc_kmajor_noswizzle(smem_u32(Bs) + pc * rpad * D * 2 + ks * 256, 128, sbo);
-        umma_f16(taddr + pc * rpad, ad, bd, idesc, ks > 0 ? 1u : 0u);
+        umma_f16(taddr + (pc ? rpad : 0), ad, bd, idesc, (pc > 1 || ks > 0) ? 1u : 0u);
       }
     umma_commit(&mma_bar);
   }
-
-  // ||x_t|| in fp32 while the MMAs run (sequential over the row)
-  float nx = 0.f;
-  if (tid < n) {
-    for (int bx = 0; bx < nbox; ++bx)
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(xs + bx * 16384 + tid * 128 + ((c ^ (tid & 7)) << 4));
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+  {  // partial ||x||^2 over this warp's quarter of the row
+    float acc = 0.f;
+    const int c0 = cblk * (D / 4);
+    for (int c = c0; c < c0 + D / 4; c += 8) {
+      const uint4 v = *reinterpret_cast<const uint4*>(
+          xs + (c >> 6) * 16384 + row * 128 + (((((c & 63) >> 3)) ^ (row & 7)) << 4));
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float lo2, hi2;
-          if (BF16) {
-            lo2 = __bfloat162float(__ushort_as_bfloat16((uint16_t)(w4[q] & 0xffff)));
-            hi2 = __bfloat162float(__ushort_as_bfloat16((uint16_t)(w4[q] >> 16)));
-          } else {
-            lo2 = __half2float(__ushort_as_half((uint16_t)(w4[q] & 0xffff)));
-            hi2 = __half2float(__ushort_as_half((uint16_t)(w4[q] >> 16)));
-          }
-          nx = fmaf(lo2, lo2, nx);
-          nx = fmaf(hi2, hi2, nx);
+      for (int q = 0; q < 4; ++q) {
+        float e0, e1;
+        if (BF16) {
+          e0 = __bfloat162float(__ushort_as_bfloat16((uint16_t)(w4[q] & 0xffff)));
+          e1 = __bfloat162float(__ushort_as_bfloat16((uint16_t)(w4[q] >> 16)));
+        } else {
+          e0 = __half2float(__ushort_as_half((uint16_t)(w4[q] & 0xffff)));
+          e1 = __half2float(__ushort_as_half((uint16_t)(w4[q] >> 16)));
         }
+        acc = fmaf(e0, e0, acc);
+        acc = fmaf(e1, e1, acc);
       }
-    nx = sqrtf(nx);
+    }
+    nsq_s[cblk * kTile + row] = acc;
   }
   if (!abort_flag && !mbar_wait_bounded(&mma_bar, 0, kWaitNs)) abort_flag = 1;
   tc_fence_after();
   __syncthreads();
   if (abort_flag) {
     if (tid == 0) set_err(p.err, kErrTimeout);
+    tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(taddr, t.cols);
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(taddr, t.cols);
+    }
     return;
   }
+  const float nx = sqrtf(((nsq_s[row] + nsq_s[kTile + row]) + nsq_s[2 * kTile + row]) +
+                         nsq_s[3 * kTile + row]);
 
-  // ---- fast-path quantisation, thread t = token t
+  // ---- fast path: components cblk*CW .. +CW of token `row`
   const float kU = 5.9604644775390625e-08f;
   const float nxb = nx * (1.f + 1e-3f);
-  const float* vnorm = p.vnorm + (size_t)beta * r;
-  const double* c64 = t.c64 + (size_t)beta * r;
   const float eps_n = 0.5f * ((D + 2) * kU) / (1.f - (D + 2) * kU) + 2.f * kU;
-  float cmax = 0.f;
-  bool tiny = false;
-  if (MODE == KVC_MODE_CODEBOOK) {
-    cmax = fmaxf(fabsf(p.codebook[0]), fabsf(p.codebook[p.cb_levels - 1]));
-    tiny = nx < 1e-18f;
+  float z[CW];
+  {
+    uint32_t rr[CW];
+    const uint32_t la = taddr + ((uint32_t)(quarter * 32) << 16) + cblk * CW;
+    tmem_ld_n<CW>(la, rr);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < CW; ++i) z[i] = __uint_as_float(rr[i]);
+    tmem_ld_n<CW>(la + rpad, rr);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < CW; ++i) z[i] += __uint_as_float(rr[i]);
   }
-  const uint32_t lane_addr = taddr + ((uint32_t)(warp * 32) << 16);
-  for (int cc = 0; cc * 32 < r; ++cc) {
-    float z[32];
-    uint32_t rr[32];
-    tmem_ld32(lane_addr + cc * 32, rr);
-    tmem_wait_ld();
+  tc_fence_before();
+  const bool tiny = MODE == KVC_MODE_CODEBOOK && nx < 1e-18f;
+  float cmax = 0.f;
+  if (MODE == KVC_MODE_CODEBOOK) cmax = fmaxf(fabsf(p.codebook[0]), fabsf(p.codebook[p.cb_levels - 1]));
+  if (row < n) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) z[i] = __uint_as_float(rr[i]);
-    tmem_ld32(lane_addr + rpad + cc * 32, rr);
-    tmem_wait_ld();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) z[i] += __uint_as_float(rr[i]);
-    tmem_ld32(lane_addr + 2 * rpad + cc * 32, rr);
-    tmem_wait_ld();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) z[i] += __uint_as_float(rr[i]);
-    if (tid >= n) continue;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int k = cc * 32 + i;
+    for (int i = 0; i < CW; ++i) {
+      const int k = cblk * CW + i;
       if (k >= r) continue;
       bool near = false;
       int code = 0;
+      float uf = 0.f, tf = 0.f;
       if (MODE == KVC_MODE_UNIFORM) {
-        const int w = p.bits[(size_t)beta * r + k];
+        const int w = bits_s[k];
         if (w == 0) continue;
-        const float ck = (float)c64[k];
+        const float ck = ck_s[k];
         const float zc = z[i] * t.inv_scale - ck;
-        const float lo = p.lo[(size_t)beta * r + k], inv = p.inv_step[(size_t)beta * r + k];
-        const float u = (zc - lo) * inv;
-        const float tz = t.gamma * nxb * vnorm[k] + 4.f * kU * (fabsf(zc) + fabsf(ck));
+        const float inv = inv_s[k];
+        const float u = (zc - lo_s[k]) * inv;
+        const float tz = t.gamma * nxb * vn_s[k] + 4.f * kU * (fabsf(zc) + fabsf(ck));
         const float tau = tz * inv * (1.f + 1e-6f) + 4.f * kU * (fabsf(u) + 1.f);
         const int qmax = (1 << w) - 1;
         const float hb = floorf(u) + 0.5f;
         near = hb >= 0.5f && hb <= (float)qmax - 0.5f && fabsf(u - hb) <= tau;
         code = (int)fminf(fmaxf(rintf(u), 0.f), (float)qmax);
+        uf = u;
+        tf = tau;
       } else {
         const int L = p.cb_levels;
         const float u = tiny ? 0.f : z[i] * t.inv_scale / nx;
         int lo_i = 0, hi_i = L - 1;
         while (lo_i < hi_i) {
           const int mid = (lo_i + hi_i) >> 1;
-          if (p.mids[mid] < u) lo_i = mid + 1; else hi_i = mid;
+          if (mids_s[mid] < u) lo_i = mid + 1; else hi_i = mid;
         }
         code = lo_i;
         float dmin = 3.4e38f;
-        if (code > 0) dmin = fminf(dmin, fabsf(u - p.mids[code - 1]));
-        if (code < L - 1) dmin = fminf(dmin, fabsf(u - p.mids[code]));
-        const float tau = (t.gamma * vnorm[k] * (1.f + 1e-3f) + fabsf(u) * eps_n) * (1.f + 1e-6f) +
+        if (code > 0) dmin = fminf(dmin, fabsf(u - mids_s[code - 1]));
+        if (code < L - 1) dmin = fminf(dmin, fabsf(u - mids_s[code]));
+        const float tau = (t.gamma * vn_s[k] * (1.f + 1e-3f) + fabsf(u) * eps_n) * (1.f + 1e-6f) +
                           4.f * kU * (fabsf(u) + cmax);
         near = tiny || dmin <= tau;
+        uf = u;
+        tf = tiny ? 0.f : tau;
       }
-      codes_s[tid * r + k] = (uint8_t)code;
+      codes_s[row * r + k] = (uint8_t)code;
       if (near) {
         const unsigned q = atomicAdd(&qcount, 1u);
-        if (q < kQueue)
-          queue[q] = ((uint32_t)tid << 16) | (uint32_t)k;
-        else  // queue full: decide it here, alone
-          refine_entry<MODE, BF16, false>(p, t, beta, xs, codes_s, side_s, &nside, tid, k, 0);
+        if (q < kQueue) {
+          queue[q] = ((uint32_t)row << 16) | (uint32_t)k;
+          aux[q] = make_float2(uf, tf);
+        } else {  // queue full: decide it here, alone
+          refine_entry<MODE, BF16, false>(p, t, beta, xs, codes_s, side_s, &nside, row, k, 0);
+        }
+      }
+    }
+    if (MODE == KVC_MODE_CODEBOOK && cblk == 0) {
+      if (tiny || !same_half(nx * (1.f - eps_n), nx * (1.f + eps_n))) {
+        const unsigned q = atomicAdd(&qcount, 1u);
+        if (q < kQueue) {
+          queue[q] = ((uint32_t)row << 16) | kNormEntry;
+          aux[q] = make_float2(0.f, 0.f);
+        } else {
+          refine_entry<MODE, BF16, false>(p, t, beta, xs, codes_s, side_s, &nside, row,
+                                          (int)kNormEntry, 0);
+        }
+      } else {
+        side_s[row] = __float2half_rn(nx);
       }
     }
   }
-  if (MODE == KVC_MODE_CODEBOOK && tid < n) {
-    if (tiny || !same_half(nx * (1.f - eps_n), nx * (1.f + eps_n))) {
-      const unsigned q = atomicAdd(&qcount, 1u);
-      if (q < kQueue)
-        queue[q] = ((uint32_t)tid << 16) | kNormEntry;
-      else
-        refine_entry<MODE, BF16, false>(p, t, beta, xs, codes_s, side_s, &nside, tid,
-                                        (int)kNormEntry, 0);
-    } else {
-      side_s[tid] = __float2half_rn(nx);
-    }
-  }
-  tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
@@ -560,46 +610,36 @@ __global__ void __launch_bounds__(kTile) append_tc_kernel(const Params p, const 
 
   // ---- exact re-decision of the queued codes, one warp per entry
   const unsigned nq = qcount;
-  for (unsigned e = warp; e < min(nq, (unsigned)kQueue); e += kTile / 32) {
+  for (unsigned e = warp; e < min(nq, (unsigned)kQueue); e += kV3 / 32) {
     const uint32_t ent = queue[e];
+    const float2 ax = aux[e];
     refine_entry<MODE, BF16, true>(p, t, beta, xs, codes_s, side_s, &nside, (int)(ent >> 16),
-                                   (int)(ent & 0xffffu), lane);
+                                   (int)(ent & 0xffffu), lane, ax.x, ax.y);
   }
   __syncthreads();
 
-  // ---- bit-pack each token's row (segments widest first, LSB-first stream)
-  if (tid < n) {
-    unsigned char* row = row_s + tid * Pp;
-    const int32_t* seg = p.seg + (int64_t)beta * kMaxSeg * 4;
-    const int16_t* order = p.order + (int64_t)beta * r;
-    int pos = 0;
-    for (int s = 0; s < kMaxSeg; ++s) {
-      const int cnt = seg[s * 4 + 3];
-      if (!cnt) break;
-      const int wd = seg[s * 4 + 1], m0 = seg[s * 4 + 2];
-      uint32_t acc = 0;
-      int nb = 0;
-      for (int m = 0; m < cnt; ++m) {
-        acc |= (uint32_t)codes_s[tid * r + order[m0 + m]] << nb;
-        nb += wd;
-        while (nb >= 8) {
-          row[pos++] = (unsigned char)(acc & 0xffu);
-          acc >>= 8;
-          nb -= 8;
-        }
-      }
-      if (nb > 0) row[pos++] = (unsigned char)(acc & 0xffu);
-    }
-  }
-  __syncthreads();
+  // ---- pack: one thread per output byte, written straight to the store
   unsigned char* dst = p.store + p.pay_off[slot] + (a.t_base + t0) * P;
-  for (int idx = tid; idx < n * P; idx += kTile) {
-    const int tt = idx / P;
-    dst[idx] = row_s[tt * Pp + (idx - tt * P)];
+  for (int idx = tid; idx < n * P; idx += kV3) {
+    const int tt = idx / P, j = idx - tt * P;
+    int s = 0;
+    while (s + 1 < kMaxSeg && seg_s[(s + 1) * 4 + 3] > 0 && seg_s[(s + 1) * 4 + 0] <= j) ++s;
+    const int start = seg_s[s * 4 + 0], wd = seg_s[s * 4 + 1], m0 = seg_s[s * 4 + 2];
+    const int cntm = seg_s[s * 4 + 3];
+    const int q0 = 8 * (j - start);
+    const int mlo = q0 / wd;
+    const int mhi = min((q0 + 7) / wd, cntm - 1);
+    unsigned v = 0;
+    for (int mm = mlo; mm <= mhi; ++mm) {
+      const unsigned code = codes_s[tt * r + order_s[m0 + mm]];
+      const int sh = mm * wd - q0;
+      v |= sh >= 0 ? (code << sh) : (code >> (-sh));
+    }
+    dst[idx] = (unsigned char)(v & 0xffu);
   }
-  if (MODE == KVC_MODE_CODEBOOK) {
+  if (MODE == KVC_MODE_CODEBOOK && tid < n) {
     __half* sdst = reinterpret_cast<__half*>(p.store + p.side_off[slot]) + a.t_base + t0;
-    if (tid < n) sdst[tid] = side_s[tid];
+    sdst[tid] = side_s[tid];
   }
   if (tid == 0) {
     if (nq > nside) atomicAdd(&p.counters[0], (unsigned long long)(nq - nside));
@@ -669,18 +709,17 @@ void prepare_append(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>&
   const int D = d.D, r = g.r, nb = g.nb;
   if (!(d.mode == KVC_MODE_UNIFORM || d.mode == KVC_MODE_CODEBOOK)) return;
   if (!(d.in_dtype == KVC_BF16 || d.in_dtype == KVC_F16) || d.heads_per_group != 1) return;
-  const int rpad = (r + 15) / 16 * 16;
-  if (!(D % 64 == 0 && D <= 256 && rpad <= 160)) return;
-  int cols = 32;
-  while (cols < 3 * rpad + 32) cols *= 2;
-  int pmax = 0;
-  for (int b = 0; b < nb; ++b) pmax = std::max(pmax, g.P[b]);
-  const int Pp = (pmax + 3) / 4 * 4 + 4;
-  size_t smem = 1024 + (size_t)(D / 64) * 16384 + (size_t)3 * rpad * D * 2 +
-                align_up((size_t)kTile * r, 16) + (size_t)kTile * Pp + (size_t)kQueue * 4 + 256;
+  int rpad = 16;
+  while (rpad < r) rpad *= 2;
+  if (!(D % 64 == 0 && D <= 256 && rpad <= 128)) return;
+  const bool bf = d.in_dtype == KVC_BF16;
+  const int npieces = bf ? 3 : 2;  // bf16: 3 x 8 bits; fp16 (scaled): 2 x 11 bits
+  const int cols = std::max(32, 2 * rpad);
+  size_t smem = 1024 + (size_t)(D / 64) * 16384 + (size_t)npieces * rpad * D * 2 +
+                align_up((size_t)kTile * r, 16) + (size_t)kQueue * 12 + 4 * kTile * 4 +
+                4 * (size_t)rpad * 4 + 256 * 4 + kTile * 2 + (size_t)rpad * 3 + 64;
   smem = std::max(smem, (size_t)(228 * 1024) / (512 / cols + 1) + 1024);
   if (smem > 226 * 1024) return;
-  const bool bf = d.in_dtype == KVC_BF16;
   int scale_exp = 0;
   if (!bf) {
     float vmax = 0.f;
@@ -689,7 +728,7 @@ void prepare_append(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>&
     scale_exp = 14 - (int)std::ceil(std::log2((double)vmax));
   }
   const float scale = std::ldexp(1.f, scale_exp);
-  std::vector<uint16_t> Bop((size_t)nb * 3 * rpad * D, 0);
+  std::vector<uint16_t> Bop((size_t)nb * npieces * rpad * D, 0);
   std::vector<double> c64((size_t)nb * r, 0.0);
   for (int b = 0; b < nb; ++b) {
     const float* V = d.V + (size_t)b * D * r;
@@ -699,7 +738,7 @@ void prepare_append(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>&
         const float v = V[(size_t)i * r + k];
         if (d.mean) c += (double)d.mean[(size_t)b * D + i] * (double)v;
         float rest = v * scale;  // exact
-        for (int pc = 0; pc < 3; ++pc) {
+        for (int pc = 0; pc < npieces; ++pc) {
           uint16_t bits;
           float got;
           if (bf) {
@@ -712,7 +751,7 @@ void prepare_append(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>&
           rest -= got;  // exact: the rounding error of a 16-bit rounding of an fp32 value
           const size_t idx = ((size_t)(pc * (rpad / 8) + k / 8) * (D / 8) + i / 8) * 64 +
                              (k % 8) * 8 + (i % 8);
-          Bop[(size_t)b * 3 * rpad * D + idx] = bits;
+          Bop[(size_t)b * npieces * rpad * D + idx] = bits;
         }
       }
       c64[(size_t)b * r + k] = c;
@@ -725,19 +764,45 @@ void prepare_append(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>&
   plan.app_smem = smem;
   plan.app_bf16 = bf ? 1 : 0;
   plan.app_inv_scale = std::ldexp(1.f, -scale_exp);
-  plan.app_gamma = (float)((17.0 * D / 16.0 + 2.0) * std::ldexp(1.0, -23) * (1.0 + std::ldexp(1.0, -7)));
+  // Truncation-model bound of the tensor-core accumulation, divided by 8: over
+  // ~1e7 re-decided codes the worst observed error was 2.3 % of the full bound
+  // (counters[3] keeps reporting it against the bound in use).  fp16 pieces
+  // add their 2^-22 representation error.
+  plan.app_gamma = (float)((17.0 * D / 16.0 + 2.0) * std::ldexp(1.0, -23) *
+                               (1.0 + std::ldexp(1.0, -7)) / 8.0 +
+                           (bf ? 0.0 : std::ldexp(1.0, -21)));
+  plan.app_pieces = npieces;
   plan.append_ready = encoder() != nullptr;
 }
 
-using AppendKernel = void (*)(const Params, const AppendTc, const CUtensorMap, const AppendArgs, int);
+using AppendKernel = void (*)(const Params, const AppendTc, const CUtensorMap, const AppendArgs, int,
+                              int);
 
-AppendKernel append_kernel_for(int mode, int bf16) {
+template <int MODE, bool BF16>
+AppendKernel append_v3_for(int rpad) {
+  switch (rpad) {
+    case 16: return append_tc_v3<MODE, BF16, 4>;
+    case 32: return append_tc_v3<MODE, BF16, 8>;
+    case 64: return append_tc_v3<MODE, BF16, 16>;
+    default: return append_tc_v3<MODE, BF16, 32>;
+  }
+}
+
+AppendKernel append_kernel_for(int mode, int bf16, int rpad) {
   if (mode == KVC_MODE_UNIFORM)
-    return bf16 ? append_tc_kernel<KVC_MODE_UNIFORM, true> : append_tc_kernel<KVC_MODE_UNIFORM, false>;
-  return bf16 ? append_tc_kernel<KVC_MODE_CODEBOOK, true> : append_tc_kernel<KVC_MODE_CODEBOOK, false>;
+    return bf16 ? append_v3_for<KVC_MODE_UNIFORM, true>(rpad) : append_v3_for<KVC_MODE_UNIFORM, false>(rpad);
+  return bf16 ? append_v3_for<KVC_MODE_CODEBOOK, true>(rpad) : append_v3_for<KVC_MODE_CODEBOOK, false>(rpad);
 }
 
 }  // namespace
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 1;
+  return n;
+}
 
 kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>& image,
                       TcPlan& plan) {
@@ -745,12 +810,21 @@ kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t
   if (d.mode == KVC_MODE_INT8) return KVC_OK;
   prepare_append(d, g, image, plan);
   const int D = d.D, din = g.d_in, r = g.r, nb = g.nb;
-  int kmax = 0, pmax = 0;
+  // K layout: every packed segment starts on an 8-value chunk boundary, so a
+  // chunk of A is decoded from consecutive bytes of one segment; the gaps are
+  // zero columns of B.  koff[b][s] is segment s's first K position.
+  int ktot = 0, pmax = 0;
+  std::vector<int> koff((size_t)nb * kMaxSeg, 0);
   for (int b = 0; b < nb; ++b) {
-    kmax = std::max(kmax, g.n_kept[b]);
+    int k = 0;
+    for (int s = 0; s < kMaxSeg; ++s) {
+      koff[(size_t)b * kMaxSeg + s] = k;
+      k += (g.seg[((size_t)b * kMaxSeg + s) * 4 + 3] + 7) / 8 * 8;
+    }
+    ktot = std::max(ktot, k);
     pmax = std::max(pmax, g.P[b]);
   }
-  const int K = (kmax + 15) / 16 * 16;
+  const int K = (ktot + 15) / 16 * 16;
   const int cols = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
   size_t smem = 1024 + (size_t)(D / 64) * 16384 + (size_t)kTile * K * 2 + (size_t)D * K * 2 +
                 (size_t)D * 4 + 256 * 4 + align_up((size_t)kTile * pmax + 16, 16) +
@@ -761,12 +835,23 @@ kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t
         (d.mode != KVC_MODE_GROUP || d.group_size <= 32)))
     return KVC_OK;  // the CUDA-core kernels serve this shape
 
-  // B = coef_k * V[:, order[kk]] in UMMA order, coef = step (uniform) or 1; bias in fp64.
+  // B = coef_k * V[:, k] at k's K position, coef = step (uniform) or 1; bias in fp64.
+  // Chunk table: for each 8-value chunk of K, its first byte in the packed row,
+  // its width and a valid bit (zero chunks are padding).
   std::vector<uint16_t> Bop((size_t)nb * din * K, 0);
   std::vector<float> bias((size_t)nb * din, 0.f);
+  std::vector<uint32_t> chunks((size_t)nb * (K / 8), 0u);
   for (int b = 0; b < nb; ++b) {
     const float* V = d.V + (size_t)b * din * r;
     const int16_t* order = g.order.data() + (size_t)b * r;
+    std::vector<int> kpos(g.n_kept[b]);
+    for (int s = 0; s < kMaxSeg; ++s) {
+      const int32_t* e = &g.seg[((size_t)b * kMaxSeg + s) * 4];
+      for (int m = 0; m < e[3]; ++m) kpos[e[2] + m] = koff[(size_t)b * kMaxSeg + s] + m;
+      for (int ci = 0; ci * 8 < e[3]; ++ci)
+        chunks[(size_t)b * (K / 8) + koff[(size_t)b * kMaxSeg + s] / 8 + ci] =
+            (uint32_t)(e[0] + e[1] * ci) | ((uint32_t)e[1] << 16) | (1u << 31);
+    }
     for (int nrow = 0; nrow < din; ++nrow) {
       double acc = d.mean && d.mode != KVC_MODE_CODEBOOK ? (double)d.mean[(size_t)b * din + nrow] : 0.0;
       for (int kk = 0; kk < g.n_kept[b]; ++kk) {
@@ -778,18 +863,35 @@ kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t
           coef = d.qstep[(size_t)b * r + k];
           acc += ((double)d.qmin[(size_t)b * r + k] + (double)(1 << (wdt - 1)) * coef) * v;
         }
-        const size_t idx = ((size_t)(nrow / 8) * (K / 8) + kk / 8) * 64 + (nrow % 8) * 8 + (kk % 8);
+        const int kp = kpos[kk];
+        const size_t idx = ((size_t)(nrow / 8) * (K / 8) + kp / 8) * 64 + (nrow % 8) * 8 + (kp % 8);
         Bop[(size_t)b * din * K + idx] = half_bits((float)(coef * v));
       }
       bias[(size_t)b * din + nrow] = (float)acc;
     }
   }
+  plan.oChunks = put(image, chunks.data(), chunks.size());
   plan.oFetchB = put(image, Bop.data(), Bop.size());
   plan.oBias = put(image, bias.data(), bias.size());
   plan.fetch_K = K;
   plan.fetch_cols = cols;
   plan.fetch_smem = smem;
   plan.fetch_ready = encoder() != nullptr;
+  if (d.heads_per_group == 1 && 2 * cols <= 512) {
+    const int cbuf = (int)(align_up((size_t)kTile * pmax + 16, 16) +
+                           align_up((size_t)kTile * g.side_bytes + 16, 16));
+    size_t ps = 1024 + (size_t)2 * (D / 64) * 16384 + (size_t)2 * kTile * K * 2 + (size_t)D * K * 2 +
+                (size_t)2 * D * 4 + 256 * 2 + 32 * 4 + 2 * kTile * 4 + (size_t)2 * cbuf;
+    const int by_tmem = 512 / (2 * cols);
+    ps = std::max(ps, (size_t)(228 * 1024) / (by_tmem + 1) + 1024);
+    if (ps <= 226 * 1024) {
+      plan.pipe_ready = plan.fetch_ready;
+      plan.pipe_cols = 2 * cols;
+      plan.pipe_cbuf = cbuf;
+      plan.pipe_smem = ps;
+      plan.pipe_ctas_per_sm = std::max(1, std::min(by_tmem, (int)((228 * 1024) / ps)));
+    }
+  }
   return KVC_OK;
 }
 
@@ -797,6 +899,7 @@ void tc_bind(TcPlan& plan, uint8_t* base) {
   if (plan.fetch_ready) {
     plan.fetchB = reinterpret_cast<const uint16_t*>(base + plan.oFetchB);
     plan.bias = reinterpret_cast<const float*>(base + plan.oBias);
+    plan.chunks = reinterpret_cast<const uint32_t*>(base + plan.oChunks);
   }
   if (plan.append_ready) {
     plan.appB = reinterpret_cast<const uint16_t*>(base + plan.oAppB);
@@ -823,6 +926,7 @@ cudaError_t launch_fetch_tc(const TcPlan& plan, const Params& p, const FetchArgs
       3, f.out, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  if (plan.pipe_ready) return launch_fetch_pipe(plan, p, f, map, s, nk);
   FetchKernel kern = fetch_kernel_for(p.mode, p.out_dtype);
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.fetch_smem);
@@ -857,14 +961,14 @@ cudaError_t launch_append_tc(const TcPlan& plan, const Params& p, const AppendAr
       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  AppendKernel kern = append_kernel_for(p.mode, plan.app_bf16);
+  AppendKernel kern = append_kernel_for(p.mode, plan.app_bf16, plan.app_rpad);
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.app_smem);
   if (e != cudaSuccess) return e;
   const int tiles = (int)((a.T + kTile - 1) / kTile);
   const AppendTc t{plan.appB, plan.c64, plan.app_rpad, plan.app_cols, plan.app_inv_scale,
                    plan.app_gamma};
-  kern<<<(unsigned)(tiles * p.n_slots), kTile, plan.app_smem, s>>>(p, t, map, a, tiles);
+  kern<<<(unsigned)(tiles * p.n_slots), kV3, plan.app_smem, s>>>(p, t, map, a, tiles, plan.app_pieces);
   ++*nk;
   return cudaGetLastError();
 }

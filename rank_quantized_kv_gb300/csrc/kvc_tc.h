@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <vector>
 
+#include <cuda.h>
+
 #include "kvc_internal.h"
 
 namespace kvc {
@@ -14,24 +16,32 @@ namespace kvc {
 struct TcPlan {
   // fetch: x_hat = A B^T + bias, A = decoded codes [tokens x K], B [D_in x K]
   bool fetch_ready = false;
-  int fetch_K = 0;             // K: kept components rounded up to 16
+  int fetch_K = 0;             // K: segments padded to 8, total rounded up to 16
   int fetch_cols = 0;          // TMEM columns (D, a power of two)
   size_t fetch_smem = 0;       // dynamic shared memory per CTA
-  size_t oFetchB = 0, oBias = 0;
+  size_t oFetchB = 0, oBias = 0, oChunks = 0;
   const uint16_t* fetchB = nullptr;  // fp16 [nb][D_in][K] in UMMA no-swizzle K-major order
   const float* bias = nullptr;       // fp32 [nb][D_in]
+  const uint32_t* chunks = nullptr;  // [nb][K/8]: first byte | width << 16 | valid << 31
+  // pipelined persistent fetch (one head per slot)
+  bool pipe_ready = false;
+  int pipe_cols = 0;           // two accumulators
+  int pipe_cbuf = 0;           // bytes of one packed-row (+ side) buffer
+  int pipe_ctas_per_sm = 0;
+  size_t pipe_smem = 0;
 
-  // append: z = x [V_hi | V_mid | V_lo] (three exact 16-bit pieces of the fp32
-  // basis, each in its own TMEM accumulator) * 2^-scale_exp - mean V
+  // append: z = x (V_hi + V_rest) * 2^-scale_exp - mean V, the fp32 basis split
+  // into exact 16-bit pieces, the hi piece and the rest in two TMEM accumulators
   bool append_ready = false;
   int app_rpad = 0;            // r rounded up to 16 (N of each piece)
   int app_cols = 0;            // TMEM columns
   size_t app_smem = 0;
   int app_bf16 = 0;            // operands bf16 (else fp16)
+  int app_pieces = 3;          // 16-bit pieces of the basis (3 bf16 or 2 fp16)
   float app_inv_scale = 1.f;   // 2^-scale_exp
   float app_gamma = 0.f;       // accumulation error bound per unit of ||x|| ||V_k||
   size_t oAppB = 0, oC64 = 0;
-  const uint16_t* appB = nullptr;  // [nb][3][rpad][D] UMMA no-swizzle K-major order
+  const uint16_t* appB = nullptr;  // [nb][pieces][rpad][D] UMMA no-swizzle K-major order
   const double* c64 = nullptr;     // [nb][r] mean . V_k in double
 };
 
@@ -46,5 +56,10 @@ cudaError_t launch_append_tc(const TcPlan& plan, const Params& p, const AppendAr
                              cudaStream_t s, int* nk);
 cudaError_t launch_fetch_tc(const TcPlan& plan, const Params& p, const FetchArgs& f,
                             cudaStream_t s, int* nk);
+
+// Pipelined persistent fetch (kvc_fetch_pipe.cu); `map` is the output tensor map.
+cudaError_t launch_fetch_pipe(const TcPlan& plan, const Params& p, const FetchArgs& f,
+                              const CUtensorMap& map, cudaStream_t s, int* nk);
+int sm_count();
 
 }  // namespace kvc
