@@ -824,6 +824,11 @@ kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t
     ktot = std::max(ktot, k);
     pmax = std::max(pmax, g.P[b]);
   }
+  // Uniform mode folds the bias into the contraction: one more chunk of A
+  // holds (1, 1, 0 ...) and the matching B columns hold the bias as fp16 hi + lo.
+  const bool fold_bias = d.mode == KVC_MODE_UNIFORM;
+  const int kones = ktot;
+  if (fold_bias) ktot += 8;
   const int K = (ktot + 15) / 16 * 16;
   const int cols = D <= 64 ? 64 : (D <= 128 ? 128 : 256);
   size_t smem = 1024 + (size_t)(D / 64) * 16384 + (size_t)kTile * K * 2 + (size_t)D * K * 2 +
@@ -868,7 +873,23 @@ kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t
         Bop[(size_t)b * din * K + idx] = half_bits((float)(coef * v));
       }
       bias[(size_t)b * din + nrow] = (float)acc;
+      if (fold_bias) {
+        const uint16_t hi = half_bits((float)acc);
+        const double rest = acc - (double)__half2float(__ushort_as_half(hi));
+        for (int e = 0; e < 2; ++e) {
+          const int kp = kones + e;
+          const size_t idx = ((size_t)(nrow / 8) * (K / 8) + kp / 8) * 64 + (nrow % 8) * 8 + (kp % 8);
+          Bop[(size_t)b * din * K + idx] = e == 0 ? hi : half_bits((float)rest);
+        }
+      }
     }
+    if (fold_bias) chunks[(size_t)b * (K / 8) + kones / 8] = 1u << 30;  // the ones chunk
+  }
+  plan.bias_folded = fold_bias;
+  {  // packed row bytes per slot (one load instead of basis_of -> P)
+    std::vector<int32_t> slotP(g.n_slots);
+    for (int sl = 0; sl < g.n_slots; ++sl) slotP[sl] = g.P[g.basis[sl]];
+    plan.oSlotP = put(image, slotP.data(), slotP.size());
   }
   plan.oChunks = put(image, chunks.data(), chunks.size());
   plan.oFetchB = put(image, Bop.data(), Bop.size());
@@ -881,7 +902,7 @@ kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t
     const int cbuf = (int)(align_up((size_t)kTile * pmax + 16, 16) +
                            align_up((size_t)kTile * g.side_bytes + 16, 16));
     size_t ps = 1024 + (size_t)2 * (D / 64) * 16384 + (size_t)2 * kTile * K * 2 + (size_t)D * K * 2 +
-                (size_t)2 * D * 4 + 256 * 2 + 32 * 4 + 2 * kTile * 4 + (size_t)2 * cbuf;
+                256 * 2 + 32 * 4 + 2 * kTile * 4 + (size_t)4 * cbuf;
     const int by_tmem = 512 / (2 * cols);
     ps = std::max(ps, (size_t)(228 * 1024) / (by_tmem + 1) + 1024);
     if (ps <= 226 * 1024) {
@@ -900,6 +921,7 @@ void tc_bind(TcPlan& plan, uint8_t* base) {
     plan.fetchB = reinterpret_cast<const uint16_t*>(base + plan.oFetchB);
     plan.bias = reinterpret_cast<const float*>(base + plan.oBias);
     plan.chunks = reinterpret_cast<const uint32_t*>(base + plan.oChunks);
+    plan.slotP = reinterpret_cast<const int32_t*>(base + plan.oSlotP);
   }
   if (plan.append_ready) {
     plan.appB = reinterpret_cast<const uint16_t*>(base + plan.oAppB);

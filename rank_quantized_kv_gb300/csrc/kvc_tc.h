@@ -19,10 +19,13 @@ struct TcPlan {
   int fetch_K = 0;             // K: segments padded to 8, total rounded up to 16
   int fetch_cols = 0;          // TMEM columns (D, a power of two)
   size_t fetch_smem = 0;       // dynamic shared memory per CTA
-  size_t oFetchB = 0, oBias = 0, oChunks = 0;
+  size_t oFetchB = 0, oBias = 0, oChunks = 0, oSlotP = 0;
   const uint16_t* fetchB = nullptr;  // fp16 [nb][D_in][K] in UMMA no-swizzle K-major order
   const float* bias = nullptr;       // fp32 [nb][D_in]
-  const uint32_t* chunks = nullptr;  // [nb][K/8]: first byte | width << 16 | valid << 31
+  const uint32_t* chunks = nullptr;  // [nb][K/8]: first byte | width << 16 | valid << 31;
+                                     // 1 << 30 marks the chunk of ones (bias columns)
+  bool bias_folded = false;          // B carries the bias (uniform mode)
+  const int32_t* slotP = nullptr;    // [n_slots] packed row bytes of each slot
   // pipelined persistent fetch (one head per slot)
   bool pipe_ready = false;
   int pipe_cols = 0;           // two accumulators
