@@ -1,24 +1,37 @@
-// Pipelined persistent fetch for one head per slot (uniform and codebook modes).
+// Warp-specialised persistent fetch for one head per slot (uniform and
+// codebook modes): x_hat = A B^T (+ bias folded into B), A the decoded codes.
 //
-// 512 threads per CTA, two CTAs per SM.  Each CTA owns a contiguous run of
-// 128-token tiles (mostly of one slot, so the basis B stays in shared memory).
-// One barrier per iteration i separates two phases:
-//   all threads:  decode of tile i (packed rows -> A[i%2]), then the epilogue
-//                 of tile i-1 (TMEM buffer (i-1)%2 -> staging (i-1)%2);
-//   one thread:   tcgen05.mma of tile i into TMEM buffer i%2, TMA store of
-//                 tile i-1, bulk prefetch of tile i+3's packed rows (a ring of
-//                 four buffers keeps three tiles of rows in flight).
-// so the MMA, the store and the prefetch of one iteration run under the next
-// iteration's arithmetic.
+// One CTA per SM walks a contiguous run of 128-token tiles.  Four roles run
+// concurrently and hand tiles on through mbarrier rings, with no CTA-wide
+// barrier in the loop:
+//   producer (one thread)  bulk-copies each tile's packed rows, side words and
+//                          its basis' chunk table into a ring of row stages,
+//                          and the basis B into one of (up to) two B buffers
+//                          when the basis changes;
+//   decoders (8 warps)     turn a row stage into the fp16 A operand, written
+//                          straight into TMEM (a ring of A buffers there);
+//   MMA (one thread)       issues tcgen05.mma of A (from TMEM) against B (from
+//                          shared memory) into one of several TMEM accumulators;
+//   epilogue (8 warps)     read an accumulator, convert to the output type,
+//                          stage it swizzled in shared memory, and one thread
+//                          TMA-stores the tile.  Up to four staging buffers keep
+//                          three tiles of stores in flight per SM: HBM write
+//                          bandwidth needs that many bytes outstanding.
+// Every ring slot has a full and an empty barrier; each wait is bounded in
+// time and a time-out sets the layer's error word and unwinds.
+//
+// Shared-memory bandwidth, not arithmetic, bounds this kernel: per tile the
+// staging write and the TMA store's read move 2 x 32 KB (D = 128, fp16) and
+// the MMA reads B.  Keeping A in TMEM takes its write and its read by the
+// tensor core (2 x 16 KB at K = 64) off the shared-memory pipe.
 //
 // Decode works on 8-value chunks of K: every packed segment starts a chunk,
 // so a chunk is w consecutive bytes of the row (w = the segment's width).
 // A code c becomes fp16 through its bit pattern: 0x6400 | c is exactly
 // 1024 + c, and one half2 subtraction of 1024 + 2^(w-1) gives c - 2^(w-1)
 // exactly (uniform; the bias enters the contraction through a chunk of ones);
-// codebook codes index an fp16 copy of the centroids, the fp16 norm is applied
-// in the epilogue.  Epilogue: warp w reads TMEM lanes 32 (w % 4).. and a
-// quarter of the columns.
+// codebook codes index an fp16 copy of the centroids, and the epilogue scales
+// by the fp16 norm.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -34,17 +47,40 @@ using namespace sm100;
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kThreads = 512;
-constexpr int kStages = 4;  // packed-row buffers: tile i+3 is fetched while tile i decodes
+constexpr int kEpiWarps = 8;   // warps 0..7: two per TMEM lane quarter
+constexpr int kDecWarps = 8;   // warps 8..15
+constexpr int kProdWarp = kEpiWarps + kDecWarps;
+constexpr int kMmaWarp = kProdWarp + 1;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kMaxRS = 8, kMaxAS = 3, kMaxTS = 4, kMaxSS = 4;
+constexpr int kNormRing = 8;   // >= A buffers + accumulators (see the decoders)
+static_assert(kNormRing >= kMaxAS + kMaxTS, "norm ring shorter than the pipeline");
+constexpr int kEpiBar = 1;     // named barriers 1, 2: the epilogue groups
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct PipeArgs {
   const uint16_t* B;       // fp16 [nb][D][K] UMMA no-swizzle K-major
-  const uint32_t* chunks;  // [nb][K/8]
+  const uint32_t* chunks;  // [nb][32] chunk table, 128 bytes per basis
   const int32_t* slotP;    // [n_slots] packed row bytes
-  int K, cols, cbuf;
+  int K, cols;             // K; TMEM columns allocated
+  int n_acc, n_a, n_rs;    // accumulators, A buffers, row stages
+  int a_col0, a_cols;      // TMEM column of the first A buffer; columns per A buffer
+  int n_stg, n_b;          // staging buffers, B buffers (1 when every slot shares a basis)
+  int rs_bytes;            // bytes of one row stage
   int64_t S;
   int tiles_per_slot, total_tiles;
+};
+
+// Position in a ring of n buffers: the buffer of the current use and the
+// parity of its barriers' phase; next() moves on one use.
+struct Ring {
+  int n, slot;
+  uint32_t phase;
+  __device__ explicit Ring(int n_) : n(n_), slot(0), phase(0u) {}
+  __device__ void next() {
+    if (++slot == n) { slot = 0; phase ^= 1u; }
+  }
 };
 
 __device__ __forceinline__ uint32_t pack_out(float a, float b, bool bf) {
@@ -61,23 +97,25 @@ __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-// 32 bits of the packed stream starting at byte a of `base` (4-byte aligned).
-__device__ __forceinline__ uint32_t bytes_at(const unsigned char* base, int a) {
+// The 64 bits of the packed stream starting at byte a of `base` (4-byte
+// aligned buffer), as two words.
+__device__ __forceinline__ uint2 bits_at(const unsigned char* base, int a) {
   const uint32_t* wp = reinterpret_cast<const uint32_t*>(base) + (a >> 2);
-  return __funnelshift_r(wp[0], wp[1], 8 * (a & 3));
+  const uint32_t w0 = wp[0], w1 = wp[1], w2 = wp[2];
+  const uint32_t sh = 8 * (a & 3);
+  return make_uint2(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh));
 }
 
 // Eight centred codes of width w (uniform mode) as fp16 pairs.
-__device__ __forceinline__ uint4 decode_uniform(const unsigned char* base, int a, int w) {
-  const uint32_t lo = bytes_at(base, a);
+__device__ __forceinline__ uint4 decode_uniform(uint2 b, int w) {
+  const uint32_t lo = b.x;
   const uint32_t sub = 0x64006400u | ((1u << (w - 1)) * 0x10001u);  // 1024 + 2^(w-1), twice
   uint32_t o[4];
   if (w == 8) {
-    const uint32_t hi = bytes_at(base, a + 4);
     o[0] = hsub2_bits(__byte_perm(lo, 0x64646464u, 0x5140), sub);
     o[1] = hsub2_bits(__byte_perm(lo, 0x64646464u, 0x5342), sub);
-    o[2] = hsub2_bits(__byte_perm(hi, 0x64646464u, 0x5140), sub);
-    o[3] = hsub2_bits(__byte_perm(hi, 0x64646464u, 0x5342), sub);
+    o[2] = hsub2_bits(__byte_perm(b.y, 0x64646464u, 0x5140), sub);
+    o[3] = hsub2_bits(__byte_perm(b.y, 0x64646464u, 0x5342), sub);
   } else if (w == 4) {
     const uint32_t L = lo & 0x0F0F0F0Fu, Hh = (lo >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
@@ -97,11 +135,8 @@ __device__ __forceinline__ uint4 decode_uniform(const unsigned char* base, int a
 }
 
 // Eight codebook values (fp16 centroids) for codes of width w.
-__device__ __forceinline__ uint4 decode_codebook(const unsigned char* base, int a, int w,
-                                                 const uint16_t* cbh) {
-  const uint32_t lo = bytes_at(base, a);
-  const uint32_t hi = w > 4 ? bytes_at(base, a + 4) : 0u;
-  const uint64_t bits = (uint64_t)lo | ((uint64_t)hi << 32);
+__device__ __forceinline__ uint4 decode_codebook(uint2 b, int w, const uint16_t* cbh) {
+  const uint64_t bits = (uint64_t)b.x | ((uint64_t)b.y << 32);
   const uint32_t mask = (1u << w) - 1u;
   uint32_t o[4];
 #pragma unroll
@@ -114,196 +149,293 @@ __device__ __forceinline__ uint4 decode_codebook(const unsigned char* base, int 
 }
 
 template <int MODE, bool OUT_BF16>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     fetch_pipe_kernel(const Params p, const PipeArgs t, const __grid_constant__ CUtensorMap omap) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full_bar[kStages], mma_bar[2];
-  __shared__ int4 stage_info[kStages];  // per buffer: row bytes, basis, tokens of its tile
+  __shared__ uint64_t row_full[kMaxRS], row_empty[kMaxRS];
+  __shared__ uint64_t a_full[kMaxAS], a_empty[kMaxAS];
+  __shared__ uint64_t acc_full[kMaxTS], acc_empty[kMaxTS];
+  __shared__ uint64_t b_full[2], b_empty[2], done_bar;
+  __shared__ uint64_t norm_full[kNormRing];  // codebook norms of a tile decoded
+  __shared__ int4 stage_hdr[kMaxRS];  // per row stage: row bytes, tokens, B buffer | first use << 1
+  __shared__ int a_info[kMaxAS];      // per A buffer: B buffer | first use << 1
   __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
+  __shared__ volatile int abort_flag;
 
   const int D = p.D, K = t.K, KC = K / 8, nbox = D / 64;
+  const int RS = t.n_rs, AS = t.n_a, TS = t.n_acc, SS = t.n_stg, NB = t.n_b;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, row = quarter * 32 + lane;
   const int G = gridDim.x;
   const int first = (int)((int64_t)t.total_tiles * blockIdx.x / G);
-  const int last = (int)((int64_t)t.total_tiles * (blockIdx.x + 1) / G);
-  const int m = last - first;
+  const int m = (int)((int64_t)t.total_tiles * (blockIdx.x + 1) / G) - first;
   const int tps = t.tiles_per_slot;
+  const size_t b_bytes = (size_t)D * K * 2;
 
-  unsigned char* stage = smem;                              // 2 x nbox x 16 KB
-  unsigned char* As = stage + 2 * nbox * 16384;             // 2 x [128 x K] fp16
-  unsigned char* Bs = As + 2 * kTile * K * 2;               // [D x K] fp16
-  uint16_t* cbh = reinterpret_cast<uint16_t*>(Bs + D * K * 2);  // [256] fp16 centroids
-  uint32_t* chunk_s = reinterpret_cast<uint32_t*>(cbh + 256);    // [KC <= 32]
-  float* norm_s = reinterpret_cast<float*>(chunk_s + 32);        // 2 x [128] codebook norms
-  unsigned char* cbuf = reinterpret_cast<unsigned char*>(norm_s + 2 * kTile);  // kStages x cbuf
-  const int side_off = t.cbuf - kTile * 2 - 16;
-  const uint32_t sbo = (uint32_t)KC * 128;
-  const uint32_t idesc = idesc_f16(kTile, D, 0);
+  unsigned char* stage = smem;                                  // SS x nbox x 16 KB
+  unsigned char* Bs = stage + SS * nbox * 16384;                // NB x [D x K] fp16
+  unsigned char* rs = Bs + NB * b_bytes;                        // RS x row stage
+  uint16_t* cbh = reinterpret_cast<uint16_t*>(rs + (size_t)RS * t.rs_bytes);  // [256]
+  float* norm_ring = reinterpret_cast<float*>(cbh + 256);       // kNormRing x [128]
+  // a row stage: [0, 128) chunk table, then the packed rows, then the side words
+  const int side_off = t.rs_bytes - (int)(((size_t)kTile * p.side_bytes + 16 + 15) & ~size_t(15));
 
-  if (warp == 0) tmem_alloc(&tmem_base, t.cols);
+  if (warp == kMmaWarp) {
+    tmem_alloc(&tmem_base, t.cols);
+  }
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) mbar_init(&full_bar[i], 1);
-    for (int i = 0; i < 2; ++i) mbar_init(&mma_bar[i], 1);
+    for (int i = 0; i < RS; ++i) { mbar_init(&row_full[i], 1); mbar_init(&row_empty[i], kDecWarps); }
+    for (int i = 0; i < AS; ++i) { mbar_init(&a_full[i], kDecWarps); mbar_init(&a_empty[i], 1); }
+    for (int i = 0; i < TS; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], kEpiWarps); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], 1); }
+    mbar_init(&done_bar, 1);
+    for (int i = 0; i < kNormRing; ++i) mbar_init(&norm_full[i], kDecWarps);
     fence_mbar_init();
     abort_flag = 0;
   }
   if (MODE == KVC_MODE_CODEBOOK)
     for (int j = tid; j < p.cb_levels; j += kThreads)
       cbh[j] = __half_as_ushort(__float2half_rn(p.codebook[j]));
-
-  // tile cursor: (slot, block) of tile `first`, advanced one tile per iteration
-  int d_slot = first / tps, d_blk = first % tps;  // tile being decoded
-  int e_slot = 0, e_blk = 0;                      // tile in the epilogue
-  int f_slot = d_slot, f_blk = d_blk;             // next tile to prefetch
-  // Slot tables for the next tile to prefetch, loaded one prefetch ahead so
-  // their latency hides under an iteration (only thread 0 prefetches).
-  struct SlotInfo { int P, beta; int64_t pay, side; };
-  auto load_info = [&](int slot) {
-    SlotInfo si{0, 0, 0, 0};
-    if (slot < p.n_slots) {
-      si.P = t.slotP[slot];
-      si.beta = p.basis_of[slot];
-      si.pay = p.pay_off[slot];
-      si.side = p.side_off[slot];
-    }
-    return si;
-  };
-  SlotInfo f_info{0, 0, 0, 0};
-  if (tid == 0) f_info = load_info(f_slot);
-  auto prefetch = [&](int bi) {  // tile (f_slot, f_blk) into buffer bi; thread 0
-    const int64_t t0 = (int64_t)f_blk * kTile;
-    const int n = (int)min((int64_t)kTile, t.S - t0);
-    const uint32_t cb = (uint32_t)((n * f_info.P + 15) & ~15);
-    const uint32_t sbb = (uint32_t)((n * p.side_bytes + 15) & ~15);
-    unsigned char* dst = cbuf + bi * t.cbuf;
-    stage_info[bi] = make_int4(f_info.P, f_info.beta, n, 0);
-    mbar_arrive_expect_tx(&full_bar[bi], cb + sbb);
-    if (cb) bulk_load(dst, p.store + f_info.pay + t0 * f_info.P, cb, &full_bar[bi]);
-    if (sbb) bulk_load(dst + side_off, p.store + f_info.side + t0 * p.side_bytes, sbb, &full_bar[bi]);
-  };
-  auto advance_f = [&]() {
-    if (++f_blk == tps) {
-      f_blk = 0;
-      ++f_slot;
-      if (tid == 0) f_info = load_info(f_slot);
-    }
-  };
-  for (int j = 0; j < kStages - 1 && j < m; ++j) {
-    if (tid == 0) prefetch(j);
-    advance_f();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t taddr0 = tmem_base;
 
-  int cur_beta = -1;
-  for (int it = 0; it <= m; ++it) {
-    const int buf = it & 1, pb = buf ^ 1;
-    // ---------------- phase A: decode of tile it, then the epilogue of tile it-1
-    // (decoding first gives MMA(it-1), issued just before, time to finish)
-    if (it < m) {
-      const int stg_in = it % kStages;
-      const int4 info = stage_info[stg_in];  // written with the prefetch (barriers since)
-      const int P = info.x, beta = info.y, n = info.z;
-      if (beta != cur_beta) {
-        // MMA(it-1) is the last reader of B
-        if (it >= 1 && !mbar_wait_bounded(&mma_bar[pb], ((it - 1) >> 1) & 1, kWaitNs))
-          abort_flag = 1;
-        const uint4* bsrc = reinterpret_cast<const uint4*>(t.B + (size_t)beta * D * K);
-        for (int i = tid; i < D * K * 2 / 16; i += kThreads)
-          reinterpret_cast<uint4*>(Bs)[i] = bsrc[i];
-        if (tid < KC) chunk_s[tid] = t.chunks[(size_t)beta * KC + tid];
-        cur_beta = beta;
-        __syncthreads();  // chunk_s before decode (uniform branch: cur_beta is CTA-wide)
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int slot = first / tps, blk = first % tps;
+      // the next slot's tables are read one slot ahead, off the critical path
+      auto info_of = [&](int sl, int& P, int& beta, int64_t& pay, int64_t& side) {
+        P = 0; beta = 0; pay = 0; side = 0;
+        if (sl < p.n_slots) { P = t.slotP[sl]; beta = p.basis_of[sl]; pay = p.pay_off[sl]; side = p.side_off[sl]; }
+      };
+      int P, beta, nP, nbeta;
+      int64_t pay, side, npay, nside;
+      info_of(slot, P, beta, pay, side);
+      info_of(slot + 1, nP, nbeta, npay, nside);
+      int cur_beta = -1, bslot = NB - 1;
+      uint32_t bload[2] = {0u, 0u};
+      int issued = 0;
+      Ring rr(RS);
+      for (int i = 0; i < m; ++i, rr.next()) {
+        const int s = rr.slot;
+        // the decode of tile i - RS released this stage
+        if (i >= RS && !mbar_wait_bounded(&row_empty[s], rr.phase ^ 1u, kWaitNs)) { abort_flag = 1; break; }
+        int first_use = 0;
+        if (beta != cur_beta) {
+          bslot = NB == 2 ? bslot ^ 1 : 0;
+          if (bload[bslot] > 0 &&
+              !mbar_wait_bounded(&b_empty[bslot], (bload[bslot] - 1) & 1, kWaitNs)) { abort_flag = 1; break; }
+          mbar_arrive_expect_tx(&b_full[bslot], (uint32_t)b_bytes);
+          bulk_load(Bs + bslot * b_bytes, t.B + (size_t)beta * D * K, (uint32_t)b_bytes, &b_full[bslot]);
+          ++bload[bslot];
+          cur_beta = beta;
+          first_use = 1;
+        }
+        const int64_t t0 = (int64_t)blk * kTile;
+        const int n = (int)min((int64_t)kTile, t.S - t0);
+        const uint32_t cb = (uint32_t)((n * P + 15) & ~15);
+        const uint32_t sbb = (uint32_t)((n * p.side_bytes + 15) & ~15);
+        unsigned char* dst = rs + (size_t)s * t.rs_bytes;
+        stage_hdr[s] = make_int4(P, n, bslot | (first_use << 1), 0);
+        mbar_arrive_expect_tx(&row_full[s], 128u + cb + sbb);
+        bulk_load(dst, t.chunks + (size_t)beta * 32, 128u, &row_full[s]);
+        if (cb) bulk_load(dst + 128, p.store + pay + t0 * P, cb, &row_full[s]);
+        if (sbb) bulk_load(dst + side_off, p.store + side + t0 * p.side_bytes, sbb, &row_full[s]);
+        ++issued;
+        if (++blk == tps) {
+          blk = 0;
+          ++slot;
+          P = nP; beta = nbeta; pay = npay; side = nside;
+          info_of(slot + 1, nP, nbeta, npay, nside);
+        }
       }
-      if (!mbar_wait_bounded(&full_bar[stg_in], (it / kStages) & 1, kWaitNs)) abort_flag = 1;
-      const unsigned char* rows = cbuf + stg_in * t.cbuf;
-      unsigned char* A = As + buf * kTile * K * 2;
-      for (int item = tid; item < kTile * KC; item += kThreads) {
-        const int tt = item & (kTile - 1), c = item >> 7;
-        const uint32_t ent = chunk_s[c];
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (tt < n) {
-          if (ent >> 31) {
-            const int a = tt * P + (int)(ent & 0xffffu), w = (int)((ent >> 16) & 0xfu);
-            v = MODE == KVC_MODE_UNIFORM ? decode_uniform(rows, a, w)
-                                         : decode_codebook(rows, a, w, cbh);
-          } else if (ent >> 30) {
-            v.x = 0x3C003C00u;  // (1, 1): the two bias columns of B
+      // copies still in flight (after a time-out) land before the CTA exits
+      for (int j = max(0, issued - RS); j < issued; ++j)
+        mbar_wait_bounded(&row_full[j % RS], (j / RS) & 1, kWaitNs);
+      for (int b2 = 0; b2 < 2; ++b2)
+        if (bload[b2]) mbar_wait_bounded(&b_full[b2], (bload[b2] - 1) & 1, kWaitNs);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sbo = (uint32_t)KC * 128;
+      const uint32_t idesc = idesc_f16(kTile, D, 0);
+      uint32_t buse[2] = {0u, 0u};
+      Ring ra(AS), rt(TS);
+      for (int i = 0; i < m; ++i, ra.next(), rt.next()) {
+        const int a = ra.slot, acc = rt.slot;
+        if (!mbar_wait_bounded(&a_full[a], ra.phase, kWaitNs)) { abort_flag = 1; break; }
+        const int info = a_info[a], bs = info & 1;
+        if (info & 2) {  // first tile on a newly loaded B: the other buffer is free when
+          if (i > 0) umma_commit(&b_empty[NB == 2 ? bs ^ 1 : 0]);  // the MMAs issued so far finish
+          if (!mbar_wait_bounded(&b_full[bs], buse[bs] & 1, kWaitNs)) { abort_flag = 1; break; }
+          ++buse[bs];
+        }
+        // the epilogue of tile i - TS released this accumulator
+        if (i >= TS && !mbar_wait_bounded(&acc_empty[acc], rt.phase ^ 1u, kWaitNs)) { abort_flag = 1; break; }
+        tc_fence_after();
+        const uint32_t a0 = taddr0 + t.a_col0 + a * t.a_cols, b0 = smem_u32(Bs + bs * b_bytes);
+        for (int ks = 0; ks < K / 16; ++ks)  // 16 fp16 of K = 8 TMEM columns of A
+          umma_f16_tmem_a(taddr0 + acc * D, a0 + ks * 8,
+                          desc_kmajor_noswizzle(b0 + ks * 256, 128, sbo), idesc, ks > 0 ? 1u : 0u);
+        umma_commit(&acc_full[acc]);
+        umma_commit(&a_empty[a]);
+      }
+      umma_commit(&done_bar);  // TMEM is released only after every MMA has finished
+      mbar_wait_bounded(&done_bar, 0, kWaitNs);
+    }
+  } else if (warp >= kEpiWarps) {
+    // ------------------------------------------------------------ decoders
+    // Warp 8 + j decodes tokens 32 (j % 4) .. of chunks j / 4, j / 4 + 2, ...:
+    // its tokens are the TMEM lanes its warp may access.  tcgen05.st is
+    // warp-collective, so a warp leaves the loop only as a whole.
+    const int dtid = tid - kEpiThreads;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int tt = dtid & (kTile - 1), c0 = dtid >> 7;
+    Ring rr(RS), ra(AS), rn(kNormRing);
+    for (int i = 0; i < m; ++i, rr.next(), ra.next(), rn.next()) {
+      const int s = rr.slot, a = ra.slot;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&row_full[s], rr.phase, kWaitNs))) {
+        abort_flag = 1;
+        break;
+      }
+      // A buffer a was last read by MMA(i - AS)
+      if (i >= AS &&
+          !__all_sync(0xffffffffu, mbar_wait_bounded(&a_empty[a], ra.phase ^ 1u, kWaitNs))) {
+        abort_flag = 1;
+        break;
+      }
+      const int4 hdr = stage_hdr[s];
+      const int P = hdr.x, n = hdr.y;
+      const unsigned char* st_base = rs + (size_t)s * t.rs_bytes;
+      const uint32_t* chunk = reinterpret_cast<const uint32_t*>(st_base);
+      const unsigned char* rows = st_base + 128;
+      // thread: token tt, chunks c0, c0 + 2, ...; four chunks' loads are
+      // issued before their arithmetic
+      const bool live = tt < n;
+      const int rowoff = tt * P;
+      const uint32_t a_tm = taddr0 + lane_base + t.a_col0 + a * t.a_cols;
+      for (int cb = c0; cb < KC; cb += 8) {
+        uint32_t ent[4];
+        uint2 bits[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = cb + 2 * u;
+          ent[u] = c < KC ? chunk[c] : 0u;
+          bits[u] = (ent[u] >> 31) && live ? bits_at(rows, rowoff + (int)(ent[u] & 0xffffu))
+                                           : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = cb + 2 * u;
+          if (c < KC) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (live) {
+              const int w = (int)((ent[u] >> 16) & 0xfu);
+              if (ent[u] >> 31)
+                v = MODE == KVC_MODE_UNIFORM ? decode_uniform(bits[u], w)
+                                             : decode_codebook(bits[u], w, cbh);
+              else if (ent[u] >> 30)
+                v.x = 0x3C003C00u;  // (1, 1): the two bias columns of B
+            }
+            tmem_st4(a_tm + c * 4, v);  // chunk c: K positions 8c .. 8c+7
           }
         }
-        *reinterpret_cast<uint4*>(A + (tt >> 3) * sbo + c * 128 + (tt & 7) * 16) = v;
-        if (MODE == KVC_MODE_CODEBOOK && c == 0)  // kept until this tile's epilogue
-          norm_s[buf * kTile + tt] =
-              tt < n ? __half2float(__ushort_as_half(
-                           reinterpret_cast<const uint16_t*>(rows + side_off)[tt]))
-                     : 0.f;
+      }
+      // Norm ring entry i % kNormRing is next written by the decode of tile
+      // i + kNormRing, which waits for MMA(i + kNormRing - AS), which waited
+      // for the epilogue of tile i + kNormRing - AS - TS >= i + 1 to release
+      // its accumulator, after the epilogue of tile i had read its norms; so
+      // the ring's barrier phases are never more than one apart.
+      if (MODE == KVC_MODE_CODEBOOK && c0 == 0)
+        norm_ring[rn.slot * kTile + tt] =
+            live ? __half2float(__ushort_as_half(
+                       reinterpret_cast<const uint16_t*>(st_base + side_off)[tt]))
+                 : 0.f;
+      if (dtid == 0) a_info[a] = hdr.z;
+      tmem_wait_st();
+      tc_fence_before();  // A is read by the MMA thread's tcgen05.mma
+      __syncwarp();
+      if (lane == 0) {
+        if (MODE == KVC_MODE_CODEBOOK) mbar_arrive(&norm_full[rn.slot]);
+        mbar_arrive(&a_full[a]);
+        mbar_arrive(&row_empty[s]);
       }
     }
-    if (it >= 1) {
-      if (!mbar_wait_bounded(&mma_bar[pb], ((it - 1) >> 1) & 1, kWaitNs)) abort_flag = 1;
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // Warp w reads TMEM lanes 32 (w % 4) .. (its tokens) and half w / 4 of the
+    // columns.  When each half is a whole number of 64-column output boxes
+    // (D = 128, 256) the two halves run as independent groups of four warps,
+    // each with its own barrier, staging boxes and TMA store; otherwise the
+    // eight warps form one group.
+    const int quarter = warp & 3, half = warp >> 2, row = quarter * 32 + lane;
+    const int nblk = D / 64;  // 32-column blocks per half
+    const bool split = (nbox & 1) == 0;
+    const int gthreads = split ? kEpiThreads / 2 : kEpiThreads;
+    const int bar_id = kEpiBar + (split ? half : 0);
+    const bool issuer = split ? (tid & (kEpiThreads / 2 - 1)) == 0 : tid == 0;
+    const int box0 = split ? half * (nbox / 2) : 0, nbox_g = split ? nbox / 2 : nbox;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    int slot = first / tps, blk = first % tps;
+    Ring rt(TS), rs_(SS), rn(kNormRing);
+    for (int i = 0; i < m; ++i, rt.next(), rs_.next(), rn.next()) {
+      const int acc = rt.slot;
+      bool late = !mbar_wait_bounded(&acc_full[acc], rt.phase, kWaitNs);
+      if (MODE == KVC_MODE_CODEBOOK)
+        late = late || !mbar_wait_bounded(&norm_full[rn.slot], rn.phase, kWaitNs);
+      if (issuer) bulk_wait_read_n(SS - 1);  // this group's store of tile i-SS has left staging
+      if (named_bar_or(bar_id, gthreads, late || abort_flag)) { abort_flag = 1; break; }
       tc_fence_after();
-      const float nrm = MODE == KVC_MODE_CODEBOOK ? norm_s[pb * kTile + row] : 1.f;
-      const uint32_t lane_addr = taddr0 + pb * D + ((uint32_t)(quarter * 32) << 16);
-      unsigned char* stg = stage + pb * nbox * 16384;
-      for (int c32 = warp >> 2; c32 < D / 32; c32 += kThreads / 128) {
-        uint32_t r[32];
-        tmem_ld32(lane_addr + c32 * 32, r);
+      const float nrm = MODE == KVC_MODE_CODEBOOK ? norm_ring[rn.slot * kTile + row] : 1.f;
+      const uint32_t lane_addr = taddr0 + acc * D + lane_off;
+      unsigned char* stg = stage + rs_.slot * nbox * 16384;
+      for (int j = 0; j < nblk; j += 2) {  // two 32-column loads in flight
+        const int c32a = half * nblk + j;
+        const bool two = j + 1 < nblk;
+        uint32_t r[2][32];
+        tmem_ld32(lane_addr + c32a * 32, r[0]);
+        if (two) tmem_ld32(lane_addr + (c32a + 1) * 32, r[1]);
         tmem_wait_ld();
-        unsigned char* dst = stg + (c32 >> 1) * 16384 + row * 128;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float x[8];
+        for (int h = 0; h < 2; ++h) {
+          if (h == 1 && !two) break;
+          const int c32 = c32a + h;
+          unsigned char* dst = stg + (c32 >> 1) * 16384 + row * 128;
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            x[e] = MODE == KVC_MODE_CODEBOOK ? __uint_as_float(r[q * 8 + e]) * nrm
-                                             : __uint_as_float(r[q * 8 + e]);
-          const int c16 = (c32 & 1) * 4 + q;
-          *reinterpret_cast<uint4*>(dst + ((c16 ^ (row & 7)) << 4)) =
-              make_uint4(pack_out(x[0], x[1], OUT_BF16), pack_out(x[2], x[3], OUT_BF16),
-                         pack_out(x[4], x[5], OUT_BF16), pack_out(x[6], x[7], OUT_BF16));
+          for (int q = 0; q < 4; ++q) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              x[e] = MODE == KVC_MODE_CODEBOOK ? __uint_as_float(r[h][q * 8 + e]) * nrm
+                                               : __uint_as_float(r[h][q * 8 + e]);
+            const int c16 = (c32 & 1) * 4 + q;
+            *reinterpret_cast<uint4*>(dst + ((c16 ^ (row & 7)) << 4)) =
+                make_uint4(pack_out(x[0], x[1], OUT_BF16), pack_out(x[2], x[3], OUT_BF16),
+                           pack_out(x[4], x[5], OUT_BF16), pack_out(x[6], x[7], OUT_BF16));
+          }
         }
       }
-    }
-    tc_fence_before();
-    fence_proxy_async_smem();
-    if (tid == 0) bulk_wait_read0();  // the store of tile it-2 has left staging buf
-    __syncthreads();
-    if (abort_flag) break;
-    // ---------------- phase B: one thread issues the asynchronous work
-    if (tid == 0) {
-      tc_fence_after();
-      if (it < m) {
-        const uint32_t a0 = smem_u32(As + buf * kTile * K * 2), b0 = smem_u32(Bs);
-        for (int ks = 0; ks < K / 16; ++ks)
-          umma_f16(taddr0 + buf * D, desc_kmajor_noswizzle(a0 + ks * 256, 128, sbo),
-                   desc_kmajor_noswizzle(b0 + ks * 256, 128, sbo), idesc, ks > 0 ? 1u : 0u);
-        umma_commit(&mma_bar[buf]);
-      }
-      if (it >= 1) {  // one head per slot: the slot is the tensor map's (b, h) index
-        unsigned char* stg = stage + pb * nbox * 16384;
-        for (int bx = 0; bx < nbox; ++bx)
-          tma_store_3d(&omap, stg + bx * 16384, bx * 64, e_blk * kTile, e_slot);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      fence_proxy_async_smem();  // staging is read by the TMA store (async proxy)
+      named_bar_sync(bar_id, gthreads);
+      if (issuer) {  // one head per slot: the slot is the tensor map's (b, h) index
+        for (int bx = box0; bx < box0 + nbox_g; ++bx)
+          tma_store_3d(&omap, stg + bx * 16384, bx * 64, blk * kTile, slot);
         bulk_commit();
       }
-      if (it + kStages - 1 < m)  // its buffer held tile it-1, decoded last iteration
-        prefetch((it + kStages - 1) % kStages);
+      if (++blk == tps) { blk = 0; ++slot; }
     }
-    if (it + kStages - 1 < m) advance_f();
-    // advance the cursors
-    e_slot = d_slot;
-    e_blk = d_blk;
-    if (++d_blk == tps) { d_blk = 0; ++d_slot; }
+    if (issuer) bulk_wait_read0();  // staging is read before the CTA exits
   }
-  if (abort_flag && tid == 0) atomicCAS(p.err, 0, kErrTimeout);
-  if (tid == 0) bulk_wait_read0();  // the stores may finish after the CTA: staging is read
   __syncthreads();
-  if (warp == 0) {
+  if (abort_flag && tid == 0) atomicCAS(p.err, 0, kErrTimeout);
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(taddr0, t.cols);
   }
@@ -320,6 +452,43 @@ PipeKernel pipe_kernel_for(int mode, int out_dtype) {
 
 }  // namespace
 
+size_t fetch_pipe_smem(int D, int K, int side_bytes, int pmax, int n_bases, FetchPipeShape* sh) {
+  const size_t rows = ((size_t)kTile * pmax + 16 + 15) & ~size_t(15);
+  const size_t side = ((size_t)kTile * side_bytes + 16 + 15) & ~size_t(15);
+  FetchPipeShape z;
+  z.rs_bytes = (int)(128 + rows + side);
+  // TMEM (512 columns): accumulators of D columns, then A buffers of K/2
+  // columns (two fp16 per column) rounded up to 32
+  z.a_cols = (K / 2 + 31) / 32 * 32;
+  z.n_a = 2;
+  z.n_acc = std::min(kMaxTS, (512 - z.n_a * z.a_cols) / D);
+  if (z.n_acc < 1) return 0;
+  if (z.n_acc * D + (z.n_a + 1) * z.a_cols <= 512) z.n_a = kMaxAS;
+  z.a_col0 = z.n_acc * D;
+  z.n_b = n_bases > 1 ? 2 : 1;
+  z.n_stg = 2;
+  z.n_rs = 3;
+  auto total = [&](const FetchPipeShape& q) {
+    return 1024 + (size_t)q.n_stg * (D / 64) * 16384 + (size_t)q.n_b * D * K * 2 +
+           (size_t)q.n_rs * q.rs_bytes + 256 * 2 + (size_t)kNormRing * kTile * 4;
+  };
+  const size_t limit = 226 * 1024;
+  if (total(z) > limit) return 0;
+  // grow, in order of benefit: staging (stores in flight), then row stages
+  auto grow = [&](int FetchPipeShape::*f, int to) {
+    while (z.*f < to) {
+      FetchPipeShape q = z;
+      ++(q.*f);
+      if (total(q) > limit) break;
+      z = q;
+    }
+  };
+  grow(&FetchPipeShape::n_stg, kMaxSS);
+  grow(&FetchPipeShape::n_rs, kMaxRS);
+  *sh = z;
+  return total(z);
+}
+
 cudaError_t launch_fetch_pipe(const TcPlan& plan, const Params& p, const FetchArgs& f,
                               const CUtensorMap& map, cudaStream_t s, int* nk) {
   PipeKernel k = pipe_kernel_for(p.mode, p.out_dtype);
@@ -328,8 +497,10 @@ cudaError_t launch_fetch_pipe(const TcPlan& plan, const Params& p, const FetchAr
   if (e != cudaSuccess) return e;
   const int tiles = (int)((f.S + kTile - 1) / kTile);
   const int total = tiles * p.n_slots;
-  const int grid = std::min(total, sm_count() * plan.pipe_ctas_per_sm);
-  const PipeArgs t{plan.fetchB, plan.chunks, plan.slotP, plan.fetch_K, plan.pipe_cols, plan.pipe_cbuf,
+  const int grid = std::min(total, sm_count());
+  const FetchPipeShape& sh = plan.pipe;
+  const PipeArgs t{plan.fetchB, plan.chunks32, plan.slotP, plan.fetch_K, plan.pipe_cols,
+                   sh.n_acc, sh.n_a, sh.n_rs, sh.a_col0, sh.a_cols, sh.n_stg, sh.n_b, sh.rs_bytes,
                    f.S, tiles, total};
   k<<<(unsigned)grid, kThreads, plan.pipe_smem, s>>>(p, t, map);
   ++*nk;

@@ -898,19 +898,21 @@ kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t
   plan.fetch_cols = cols;
   plan.fetch_smem = smem;
   plan.fetch_ready = encoder() != nullptr;
-  if (d.heads_per_group == 1 && 2 * cols <= 512) {
-    const int cbuf = (int)(align_up((size_t)kTile * pmax + 16, 16) +
-                           align_up((size_t)kTile * g.side_bytes + 16, 16));
-    size_t ps = 1024 + (size_t)2 * (D / 64) * 16384 + (size_t)2 * kTile * K * 2 + (size_t)D * K * 2 +
-                256 * 2 + 32 * 4 + 2 * kTile * 4 + (size_t)4 * cbuf;
-    const int by_tmem = 512 / (2 * cols);
-    ps = std::max(ps, (size_t)(228 * 1024) / (by_tmem + 1) + 1024);
-    if (ps <= 226 * 1024) {
+  if (d.heads_per_group == 1 && K <= 256) {
+    // the chunk table again, padded to 32 entries: one 128-byte bulk copy per tile
+    std::vector<uint32_t> c32((size_t)nb * 32, 0u);
+    for (int b = 0; b < nb; ++b)
+      for (int c = 0; c < K / 8; ++c) c32[(size_t)b * 32 + c] = chunks[(size_t)b * (K / 8) + c];
+    plan.oChunks32 = put(image, c32.data(), c32.size());
+    FetchPipeShape sh;
+    const size_t ps = fetch_pipe_smem(D, K, g.side_bytes, pmax, nb, &sh);
+    if (ps > 0) {
       plan.pipe_ready = plan.fetch_ready;
-      plan.pipe_cols = 2 * cols;
-      plan.pipe_cbuf = cbuf;
+      int cols_alloc = 32;  // TMEM allocations are powers of two
+      while (cols_alloc < sh.a_col0 + sh.n_a * sh.a_cols) cols_alloc *= 2;
+      plan.pipe_cols = cols_alloc;
+      plan.pipe = sh;
       plan.pipe_smem = ps;
-      plan.pipe_ctas_per_sm = std::max(1, std::min(by_tmem, (int)((228 * 1024) / ps)));
     }
   }
   return KVC_OK;
@@ -922,6 +924,7 @@ void tc_bind(TcPlan& plan, uint8_t* base) {
     plan.bias = reinterpret_cast<const float*>(base + plan.oBias);
     plan.chunks = reinterpret_cast<const uint32_t*>(base + plan.oChunks);
     plan.slotP = reinterpret_cast<const int32_t*>(base + plan.oSlotP);
+    if (plan.pipe_ready) plan.chunks32 = reinterpret_cast<const uint32_t*>(base + plan.oChunks32);
   }
   if (plan.append_ready) {
     plan.appB = reinterpret_cast<const uint16_t*>(base + plan.oAppB);

@@ -11,6 +11,18 @@
 
 namespace kvc {
 
+// Ring sizes of the warp-specialised fetch (kvc_fetch_pipe.cu).
+struct FetchPipeShape {
+  int n_acc = 0;     // TMEM accumulators of D columns
+  int n_a = 0;       // A operand buffers (in TMEM after the accumulators)
+  int a_col0 = 0;    // TMEM column of the first A buffer
+  int a_cols = 0;    // TMEM columns of one A buffer
+  int n_rs = 0;      // row stages (packed rows, side words, chunk table)
+  int n_stg = 0;     // output staging buffers
+  int n_b = 0;       // B buffers
+  int rs_bytes = 0;  // bytes of one row stage
+};
+
 // Tables the tensor-core kernels need, appended to the layer's parameter
 // block by tc_prepare (as offsets) and turned into device pointers by tc_bind.
 struct TcPlan {
@@ -26,11 +38,12 @@ struct TcPlan {
                                      // 1 << 30 marks the chunk of ones (bias columns)
   bool bias_folded = false;          // B carries the bias (uniform mode)
   const int32_t* slotP = nullptr;    // [n_slots] packed row bytes of each slot
-  // pipelined persistent fetch (one head per slot)
+  size_t oChunks32 = 0;
+  const uint32_t* chunks32 = nullptr;  // [nb][32]: the chunk table padded to 128 bytes
+  // warp-specialised persistent fetch (one head per slot), one CTA per SM
   bool pipe_ready = false;
-  int pipe_cols = 0;           // two accumulators
-  int pipe_cbuf = 0;           // bytes of one packed-row (+ side) buffer
-  int pipe_ctas_per_sm = 0;
+  int pipe_cols = 0;           // TMEM columns: pipe_acc accumulators of D columns
+  FetchPipeShape pipe;
   size_t pipe_smem = 0;
 
   // append: z = x (V_hi + V_rest) * 2^-scale_exp - mean V, the fp32 basis split
@@ -60,7 +73,10 @@ cudaError_t launch_append_tc(const TcPlan& plan, const Params& p, const AppendAr
 cudaError_t launch_fetch_tc(const TcPlan& plan, const Params& p, const FetchArgs& f,
                             cudaStream_t s, int* nk);
 
-// Pipelined persistent fetch (kvc_fetch_pipe.cu); `map` is the output tensor map.
+// Warp-specialised persistent fetch (kvc_fetch_pipe.cu); `map` is the output
+// tensor map.  fetch_pipe_smem sizes its rings for D, K, the side bytes, the
+// largest packed row and the number of bases; 0 when they do not fit.
+size_t fetch_pipe_smem(int D, int K, int side_bytes, int pmax, int n_bases, FetchPipeShape* sh);
 cudaError_t launch_fetch_pipe(const TcPlan& plan, const Params& p, const FetchArgs& f,
                               const CUtensorMap& map, cudaStream_t s, int* nk);
 int sm_count();
