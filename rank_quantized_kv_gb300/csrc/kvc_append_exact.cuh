@@ -1,0 +1,133 @@
+// Exact re-decision of quantiser outputs near a rounding boundary, shared by
+// the tensor-core append kernels (sm_103a).
+//
+// The tensor-core projection z32 carries an accumulation error bounded by
+//   |z32 - z| <= gamma * ||x|| * ||V_k|| + 2^-21 (|z| + |mean . V_k|)
+// (gamma from a model of aligned, truncated fp32 accumulation; see the host
+// plan).  Codes whose fast-path value lies within that bound (through the
+// quantiser's own roundings) of a rounding boundary are queued and re-decided
+// here by one warp with a compensated fp32 dot product (error ~1e-13
+// relative) finished in double precision.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kvc_internal.h"
+
+namespace kvc {
+namespace {
+
+__device__ __forceinline__ void set_err(int* err, int code) { atomicCAS(err, 0, code); }
+
+// True when every value in [lo, hi] rounds to the same fp16.
+__device__ __forceinline__ bool same_half(float lo, float hi) {
+  return __half_as_ushort(__float2half_rn(lo)) == __half_as_ushort(__float2half_rn(hi));
+}
+
+constexpr int kQueue = 512;
+constexpr uint32_t kNormEntry = 0xFFFFu;
+
+struct AppendTc {
+  const uint16_t* B;    // [nb][3][rpad][D]
+  const double* c64;    // [nb][r]
+  int rpad, cols;
+  float inv_scale, gamma;
+};
+
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// x_t . w with x_t a row of the swizzled x tile (w == nullptr: x_t . x_t),
+// compensated fp32 (TwoProd / TwoSum) finished in double.  WARP: the 32 lanes
+// split the row and the result is on every lane; else one thread does it all.
+template <bool BF16, bool WARP>
+__device__ double dot2_row(const unsigned char* xs, int t, int D, const float* w, int lane) {
+  float S = 0.f, C = 0.f;
+  for (int i = WARP ? lane : 0; i < D; i += WARP ? 32 : 1) {
+    const unsigned char* src =
+        xs + (i >> 6) * 16384 + t * 128 + ((((i & 63) >> 3) ^ (t & 7)) << 4) + (i & 7) * 2;
+    const uint16_t raw = *reinterpret_cast<const uint16_t*>(src);
+    const float xv = BF16 ? __bfloat162float(__ushort_as_bfloat16(raw))
+                          : __half2float(__ushort_as_half(raw));
+    const float wv = w ? w[i] : xv;
+    const float pr = xv * wv;
+    const float pe = fmaf(xv, wv, -pr);
+    float s, e;
+    two_sum(S, pr, s, e);
+    S = s;
+    C += pe + e;
+  }
+  if (WARP) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float So = __shfl_xor_sync(0xffffffffu, S, o);
+      const float Co = __shfl_xor_sync(0xffffffffu, C, o);
+      float s, e;
+      two_sum(S, So, s, e);
+      S = s;
+      C = C + Co + e;
+    }
+  }
+  return (double)S + (double)C;
+}
+
+// Decide code k of token tt exactly (or, k == kNormEntry, the fp16 norm of a
+// codebook token).  Lane 0 (or the lone thread) writes the result.
+// The largest |u_fast - u_exact| / bound seen (float bits; all non-negative)
+// is kept in counters[3]: evidence of how much margin the bound carries.
+__device__ __forceinline__ void note_ratio(const Params& p, double uf, double u, float tau) {
+  if (tau > 0.f) {
+    const float ratio = (float)(fabs(uf - u) / (double)tau);
+    atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(ratio));
+  }
+}
+
+template <int MODE, bool BF16, bool WARP>
+__device__ void refine_entry(const Params& p, const AppendTc& t, int beta, const unsigned char* xs,
+                             unsigned char* codes_s, __half* side_s, unsigned* nside, int tt, int k,
+                             int lane, float uf = 0.f, float tau = 0.f) {
+  const int D = p.D, r = p.r;
+  const float* Vt = p.Vt + (size_t)beta * r * D;
+  if (MODE == KVC_MODE_UNIFORM) {
+    const double z64 = dot2_row<BF16, WARP>(xs, tt, D, Vt + (size_t)k * D, lane) -
+                       t.c64[(size_t)beta * r + k];
+    if (lane == 0) {
+      const int qmax = (1 << p.bits[(size_t)beta * r + k]) - 1;
+      const double u64 =
+          (z64 - (double)p.lo[(size_t)beta * r + k]) / (double)p.step[(size_t)beta * r + k];
+      codes_s[tt * r + k] = (uint8_t)(int)fmin(fmax(rint(u64), 0.0), (double)qmax);
+      note_ratio(p, uf, u64, tau);
+    }
+  } else {
+    const double n64 = sqrt(dot2_row<BF16, WARP>(xs, tt, D, nullptr, lane));
+    if (k == (int)kNormEntry) {
+      if (lane == 0) {
+        side_s[tt] = __double2half(n64);
+        atomicAdd(nside, 1u);
+      }
+    } else {
+      const double z64 = dot2_row<BF16, WARP>(xs, tt, D, Vt + (size_t)k * D, lane);
+      if (lane == 0) {
+        const double u64 = n64 > 0.0 ? z64 / n64 : 0.0;
+        note_ratio(p, uf, u64, tau);
+        double best = fabs(u64 - (double)p.codebook[0]);
+        int bi = 0;
+        for (int j = 1; j < p.cb_levels; ++j) {
+          const double d = fabs(u64 - (double)p.codebook[j]);
+          if (d < best) {
+            best = d;
+            bi = j;
+          }
+        }
+        codes_s[tt * r + k] = (uint8_t)bi;
+      }
+    }
+  }
+}
+
+}  // namespace
+}  // namespace kvc

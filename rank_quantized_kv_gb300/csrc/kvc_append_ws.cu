@@ -1,0 +1,648 @@
+// Warp-specialised persistent append for one head per slot (uniform and
+// codebook modes): z = x V (tensor cores), quantise, pack, write the rows.
+//
+// One CTA per SM walks a contiguous run of 128-token tiles.  Three roles hand
+// tiles on through mbarrier rings:
+//   producer (one thread)  TMA-loads each x tile (128-byte swizzle, the A
+//                          operand as is) together with its basis' quantiser
+//                          table into a ring of x stages, and the basis B into
+//                          one of (up to) two B buffers when the basis changes;
+//   MMA (one thread)       one chain of tcgen05.mma per tile with the basis'
+//                          exact 16-bit pieces stacked along N, so x is read
+//                          once: accumulator columns [piece][component];
+//   quantiser (16 warps)   warp w owns TMEM lanes 32 (w % 4) .. (its tokens)
+//                          and a quarter w / 4 of the components: ||x||, the
+//                          fast-path codes z = hi + (mid + lo), the exact
+//                          re-decision of codes near a boundary (one warp per
+//                          queued code, V^T from shared memory), bit-packing
+//                          and a coalesced copy of the packed rows to the store.
+// Codes are staged at chunk-aligned positions: every packed segment starts on
+// an 8-code chunk, and 8 codes of width w pack into exactly w bytes, so each
+// (token, chunk) packs on its own from one 64-bit load.
+// The x stage is released once the rows are packed (the re-decision reads x,
+// the packing the stage's table), the accumulator right after the quantiser
+// has read it.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "kvc_append_exact.cuh"
+#include "kvc_sm100.cuh"
+#include "kvc_tc.h"
+
+namespace kvc {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int kTile = 128;
+constexpr int kQWarps = 16;  // quantiser warps 0..15
+constexpr int kQThreads = kQWarps * 32;
+constexpr int kProdWarp = kQWarps;
+constexpr int kMmaWarp = kQWarps + 1;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kMaxXS = 4, kMaxTS = 4;
+constexpr int kQBar = 1;  // named barrier of the quantiser warps
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+struct AppendWsArgs {
+  const uint16_t* B;        // [nb][pieces * rpad][D] UMMA no-swizzle K-major
+  const double* c64;        // [nb][r] mean . V_k
+  const unsigned char* tab; // [nb][tab_bytes] quantiser table of each basis
+  int rpad, npieces, acc_stride, cols;  // accumulator columns and stride; TMEM allocated
+  int n_acc, n_x, n_b;      // accumulators, x stages, B buffers
+  int x_stage, tab_bytes, pmax;
+  int ks;                   // bytes per token row of the code staging (chunk-aligned)
+  int vt_smem;              // V^T of the basis kept in shared memory beside B
+  float inv_scale, gamma;
+  int tiles_per_slot, total_tiles;
+};
+
+// Per-basis quantiser table (host layout in append_ws_table), per component:
+//   q4    uniform fast path u = fma(z, A, Bc), bound tau = fma(T1, ||x||, T2)
+//         (A = 2^-s / step, Bc = -(mean . V_k + lo) / step; see the plan);
+//   c64   mean . V_k, inv64 1/step (double), lo, vn = ||V_k|| (rounded up);
+//   qk    qmax | chunk-aligned position << 16 (0xFFFF: not kept);
+// then the pack chunks.
+struct Tab {
+  const float4* q4;
+  const double *c64, *inv64;
+  const float *lo, *vn;
+  const uint32_t* qk;
+  const uint32_t* chunk;  // [32]: first byte | width << 16 | (codes - 1) << 20 | valid << 31
+  __device__ Tab(const unsigned char* base, int rpad)
+      : q4(reinterpret_cast<const float4*>(base)),
+        c64(reinterpret_cast<const double*>(q4 + rpad)),
+        inv64(c64 + rpad),
+        lo(reinterpret_cast<const float*>(inv64 + rpad)),
+        vn(lo + rpad),
+        qk(reinterpret_cast<const uint32_t*>(vn + rpad)),
+        chunk(qk + rpad) {}
+};
+
+struct XHdr {  // per x stage, written by the producer
+  int n, info, slot, P;     // tokens; B buffer | first use << 1; slot; packed row bytes
+  int beta, pad;            // basis
+  long long row0;           // store row of the tile's first token
+  long long pay, side;      // the slot's payload and side-word offsets in the store
+};
+
+// Position in a ring of n buffers: the buffer of the current use and the
+// parity of its barriers' phase; next() moves on one use.
+struct Ring {
+  int n, slot;
+  uint32_t phase;
+  __device__ explicit Ring(int n_) : n(n_), slot(0), phase(0u) {}
+  __device__ void next() {
+    if (++slot == n) { slot = 0; phase ^= 1u; }
+  }
+};
+
+// Decide code k of token tt exactly (k == kNormEntry: the fp16 norm of a
+// codebook token) from x in shared memory, V^T row k (shared or global) and
+// the basis table; lane 0 (or the lone thread) writes the result.
+// Division-free (fp64 is slow here): 1/step in double, and the nearest
+// centroid found by comparing z against the midpoints scaled by ||x||.
+template <int MODE, bool BF16, bool WARP>
+__device__ void refine_ws(const Params& p, const Tab& tb, const float* Vt, const float* cb_s,
+                          const unsigned char* xs, unsigned char* codes_s, int ks, __half* side_s,
+                          unsigned* nside, int tt, int k, int lane, float uf, float tau) {
+  const int D = p.D;
+  const int kp = k == (int)kNormEntry ? 0 : (int)(tb.qk[k] >> 16);
+  if (MODE == KVC_MODE_UNIFORM) {
+    const double z64 = dot2_row<BF16, WARP>(xs, tt, D, Vt + (size_t)k * D, lane) - tb.c64[k];
+    if (lane == 0) {
+      const int qmax = (int)(tb.qk[k] & 0xffffu);
+      const double u64 = (z64 - (double)tb.lo[k]) * tb.inv64[k];
+      codes_s[tt * ks + kp] = (uint8_t)(int)fmin(fmax(rint(u64), 0.0), (double)qmax);
+      if (tau > 0.f) atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(
+                                                   fabsf(uf - (float)u64) / tau));
+    }
+  } else {
+    const double n64 = sqrt(dot2_row<BF16, WARP>(xs, tt, D, nullptr, lane));
+    if (k == (int)kNormEntry) {
+      if (lane == 0) {
+        side_s[tt] = __double2half(n64);
+        atomicAdd(nside, 1u);
+      }
+    } else {
+      const double z64 = dot2_row<BF16, WARP>(xs, tt, D, Vt + (size_t)k * D, lane);
+      if (lane == 0) {
+        // nearest centroid, ties to the lower one: the number of exact
+        // midpoints m (double, from the fp32 centroids) with m ||x|| < z;
+        // ||x|| = 0 means u = 0
+        const double nn = n64 > 0.0 ? n64 : 1.0, zz = n64 > 0.0 ? z64 : 0.0;
+        int lo_i = 0, hi_i = p.cb_levels - 1;
+        while (lo_i < hi_i) {
+          const int mid = (lo_i + hi_i) >> 1;
+          const double m = 0.5 * ((double)cb_s[mid] + (double)cb_s[mid + 1]);
+          if (m * nn < zz) lo_i = mid + 1; else hi_i = mid;
+        }
+        codes_s[tt * ks + kp] = (uint8_t)lo_i;
+        if (tau > 0.f && n64 > 0.0)
+          atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(
+                                        fabsf(uf - (float)z64 / (float)n64) / tau));
+      }
+    }
+  }
+}
+
+template <int MODE, bool BF16, int CW>
+__global__ void __launch_bounds__(kThreads, 1)
+    append_ws_kernel(const Params p, const AppendWsArgs t, const __grid_constant__ CUtensorMap xmap,
+                     const AppendArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t x_full[kMaxXS], x_empty[kMaxXS];
+  __shared__ uint64_t acc_full[kMaxTS], acc_empty[kMaxTS];
+  __shared__ uint64_t b_full[2], b_empty[2], done_bar;
+  __shared__ XHdr hdr[kMaxXS];
+  __shared__ uint32_t tmem_base;
+  __shared__ unsigned qcount, nside;
+  __shared__ volatile int abort_flag;
+
+  constexpr int rpad = 4 * CW;
+  const int D = p.D, r = p.r, nbox = D / 64;
+  const int XS = t.n_x, TS = t.n_acc, NB = t.n_b;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x;
+  const int first = (int)((int64_t)t.total_tiles * blockIdx.x / G);
+  const int m = (int)((int64_t)t.total_tiles * (blockIdx.x + 1) / G) - first;
+  const int tps = t.tiles_per_slot;
+  const size_t b_bytes = (size_t)t.npieces * rpad * D * 2;
+
+  const size_t vt_bytes = t.vt_smem ? (size_t)r * D * 4 : 0;
+  unsigned char* xst = smem;                                        // XS x (x tile, table)
+  unsigned char* Bs = xst + (size_t)XS * t.x_stage;                 // NB x (B, V^T)
+  unsigned char* codes_s = Bs + NB * (b_bytes + vt_bytes);          // [128][ks] chunk-aligned
+  unsigned char* out_s = codes_s + (size_t)kTile * t.ks;            // [128][P] packed rows
+  uint32_t* queue = reinterpret_cast<uint32_t*>(out_s + ((kTile * t.pmax + 16 + 15) & ~15));
+  float2* aux = reinterpret_cast<float2*>(queue + kQueue);
+  float* nsq_s = reinterpret_cast<float*>(aux + kQueue);            // [4][128]
+  float* mids_s = nsq_s + 4 * kTile;                                // [256]
+  float* cb_s = mids_s + 256;                                       // [256]
+  __half* side_s = reinterpret_cast<__half*>(cb_s + 256);           // [128]
+  const int tab_off = nbox * 16384;                                 // table after the x boxes
+
+  if (warp == kMmaWarp) tmem_alloc(&tmem_base, t.cols);
+  if (tid == 0) {
+    for (int i = 0; i < XS; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], kQWarps); }
+    for (int i = 0; i < TS; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], kQWarps); }
+    // a B buffer is free once the MMAs and the quantiser are both past it
+    for (int i = 0; i < 2; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], 2); }
+    mbar_init(&done_bar, 1);
+    fence_mbar_init();
+    abort_flag = 0;
+    qcount = 0;
+    nside = 0;
+  }
+  if (MODE == KVC_MODE_CODEBOOK) {
+    for (int j = tid; j < p.cb_levels - 1; j += kThreads) mids_s[j] = p.mids[j];
+    for (int j = tid; j < p.cb_levels; j += kThreads) cb_s[j] = p.codebook[j];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr0 = tmem_base;
+
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int slot = first / tps, blk = first % tps;
+      // a slot's tables are read one slot ahead, off the critical path
+      struct SlotInfo { int beta, P; long long pay, side; };
+      auto info_of = [&](int sl) {
+        SlotInfo si{0, 0, 0, 0};
+        if (sl < p.n_slots) {
+          si.beta = p.basis_of[sl];
+          si.P = p.P[si.beta];
+          si.pay = p.pay_off[sl];
+          si.side = p.side_off[sl];
+        }
+        return si;
+      };
+      SlotInfo cur = info_of(slot), nxt = info_of(slot + 1);
+      int beta = cur.beta;
+      int cur_beta = -1, bslot = NB - 1, issued = 0;
+      uint32_t bload[2] = {0u, 0u};
+      Ring rx(XS);
+      for (int i = 0; i < m; ++i, rx.next()) {
+        const int s = rx.slot;
+        // the quantiser of tile i - XS released this stage
+        if (i >= XS && !mbar_wait_bounded(&x_empty[s], rx.phase ^ 1u, kWaitNs)) { abort_flag = 1; break; }
+        int first_use = 0;
+        if (beta != cur_beta) {
+          bslot = NB == 2 ? bslot ^ 1 : 0;
+          if (bload[bslot] > 0 &&
+              !mbar_wait_bounded(&b_empty[bslot], (bload[bslot] - 1) & 1, kWaitNs)) { abort_flag = 1; break; }
+          unsigned char* bdst = Bs + bslot * (b_bytes + vt_bytes);
+          mbar_arrive_expect_tx(&b_full[bslot], (uint32_t)(b_bytes + vt_bytes));
+          bulk_load(bdst, t.B + (size_t)beta * (b_bytes / 2), (uint32_t)b_bytes, &b_full[bslot]);
+          if (vt_bytes)
+            bulk_load(bdst + b_bytes, p.Vt + (size_t)beta * r * D, (uint32_t)vt_bytes, &b_full[bslot]);
+          ++bload[bslot];
+          cur_beta = beta;
+          first_use = 1;
+        }
+        const int64_t t0 = (int64_t)blk * kTile;
+        unsigned char* dst = xst + (size_t)s * t.x_stage;
+        hdr[s] = XHdr{(int)min((int64_t)kTile, a.T - t0), bslot | (first_use << 1), slot, cur.P,
+                      beta, 0, (long long)(a.t_base + t0), cur.pay, cur.side};
+        mbar_arrive_expect_tx(&x_full[s], (uint32_t)(nbox * 16384 + t.tab_bytes));
+        const int bb = slot / p.H, hh = slot - bb * p.H;
+        for (int bx = 0; bx < nbox; ++bx)
+          tma_load_4d(dst + bx * 16384, &xmap, &x_full[s], bx * 64, (int)t0, hh, bb);
+        bulk_load(dst + tab_off, t.tab + (size_t)beta * t.tab_bytes, (uint32_t)t.tab_bytes, &x_full[s]);
+        ++issued;
+        if (++blk == tps) {
+          blk = 0;
+          ++slot;
+          cur = nxt;
+          nxt = info_of(slot + 1);
+          beta = cur.beta;
+        }
+      }
+      // copies still in flight (after a time-out) land before the CTA exits
+      for (int j = max(0, issued - XS); j < issued; ++j)
+        mbar_wait_bounded(&x_full[j % XS], (j / XS) & 1, kWaitNs);
+      for (int b2 = 0; b2 < 2; ++b2)
+        if (bload[b2]) mbar_wait_bounded(&b_full[b2], (bload[b2] - 1) & 1, kWaitNs);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const int ncols = t.npieces * rpad;
+      const bool stacked = ncols <= 256;  // one chain with the pieces along N
+      const uint32_t idesc = idesc_f16(kTile, stacked ? ncols : rpad, BF16 ? 1 : 0);
+      const uint32_t sbo = (uint32_t)(D / 8) * 128;
+      uint32_t buse[2] = {0u, 0u};
+      Ring rx(XS), rt(TS);
+      for (int i = 0; i < m; ++i, rx.next(), rt.next()) {
+        const int s = rx.slot, acc = rt.slot;
+        if (!mbar_wait_bounded(&x_full[s], rx.phase, kWaitNs)) { abort_flag = 1; break; }
+        const int info = hdr[s].info, bs = info & 1;
+        if (info & 2) {  // first tile on a newly loaded B: the other buffer is free when
+          if (i > 0) umma_commit(&b_empty[NB == 2 ? bs ^ 1 : 0]);  // the MMAs issued so far finish
+          if (!mbar_wait_bounded(&b_full[bs], buse[bs] & 1, kWaitNs)) { abort_flag = 1; break; }
+          ++buse[bs];
+        }
+        // the quantiser of tile i - TS released this accumulator
+        if (i >= TS && !mbar_wait_bounded(&acc_empty[acc], rt.phase ^ 1u, kWaitNs)) { abort_flag = 1; break; }
+        tc_fence_after();
+        const uint32_t xa = smem_u32(xst + (size_t)s * t.x_stage);
+        const uint32_t b0 = smem_u32(Bs + bs * (b_bytes + vt_bytes));
+        const uint32_t d0 = taddr0 + acc * t.acc_stride;
+        for (int pc = 0; pc < (stacked ? 1 : t.npieces); ++pc)
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint64_t ad = desc_kmajor_sw128(xa + (ks >> 2) * 16384 + (ks & 3) * 32);
+            const uint64_t bd = desc_kmajor_noswizzle(b0 + pc * (rpad / 8) * sbo + ks * 256, 128, sbo);
+            umma_f16(d0 + pc * rpad, ad, bd, idesc, ks > 0 ? 1u : 0u);
+          }
+        umma_commit(&acc_full[acc]);
+      }
+      umma_commit(&done_bar);  // TMEM is released only after every MMA has finished
+      mbar_wait_bounded(&done_bar, 0, kWaitNs);
+    }
+  } else {
+    // ------------------------------------------------------------ quantiser
+    const int quarter = warp & 3, cblk = warp >> 2, row = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int ks = t.ks;
+    const float kU = 5.9604644775390625e-08f;
+    const float kU4 = 2.384185791015625e-07f;  // 2^-22
+    const float eps_n = 0.5f * ((D + 2) * kU) / (1.f - (D + 2) * kU) + 2.f * kU;
+    const float cmax = MODE == KVC_MODE_CODEBOOK
+                           ? fmaxf(fabsf(p.codebook[0]), fabsf(p.codebook[p.cb_levels - 1]))
+                           : 0.f;
+    Ring rx(XS), rt(TS);
+    int prev_bs = -1;
+    for (int i = 0; i < m; ++i, rx.next(), rt.next()) {
+      const int s = rx.slot, acc = rt.slot;
+      bool late = !mbar_wait_bounded(&x_full[s], rx.phase, kWaitNs);
+      late = late || !mbar_wait_bounded(&acc_full[acc], rt.phase, kWaitNs);
+      const unsigned char* xs = xst + (size_t)s * t.x_stage;
+      const Tab tb(xs + tab_off, rpad);
+      const XHdr hd = hdr[s];
+      const int n = hd.n, bs = hd.info & 1;
+      // V^T for the re-decision: beside B (visible: the MMA waited for B before
+      // committing this tile's accumulator) or in global memory
+      const float* Vt = t.vt_smem ? reinterpret_cast<const float*>(Bs + bs * (b_bytes + vt_bytes) + b_bytes)
+                                  : p.Vt + (size_t)hd.beta * r * D;
+      // partial ||x||^2 over this warp's quarter of the row
+      {
+        float sq = 0.f;
+        const int c0 = cblk * (D / 4);
+        for (int c = c0; c < c0 + D / 4; c += 8) {
+          const uint4 v = *reinterpret_cast<const uint4*>(
+              xs + (c >> 6) * 16384 + row * 128 + ((((c & 63) >> 3) ^ (row & 7)) << 4));
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float e0, e1;
+            if (BF16) {
+              e0 = __uint_as_float(w4[q] << 16);
+              e1 = __uint_as_float(w4[q] & 0xffff0000u);
+            } else {
+              e0 = __half2float(__ushort_as_half((uint16_t)(w4[q] & 0xffff)));
+              e1 = __half2float(__ushort_as_half((uint16_t)(w4[q] >> 16)));
+            }
+            sq = fmaf(e0, e0, sq);
+            sq = fmaf(e1, e1, sq);
+          }
+        }
+        nsq_s[cblk * kTile + row] = sq;
+      }
+      // z = hi + (mid + lo) for this thread's components
+      float z[CW];
+      {
+        tc_fence_after();
+        const uint32_t la = taddr0 + acc * t.acc_stride + lane_off + cblk * CW;
+        uint32_t rr[CW];
+#pragma unroll
+        for (int j = 0; j < CW; ++j) z[j] = 0.f;
+        for (int pc = t.npieces - 1; pc >= 1; --pc) {
+          tmem_ld_n<CW>(la + pc * rpad, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < CW; ++j) z[j] += __uint_as_float(rr[j]);
+        }
+        tmem_ld_n<CW>(la, rr);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < CW; ++j) z[j] = __uint_as_float(rr[j]) + z[j];
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      }
+      // B1: norms complete; the previous tile's queue and staging are done with
+      if (named_bar_or(kQBar, kQThreads, late || abort_flag)) { abort_flag = 1; break; }
+      // the first tile on a new B buffer: the other buffer's last reader was the
+      // previous tile, finished now
+      if (tid == 0 && NB == 2 && (hd.info & 2) && prev_bs >= 0) mbar_arrive(&b_empty[bs ^ 1]);
+      prev_bs = bs;
+      const float nx = sqrtf(((nsq_s[row] + nsq_s[kTile + row]) + nsq_s[2 * kTile + row]) +
+                             nsq_s[3 * kTile + row]);
+      const bool tiny = MODE == KVC_MODE_CODEBOOK && nx < 1e-18f;
+      if (row < n) {
+        unsigned char* crow = codes_s + row * ks;
+#pragma unroll
+        for (int j = 0; j < CW; ++j) {
+          const int k = cblk * CW + j;  // < rpad; components past r are not kept
+          const uint32_t qk = tb.qk[k];
+          const int kp = (qk >> 16) == 0xFFFFu ? ks - 1 : (int)(qk >> 16);  // not kept: scratch byte
+          bool near = false;
+          int code = 0;
+          float uf = 0.f, tf = 0.f;
+          if (MODE == KVC_MODE_UNIFORM) {
+            // u = (z - mean . V_k - lo) / step; tau bounds |u - u_exact| (see the plan)
+            const float4 q = tb.q4[k];
+            const float qmax = (float)(qk & 0xFFFFu);
+            const float u = fmaf(z[j], q.x, q.y);
+            const float tau = fmaf(kU4, fabsf(u), fmaf(q.z, nx, q.w));
+            const float hb = floorf(u) + 0.5f;
+            near = hb >= 0.5f && hb <= qmax - 0.5f && fabsf(u - hb) <= tau;
+            code = (int)fminf(fmaxf(rintf(u), 0.f), qmax);
+            uf = u;
+            tf = tau;
+          } else {
+            const int L = p.cb_levels;
+            const float u = tiny ? 0.f : z[j] * t.inv_scale / nx;
+            int lo_i = 0, hi_i = L - 1;
+            while (lo_i < hi_i) {
+              const int mid = (lo_i + hi_i) >> 1;
+              if (mids_s[mid] < u) lo_i = mid + 1; else hi_i = mid;
+            }
+            code = lo_i;
+            float dmin = 3.4e38f;
+            if (code > 0) dmin = fminf(dmin, fabsf(u - mids_s[code - 1]));
+            if (code < L - 1) dmin = fminf(dmin, fabsf(u - mids_s[code]));
+            const float tau = (t.gamma * tb.vn[k] * (1.f + 1e-3f) + fabsf(u) * eps_n) * (1.f + 1e-6f) +
+                              4.f * kU * (fabsf(u) + cmax);
+            near = tiny || dmin <= tau;
+            uf = u;
+            tf = tiny ? 0.f : tau;
+          }
+          crow[kp] = (uint8_t)code;
+          if (near) {
+            const unsigned q = atomicAdd(&qcount, 1u);
+            if (q < kQueue) {
+              queue[q] = ((uint32_t)row << 16) | (uint32_t)k;
+              aux[q] = make_float2(uf, tf);
+            } else {  // queue full: decide it here, alone
+              refine_ws<MODE, BF16, false>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside, row, k,
+                                           0, uf, tf);
+            }
+          }
+        }
+        if (MODE == KVC_MODE_CODEBOOK && cblk == 0) {
+          if (tiny || !same_half(nx * (1.f - eps_n), nx * (1.f + eps_n))) {
+            const unsigned q = atomicAdd(&qcount, 1u);
+            if (q < kQueue) {
+              queue[q] = ((uint32_t)row << 16) | kNormEntry;
+              aux[q] = make_float2(0.f, 0.f);
+            } else {
+              refine_ws<MODE, BF16, false>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside, row,
+                                           (int)kNormEntry, 0, 0.f, 0.f);
+            }
+          } else {
+            side_s[row] = __float2half_rn(nx);
+          }
+        }
+      }
+      named_bar_sync(kQBar, kQThreads);  // B2: fast-path codes and the queue complete
+      const unsigned nq = qcount;
+      for (unsigned e = warp; e < min(nq, (unsigned)kQueue); e += kQWarps) {
+        const uint32_t ent = queue[e];
+        const float2 ax = aux[e];
+        refine_ws<MODE, BF16, true>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside,
+                                    (int)(ent >> 16), (int)(ent & 0xffffu), lane, ax.x, ax.y);
+      }
+      named_bar_sync(kQBar, kQThreads);  // B3: every code decided
+      if (tid == 0) {
+        if (nq > nside) atomicAdd(&p.counters[0], (unsigned long long)(nq - nside));
+        if (nside) atomicAdd(&p.counters[1], (unsigned long long)nside);
+        if (hd.slot == 0) atomicAdd(&p.counters[2], (unsigned long long)n);
+      }
+      // pack: one thread per (token, 8-code chunk) -> w bytes, LSB-first
+      const int P = hd.P;
+      for (int item = tid; item < kTile * 32; item += kQThreads) {
+        const int tt = item & (kTile - 1), c = item >> 7;
+        const uint32_t ent = tb.chunk[c];
+        if (!(ent >> 31)) break;  // chunks are contiguous from 0: c is past the last one
+        if (tt >= n) continue;
+        const int wd = (int)((ent >> 16) & 0xfu), nc = (int)((ent >> 20) & 7u) + 1;
+        uint64_t v = *reinterpret_cast<const uint64_t*>(codes_s + tt * ks + c * 8);
+        if (nc < 8) v &= (1ull << (8 * nc)) - 1ull;
+        uint64_t packed = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) packed |= ((v >> (8 * j)) & 0xffull) << (wd * j);
+        unsigned char* o = out_s + tt * P + (int)(ent & 0xffffu);
+        const int nbytes = (nc * wd + 7) >> 3;
+        for (int j = 0; j < nbytes; ++j) o[j] = (unsigned char)(packed >> (8 * j));
+      }
+      named_bar_sync(kQBar, kQThreads);  // B4: packed rows staged; the stage (x, table) is free
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&x_empty[s]);
+      unsigned char* dst = p.store + hd.pay + hd.row0 * P;
+      for (int idx = tid; idx < n * P; idx += kQThreads) dst[idx] = out_s[idx];
+      if (MODE == KVC_MODE_CODEBOOK && tid < n)
+        reinterpret_cast<__half*>(p.store + hd.side)[hd.row0 + tid] = side_s[tid];
+      if (tid == 0) {  // the next tile starts with an empty queue (read above, before B3)
+        qcount = 0;
+        nside = 0;
+      }
+    }
+  }
+  __syncthreads();
+  if (abort_flag && tid == 0) atomicCAS(p.err, 0, kErrTimeout);
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(taddr0, t.cols);
+  }
+}
+
+using WsKernel = void (*)(const Params, const AppendWsArgs, const CUtensorMap, const AppendArgs);
+
+template <int MODE, bool BF16>
+WsKernel ws_for(int rpad) {
+  switch (rpad) {
+    case 16: return append_ws_kernel<MODE, BF16, 4>;
+    case 32: return append_ws_kernel<MODE, BF16, 8>;
+    case 64: return append_ws_kernel<MODE, BF16, 16>;
+    default: return append_ws_kernel<MODE, BF16, 32>;
+  }
+}
+
+WsKernel ws_kernel_for(int mode, int bf16, int rpad) {
+  if (mode == KVC_MODE_UNIFORM)
+    return bf16 ? ws_for<KVC_MODE_UNIFORM, true>(rpad) : ws_for<KVC_MODE_UNIFORM, false>(rpad);
+  return bf16 ? ws_for<KVC_MODE_CODEBOOK, true>(rpad) : ws_for<KVC_MODE_CODEBOOK, false>(rpad);
+}
+
+}  // namespace
+
+size_t append_ws_tab_bytes(int rpad) { return ((size_t)rpad * 44 + 128 + 15) & ~size_t(15); }
+
+namespace {
+float round_up_f(double v) {  // the smallest float >= v
+  float f = (float)v;
+  if ((double)f < v) f = std::nextafter(f, INFINITY);
+  return f;
+}
+}  // namespace
+
+int append_ws_table(const Geo& g, const kvc_layer_desc& d, int rpad, const double* c64,
+                    double inv_scale, double gamma, int b, unsigned char* out) {
+  const int r = g.r, D = d.D;
+  float4* q4 = reinterpret_cast<float4*>(out);
+  double* c = reinterpret_cast<double*>(q4 + rpad);
+  double* inv64 = c + rpad;
+  float* lo = reinterpret_cast<float*>(inv64 + rpad);
+  float* vn = lo + rpad;
+  uint32_t* qk = reinterpret_cast<uint32_t*>(vn + rpad);
+  uint32_t* chunk = qk + rpad;
+  for (int k = 0; k < rpad; ++k) {
+    const bool in = k < r;
+    const size_t bk = (size_t)b * r + k;
+    const bool q = in && d.mode == KVC_MODE_UNIFORM && g.bits[bk] > 0;
+    double ss = 0.0;  // ||V_k|| rounded up, as the parameter block's
+    for (int i = 0; in && i < D; ++i) {
+      const double v = d.V[((size_t)b * D + i) * r + k];
+      ss += v * v;
+    }
+    vn[k] = in ? std::nextafter((float)std::sqrt(ss), INFINITY) : 0.f;
+    c[k] = in ? c64[bk] : 0.0;
+    lo[k] = q ? d.qmin[bk] : 0.f;
+    inv64[k] = q ? 1.0 / (double)d.qstep[bk] : 0.0;
+    q4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (q) {
+      // u = fma(z_tc, A, Bc) with A, Bc rounded once from double.  |u - u_exact|
+      // <= [gamma ||x|| ||V_k|| (tensor-core accumulation) + 2^-24 |z| (A) ]
+      //    / step + 2^-24 |c + lo| / step (Bc) + 2^-24 |u| (fma), |z| <= ||x|| ||V_k||;
+      // T1, T2 carry twice that, ||x|| a 1e-3 margin, the kernel 2^-22 (|u| + 1).
+      const double st = (double)d.qstep[bk];
+      q4[k].x = (float)(inv_scale / st);
+      q4[k].y = (float)(-(c64[bk] + (double)d.qmin[bk]) / st);
+      q4[k].z = round_up_f((double)vn[k] / st * (gamma + std::ldexp(1.0, -23)) *
+                           (1.0 + std::ldexp(1.0, -20)) * (1.0 + 1e-3));
+      q4[k].w = round_up_f((std::fabs(c64[bk]) + std::fabs((double)d.qmin[bk])) / st *
+                           std::ldexp(1.0, -23));
+    }
+    const int width = in ? g.bits[bk] : 0;
+    qk[k] = (uint32_t)(d.mode == KVC_MODE_UNIFORM ? (width ? (1 << width) - 1 : 0) : 0) |
+            (0xFFFFu << 16);
+  }
+  // chunk-aligned positions: segment s (packed order) starts on a chunk
+  int nch = 0;
+  for (int sg = 0; sg < kMaxSeg; ++sg) {
+    const int32_t* e = &g.seg[((size_t)b * kMaxSeg + sg) * 4];
+    if (!e[3]) break;
+    for (int mm = 0; mm < e[3]; ++mm) {
+      const int k = g.order[(size_t)b * r + e[2] + mm];
+      qk[k] = (qk[k] & 0xFFFFu) | ((uint32_t)(nch * 8 + mm) << 16);
+    }
+    for (int ci = 0; ci * 8 < e[3]; ++ci) {
+      if (nch == 32) return -1;
+      const int nc = std::min(8, e[3] - ci * 8);
+      chunk[nch++] = (uint32_t)(e[0] + e[1] * ci) | ((uint32_t)e[1] << 16) |
+                     ((uint32_t)(nc - 1) << 20) | (1u << 31);
+    }
+  }
+  for (int j = nch; j < 32; ++j) chunk[j] = 0u;
+  return nch;
+}
+
+size_t append_ws_plan(int D, int r, int rpad, int npieces, int pmax, int max_chunks, int n_bases,
+                      AppendWsShape* sh) {
+  AppendWsShape z;
+  const int ncols = npieces * rpad;
+  z.acc_stride = (ncols + 31) / 32 * 32;
+  z.n_acc = std::min(kMaxTS, 512 / z.acc_stride);
+  if (z.n_acc < 1 || max_chunks < 1 || max_chunks > 32) return 0;
+  int cols = 32;
+  while (cols < z.n_acc * z.acc_stride) cols *= 2;
+  z.cols = cols;
+  z.tab_bytes = (int)append_ws_tab_bytes(rpad);
+  z.x_stage = ((D / 64) * 16384 + z.tab_bytes + 1023) / 1024 * 1024;
+  z.n_b = n_bases > 1 ? 2 : 1;
+  z.ks = max_chunks * 8 + 8;  // the extra 8 bytes spread the rows over the banks
+  const size_t limit = 226 * 1024;
+  for (int vt = 1; vt >= 0; --vt) {
+    const size_t fixed = 1024 + (size_t)z.n_b * ((size_t)ncols * D * 2 + (vt ? (size_t)r * D * 4 : 0)) +
+                         (size_t)kTile * z.ks + (((size_t)kTile * pmax + 16 + 15) & ~size_t(15)) +
+                         (size_t)kQueue * 12 + 4 * kTile * 4 + 2 * 256 * 4 + kTile * 2;
+    for (int xs = kMaxXS; xs >= (vt ? 3 : 2); --xs)
+      if (fixed + (size_t)xs * z.x_stage <= limit) {
+        z.n_x = xs;
+        z.vt_smem = vt;
+        *sh = z;
+        return fixed + (size_t)xs * z.x_stage;
+      }
+  }
+  return 0;
+}
+
+cudaError_t launch_append_ws(const TcPlan& plan, const Params& p, const AppendArgs& a,
+                             const CUtensorMap& xmap, cudaStream_t s, int* nk) {
+  WsKernel k = ws_kernel_for(p.mode, plan.app_bf16, plan.app_rpad);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)plan.ws_smem);
+  if (e != cudaSuccess) return e;
+  const int tiles = (int)((a.T + kTile - 1) / kTile);
+  const int total = tiles * p.n_slots;
+  const int grid = std::min(total, sm_count());
+  const AppendWsShape& sh = plan.ws;
+  const AppendWsArgs t{plan.appB,    plan.c64,     plan.wsTab,   plan.app_rpad,      plan.app_pieces,
+                       sh.acc_stride, sh.cols,      sh.n_acc,     sh.n_x,             sh.n_b,
+                       sh.x_stage,    sh.tab_bytes, plan.ws_pmax, sh.ks,              sh.vt_smem,
+                       plan.app_inv_scale, plan.app_gamma, tiles, total};
+  k<<<(unsigned)grid, kThreads, plan.ws_smem, s>>>(p, t, xmap, a);
+  ++*nk;
+  return cudaGetLastError();
+}
+
+}  // namespace kvc

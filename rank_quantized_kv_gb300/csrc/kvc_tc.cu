@@ -23,6 +23,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "kvc_append_exact.cuh"
 #include "kvc_sm100.cuh"
 #include "kvc_tc.h"
 
@@ -41,13 +42,6 @@ struct FetchTc {
   int K;
   int cols;
 };
-
-__device__ __forceinline__ void set_err(int* err, int code) { atomicCAS(err, 0, code); }
-
-// True when every value in [lo, hi] rounds to the same fp16.
-__device__ __forceinline__ bool same_half(float lo, float hi) {
-  return __half_as_ushort(__float2half_rn(lo)) == __half_as_ushort(__float2half_rn(hi));
-}
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
@@ -271,110 +265,6 @@ __global__ void __launch_bounds__(kTile) fetch_tc_kernel(const Params p, const F
 // Codes closer than that (through the quantiser's own roundings) to a rounding
 // boundary are queued and re-decided by a warp with a compensated fp32 dot
 // product (error ~ 1e-13 relative) finished in double precision.
-
-constexpr int kQueue = 512;
-constexpr uint32_t kNormEntry = 0xFFFFu;
-
-struct AppendTc {
-  const uint16_t* B;    // [nb][3][rpad][D]
-  const double* c64;    // [nb][r]
-  int rpad, cols;
-  float inv_scale, gamma;
-};
-
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = a + b;
-  const float bb = s - a;
-  e = (a - (s - bb)) + (b - bb);
-}
-
-// x_t . w with x_t a row of the swizzled x tile (w == nullptr: x_t . x_t),
-// compensated fp32 (TwoProd / TwoSum) finished in double.  WARP: the 32 lanes
-// split the row and the result is on every lane; else one thread does it all.
-template <bool BF16, bool WARP>
-__device__ double dot2_row(const unsigned char* xs, int t, int D, const float* w, int lane) {
-  float S = 0.f, C = 0.f;
-  for (int i = WARP ? lane : 0; i < D; i += WARP ? 32 : 1) {
-    const unsigned char* src =
-        xs + (i >> 6) * 16384 + t * 128 + ((((i & 63) >> 3) ^ (t & 7)) << 4) + (i & 7) * 2;
-    const uint16_t raw = *reinterpret_cast<const uint16_t*>(src);
-    const float xv = BF16 ? __bfloat162float(__ushort_as_bfloat16(raw))
-                          : __half2float(__ushort_as_half(raw));
-    const float wv = w ? w[i] : xv;
-    const float pr = xv * wv;
-    const float pe = fmaf(xv, wv, -pr);
-    float s, e;
-    two_sum(S, pr, s, e);
-    S = s;
-    C += pe + e;
-  }
-  if (WARP) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float So = __shfl_xor_sync(0xffffffffu, S, o);
-      const float Co = __shfl_xor_sync(0xffffffffu, C, o);
-      float s, e;
-      two_sum(S, So, s, e);
-      S = s;
-      C = C + Co + e;
-    }
-  }
-  return (double)S + (double)C;
-}
-
-// Decide code k of token tt exactly (or, k == kNormEntry, the fp16 norm of a
-// codebook token).  Lane 0 (or the lone thread) writes the result.
-// The largest |u_fast - u_exact| / bound seen (float bits; all non-negative)
-// is kept in counters[3]: evidence of how much margin the bound carries.
-__device__ __forceinline__ void note_ratio(const Params& p, double uf, double u, float tau) {
-  if (tau > 0.f) {
-    const float ratio = (float)(fabs(uf - u) / (double)tau);
-    atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(ratio));
-  }
-}
-
-template <int MODE, bool BF16, bool WARP>
-__device__ void refine_entry(const Params& p, const AppendTc& t, int beta, const unsigned char* xs,
-                             unsigned char* codes_s, __half* side_s, unsigned* nside, int tt, int k,
-                             int lane, float uf = 0.f, float tau = 0.f) {
-  const int D = p.D, r = p.r;
-  const float* Vt = p.Vt + (size_t)beta * r * D;
-  if (MODE == KVC_MODE_UNIFORM) {
-    const double z64 = dot2_row<BF16, WARP>(xs, tt, D, Vt + (size_t)k * D, lane) -
-                       t.c64[(size_t)beta * r + k];
-    if (lane == 0) {
-      const int qmax = (1 << p.bits[(size_t)beta * r + k]) - 1;
-      const double u64 =
-          (z64 - (double)p.lo[(size_t)beta * r + k]) / (double)p.step[(size_t)beta * r + k];
-      codes_s[tt * r + k] = (uint8_t)(int)fmin(fmax(rint(u64), 0.0), (double)qmax);
-      note_ratio(p, uf, u64, tau);
-    }
-  } else {
-    const double n64 = sqrt(dot2_row<BF16, WARP>(xs, tt, D, nullptr, lane));
-    if (k == (int)kNormEntry) {
-      if (lane == 0) {
-        side_s[tt] = __double2half(n64);
-        atomicAdd(nside, 1u);
-      }
-    } else {
-      const double z64 = dot2_row<BF16, WARP>(xs, tt, D, Vt + (size_t)k * D, lane);
-      if (lane == 0) {
-        const double u64 = n64 > 0.0 ? z64 / n64 : 0.0;
-        note_ratio(p, uf, u64, tau);
-        double best = fabs(u64 - (double)p.codebook[0]);
-        int bi = 0;
-        for (int j = 1; j < p.cb_levels; ++j) {
-          const double d = fabs(u64 - (double)p.codebook[j]);
-          if (d < best) {
-            best = d;
-            bi = j;
-          }
-        }
-        codes_s[tt * r + k] = (uint8_t)bi;
-      }
-    }
-  }
-}
 
 // ---------------------------------------------------------------- append, 512 threads
 //
@@ -773,6 +663,26 @@ void prepare_append(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>&
                            (bf ? 0.0 : std::ldexp(1.0, -21)));
   plan.app_pieces = npieces;
   plan.append_ready = encoder() != nullptr;
+  // the persistent warp-specialised kernel, where its tables and rings fit
+  int pmax = 0;
+  for (int b = 0; b < nb; ++b) pmax = std::max(pmax, g.P[b]);
+  const size_t tab_bytes = append_ws_tab_bytes(rpad);
+  std::vector<unsigned char> tab((size_t)nb * tab_bytes, 0);
+  int max_chunks = 0;
+  for (int b = 0; b < nb && max_chunks >= 0; ++b) {
+    const int nch = append_ws_table(g, d, rpad, c64.data(), (double)plan.app_inv_scale,
+                                    (double)plan.app_gamma, b, tab.data() + (size_t)b * tab_bytes);
+    max_chunks = nch < 0 ? -1 : std::max(max_chunks, nch);
+  }
+  AppendWsShape ws;
+  const size_t wsm = max_chunks > 0 ? append_ws_plan(D, r, rpad, npieces, pmax, max_chunks, nb, &ws) : 0;
+  if (wsm > 0 && plan.append_ready) {
+    plan.oWsTab = put(image, tab.data(), tab.size());
+    plan.ws = ws;
+    plan.ws_smem = wsm;
+    plan.ws_pmax = pmax;
+    plan.ws_ready = true;
+  }
 }
 
 using AppendKernel = void (*)(const Params, const AppendTc, const CUtensorMap, const AppendArgs, int,
@@ -929,6 +839,7 @@ void tc_bind(TcPlan& plan, uint8_t* base) {
   if (plan.append_ready) {
     plan.appB = reinterpret_cast<const uint16_t*>(base + plan.oAppB);
     plan.c64 = reinterpret_cast<const double*>(base + plan.oC64);
+    if (plan.ws_ready) plan.wsTab = reinterpret_cast<const unsigned char*>(base + plan.oWsTab);
   }
 }
 
@@ -986,6 +897,7 @@ cudaError_t launch_append_tc(const TcPlan& plan, const Params& p, const AppendAr
       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  if (plan.ws_ready) return launch_append_ws(plan, p, a, map, s, nk);
   AppendKernel kern = append_kernel_for(p.mode, plan.app_bf16, plan.app_rpad);
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.app_smem);

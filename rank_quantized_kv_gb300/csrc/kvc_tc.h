@@ -23,6 +23,19 @@ struct FetchPipeShape {
   int rs_bytes = 0;  // bytes of one row stage
 };
 
+// Ring sizes of the warp-specialised append (kvc_append_ws.cu).
+struct AppendWsShape {
+  int acc_stride = 0;  // TMEM columns per accumulator (pieces x rpad, rounded up to 32)
+  int n_acc = 0;       // accumulators
+  int cols = 0;        // TMEM columns allocated
+  int tab_bytes = 0;   // bytes of one basis' quantiser table
+  int x_stage = 0;     // bytes of one x stage (x tile + table)
+  int n_x = 0;         // x stages
+  int n_b = 0;         // B buffers
+  int ks = 0;          // bytes per token row of the chunk-aligned code staging
+  int vt_smem = 0;     // V^T kept in shared memory beside B
+};
+
 // Tables the tensor-core kernels need, appended to the layer's parameter
 // block by tc_prepare (as offsets) and turned into device pointers by tc_bind.
 struct TcPlan {
@@ -59,6 +72,13 @@ struct TcPlan {
   size_t oAppB = 0, oC64 = 0;
   const uint16_t* appB = nullptr;  // [nb][pieces][rpad][D] UMMA no-swizzle K-major order
   const double* c64 = nullptr;     // [nb][r] mean . V_k in double
+  // warp-specialised persistent append (one head per slot), one CTA per SM
+  bool ws_ready = false;
+  AppendWsShape ws;
+  size_t ws_smem = 0;
+  int ws_pmax = 0;                   // largest packed row
+  size_t oWsTab = 0;
+  const unsigned char* wsTab = nullptr;  // [nb][tab_bytes] quantiser tables
 };
 
 kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>& image,
@@ -79,6 +99,16 @@ cudaError_t launch_fetch_tc(const TcPlan& plan, const Params& p, const FetchArgs
 size_t fetch_pipe_smem(int D, int K, int side_bytes, int pmax, int n_bases, FetchPipeShape* sh);
 cudaError_t launch_fetch_pipe(const TcPlan& plan, const Params& p, const FetchArgs& f,
                               const CUtensorMap& map, cudaStream_t s, int* nk);
+// Warp-specialised append (kvc_append_ws.cu): table bytes per basis, one
+// basis' table, the ring plan (0 when it does not fit), the launcher.
+size_t append_ws_tab_bytes(int rpad);
+int append_ws_table(const Geo& g, const kvc_layer_desc& d, int rpad, const double* c64,
+                    double inv_scale, double gamma, int b,
+                    unsigned char* out);  // returns the basis' pack chunks, -1 if over 32
+size_t append_ws_plan(int D, int r, int rpad, int npieces, int pmax, int max_chunks, int n_bases,
+                      AppendWsShape* sh);
+cudaError_t launch_append_ws(const TcPlan& plan, const Params& p, const AppendArgs& a,
+                             const CUtensorMap& xmap, cudaStream_t s, int* nk);
 int sm_count();
 
 }  // namespace kvc
