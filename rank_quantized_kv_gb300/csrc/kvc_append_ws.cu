@@ -150,6 +150,45 @@ __device__ void refine_ws(const Params& p, const Tab& tb, const float* Vt, const
   }
 }
 
+// Uniform fast path: u = (z - mean . V_k - lo) / step as one fma of the
+// table's fused constants, the bound tau on |u - u_exact| (host derivation in
+// append_ws_table), and whether a rounding boundary lies within tau.
+__device__ __forceinline__ int fast_uniform(const Tab& tb, int k, uint32_t qk, float z, float nx,
+                                            float& u, float& tau, bool& near) {
+  constexpr float kU4 = 2.384185791015625e-07f;  // 2^-22
+  const float4 q = tb.q4[k];
+  const float qmax = (float)(qk & 0xFFFFu);
+  u = fmaf(z, q.x, q.y);
+  tau = fmaf(kU4, fabsf(u), fmaf(q.z, nx, q.w));
+  const float hb = floorf(u) + 0.5f;
+  near = hb >= 0.5f && hb <= qmax - 0.5f && fabsf(u - hb) <= tau;
+  return (int)fminf(fmaxf(rintf(u), 0.f), qmax);
+}
+
+// Codebook fast path: u = z / ||x||, the nearest centroid by the fp32
+// midpoints, and whether a midpoint lies within the bound of u's error.
+__device__ __forceinline__ int fast_codebook(const Params& p, const Tab& tb, int k,
+                                             const float* mids_s, float z, float inv_scale,
+                                             float gamma, float nx, float eps_n, float cmax,
+                                             bool tiny, float& u, float& tau, bool& near) {
+  constexpr float kU = 5.9604644775390625e-08f;
+  const int L = p.cb_levels;
+  u = tiny ? 0.f : z * inv_scale / nx;
+  int lo_i = 0, hi_i = L - 1;
+  while (lo_i < hi_i) {
+    const int mid = (lo_i + hi_i) >> 1;
+    if (mids_s[mid] < u) lo_i = mid + 1; else hi_i = mid;
+  }
+  float dmin = 3.4e38f;
+  if (lo_i > 0) dmin = fminf(dmin, fabsf(u - mids_s[lo_i - 1]));
+  if (lo_i < L - 1) dmin = fminf(dmin, fabsf(u - mids_s[lo_i]));
+  tau = (gamma * tb.vn[k] * (1.f + 1e-3f) + fabsf(u) * eps_n) * (1.f + 1e-6f) +
+        4.f * kU * (fabsf(u) + cmax);
+  near = tiny || dmin <= tau;
+  if (tiny) tau = 0.f;
+  return lo_i;
+}
+
 template <int MODE, bool BF16, int CW>
 __global__ void __launch_bounds__(kThreads, 1)
     append_ws_kernel(const Params p, const AppendWsArgs t, const __grid_constant__ CUtensorMap xmap,
@@ -313,7 +352,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int ks = t.ks;
     const float kU = 5.9604644775390625e-08f;
-    const float kU4 = 2.384185791015625e-07f;  // 2^-22
     const float eps_n = 0.5f * ((D + 2) * kU) / (1.f - (D + 2) * kU) + 2.f * kU;
     const float cmax = MODE == KVC_MODE_CODEBOOK
                            ? fmaxf(fabsf(p.codebook[0]), fabsf(p.codebook[p.cb_levels - 1]))
@@ -389,54 +427,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool tiny = MODE == KVC_MODE_CODEBOOK && nx < 1e-18f;
       if (row < n) {
         unsigned char* crow = codes_s + row * ks;
+        // fast path: every code, and a mask of the ones near a boundary
+        uint32_t nmask = 0;
 #pragma unroll
         for (int j = 0; j < CW; ++j) {
           const int k = cblk * CW + j;  // < rpad; components past r are not kept
           const uint32_t qk = tb.qk[k];
           const int kp = (qk >> 16) == 0xFFFFu ? ks - 1 : (int)(qk >> 16);  // not kept: scratch byte
-          bool near = false;
-          int code = 0;
-          float uf = 0.f, tf = 0.f;
-          if (MODE == KVC_MODE_UNIFORM) {
-            // u = (z - mean . V_k - lo) / step; tau bounds |u - u_exact| (see the plan)
-            const float4 q = tb.q4[k];
-            const float qmax = (float)(qk & 0xFFFFu);
-            const float u = fmaf(z[j], q.x, q.y);
-            const float tau = fmaf(kU4, fabsf(u), fmaf(q.z, nx, q.w));
-            const float hb = floorf(u) + 0.5f;
-            near = hb >= 0.5f && hb <= qmax - 0.5f && fabsf(u - hb) <= tau;
-            code = (int)fminf(fmaxf(rintf(u), 0.f), qmax);
-            uf = u;
-            tf = tau;
-          } else {
-            const int L = p.cb_levels;
-            const float u = tiny ? 0.f : z[j] * t.inv_scale / nx;
-            int lo_i = 0, hi_i = L - 1;
-            while (lo_i < hi_i) {
-              const int mid = (lo_i + hi_i) >> 1;
-              if (mids_s[mid] < u) lo_i = mid + 1; else hi_i = mid;
-            }
-            code = lo_i;
-            float dmin = 3.4e38f;
-            if (code > 0) dmin = fminf(dmin, fabsf(u - mids_s[code - 1]));
-            if (code < L - 1) dmin = fminf(dmin, fabsf(u - mids_s[code]));
-            const float tau = (t.gamma * tb.vn[k] * (1.f + 1e-3f) + fabsf(u) * eps_n) * (1.f + 1e-6f) +
-                              4.f * kU * (fabsf(u) + cmax);
-            near = tiny || dmin <= tau;
-            uf = u;
-            tf = tiny ? 0.f : tau;
-          }
+          float uf, tf;
+          bool near;
+          const int code = MODE == KVC_MODE_UNIFORM
+                               ? fast_uniform(tb, k, qk, z[j], nx, uf, tf, near)
+                               : fast_codebook(p, tb, k, mids_s, z[j], t.inv_scale, t.gamma, nx,
+                                               eps_n, cmax, tiny, uf, tf, near);
           crow[kp] = (uint8_t)code;
-          if (near) {
+          nmask |= (uint32_t)near << j;
+        }
+        // queue the near ones (rare); past the queue's end they are decided
+        // below, one at a time, by their own thread
+        uint32_t ovf = 0;
+        if (nmask) {
+#pragma unroll
+          for (int j = 0; j < CW; ++j) {
+            if (!((nmask >> j) & 1u)) continue;
+            const int k = cblk * CW + j;
+            float uf, tf;
+            bool near;
+            if (MODE == KVC_MODE_UNIFORM)
+              fast_uniform(tb, k, tb.qk[k], z[j], nx, uf, tf, near);
+            else
+              fast_codebook(p, tb, k, mids_s, z[j], t.inv_scale, t.gamma, nx, eps_n, cmax, tiny, uf,
+                            tf, near);
             const unsigned q = atomicAdd(&qcount, 1u);
             if (q < kQueue) {
               queue[q] = ((uint32_t)row << 16) | (uint32_t)k;
               aux[q] = make_float2(uf, tf);
-            } else {  // queue full: decide it here, alone
-              refine_ws<MODE, BF16, false>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside, row, k,
-                                           0, uf, tf);
+            } else {
+              ovf |= 1u << j;
             }
           }
+        }
+        for (; ovf; ovf &= ovf - 1) {
+          const int k = cblk * CW + (__ffs(ovf) - 1);
+          refine_ws<MODE, BF16, false>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside, row, k, 0,
+                                       0.f, 0.f);
         }
         if (MODE == KVC_MODE_CODEBOOK && cblk == 0) {
           if (tiny || !same_half(nx * (1.f - eps_n), nx * (1.f + eps_n))) {

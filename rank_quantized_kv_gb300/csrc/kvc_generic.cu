@@ -535,19 +535,12 @@ __device__ __forceinline__ void load8(const void* x, int dt, int64_t off, float 
 }
 
 template <int TPR>
-__global__ void __launch_bounds__(256) append_int8_vec(Params p, AppendArgs a) {
-  const int64_t gt = (int64_t)blockIdx.x * 256 + threadIdx.x;
-  const int64_t rows = (int64_t)p.n_slots * a.T;
-  const int64_t row = gt / TPR;
-  const int j = (int)(gt % TPR);
-  const bool valid = row < rows;
-  int slot = 0;
-  int64_t t = 0;
+__device__ __forceinline__ void append_int8_row(const Params& p, const AppendArgs& a, int slot,
+                                                int64_t t, int j) {
+  const bool valid = t < a.T;
   float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (valid) {
-    slot = (int)(row / a.T);
-    t = row - (int64_t)slot * a.T;
-    const int b = slot / p.H, h = slot % p.H;
+    const int b = slot / p.H, h = slot - b * p.H;
     load8(a.x, p.in_dtype, (int64_t)b * a.sb + (int64_t)h * a.sh + t * a.st + 8 * j, v);
   }
   float am = 0.f;
@@ -595,15 +588,24 @@ __global__ void __launch_bounds__(256) append_int8_vec(Params p, AppendArgs a) {
   if ((threadIdx.x & 31) == 0 && nref) atomicAdd(&p.counters[0], (unsigned long long)nref);
 }
 
+// Grid: x over blocks of 256 / TPR tokens, y over slots (strided when there
+// are more than 65535), so no thread divides by a runtime value.
+template <int TPR>
+__global__ void __launch_bounds__(256) append_int8_vec(Params p, AppendArgs a) {
+  const int j = (int)(threadIdx.x % TPR);
+  const int64_t t = (int64_t)blockIdx.x * (256 / TPR) + threadIdx.x / TPR;
+  for (int slot = blockIdx.y; slot < p.n_slots; slot += gridDim.y)
+    append_int8_row<TPR>(p, a, slot, t, j);
+}
+
+// Grid as append_int8_vec.
 template <int TPR>
 __global__ void __launch_bounds__(256) fetch_int8_vec(Params p, FetchArgs f) {
-  const int64_t gt = (int64_t)blockIdx.x * 256 + threadIdx.x;
-  const int64_t row = gt / TPR;
-  if (row >= (int64_t)p.n_slots * f.S) return;
-  const int j = (int)(gt % TPR);
-  const int slot = (int)(row / f.S);
-  const int64_t t = row - (int64_t)slot * f.S;
-  const int b = slot / p.H, h = slot % p.H;
+  const int j = (int)(threadIdx.x % TPR);
+  const int64_t t = (int64_t)blockIdx.x * (256 / TPR) + threadIdx.x / TPR;
+  if (t >= f.S) return;
+  for (int slot = blockIdx.y; slot < p.n_slots; slot += gridDim.y) {
+  const int b = slot / p.H, h = slot - b * p.H;
   const uint2 q = *reinterpret_cast<const uint2*>(p.store + p.pay_off[slot] + t * p.D + 8 * j);
   const float s = __half2float(reinterpret_cast<const __half*>(p.store + p.side_off[slot])[t]);
   const uint32_t w[2] = {q.x, q.y};
@@ -622,6 +624,7 @@ __global__ void __launch_bounds__(256) fetch_int8_vec(Params p, FetchArgs f) {
   }
   uint16_t* out = static_cast<uint16_t*>(f.out) + (((int64_t)b * p.H + h) * f.ld_s + t) * p.D + 8 * j;
   *reinterpret_cast<uint4*>(out) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 }  // namespace
@@ -665,7 +668,7 @@ cudaError_t launch_append_int8(const Params& p, const AppendArgs& a, cudaStream_
                    (a.sh * esz) % 16 == 0 && (a.sb * esz) % 16 == 0;
   if (vec) {
     const int tpr = p.D / 8;
-    const unsigned grid = (unsigned)((toks * tpr + 255) / 256);
+    const dim3 grid((unsigned)((a.T * tpr + 255) / 256), (unsigned)std::min(p.n_slots, 65535));
     if (tpr == 8) append_int8_vec<8><<<grid, 256, 0, s>>>(p, a);
     else if (tpr == 16) append_int8_vec<16><<<grid, 256, 0, s>>>(p, a);
     else append_int8_vec<32><<<grid, 256, 0, s>>>(p, a);
@@ -683,7 +686,7 @@ cudaError_t launch_fetch_int8(const Params& p, const FetchArgs& f, cudaStream_t 
                    reinterpret_cast<uintptr_t>(f.out) % 16 == 0;
   if (vec) {
     const int tpr = p.D / 8;
-    const unsigned grid = (unsigned)((toks * tpr + 255) / 256);
+    const dim3 grid((unsigned)((f.S * tpr + 255) / 256), (unsigned)std::min(p.n_slots, 65535));
     if (tpr == 8) fetch_int8_vec<8><<<grid, 256, 0, s>>>(p, f);
     else if (tpr == 16) fetch_int8_vec<16><<<grid, 256, 0, s>>>(p, f);
     else fetch_int8_vec<32><<<grid, 256, 0, s>>>(p, f);
