@@ -167,21 +167,32 @@ __device__ __forceinline__ int fast_uniform(const Tab& tb, int k, uint32_t qk, f
 
 // Codebook fast path: u = z / ||x||, the nearest centroid by the fp32
 // midpoints, and whether a midpoint lies within the bound of u's error.
+// Up to 8 levels the 7 midpoints sit in registers (+inf past the last): the
+// code is the number of midpoints below u, the distance the nearest one.
 __device__ __forceinline__ int fast_codebook(const Params& p, const Tab& tb, int k,
-                                             const float* mids_s, float z, float inv_scale,
-                                             float gamma, float nx, float eps_n, float cmax,
+                                             const float* mids_s, const float (&mreg)[7], float z,
+                                             float rnx, float gamma, float eps_n, float cmax,
                                              bool tiny, float& u, float& tau, bool& near) {
   constexpr float kU = 5.9604644775390625e-08f;
   const int L = p.cb_levels;
-  u = tiny ? 0.f : z * inv_scale / nx;
-  int lo_i = 0, hi_i = L - 1;
-  while (lo_i < hi_i) {
-    const int mid = (lo_i + hi_i) >> 1;
-    if (mids_s[mid] < u) lo_i = mid + 1; else hi_i = mid;
-  }
+  u = z * rnx;  // rnx = 2^-s fl(1 / ||x||) (0 for a tiny ||x||): two roundings, as z 2^-s / ||x||
+  int lo_i = 0;
   float dmin = 3.4e38f;
-  if (lo_i > 0) dmin = fminf(dmin, fabsf(u - mids_s[lo_i - 1]));
-  if (lo_i < L - 1) dmin = fminf(dmin, fabsf(u - mids_s[lo_i]));
+  if (L <= 8) {
+#pragma unroll
+    for (int j = 0; j < 7; ++j) {
+      lo_i += mreg[j] < u ? 1 : 0;
+      dmin = fminf(dmin, fabsf(u - mreg[j]));
+    }
+  } else {
+    int hi_i = L - 1;
+    while (lo_i < hi_i) {
+      const int mid = (lo_i + hi_i) >> 1;
+      if (mids_s[mid] < u) lo_i = mid + 1; else hi_i = mid;
+    }
+    if (lo_i > 0) dmin = fminf(dmin, fabsf(u - mids_s[lo_i - 1]));
+    if (lo_i < L - 1) dmin = fminf(dmin, fabsf(u - mids_s[lo_i]));
+  }
   tau = (gamma * tb.vn[k] * (1.f + 1e-3f) + fabsf(u) * eps_n) * (1.f + 1e-6f) +
         4.f * kU * (fabsf(u) + cmax);
   near = tiny || dmin <= tau;
@@ -205,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ volatile int abort_flag;
 
   constexpr int rpad = 4 * CW;
+  constexpr int SB = CW < 16 ? CW : 16;  // components per TMEM read
   const int D = p.D, r = p.r, nbox = D / 64;
   const int XS = t.n_x, TS = t.n_acc, NB = t.n_b;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -356,6 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float cmax = MODE == KVC_MODE_CODEBOOK
                            ? fmaxf(fabsf(p.codebook[0]), fabsf(p.codebook[p.cb_levels - 1]))
                            : 0.f;
+    float mreg[7];
+#pragma unroll
+    for (int j = 0; j < 7; ++j)
+      mreg[j] = MODE == KVC_MODE_CODEBOOK && j < p.cb_levels - 1 ? mids_s[j] : INFINITY;
     Ring rx(XS), rt(TS);
     int prev_bs = -1;
     for (int i = 0; i < m; ++i, rx.next(), rt.next()) {
@@ -394,28 +410,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         nsq_s[cblk * kTile + row] = sq;
       }
-      // z = hi + (mid + lo) for this thread's components
-      float z[CW];
-      {
-        tc_fence_after();
-        const uint32_t la = taddr0 + acc * t.acc_stride + lane_off + cblk * CW;
-        uint32_t rr[CW];
-#pragma unroll
-        for (int j = 0; j < CW; ++j) z[j] = 0.f;
-        for (int pc = t.npieces - 1; pc >= 1; --pc) {
-          tmem_ld_n<CW>(la + pc * rpad, rr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < CW; ++j) z[j] += __uint_as_float(rr[j]);
-        }
-        tmem_ld_n<CW>(la, rr);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < CW; ++j) z[j] = __uint_as_float(rr[j]) + z[j];
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[acc]);
-      }
       // B1: norms complete; the previous tile's queue and staging are done with
       if (named_bar_or(kQBar, kQThreads, late || abort_flag)) { abort_flag = 1; break; }
       // the first tile on a new B buffer: the other buffer's last reader was the
@@ -425,21 +419,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float nx = sqrtf(((nsq_s[row] + nsq_s[kTile + row]) + nsq_s[2 * kTile + row]) +
                              nsq_s[3 * kTile + row]);
       const bool tiny = MODE == KVC_MODE_CODEBOOK && nx < 1e-18f;
-      if (row < n) {
-        unsigned char* crow = codes_s + row * ks;
-        // fast path: every code, and a mask of the ones near a boundary
+      const float rnx = MODE == KVC_MODE_CODEBOOK && !tiny ? t.inv_scale * (1.f / nx) : 0.f;
+      const bool live = row < n;
+      unsigned char* crow = codes_s + row * ks;
+      // components in sub-blocks of SB: z = hi + (mid + lo) from TMEM, the
+      // fast-path codes, a mask of the ones near a boundary
+      tc_fence_after();
+      const uint32_t la0 = taddr0 + acc * t.acc_stride + lane_off + cblk * CW;
+#pragma unroll
+      for (int sb = 0; sb < CW / SB; ++sb) {
+        float z[SB];
+        {
+          const uint32_t la = la0 + sb * SB;
+          uint32_t rr[SB];
+#pragma unroll
+          for (int j = 0; j < SB; ++j) z[j] = 0.f;
+          for (int pc = t.npieces - 1; pc >= 1; --pc) {
+            tmem_ld_n<SB>(la + pc * rpad, rr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < SB; ++j) z[j] += __uint_as_float(rr[j]);
+          }
+          tmem_ld_n<SB>(la, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < SB; ++j) z[j] = __uint_as_float(rr[j]) + z[j];
+        }
+        if (!live) continue;
         uint32_t nmask = 0;
 #pragma unroll
-        for (int j = 0; j < CW; ++j) {
-          const int k = cblk * CW + j;  // < rpad; components past r are not kept
+        for (int j = 0; j < SB; ++j) {
+          const int k = cblk * CW + sb * SB + j;  // < rpad; components past r are not kept
           const uint32_t qk = tb.qk[k];
           const int kp = (qk >> 16) == 0xFFFFu ? ks - 1 : (int)(qk >> 16);  // not kept: scratch byte
           float uf, tf;
           bool near;
           const int code = MODE == KVC_MODE_UNIFORM
                                ? fast_uniform(tb, k, qk, z[j], nx, uf, tf, near)
-                               : fast_codebook(p, tb, k, mids_s, z[j], t.inv_scale, t.gamma, nx,
-                                               eps_n, cmax, tiny, uf, tf, near);
+                               : fast_codebook(p, tb, k, mids_s, mreg, z[j], rnx, t.gamma, eps_n,
+                                               cmax, tiny, uf, tf, near);
           crow[kp] = (uint8_t)code;
           nmask |= (uint32_t)near << j;
         }
@@ -448,16 +466,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ovf = 0;
         if (nmask) {
 #pragma unroll
-          for (int j = 0; j < CW; ++j) {
+          for (int j = 0; j < SB; ++j) {
             if (!((nmask >> j) & 1u)) continue;
-            const int k = cblk * CW + j;
+            const int k = cblk * CW + sb * SB + j;
             float uf, tf;
             bool near;
             if (MODE == KVC_MODE_UNIFORM)
               fast_uniform(tb, k, tb.qk[k], z[j], nx, uf, tf, near);
             else
-              fast_codebook(p, tb, k, mids_s, z[j], t.inv_scale, t.gamma, nx, eps_n, cmax, tiny, uf,
-                            tf, near);
+              fast_codebook(p, tb, k, mids_s, mreg, z[j], rnx, t.gamma, eps_n, cmax, tiny, uf, tf,
+                            near);
             const unsigned q = atomicAdd(&qcount, 1u);
             if (q < kQueue) {
               queue[q] = ((uint32_t)row << 16) | (uint32_t)k;
@@ -468,10 +486,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         for (; ovf; ovf &= ovf - 1) {
-          const int k = cblk * CW + (__ffs(ovf) - 1);
+          const int k = cblk * CW + sb * SB + (__ffs(ovf) - 1);
           refine_ws<MODE, BF16, false>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside, row, k, 0,
                                        0.f, 0.f);
         }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (live) {
         if (MODE == KVC_MODE_CODEBOOK && cblk == 0) {
           if (tiny || !same_half(nx * (1.f - eps_n), nx * (1.f + eps_n))) {
             const unsigned q = atomicAdd(&qcount, 1u);

@@ -534,43 +534,60 @@ __device__ __forceinline__ void load8(const void* x, int dt, int64_t off, float 
   }
 }
 
+// One token row, 16 values per thread: its absmax over the TPR threads, the
+// int8 codes q = rint(v / s), s = max(a / 127, 1e-8), and fp16(s).  Returns
+// the number of codes re-decided.  The fast u = v fl(127 / a) is within
+// 1.5e-5 of 127 v / a (two roundings, |u| <= 127, so no clamp is needed); a
+// code within 3e-5 of a half is decided exactly: for 16-bit inputs 254 |v|
+// and (2k + 1) a are exact in fp32 (at most 19 significant bits each), so the
+// sign of their difference decides it; an exact tie, fp32 inputs, a < 2e-6
+// and a >= 1e30 take the float64 path.
 template <int TPR>
-__device__ __forceinline__ void append_int8_row(const Params& p, const AppendArgs& a, int slot,
-                                                int64_t t, int j) {
+__device__ __forceinline__ unsigned append_int8_row(const Params& p, const AppendArgs& a, int slot,
+                                                    int64_t t, int j) {
   const bool valid = t < a.T;
-  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = 0.f;
   if (valid) {
     const int b = slot / p.H, h = slot - b * p.H;
-    load8(a.x, p.in_dtype, (int64_t)b * a.sb + (int64_t)h * a.sh + t * a.st + 8 * j, v);
+    const int64_t off = (int64_t)b * a.sb + (int64_t)h * a.sh + t * a.st + 16 * j;
+    float (&v0)[8] = *reinterpret_cast<float(*)[8]>(&v[0]);
+    float (&v1)[8] = *reinterpret_cast<float(*)[8]>(&v[8]);
+    load8(a.x, p.in_dtype, off, v0);
+    load8(a.x, p.in_dtype, off + 8, v1);
   }
   float am = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(v[i]));
+  for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(v[i]));
 #pragma unroll
   for (int o = TPR / 2; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, o));
   unsigned nref = 0;
   if (valid) {
     const bool slow = !(am > 2e-6f);
+    const bool exact16 = p.in_dtype != KVC_F32 && am < 1e30f;  // no overflow in 254 v
     const float inv = slow ? 0.f : 127.f / am;
     double s64 = -1.0;
-    uint32_t packed[2] = {0u, 0u};
+    uint32_t packed[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 16; ++i) {
       const float u = v[i] * inv;
-      const float au = fabsf(u);
-      float q;
-      if (slow || fabsf(au - floorf(au) - 0.5f) < 1e-4f) {
-        if (s64 < 0.0) s64 = fmax((double)am / 127.0, 1e-8);
-        q = (float)rint((double)v[i] / s64);
+      float q = rintf(u);
+      if (slow || fabsf(u - q) > 0.5f - 3e-5f) {
         ++nref;
-      } else {
-        q = rintf(u);
+        const float k = floorf(fabsf(u));
+        const float d = exact16 && !slow ? 254.f * fabsf(v[i]) - (2.f * k + 1.f) * am : 0.f;
+        if (d != 0.f) {
+          q = copysignf(d > 0.f ? k + 1.f : k, v[i]);
+        } else {  // an exact tie, fp32 input or a tiny row: as float64 decides it
+          if (s64 < 0.0) s64 = fmax((double)am / 127.0, 1e-8);
+          q = (float)fmin(fmax(rint((double)v[i] / s64), -127.0), 127.0);
+        }
       }
-      const int qi = (int)fminf(fmaxf(q, -127.f), 127.f);
-      packed[i >> 2] |= ((uint32_t)qi & 0xffu) << (8 * (i & 3));
+      packed[i >> 2] |= ((uint32_t)__float2int_rn(q) & 0xffu) << (8 * (i & 3));
     }
-    uint8_t* dst = p.store + p.pay_off[slot] + (a.t_base + t) * p.D + 8 * j;
-    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+    uint8_t* dst = p.store + p.pay_off[slot] + (a.t_base + t) * p.D + 16 * j;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     if (j == 0) {
       const float s32 = am / 127.f;
       __half s16;
@@ -581,21 +598,34 @@ __device__ __forceinline__ void append_int8_row(const Params& p, const AppendArg
         s16 = __double2half(s64);
       }
       reinterpret_cast<__half*>(p.store + p.side_off[slot])[a.t_base + t] = s16;
-      if (slot == 0) atomicAdd(&p.counters[2], 1ull);
     }
   }
-  nref = __reduce_add_sync(kFull, nref);
-  if ((threadIdx.x & 31) == 0 && nref) atomicAdd(&p.counters[0], (unsigned long long)nref);
+  return nref;
 }
 
 // Grid: x over blocks of 256 / TPR tokens, y over slots (strided when there
-// are more than 65535), so no thread divides by a runtime value.
+// are more than 65535), so no thread divides by a runtime value.  Counters
+// are summed per block, then added once.
 template <int TPR>
 __global__ void __launch_bounds__(256) append_int8_vec(Params p, AppendArgs a) {
+  __shared__ unsigned blk_ref;
+  if (threadIdx.x == 0) blk_ref = 0;
+  __syncthreads();
   const int j = (int)(threadIdx.x % TPR);
   const int64_t t = (int64_t)blockIdx.x * (256 / TPR) + threadIdx.x / TPR;
+  unsigned nref = 0;
   for (int slot = blockIdx.y; slot < p.n_slots; slot += gridDim.y)
-    append_int8_row<TPR>(p, a, slot, t, j);
+    nref += append_int8_row<TPR>(p, a, slot, t, j);
+  nref = __reduce_add_sync(kFull, nref);
+  if ((threadIdx.x & 31) == 0 && nref) atomicAdd(&blk_ref, nref);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (blk_ref) atomicAdd(&p.counters[0], (unsigned long long)blk_ref);
+    if (blockIdx.y == 0) {  // tokens appended, counted on slot 0
+      const int64_t rows = min((int64_t)(256 / TPR), a.T - (int64_t)blockIdx.x * (256 / TPR));
+      if (rows > 0) atomicAdd(&p.counters[2], (unsigned long long)rows);
+    }
+  }
 }
 
 // Grid as append_int8_vec.
@@ -667,11 +697,11 @@ cudaError_t launch_append_int8(const Params& p, const AppendArgs& a, cudaStream_
                    reinterpret_cast<uintptr_t>(a.x) % 16 == 0 && (a.st * esz) % 16 == 0 &&
                    (a.sh * esz) % 16 == 0 && (a.sb * esz) % 16 == 0;
   if (vec) {
-    const int tpr = p.D / 8;
+    const int tpr = p.D / 16;  // 16 values per thread
     const dim3 grid((unsigned)((a.T * tpr + 255) / 256), (unsigned)std::min(p.n_slots, 65535));
-    if (tpr == 8) append_int8_vec<8><<<grid, 256, 0, s>>>(p, a);
-    else if (tpr == 16) append_int8_vec<16><<<grid, 256, 0, s>>>(p, a);
-    else append_int8_vec<32><<<grid, 256, 0, s>>>(p, a);
+    if (tpr == 4) append_int8_vec<4><<<grid, 256, 0, s>>>(p, a);
+    else if (tpr == 8) append_int8_vec<8><<<grid, 256, 0, s>>>(p, a);
+    else append_int8_vec<16><<<grid, 256, 0, s>>>(p, a);
   } else {
     append_int8_kernel<<<(unsigned)((toks + kI8Warps - 1) / kI8Warps), kI8Warps * 32, 0, s>>>(p, a);
   }
