@@ -104,6 +104,26 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+# ----------------------------------------------------------------------------- multi-rank
+
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Each value's maximum over the ranks (a job takes as long as its slowest
+    rank); the values unchanged on one rank."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(world, units_per_rank, ms):
+    """Whole-job units per second: every rank processes units_per_rank (weak
+    scaling replicas) in ms milliseconds."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def build_layers(wl, dev):
@@ -175,7 +195,9 @@ def gpu_arm(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    wl = WORKLOADS[args.workload]
+    wl = dict(WORKLOADS[args.workload])
+    if args.seq:
+        wl["S"] = args.seq
     B, H, D, S = wl["B"], wl["H"], wl["D"], wl["S"]
     layers, inputs = build_layers(wl, dev)
     for L in layers:
@@ -238,13 +260,10 @@ def gpu_arm(args, rank, world):
     for L in layers:
         if L.sync_status() != 0:
             raise RuntimeError("device error in the timed region")
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, = max_over_ranks([total_ms], dist, dev)
     ms_per_step = total_ms / args.steps
     units = B * H * S                                   # KV tokens per step per rank
-    value = world * units / (ms_per_step / 1e3)
+    value = job_throughput(world, units, ms_per_step)
 
     # e2e: pinned host inputs in, fetched rows out, every step
     hosts_in = [x.cpu().pin_memory() for x in inputs]
@@ -275,10 +294,7 @@ def gpu_arm(args, rank, world):
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
     e2e_ms /= e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms, = max_over_ranks([e2e_ms], dist, dev)
     if rank != 0:
         return None
 
@@ -327,7 +343,7 @@ def gpu_arm(args, rank, world):
                    "choices": list(wl.get("choices", [])), "path": args.path,
                    "parallelism": f"replicas{world}", "l2": "flushed between timed steps",
                    "step": "per tensor (K, V): trim all, append S tokens, fetch S tokens"},
-        "e2e": {"value": world * units / (e2e_ms / 1e3), "unit": "KV tokens/s",
+        "e2e": {"value": job_throughput(world, units, e2e_ms), "unit": "KV tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
         "roofline": roof,
@@ -479,6 +495,8 @@ def main():
     ap.add_argument("--path", choices=["auto", "generic"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--seq", type=int, default=0,
+                    help="tokens per (b, h) instead of the workload's S (profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
