@@ -10,8 +10,9 @@
 //   MMA (one thread)       one chain of tcgen05.mma per tile with the basis'
 //                          exact 16-bit pieces stacked along N, so x is read
 //                          once: accumulator columns [piece][component];
-//   quantiser (16 warps)   warp w owns TMEM lanes 32 (w % 4) .. (its tokens)
-//                          and a quarter w / 4 of the components: ||x||, the
+//   quantiser (2 x 8 warps) two groups take alternate tiles; warp w of a group
+//                          owns TMEM lanes 32 (w % 4) .. (its tokens) and half
+//                          w / 4 of the components: ||x||, the
 //                          fast-path codes z = hi + (mid + lo), the exact
 //                          re-decision of codes near a boundary (one warp per
 //                          queued code, V^T from shared memory), bit-packing
@@ -39,11 +40,14 @@ using namespace sm100;
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kQWarps = 16;  // quantiser warps 0..15
+// Two quantiser groups of 8 warps take alternate tiles, so one group's
+// barrier and re-decision latency hides under the other's work.  Warp w of a
+// group reads TMEM lanes 32 (w % 4) .. (its tokens) and column half w / 4.
+constexpr int kQG = 2;
+constexpr int kQWarps = 8;   // warps of one group
 constexpr int kQThreads = kQWarps * 32;
-constexpr int kProdWarp = kQWarps;
-constexpr int kMmaWarp = kQWarps + 1;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kNCB = kQWarps / 4;  // column blocks per group
+constexpr int kThreadsWs = (kQG * kQWarps + 2) * 32;
 constexpr int kMaxXS = 4, kMaxTS = 4;
 constexpr int kQBar = 1;  // named barrier of the quantiser warps
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -100,6 +104,13 @@ struct Ring {
     if (++slot == n) { slot = 0; phase ^= 1u; }
   }
 };
+
+// Shared-memory scratch of one quantiser group: code staging, packed rows,
+// the re-decision queue and its aux values, partial norms, side words.
+__host__ __device__ constexpr size_t ws_group_bytes(int ks, int pmax) {
+  return ((size_t)kTile * ks + (((size_t)kTile * pmax + 16 + 15) & ~size_t(15)) +
+          (size_t)kQueue * 12 + kNCB * kTile * 4 + kTile * 2 + 15) & ~size_t(15);
+}
 
 // Decide code k of token tt exactly (k == kNormEntry: the fp16 norm of a
 // codebook token) from x in shared memory, V^T row k (shared or global) and
@@ -201,7 +212,7 @@ __device__ __forceinline__ int fast_codebook(const Params& p, const Tab& tb, int
 }
 
 template <int MODE, bool BF16, int CW>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsWs, 1)
     append_ws_kernel(const Params p, const AppendWsArgs t, const __grid_constant__ CUtensorMap xmap,
                      const AppendArgs a) {
   extern __shared__ unsigned char smem_raw[];
@@ -212,11 +223,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t b_full[2], b_empty[2], done_bar;
   __shared__ XHdr hdr[kMaxXS];
   __shared__ uint32_t tmem_base;
-  __shared__ unsigned qcount, nside;
+  __shared__ unsigned qcount_g[2], nside_g[2];
   __shared__ volatile int abort_flag;
 
-  constexpr int rpad = 4 * CW;
+  constexpr int rpad = kNCB * CW;         // CW: components per thread
   constexpr int SB = CW < 16 ? CW : 16;  // components per TMEM read
+  constexpr int QG = kQG;
+  constexpr int kProdWarp = QG * kQWarps, kMmaWarp = kProdWarp + 1;
+  constexpr int kThreads = kThreadsWs;
   const int D = p.D, r = p.r, nbox = D / 64;
   const int XS = t.n_x, TS = t.n_acc, NB = t.n_b;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -229,27 +243,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const size_t vt_bytes = t.vt_smem ? (size_t)r * D * 4 : 0;
   unsigned char* xst = smem;                                        // XS x (x tile, table)
   unsigned char* Bs = xst + (size_t)XS * t.x_stage;                 // NB x (B, V^T)
-  unsigned char* codes_s = Bs + NB * (b_bytes + vt_bytes);          // [128][ks] chunk-aligned
-  unsigned char* out_s = codes_s + (size_t)kTile * t.ks;            // [128][P] packed rows
-  uint32_t* queue = reinterpret_cast<uint32_t*>(out_s + ((kTile * t.pmax + 16 + 15) & ~15));
-  float2* aux = reinterpret_cast<float2*>(queue + kQueue);
-  float* nsq_s = reinterpret_cast<float*>(aux + kQueue);            // [4][128]
-  float* mids_s = nsq_s + 4 * kTile;                                // [256]
+  unsigned char* grp0 = Bs + NB * (b_bytes + vt_bytes);             // QG x group scratch
+  float* mids_s = reinterpret_cast<float*>(grp0 + QG * ws_group_bytes(t.ks, t.pmax));  // [256]
   float* cb_s = mids_s + 256;                                       // [256]
-  __half* side_s = reinterpret_cast<__half*>(cb_s + 256);           // [128]
   const int tab_off = nbox * 16384;                                 // table after the x boxes
 
   if (warp == kMmaWarp) tmem_alloc(&tmem_base, t.cols);
   if (tid == 0) {
     for (int i = 0; i < XS; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], kQWarps); }
     for (int i = 0; i < TS; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], kQWarps); }
-    // a B buffer is free once the MMAs and the quantiser are both past it
-    for (int i = 0; i < 2; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], 2); }
+    // a B buffer is free once the MMAs are past it, and (V^T beside it) the
+    // quantiser too
+    for (int i = 0; i < 2; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], vt_bytes ? 2 : 1); }
     mbar_init(&done_bar, 1);
     fence_mbar_init();
     abort_flag = 0;
-    qcount = 0;
-    nside = 0;
+    qcount_g[0] = qcount_g[1] = 0;
+    nside_g[0] = nside_g[1] = 0;
   }
   if (MODE == KVC_MODE_CODEBOOK) {
     for (int j = tid; j < p.cb_levels - 1; j += kThreads) mids_s[j] = p.mids[j];
@@ -360,7 +370,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ quantiser
-    const int quarter = warp & 3, cblk = warp >> 2, row = quarter * 32 + lane;
+    const int g = warp / kQWarps, wq = warp - g * kQWarps, qt = tid - g * kQThreads;
+    const int quarter = wq & 3, cblk = wq >> 2, row = quarter * 32 + lane;
+    const int qbar = kQBar + g;
+    unsigned char* gbase = grp0 + (size_t)g * ws_group_bytes(t.ks, t.pmax);
+    unsigned char* codes_s = gbase;                                   // [128][ks] chunk-aligned
+    unsigned char* out_s = codes_s + (size_t)kTile * t.ks;            // [128][P] packed rows
+    uint32_t* queue = reinterpret_cast<uint32_t*>(out_s + ((kTile * t.pmax + 16 + 15) & ~15));
+    float2* aux = reinterpret_cast<float2*>(queue + kQueue);
+    float* nsq_s = reinterpret_cast<float*>(aux + kQueue);            // [2][128]
+    __half* side_s = reinterpret_cast<__half*>(nsq_s + kNCB * kTile); // [128]
+    unsigned& qcount = qcount_g[g];
+    unsigned& nside = nside_g[g];
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int ks = t.ks;
     const float kU = 5.9604644775390625e-08f;
@@ -373,8 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < 7; ++j)
       mreg[j] = MODE == KVC_MODE_CODEBOOK && j < p.cb_levels - 1 ? mids_s[j] : INFINITY;
     Ring rx(XS), rt(TS);
+    for (int j = 0; j < g; ++j) { rx.next(); rt.next(); }
     int prev_bs = -1;
-    for (int i = 0; i < m; ++i, rx.next(), rt.next()) {
+    for (int i = g; i < m; i += QG) {
+      if (i > g)
+        for (int j = 0; j < QG; ++j) { rx.next(); rt.next(); }
       const int s = rx.slot, acc = rt.slot;
       bool late = !mbar_wait_bounded(&x_full[s], rx.phase, kWaitNs);
       late = late || !mbar_wait_bounded(&acc_full[acc], rt.phase, kWaitNs);
@@ -386,11 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // committing this tile's accumulator) or in global memory
       const float* Vt = t.vt_smem ? reinterpret_cast<const float*>(Bs + bs * (b_bytes + vt_bytes) + b_bytes)
                                   : p.Vt + (size_t)hd.beta * r * D;
-      // partial ||x||^2 over this warp's quarter of the row
+      // partial ||x||^2 over this warp's half of the row
       {
         float sq = 0.f;
-        const int c0 = cblk * (D / 4);
-        for (int c = c0; c < c0 + D / 4; c += 8) {
+        const int c0 = cblk * (D / 2);
+        for (int c = c0; c < c0 + D / 2; c += 8) {
           const uint4 v = *reinterpret_cast<const uint4*>(
               xs + (c >> 6) * 16384 + row * 128 + ((((c & 63) >> 3) ^ (row & 7)) << 4));
           const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
@@ -411,13 +435,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         nsq_s[cblk * kTile + row] = sq;
       }
       // B1: norms complete; the previous tile's queue and staging are done with
-      if (named_bar_or(kQBar, kQThreads, late || abort_flag)) { abort_flag = 1; break; }
+      if (named_bar_or(qbar, kQThreads, late || abort_flag)) { abort_flag = 1; break; }
       // the first tile on a new B buffer: the other buffer's last reader was the
       // previous tile, finished now
-      if (tid == 0 && NB == 2 && (hd.info & 2) && prev_bs >= 0) mbar_arrive(&b_empty[bs ^ 1]);
+      if (vt_bytes && qt == 0 && NB == 2 && (hd.info & 2) && prev_bs >= 0) mbar_arrive(&b_empty[bs ^ 1]);
       prev_bs = bs;
-      const float nx = sqrtf(((nsq_s[row] + nsq_s[kTile + row]) + nsq_s[2 * kTile + row]) +
-                             nsq_s[3 * kTile + row]);
+      const float nx = sqrtf(nsq_s[row] + nsq_s[kTile + row]);
       const bool tiny = MODE == KVC_MODE_CODEBOOK && nx < 1e-18f;
       const float rnx = MODE == KVC_MODE_CODEBOOK && !tiny ? t.inv_scale * (1.f / nx) : 0.f;
       const bool live = row < n;
@@ -510,23 +533,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      named_bar_sync(kQBar, kQThreads);  // B2: fast-path codes and the queue complete
+      named_bar_sync(qbar, kQThreads);  // B2: fast-path codes and the queue complete
       const unsigned nq = qcount;
-      for (unsigned e = warp; e < min(nq, (unsigned)kQueue); e += kQWarps) {
+      for (unsigned e = wq; e < min(nq, (unsigned)kQueue); e += kQWarps) {
         const uint32_t ent = queue[e];
         const float2 ax = aux[e];
         refine_ws<MODE, BF16, true>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside,
                                     (int)(ent >> 16), (int)(ent & 0xffffu), lane, ax.x, ax.y);
       }
-      named_bar_sync(kQBar, kQThreads);  // B3: every code decided
-      if (tid == 0) {
+      named_bar_sync(qbar, kQThreads);  // B3: every code decided
+      if (qt == 0) {
         if (nq > nside) atomicAdd(&p.counters[0], (unsigned long long)(nq - nside));
         if (nside) atomicAdd(&p.counters[1], (unsigned long long)nside);
         if (hd.slot == 0) atomicAdd(&p.counters[2], (unsigned long long)n);
       }
       // pack: one thread per (token, 8-code chunk) -> w bytes, LSB-first
       const int P = hd.P;
-      for (int item = tid; item < kTile * 32; item += kQThreads) {
+      for (int item = qt; item < kTile * 32; item += kQThreads) {
         const int tt = item & (kTile - 1), c = item >> 7;
         const uint32_t ent = tb.chunk[c];
         if (!(ent >> 31)) break;  // chunks are contiguous from 0: c is past the last one
@@ -541,14 +564,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nbytes = (nc * wd + 7) >> 3;
         for (int j = 0; j < nbytes; ++j) o[j] = (unsigned char)(packed >> (8 * j));
       }
-      named_bar_sync(kQBar, kQThreads);  // B4: packed rows staged; the stage (x, table) is free
+      named_bar_sync(qbar, kQThreads);  // B4: packed rows staged; the stage (x, table) is free
       __syncwarp();
       if (lane == 0) mbar_arrive(&x_empty[s]);
       unsigned char* dst = p.store + hd.pay + hd.row0 * P;
-      for (int idx = tid; idx < n * P; idx += kQThreads) dst[idx] = out_s[idx];
-      if (MODE == KVC_MODE_CODEBOOK && tid < n)
-        reinterpret_cast<__half*>(p.store + hd.side)[hd.row0 + tid] = side_s[tid];
-      if (tid == 0) {  // the next tile starts with an empty queue (read above, before B3)
+      for (int idx = qt; idx < n * P; idx += kQThreads) dst[idx] = out_s[idx];
+      if (MODE == KVC_MODE_CODEBOOK && qt < n)
+        reinterpret_cast<__half*>(p.store + hd.side)[hd.row0 + qt] = side_s[qt];
+      if (qt == 0) {  // the next tile starts with an empty queue (read above, before B3)
         qcount = 0;
         nside = 0;
       }
@@ -567,10 +590,10 @@ using WsKernel = void (*)(const Params, const AppendWsArgs, const CUtensorMap, c
 template <int MODE, bool BF16>
 WsKernel ws_for(int rpad) {
   switch (rpad) {
-    case 16: return append_ws_kernel<MODE, BF16, 4>;
-    case 32: return append_ws_kernel<MODE, BF16, 8>;
-    case 64: return append_ws_kernel<MODE, BF16, 16>;
-    default: return append_ws_kernel<MODE, BF16, 32>;
+    case 16: return append_ws_kernel<MODE, BF16, 8>;
+    case 32: return append_ws_kernel<MODE, BF16, 16>;
+    case 64: return append_ws_kernel<MODE, BF16, 32>;
+    default: return append_ws_kernel<MODE, BF16, 64>;
   }
 }
 
@@ -668,10 +691,10 @@ size_t append_ws_plan(int D, int r, int rpad, int npieces, int pmax, int max_chu
   z.n_b = n_bases > 1 ? 2 : 1;
   z.ks = max_chunks * 8 + 8;  // the extra 8 bytes spread the rows over the banks
   const size_t limit = 226 * 1024;
-  for (int vt = 1; vt >= 0; --vt) {
+  const int qg = kQG;  // two groups: V^T stays in global memory (see the kernel)
+  for (int vt = 0; vt >= 0; --vt) {
     const size_t fixed = 1024 + (size_t)z.n_b * ((size_t)ncols * D * 2 + (vt ? (size_t)r * D * 4 : 0)) +
-                         (size_t)kTile * z.ks + (((size_t)kTile * pmax + 16 + 15) & ~size_t(15)) +
-                         (size_t)kQueue * 12 + 4 * kTile * 4 + 2 * 256 * 4 + kTile * 2;
+                         (size_t)qg * ws_group_bytes(z.ks, pmax) + 2 * 256 * 4;
     for (int xs = kMaxXS; xs >= (vt ? 3 : 2); --xs)
       if (fixed + (size_t)xs * z.x_stage <= limit) {
         z.n_x = xs;
@@ -697,7 +720,7 @@ cudaError_t launch_append_ws(const TcPlan& plan, const Params& p, const AppendAr
                        sh.acc_stride, sh.cols,      sh.n_acc,     sh.n_x,             sh.n_b,
                        sh.x_stage,    sh.tab_bytes, plan.ws_pmax, sh.ks,              sh.vt_smem,
                        plan.app_inv_scale, plan.app_gamma, tiles, total};
-  k<<<(unsigned)grid, kThreads, plan.ws_smem, s>>>(p, t, xmap, a);
+  k<<<(unsigned)grid, kThreadsWs, plan.ws_smem, s>>>(p, t, xmap, a);
   ++*nk;
   return cudaGetLastError();
 }
