@@ -44,24 +44,70 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
 // x_t . w with x_t a row of the swizzled x tile (w == nullptr: x_t . x_t),
 // compensated fp32 (TwoProd / TwoSum) finished in double.  WARP: the 32 lanes
 // split the row and the result is on every lane; else one thread does it all.
+// Double-float values (hi + lo, |lo| <= ulp(hi) / 2): ~2^-44 relative
+// precision with fp32 instructions only (fp64 throughput is very low here).
+struct ff2 {
+  float hi, lo;
+};
+
+__device__ __forceinline__ ff2 fast_two_sum(float a, float b) {  // |a| >= |b|
+  const float s = a + b;
+  return ff2{s, b - (s - a)};
+}
+__device__ __forceinline__ ff2 ff_add(ff2 a, ff2 b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  e += a.lo + b.lo;
+  return fast_two_sum(s, e);
+}
+__device__ __forceinline__ ff2 ff_mul(ff2 a, ff2 b) {
+  const float p = a.hi * b.hi;
+  float e = fmaf(a.hi, b.hi, -p);
+  e = fmaf(a.hi, b.lo, e);
+  e = fmaf(a.lo, b.hi, e);
+  return fast_two_sum(p, e);
+}
+__device__ __forceinline__ ff2 ff_sqrt(ff2 a) {  // a >= 0
+  const float h = sqrtf(a.hi);
+  if (h == 0.f) return ff2{0.f, 0.f};
+  const float r = fmaf(-h, h, a.hi) + a.lo;
+  return fast_two_sum(h, r / (2.f * h));
+}
+__device__ __forceinline__ bool ff_less(ff2 a, ff2 b) {
+  return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
+}
+
 template <bool BF16, bool WARP>
-__device__ double dot2_row(const unsigned char* xs, int t, int D, const float* w, int lane) {
+__device__ ff2 dot2_ff(const unsigned char* xs, int t, int D, const float* w, int lane) {
   float S = 0.f, C = 0.f;
-  for (int i = WARP ? lane : 0; i < D; i += WARP ? 32 : 1) {
+  auto term = [&](int i, float wv, bool self) {
     const unsigned char* src =
         xs + (i >> 6) * 16384 + t * 128 + ((((i & 63) >> 3) ^ (t & 7)) << 4) + (i & 7) * 2;
     const uint16_t raw = *reinterpret_cast<const uint16_t*>(src);
     const float xv = BF16 ? __bfloat162float(__ushort_as_bfloat16(raw))
                           : __half2float(__ushort_as_half(raw));
-    const float wv = w ? w[i] : xv;
-    const float pr = xv * wv;
-    const float pe = fmaf(xv, wv, -pr);
+    const float wx = self ? xv : wv;
+    const float pr = xv * wx;
+    const float pe = fmaf(xv, wx, -pr);
     float s, e;
     two_sum(S, pr, s, e);
     S = s;
     C += pe + e;
-  }
+  };
   if (WARP) {
+    // the lane's (at most 8) entries of w are loaded before the arithmetic:
+    // one memory latency instead of one per entry
+    float wv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = lane + 32 * j;
+      wv[j] = (w && i < D) ? w[i] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = lane + 32 * j;
+      if (i < D) term(i, wv[j], w == nullptr);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float So = __shfl_xor_sync(0xffffffffu, S, o);
@@ -71,8 +117,18 @@ __device__ double dot2_row(const unsigned char* xs, int t, int D, const float* w
       S = s;
       C = C + Co + e;
     }
+  } else {
+    for (int i = 0; i < D; ++i) term(i, w ? w[i] : 0.f, w == nullptr);
   }
-  return (double)S + (double)C;
+  float s, e;
+  two_sum(S, C, s, e);
+  return ff2{s, e};
+}
+
+template <bool BF16, bool WARP>
+__device__ double dot2_row(const unsigned char* xs, int t, int D, const float* w, int lane) {
+  const ff2 v = dot2_ff<BF16, WARP>(xs, t, D, w, lane);
+  return (double)v.hi + (double)v.lo;
 }
 
 // Decide code k of token tt exactly (or, k == kNormEntry, the fp16 norm of a

@@ -60,7 +60,7 @@ struct AppendWsArgs {
   int n_acc, n_x, n_b;      // accumulators, x stages, B buffers
   int x_stage, tab_bytes, pmax;
   int ks;                   // bytes per token row of the code staging (chunk-aligned)
-  int vt_smem;              // V^T of the basis kept in shared memory beside B
+  int vt_smem;              // each group keeps its basis' V^T in shared memory
   float inv_scale, gamma;
   int tiles_per_slot, total_tiles;
 };
@@ -68,20 +68,21 @@ struct AppendWsArgs {
 // Per-basis quantiser table (host layout in append_ws_table), per component:
 //   q4    uniform fast path u = fma(z, A, Bc), bound tau = fma(T1, ||x||, T2)
 //         (A = 2^-s / step, Bc = -(mean . V_k + lo) / step; see the plan);
-//   c64   mean . V_k, inv64 1/step (double), lo, vn = ||V_k|| (rounded up);
+//   cff   mean . V_k, iff 1/step (as double-float pairs), lo, vn = ||V_k||
+//         (rounded up);
 //   qk    qmax | chunk-aligned position << 16 (0xFFFF: not kept);
 // then the pack chunks.
 struct Tab {
   const float4* q4;
-  const double *c64, *inv64;
+  const float2 *cff, *iff;
   const float *lo, *vn;
   const uint32_t* qk;
   const uint32_t* chunk;  // [32]: first byte | width << 16 | (codes - 1) << 20 | valid << 31
   __device__ Tab(const unsigned char* base, int rpad)
       : q4(reinterpret_cast<const float4*>(base)),
-        c64(reinterpret_cast<const double*>(q4 + rpad)),
-        inv64(c64 + rpad),
-        lo(reinterpret_cast<const float*>(inv64 + rpad)),
+        cff(reinterpret_cast<const float2*>(q4 + rpad)),
+        iff(cff + rpad),
+        lo(reinterpret_cast<const float*>(iff + rpad)),
         vn(lo + rpad),
         qk(reinterpret_cast<const uint32_t*>(vn + rpad)),
         chunk(qk + rpad) {}
@@ -113,10 +114,11 @@ __host__ __device__ constexpr size_t ws_group_bytes(int ks, int pmax) {
 }
 
 // Decide code k of token tt exactly (k == kNormEntry: the fp16 norm of a
-// codebook token) from x in shared memory, V^T row k (shared or global) and
-// the basis table; lane 0 (or the lone thread) writes the result.
-// Division-free (fp64 is slow here): 1/step in double, and the nearest
-// centroid found by comparing z against the midpoints scaled by ||x||.
+// codebook token) from x in shared memory, V^T row k and the basis table;
+// lane 0 (or the lone thread) writes the result.  Double-float arithmetic
+// (no fp64: its throughput is very low here): z from the compensated dot,
+// u = (z - c - lo) (1/step), rounded half to even on the exact pair; the
+// nearest centroid by comparing z with the exact midpoints times ||x||.
 template <int MODE, bool BF16, bool WARP>
 __device__ void refine_ws(const Params& p, const Tab& tb, const float* Vt, const float* cb_s,
                           const unsigned char* xs, unsigned char* codes_s, int ks, __half* side_s,
@@ -124,38 +126,59 @@ __device__ void refine_ws(const Params& p, const Tab& tb, const float* Vt, const
   const int D = p.D;
   const int kp = k == (int)kNormEntry ? 0 : (int)(tb.qk[k] >> 16);
   if (MODE == KVC_MODE_UNIFORM) {
-    const double z64 = dot2_row<BF16, WARP>(xs, tt, D, Vt + (size_t)k * D, lane) - tb.c64[k];
+    const ff2 z = dot2_ff<BF16, WARP>(xs, tt, D, Vt + (size_t)k * D, lane);
     if (lane == 0) {
+      const float2 c = tb.cff[k], iv = tb.iff[k];
+      const ff2 zl = ff_add(ff_add(z, ff2{-c.x, -c.y}), ff2{-tb.lo[k], 0.f});
+      const ff2 u = ff_mul(zl, ff2{iv.x, iv.y});
+      // rint of hi + lo: f = hi - rint(hi) is exact; lo moves the result only
+      // from an exact half of hi
+      const float r = rintf(u.hi), f = u.hi - r;
+      float q = r;
+      if (f == 0.5f && u.lo > 0.f) q = r + 1.f;
+      else if (f == -0.5f && u.lo < 0.f) q = r - 1.f;
       const int qmax = (int)(tb.qk[k] & 0xffffu);
-      const double u64 = (z64 - (double)tb.lo[k]) * tb.inv64[k];
-      codes_s[tt * ks + kp] = (uint8_t)(int)fmin(fmax(rint(u64), 0.0), (double)qmax);
+      codes_s[tt * ks + kp] = (uint8_t)(int)fminf(fmaxf(q, 0.f), (float)qmax);
       if (tau > 0.f) atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(
-                                                   fabsf(uf - (float)u64) / tau));
+                                                   fabsf(uf - u.hi) / tau));
     }
   } else {
-    const double n64 = sqrt(dot2_row<BF16, WARP>(xs, tt, D, nullptr, lane));
+    const ff2 nrm = ff_sqrt(dot2_ff<BF16, WARP>(xs, tt, D, nullptr, lane));
     if (k == (int)kNormEntry) {
       if (lane == 0) {
-        side_s[tt] = __double2half(n64);
+        // fp16 of hi + lo: hi's rounding, unless hi is exactly halfway between
+        // two fp16 values, where lo's sign decides (0: hi's own tie rule)
+        __half h = __float2half_rn(nrm.hi);
+        const float hf = __half2float(h);
+        if (hf != nrm.hi && nrm.lo != 0.f) {
+          const unsigned short hb = __half_as_ushort(h);
+          const unsigned short ob = hf < nrm.hi ? (unsigned short)(hb + 1) : (unsigned short)(hb - 1);
+          const float of = __half2float(__ushort_as_half(ob));
+          if (0.5f * (hf + of) == nrm.hi && ((of > hf) == (nrm.lo > 0.f))) h = __ushort_as_half(ob);
+        }
+        side_s[tt] = h;
         atomicAdd(nside, 1u);
       }
     } else {
-      const double z64 = dot2_row<BF16, WARP>(xs, tt, D, Vt + (size_t)k * D, lane);
+      const ff2 z = dot2_ff<BF16, WARP>(xs, tt, D, Vt + (size_t)k * D, lane);
       if (lane == 0) {
         // nearest centroid, ties to the lower one: the number of exact
-        // midpoints m (double, from the fp32 centroids) with m ||x|| < z;
-        // ||x|| = 0 means u = 0
-        const double nn = n64 > 0.0 ? n64 : 1.0, zz = n64 > 0.0 ? z64 : 0.0;
+        // midpoints m (double-float, from the fp32 centroids) with
+        // m ||x|| < z; ||x|| = 0 means u = 0
+        const bool zero = nrm.hi == 0.f;
         int lo_i = 0, hi_i = p.cb_levels - 1;
         while (lo_i < hi_i) {
           const int mid = (lo_i + hi_i) >> 1;
-          const double m = 0.5 * ((double)cb_s[mid] + (double)cb_s[mid + 1]);
-          if (m * nn < zz) lo_i = mid + 1; else hi_i = mid;
+          float ms, me;
+          two_sum(cb_s[mid], cb_s[mid + 1], ms, me);
+          const ff2 m{0.5f * ms, 0.5f * me};
+          const bool below = zero ? m.hi < 0.f : ff_less(ff_mul(m, nrm), z);
+          if (below) lo_i = mid + 1; else hi_i = mid;
         }
         codes_s[tt * ks + kp] = (uint8_t)lo_i;
-        if (tau > 0.f && n64 > 0.0)
+        if (tau > 0.f && !zero)
           atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(
-                                        fabsf(uf - (float)z64 / (float)n64) / tau));
+                                        fabsf(uf - z.hi / nrm.hi) / tau));
       }
     }
   }
@@ -240,11 +263,12 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
   const int tps = t.tiles_per_slot;
   const size_t b_bytes = (size_t)t.npieces * rpad * D * 2;
 
-  const size_t vt_bytes = t.vt_smem ? (size_t)r * D * 4 : 0;
+  const size_t vt_bytes = t.vt_smem ? (size_t)r * D * 4 : 0;  // per group
   unsigned char* xst = smem;                                        // XS x (x tile, table)
   unsigned char* Bs = xst + (size_t)XS * t.x_stage;                 // NB x (B, V^T)
-  unsigned char* grp0 = Bs + NB * (b_bytes + vt_bytes);             // QG x group scratch
-  float* mids_s = reinterpret_cast<float*>(grp0 + QG * ws_group_bytes(t.ks, t.pmax));  // [256]
+  unsigned char* grp0 = Bs + NB * b_bytes;                          // QG x group scratch
+  float* vt0 = reinterpret_cast<float*>(grp0 + QG * ws_group_bytes(t.ks, t.pmax));  // QG x V^T
+  float* mids_s = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(vt0) + QG * vt_bytes);
   float* cb_s = mids_s + 256;                                       // [256]
   const int tab_off = nbox * 16384;                                 // table after the x boxes
 
@@ -252,9 +276,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
   if (tid == 0) {
     for (int i = 0; i < XS; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], kQWarps); }
     for (int i = 0; i < TS; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], kQWarps); }
-    // a B buffer is free once the MMAs are past it, and (V^T beside it) the
-    // quantiser too
-    for (int i = 0; i < 2; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], vt_bytes ? 2 : 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&b_full[i], 1); mbar_init(&b_empty[i], 1); }
     mbar_init(&done_bar, 1);
     fence_mbar_init();
     abort_flag = 0;
@@ -300,11 +322,9 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
           bslot = NB == 2 ? bslot ^ 1 : 0;
           if (bload[bslot] > 0 &&
               !mbar_wait_bounded(&b_empty[bslot], (bload[bslot] - 1) & 1, kWaitNs)) { abort_flag = 1; break; }
-          unsigned char* bdst = Bs + bslot * (b_bytes + vt_bytes);
-          mbar_arrive_expect_tx(&b_full[bslot], (uint32_t)(b_bytes + vt_bytes));
-          bulk_load(bdst, t.B + (size_t)beta * (b_bytes / 2), (uint32_t)b_bytes, &b_full[bslot]);
-          if (vt_bytes)
-            bulk_load(bdst + b_bytes, p.Vt + (size_t)beta * r * D, (uint32_t)vt_bytes, &b_full[bslot]);
+          mbar_arrive_expect_tx(&b_full[bslot], (uint32_t)b_bytes);
+          bulk_load(Bs + bslot * b_bytes, t.B + (size_t)beta * (b_bytes / 2), (uint32_t)b_bytes,
+                    &b_full[bslot]);
           ++bload[bslot];
           cur_beta = beta;
           first_use = 1;
@@ -355,7 +375,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
         if (i >= TS && !mbar_wait_bounded(&acc_empty[acc], rt.phase ^ 1u, kWaitNs)) { abort_flag = 1; break; }
         tc_fence_after();
         const uint32_t xa = smem_u32(xst + (size_t)s * t.x_stage);
-        const uint32_t b0 = smem_u32(Bs + bs * (b_bytes + vt_bytes));
+        const uint32_t b0 = smem_u32(Bs + bs * b_bytes);
         const uint32_t d0 = taddr0 + acc * t.acc_stride;
         for (int pc = 0; pc < (stacked ? 1 : t.npieces); ++pc)
           for (int ks = 0; ks < D / 16; ++ks) {
@@ -382,6 +402,8 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
     __half* side_s = reinterpret_cast<__half*>(nsq_s + kNCB * kTile); // [128]
     unsigned& qcount = qcount_g[g];
     unsigned& nside = nside_g[g];
+    float* vt_s = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(vt0) + g * vt_bytes);
+    int vt_beta = -1;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int ks = t.ks;
     const float kU = 5.9604644775390625e-08f;
@@ -395,7 +417,6 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       mreg[j] = MODE == KVC_MODE_CODEBOOK && j < p.cb_levels - 1 ? mids_s[j] : INFINITY;
     Ring rx(XS), rt(TS);
     for (int j = 0; j < g; ++j) { rx.next(); rt.next(); }
-    int prev_bs = -1;
     for (int i = g; i < m; i += QG) {
       if (i > g)
         for (int j = 0; j < QG; ++j) { rx.next(); rt.next(); }
@@ -405,11 +426,21 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       const unsigned char* xs = xst + (size_t)s * t.x_stage;
       const Tab tb(xs + tab_off, rpad);
       const XHdr hd = hdr[s];
-      const int n = hd.n, bs = hd.info & 1;
+      const int n = hd.n;
       // V^T for the re-decision: beside B (visible: the MMA waited for B before
       // committing this tile's accumulator) or in global memory
-      const float* Vt = t.vt_smem ? reinterpret_cast<const float*>(Bs + bs * (b_bytes + vt_bytes) + b_bytes)
-                                  : p.Vt + (size_t)hd.beta * r * D;
+      // V^T for the re-decision: the group's copy (refreshed when the basis
+      // changes; B1 below publishes it) or global memory
+      const float* Vt = p.Vt + (size_t)hd.beta * r * D;
+      if (t.vt_smem) {
+        if (hd.beta != vt_beta) {
+          const float4* src = reinterpret_cast<const float4*>(Vt);
+          float4* dst = reinterpret_cast<float4*>(vt_s);
+          for (int e = qt; e < r * D / 4; e += kQThreads) dst[e] = src[e];
+          vt_beta = hd.beta;
+        }
+        Vt = vt_s;
+      }
       // partial ||x||^2 over this warp's half of the row
       {
         float sq = 0.f;
@@ -438,8 +469,6 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       if (named_bar_or(qbar, kQThreads, late || abort_flag)) { abort_flag = 1; break; }
       // the first tile on a new B buffer: the other buffer's last reader was the
       // previous tile, finished now
-      if (vt_bytes && qt == 0 && NB == 2 && (hd.info & 2) && prev_bs >= 0) mbar_arrive(&b_empty[bs ^ 1]);
-      prev_bs = bs;
       const float nx = sqrtf(nsq_s[row] + nsq_s[kTile + row]);
       const bool tiny = MODE == KVC_MODE_CODEBOOK && nx < 1e-18f;
       const float rnx = MODE == KVC_MODE_CODEBOOK && !tiny ? t.inv_scale * (1.f / nx) : 0.f;
@@ -449,7 +478,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       // fast-path codes, a mask of the ones near a boundary
       tc_fence_after();
       const uint32_t la0 = taddr0 + acc * t.acc_stride + lane_off + cblk * CW;
-#pragma unroll
+#pragma unroll(CW <= 16 ? CW / SB : 1)  // wide ranks: one sub-block of code, not CW / SB
       for (int sb = 0; sb < CW / SB; ++sb) {
         float z[SB];
         {
@@ -619,9 +648,9 @@ int append_ws_table(const Geo& g, const kvc_layer_desc& d, int rpad, const doubl
                     double inv_scale, double gamma, int b, unsigned char* out) {
   const int r = g.r, D = d.D;
   float4* q4 = reinterpret_cast<float4*>(out);
-  double* c = reinterpret_cast<double*>(q4 + rpad);
-  double* inv64 = c + rpad;
-  float* lo = reinterpret_cast<float*>(inv64 + rpad);
+  float2* cff = reinterpret_cast<float2*>(q4 + rpad);
+  float2* iff = cff + rpad;
+  float* lo = reinterpret_cast<float*>(iff + rpad);
   float* vn = lo + rpad;
   uint32_t* qk = reinterpret_cast<uint32_t*>(vn + rpad);
   uint32_t* chunk = qk + rpad;
@@ -635,9 +664,13 @@ int append_ws_table(const Geo& g, const kvc_layer_desc& d, int rpad, const doubl
       ss += v * v;
     }
     vn[k] = in ? std::nextafter((float)std::sqrt(ss), INFINITY) : 0.f;
-    c[k] = in ? c64[bk] : 0.0;
+    const auto pair = [](double v) {  // v as hi + lo, two floats
+      const float hi = (float)v;
+      return make_float2(hi, (float)(v - (double)hi));
+    };
+    cff[k] = pair(in ? c64[bk] : 0.0);
     lo[k] = q ? d.qmin[bk] : 0.f;
-    inv64[k] = q ? 1.0 / (double)d.qstep[bk] : 0.0;
+    iff[k] = pair(q ? 1.0 / (double)d.qstep[bk] : 0.0);
     q4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (q) {
       // u = fma(z_tc, A, Bc) with A, Bc rounded once from double.  |u - u_exact|
@@ -691,10 +724,10 @@ size_t append_ws_plan(int D, int r, int rpad, int npieces, int pmax, int max_chu
   z.n_b = n_bases > 1 ? 2 : 1;
   z.ks = max_chunks * 8 + 8;  // the extra 8 bytes spread the rows over the banks
   const size_t limit = 226 * 1024;
-  const int qg = kQG;  // two groups: V^T stays in global memory (see the kernel)
-  for (int vt = 0; vt >= 0; --vt) {
-    const size_t fixed = 1024 + (size_t)z.n_b * ((size_t)ncols * D * 2 + (vt ? (size_t)r * D * 4 : 0)) +
-                         (size_t)qg * ws_group_bytes(z.ks, pmax) + 2 * 256 * 4;
+  for (int vt = 1; vt >= 0; --vt) {  // the groups' V^T copies where they fit
+    const size_t fixed = 1024 + (size_t)z.n_b * ncols * D * 2 +
+                         (size_t)kQG * (ws_group_bytes(z.ks, pmax) + (vt ? (size_t)r * D * 4 : 0)) +
+                         2 * 256 * 4;
     for (int xs = kMaxXS; xs >= (vt ? 3 : 2); --xs)
       if (fixed + (size_t)xs * z.x_stage <= limit) {
         z.n_x = xs;
