@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "kvc_ff.cuh"
 #include "kvc_internal.h"
 
 namespace kvc {
@@ -35,48 +36,10 @@ struct AppendTc {
   float inv_scale, gamma;
 };
 
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = a + b;
-  const float bb = s - a;
-  e = (a - (s - bb)) + (b - bb);
-}
 
 // x_t . w with x_t a row of the swizzled x tile (w == nullptr: x_t . x_t),
 // compensated fp32 (TwoProd / TwoSum) finished in double.  WARP: the 32 lanes
 // split the row and the result is on every lane; else one thread does it all.
-// Double-float values (hi + lo, |lo| <= ulp(hi) / 2): ~2^-44 relative
-// precision with fp32 instructions only (fp64 throughput is very low here).
-struct ff2 {
-  float hi, lo;
-};
-
-__device__ __forceinline__ ff2 fast_two_sum(float a, float b) {  // |a| >= |b|
-  const float s = a + b;
-  return ff2{s, b - (s - a)};
-}
-__device__ __forceinline__ ff2 ff_add(ff2 a, ff2 b) {
-  float s, e;
-  two_sum(a.hi, b.hi, s, e);
-  e += a.lo + b.lo;
-  return fast_two_sum(s, e);
-}
-__device__ __forceinline__ ff2 ff_mul(ff2 a, ff2 b) {
-  const float p = a.hi * b.hi;
-  float e = fmaf(a.hi, b.hi, -p);
-  e = fmaf(a.hi, b.lo, e);
-  e = fmaf(a.lo, b.hi, e);
-  return fast_two_sum(p, e);
-}
-__device__ __forceinline__ ff2 ff_sqrt(ff2 a) {  // a >= 0
-  const float h = sqrtf(a.hi);
-  if (h == 0.f) return ff2{0.f, 0.f};
-  const float r = fmaf(-h, h, a.hi) + a.lo;
-  return fast_two_sum(h, r / (2.f * h));
-}
-__device__ __forceinline__ bool ff_less(ff2 a, ff2 b) {
-  return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
-}
-
 template <bool BF16, bool WARP>
 __device__ ff2 dot2_ff(const unsigned char* xs, int t, int D, const float* w, int lane) {
   float S = 0.f, C = 0.f;

@@ -131,12 +131,7 @@ __device__ void refine_ws(const Params& p, const Tab& tb, const float* Vt, const
       const float2 c = tb.cff[k], iv = tb.iff[k];
       const ff2 zl = ff_add(ff_add(z, ff2{-c.x, -c.y}), ff2{-tb.lo[k], 0.f});
       const ff2 u = ff_mul(zl, ff2{iv.x, iv.y});
-      // rint of hi + lo: f = hi - rint(hi) is exact; lo moves the result only
-      // from an exact half of hi
-      const float r = rintf(u.hi), f = u.hi - r;
-      float q = r;
-      if (f == 0.5f && u.lo > 0.f) q = r + 1.f;
-      else if (f == -0.5f && u.lo < 0.f) q = r - 1.f;
+      const float q = ff_rint(u);
       const int qmax = (int)(tb.qk[k] & 0xffffu);
       codes_s[tt * ks + kp] = (uint8_t)(int)fminf(fmaxf(q, 0.f), (float)qmax);
       if (tau > 0.f) atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(
@@ -146,16 +141,7 @@ __device__ void refine_ws(const Params& p, const Tab& tb, const float* Vt, const
     const ff2 nrm = ff_sqrt(dot2_ff<BF16, WARP>(xs, tt, D, nullptr, lane));
     if (k == (int)kNormEntry) {
       if (lane == 0) {
-        // fp16 of hi + lo: hi's rounding, unless hi is exactly halfway between
-        // two fp16 values, where lo's sign decides (0: hi's own tie rule)
-        __half h = __float2half_rn(nrm.hi);
-        const float hf = __half2float(h);
-        if (hf != nrm.hi && nrm.lo != 0.f) {
-          const unsigned short hb = __half_as_ushort(h);
-          const unsigned short ob = hf < nrm.hi ? (unsigned short)(hb + 1) : (unsigned short)(hb - 1);
-          const float of = __half2float(__ushort_as_half(ob));
-          if (0.5f * (hf + of) == nrm.hi && ((of > hf) == (nrm.lo > 0.f))) h = __ushort_as_half(ob);
-        }
+        const __half h = ff_to_half(nrm);
         side_s[tt] = h;
         atomicAdd(nside, 1u);
       }

@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "kvc_ff.cuh"
 #include "kvc_internal.h"
 
 namespace kvc {
@@ -50,11 +51,6 @@ __device__ __forceinline__ float warp_maxf(float v) {
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
   return v;
 }
-__device__ __forceinline__ double warp_maxd(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(kFull, v, o));
-  return v;
-}
 
 // gamma_n = n u / (1 - n u)
 __device__ __forceinline__ float gamma_n(int n) {
@@ -68,6 +64,36 @@ __device__ __forceinline__ double dot64(const float* x, const float* m, const fl
   double acc = 0.0;
   for (int i = lane; i < n; i += 32) acc = fma((double)x[i] - (double)m[i], (double)w[i], acc);
   return warp_sum(acc);
+}
+
+// sum_i (x_i - m_i) * w_i as a double-float (compensated fp32: x - m and each
+// product split exactly, TwoSum accumulation), one warp, on every lane.
+__device__ __forceinline__ ff2 dot_ff(const float* x, const float* m, const float* w, int n,
+                                      int lane) {
+  float S = 0.f, C = 0.f;
+  for (int i = lane; i < n; i += 32) {
+    float dh, dl;
+    two_sum(x[i], -m[i], dh, dl);
+    const float wi = w[i];
+    const float pr = dh * wi;
+    const float pe = fmaf(dh, wi, -pr);
+    float s, e;
+    two_sum(S, pr, s, e);
+    S = s;
+    C += pe + e + dl * wi;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float So = __shfl_xor_sync(kFull, S, o);
+    const float Co = __shfl_xor_sync(kFull, C, o);
+    float s, e;
+    two_sum(S, So, s, e);
+    S = s;
+    C = C + Co + e;
+  }
+  float s, e;
+  two_sum(S, C, s, e);
+  return ff2{s, e};
 }
 
 // sum_i x_i^2 in double precision, one warp.
@@ -174,18 +200,28 @@ __device__ void quant_group(const Params& p, int beta, const float* vnorm, const
       atomicAdd(nref, (unsigned)__popc(nmask));
       atomicAdd(nside, 1u);
     }
-    double zmine = 0.0;
+    // double-float throughout (fp64 throughput is very low here)
+    ff2 zmine{0.f, 0.f};
     while (todo) {
       const int f = __ffs(todo) - 1;
       todo &= todo - 1;
-      const double z64 =
-          dot64(c.xs, c.mean, p.Vt + ((int64_t)beta * p.r + first + f) * p.d_in, p.d_in, lane);
-      if (lane == f) zmine = z64;
+      const ff2 z2 =
+          dot_ff(c.xs, c.mean, p.Vt + ((int64_t)beta * p.r + first + f) * p.d_in, p.d_in, lane);
+      if (lane == f) zmine = z2;
     }
-    const double a64 = warp_maxd(cand ? fabs(zmine) : 0.0);
-    const double s64 = fmax(a64 / (double)qmax, 1e-8);
-    s16 = __double2half(s64);
-    if ((nmask >> lane) & 1u) q = (int)fmin(fmax(rint(zmine / s64), -(double)qmax), (double)qmax);
+    ff2 a2 = cand ? ff_abs(zmine) : ff2{0.f, 0.f};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const ff2 b2{__shfl_xor_sync(kFull, a2.hi, o), __shfl_xor_sync(kFull, a2.lo, o)};
+      if (ff_less(a2, b2)) a2 = b2;
+    }
+    // s = max(a / qmax, 1e-8), the floor as the double 1e-8 in two floats
+    ff2 s2 = ff_div_f(a2, (float)qmax);
+    const ff2 floor2{1e-8f, (float)(1e-8 - (double)1e-8f)};  // folded at compile time
+    if (ff_less(s2, floor2)) s2 = floor2;
+    s16 = ff_to_half(s2);
+    if ((nmask >> lane) & 1u)
+      q = (int)fminf(fmaxf(ff_rint(ff_div(zmine, s2)), -(float)qmax), (float)qmax);
   }
   if (valid) c.codes[k] = (uint8_t)(q + off);
   if (lane == 0) c.side[gi] = s16;
