@@ -58,6 +58,15 @@ __device__ __forceinline__ float gamma_n(int n) {
   return nu / (1.f - nu);
 }
 
+// The projection sums d_in products in blocks of kProjBlk (fp32 fma), then
+// adds the block sums: every term passes through at most kProjBlk + (number
+// of blocks) roundings, plus one for x - mean, so the error is at most
+// gamma_{that + 1} sum |(x_i - m_i) V_ik| <= gamma ||x - m|| ||V_k||.
+constexpr int kProjBlk = 32;
+__device__ __forceinline__ float proj_gamma(int d_in) {
+  return gamma_n(kProjBlk + (d_in + kProjBlk - 1) / kProjBlk + 2);
+}
+
 // sum_i (x_i - m_i) * w_i in double precision, one warp, result on every lane.
 __device__ __forceinline__ double dot64(const float* x, const float* m, const float* w, int n,
                                         int lane) {
@@ -127,7 +136,7 @@ __device__ void quant_uniform(const Params& p, int beta, const float* vnorm, con
   const int k = chunk * 32 + lane;
   const bool valid = k < p.r;
   const int w = valid ? p.bits[beta * p.r + k] : 0;
-  const float gam = gamma_n(p.d_in + 2);
+  const float gam = proj_gamma(p.d_in);
   int code = 0;
   bool near = false;
   float lo = 0.f, step = 1.f;
@@ -171,7 +180,7 @@ __device__ void quant_group(const Params& p, int beta, const float* vnorm, const
   const int off = 1 << (w - 1);
   const int k = first + lane;
   const bool valid = lane < cnt;
-  const float gam = gamma_n(p.d_in + 2);
+  const float gam = proj_gamma(p.d_in);
   const float z = valid ? c.zs[k] : 0.f;
   const float az = fabsf(z);
   const float tz = valid ? gam * c.nrm * vnorm[k] * (1.f + 1e-3f) : 0.f;
@@ -247,7 +256,7 @@ __device__ void quant_codebook(const Params& p, int beta, const float* vnorm, co
   float dmin = 3.4e38f;
   if (idx > 0) dmin = fminf(dmin, fabsf(u - p.mids[idx - 1]));
   if (idx < L - 1) dmin = fminf(dmin, fabsf(u - p.mids[idx]));
-  const float gam = gamma_n(p.d_in + 2);
+  const float gam = proj_gamma(p.d_in);
   const float eps_n = 0.5f * gam + 2.f * kU;
   const float cmax = fmaxf(fabsf(p.codebook[0]), fabsf(p.codebook[L - 1]));
   const float tau_u = tiny ? 0.f
@@ -307,7 +316,8 @@ append_generic_kernel(Params p, AppendArgs a) {
   const int b = slot / p.Hg, g = slot % p.Hg;
 
   float* xs = reinterpret_cast<float*>(smem);      // [TT][d_in]
-  float* zs = xs + kAppTT * d_in;                  // [TT][r]
+  float* xc = xs + kAppTT * d_in;                  // [TT][d_in] fl(x - mean)
+  float* zs = xc + kAppTT * d_in;                  // [TT][r]
   float* nrm = zs + kAppTT * r;                    // [TT]
   __half* side = reinterpret_cast<__half*>(nrm + kAppTT);  // [TT][n_side]
   const int n_side = p.side_bytes / 2;
@@ -327,6 +337,7 @@ append_generic_kernel(Params p, AppendArgs a) {
       v = load_in(a.x, p.in_dtype, (int64_t)b * a.sb + (int64_t)h * a.sh + (t0 + t) * a.st + dd);
     }
     xs[idx] = v;
+    xc[idx] = t < n ? v - mean[i] : 0.f;  // the projection's one rounding of x - mean
   }
   __syncthreads();
 
@@ -335,23 +346,45 @@ append_generic_kernel(Params p, AppendArgs a) {
   for (int t = warp; t < kAppTT; t += nwarps) {
     float acc = 0.f;
     for (int i = lane; i < d_in; i += 32) {
-      const float d = xs[t * d_in + i] - mean[i];
+      const float d = xc[t * d_in + i];
       acc = fmaf(d, d, acc);
     }
     acc = warp_sumf(acc);
     if (lane == 0) nrm[t] = sqrtf(acc);  // the bounds below carry their own margin
   }
-  // 3. projection, sequential fp32 FMA per component
+  // 3. projection: fp32 fma in blocks of kProjBlk terms, then the block sums
   const float* V = p.V + (int64_t)beta * d_in * r;
   for (int k = threadIdx.x; k < r; k += blockDim.x) {
     float acc[kAppTT];
 #pragma unroll
     for (int t = 0; t < kAppTT; ++t) acc[t] = 0.f;
-    for (int i = 0; i < d_in; ++i) {
-      const float v = V[(int64_t)i * r + k];
-      const float m = mean[i];
+    for (int i0 = 0; i0 < d_in; i0 += kProjBlk) {
+      float blk[kAppTT];
 #pragma unroll
-      for (int t = 0; t < kAppTT; ++t) acc[t] = fmaf(xs[t * d_in + i] - m, v, acc[t]);
+      for (int t = 0; t < kAppTT; ++t) blk[t] = 0.f;
+      if (i0 + kProjBlk > d_in || d_in % 4) {  // a partial block or unaligned rows
+        for (int i = i0; i < min(i0 + kProjBlk, d_in); ++i) {
+          const float v = V[(int64_t)i * r + k];
+#pragma unroll
+          for (int t = 0; t < kAppTT; ++t) blk[t] = fmaf(xc[t * d_in + i], v, blk[t]);
+        }
+      } else {  // whole block, 4 columns per 128-bit load
+#pragma unroll 2
+      for (int i = i0; i < i0 + kProjBlk; i += 4) {
+        const float v0 = V[(int64_t)i * r + k], v1 = V[(int64_t)(i + 1) * r + k];
+        const float v2 = V[(int64_t)(i + 2) * r + k], v3 = V[(int64_t)(i + 3) * r + k];
+#pragma unroll
+        for (int t = 0; t < kAppTT; ++t) {
+          const float4 c4 = *reinterpret_cast<const float4*>(xc + t * d_in + i);
+          blk[t] = fmaf(c4.x, v0, blk[t]);
+          blk[t] = fmaf(c4.y, v1, blk[t]);
+          blk[t] = fmaf(c4.z, v2, blk[t]);
+          blk[t] = fmaf(c4.w, v3, blk[t]);
+        }
+      }
+      }
+#pragma unroll
+      for (int t = 0; t < kAppTT; ++t) acc[t] += blk[t];
     }
 #pragma unroll
     for (int t = 0; t < kAppTT; ++t) zs[t * r + k] = acc[t];
@@ -698,7 +731,7 @@ __global__ void __launch_bounds__(256) fetch_int8_vec(Params p, FetchArgs f) {
 cudaError_t launch_append_generic(const Params& p, const AppendArgs& a, cudaStream_t s, int* nk) {
   if (a.T <= 0) return cudaSuccess;
   const int n_side = p.side_bytes / 2;
-  const size_t smem = sizeof(float) * (kAppTT * p.d_in + kAppTT * p.r + kAppTT) +
+  const size_t smem = sizeof(float) * (2 * kAppTT * p.d_in + kAppTT * p.r + kAppTT) +
                       sizeof(__half) * kAppTT * (n_side > 0 ? n_side : 1) + kAppTT * p.r + 16;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(append_generic_kernel,
