@@ -60,7 +60,8 @@ constexpr int kEpiBar = 1;     // named barriers 1, 2: the epilogue groups
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct PipeArgs {
-  const uint16_t* B;       // fp16 [nb][D][K] UMMA no-swizzle K-major
+  const uint16_t* B;       // fp16 [nb][D_in][K] UMMA no-swizzle K-major (D_in = hpg D)
+  const float* bias;       // fp32 [nb][D_in] (group mode: added in the epilogue)
   const uint32_t* chunks;  // [nb][32] chunk table, 128 bytes per basis
   const int32_t* slotP;    // [n_slots] packed row bytes
   int K, cols;             // K; TMEM columns allocated
@@ -90,6 +91,11 @@ __device__ __forceinline__ uint32_t pack_out(float a, float b, bool bf) {
   }
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 __device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
@@ -164,7 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_base;
   __shared__ volatile int abort_flag;
 
+  constexpr bool GRP = MODE == KVC_MODE_GROUP;  // a slot is a head group: A once, hpg heads of B
   const int D = p.D, K = t.K, KC = K / 8, nbox = D / 64;
+  const int HPG = GRP ? p.hpg : 1;
   const int RS = t.n_rs, AS = t.n_a, TS = t.n_acc, SS = t.n_stg, NB = t.n_b;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x;
@@ -217,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       info_of(slot + 1, nP, nbeta, npay, nside);
       int cur_beta = -1, bslot = NB - 1;
       uint32_t bload[2] = {0u, 0u};
+      uint32_t gload = 0;  // group mode: head slices loaded
       int issued = 0;
       Ring rr(RS);
       for (int i = 0; i < m; ++i, rr.next()) {
@@ -224,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the decode of tile i - RS released this stage
         if (i >= RS && !mbar_wait_bounded(&row_empty[s], rr.phase ^ 1u, kWaitNs)) { abort_flag = 1; break; }
         int first_use = 0;
-        if (beta != cur_beta) {
+        if (!GRP && beta != cur_beta) {
           bslot = NB == 2 ? bslot ^ 1 : 0;
           if (bload[bslot] > 0 &&
               !mbar_wait_bounded(&b_empty[bslot], (bload[bslot] - 1) & 1, kWaitNs)) { abort_flag = 1; break; }
@@ -245,6 +254,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (cb) bulk_load(dst + 128, p.store + pay + t0 * P, cb, &row_full[s]);
         if (sbb) bulk_load(dst + side_off, p.store + side + t0 * p.side_bytes, sbb, &row_full[s]);
         ++issued;
+        if (GRP) {  // the hpg heads' slices of B through a ring of two buffers
+          for (int j = 0; j < HPG; ++j, ++gload) {
+            const int bs = (int)(gload & 1u);
+            if (gload >= 2 && !mbar_wait_bounded(&b_empty[bs], ((gload >> 1) - 1) & 1, kWaitNs)) {
+              abort_flag = 1;
+              break;
+            }
+            mbar_arrive_expect_tx(&b_full[bs], (uint32_t)b_bytes);
+            bulk_load(Bs + bs * b_bytes, t.B + ((size_t)beta * HPG + j) * D * K, (uint32_t)b_bytes,
+                      &b_full[bs]);
+          }
+          if (abort_flag) break;
+        }
         if (++blk == tps) {
           blk = 0;
           ++slot;
@@ -257,6 +279,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(&row_full[j % RS], (j / RS) & 1, kWaitNs);
       for (int b2 = 0; b2 < 2; ++b2)
         if (bload[b2]) mbar_wait_bounded(&b_full[b2], (bload[b2] - 1) & 1, kWaitNs);
+      for (uint32_t u = gload >= 2 ? gload - 2 : 0; u < gload; ++u)
+        mbar_wait_bounded(&b_full[u & 1], (u >> 1) & 1, kWaitNs);
+    }
+  } else if (warp == kMmaWarp && GRP) {
+    // ------------------------------------------------------------ MMA issuer, group mode
+    // per tile: A once, then one accumulator per head (units u = tile * hpg + j)
+    if (lane == 0) {
+      const uint32_t sbo = (uint32_t)KC * 128;
+      const uint32_t idesc = idesc_f16(kTile, D, 0);
+      Ring ra(AS), rt(TS);
+      uint32_t u = 0;
+      for (int i = 0; i < m && !abort_flag; ++i, ra.next()) {
+        const int a = ra.slot;
+        if (!mbar_wait_bounded(&a_full[a], ra.phase, kWaitNs)) { abort_flag = 1; break; }
+        const uint32_t a0 = taddr0 + t.a_col0 + a * t.a_cols;
+        for (int j = 0; j < HPG; ++j, ++u, rt.next()) {
+          const int acc = rt.slot, bs = (int)(u & 1u);
+          if (!mbar_wait_bounded(&b_full[bs], (u >> 1) & 1, kWaitNs)) { abort_flag = 1; break; }
+          // the epilogue of unit u - TS released this accumulator
+          if (u >= (uint32_t)TS && !mbar_wait_bounded(&acc_empty[acc], rt.phase ^ 1u, kWaitNs)) {
+            abort_flag = 1;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t b0 = smem_u32(Bs + bs * b_bytes);
+          for (int ks = 0; ks < K / 16; ++ks)
+            umma_f16_tmem_a(taddr0 + acc * D, a0 + ks * 8,
+                            desc_kmajor_noswizzle(b0 + ks * 256, 128, sbo), idesc, ks > 0 ? 1u : 0u);
+          umma_commit(&acc_full[acc]);
+          umma_commit(&b_empty[bs]);
+        }
+        umma_commit(&a_empty[a]);
+      }
+      umma_commit(&done_bar);
+      mbar_wait_bounded(&done_bar, 0, kWaitNs);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -295,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int dtid = tid - kEpiThreads;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int tt = dtid & (kTile - 1), c0 = dtid >> 7;
+    const int n_groups = p.n_groups;
     Ring rr(RS), ra(AS), rn(kNormRing);
     for (int i = 0; i < m; ++i, rr.next(), ra.next(), rn.next()) {
       const int s = rr.slot, a = ra.slot;
@@ -335,11 +393,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
             if (live) {
               const int w = (int)((ent[u] >> 16) & 0xfu);
-              if (ent[u] >> 31)
-                v = MODE == KVC_MODE_UNIFORM ? decode_uniform(bits[u], w)
-                                             : decode_codebook(bits[u], w, cbh);
-              else if (ent[u] >> 30)
+              if (ent[u] >> 31) {
+                v = MODE == KVC_MODE_CODEBOOK ? decode_codebook(bits[u], w, cbh)
+                                              : decode_uniform(bits[u], w);
+                if (GRP) {  // (code - 2^(w-1)) * s, one fp16 rounding; s: the chunk's group scale
+                  const uint32_t sg = (uint32_t)reinterpret_cast<const uint16_t*>(
+                      st_base + side_off)[tt * n_groups + (int)((ent[u] >> 20) & 0xffu)];
+                  const uint32_t s2 = sg | (sg << 16);
+                  v = make_uint4(hmul2_bits(v.x, s2), hmul2_bits(v.y, s2), hmul2_bits(v.z, s2),
+                                 hmul2_bits(v.w, s2));
+                }
+              } else if (ent[u] >> 30) {
                 v.x = 0x3C003C00u;  // (1, 1): the two bias columns of B
+              }
             }
             tmem_st4(a_tm + c * 4, v);  // chunk c: K positions 8c .. 8c+7
           }
@@ -380,9 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool issuer = split ? (tid & (kEpiThreads / 2 - 1)) == 0 : tid == 0;
     const int box0 = split ? half * (nbox / 2) : 0, nbox_g = split ? nbox / 2 : nbox;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    int slot = first / tps, blk = first % tps;
+    int slot = first / tps, blk = first % tps, head = 0;
     Ring rt(TS), rs_(SS), rn(kNormRing);
-    for (int i = 0; i < m; ++i, rt.next(), rs_.next(), rn.next()) {
+    for (int i = 0; i < m * HPG; ++i, rt.next(), rs_.next()) {  // units: tile x head
       const int acc = rt.slot;
       bool late = !mbar_wait_bounded(&acc_full[acc], rt.phase, kWaitNs);
       if (MODE == KVC_MODE_CODEBOOK)
@@ -391,6 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (named_bar_or(bar_id, gthreads, late || abort_flag)) { abort_flag = 1; break; }
       tc_fence_after();
       const float nrm = MODE == KVC_MODE_CODEBOOK ? norm_ring[rn.slot * kTile + row] : 1.f;
+      const float* brow = GRP ? t.bias + ((size_t)p.basis_of[slot] * HPG + head) * D : nullptr;
       const uint32_t lane_addr = taddr0 + acc * D + lane_off;
       unsigned char* stg = stage + rs_.slot * nbox * 16384;
       for (int j = 0; j < nblk; j += 2) {  // two 32-column loads in flight
@@ -412,6 +479,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 8; ++e)
               x[e] = MODE == KVC_MODE_CODEBOOK ? __uint_as_float(r[h][q * 8 + e]) * nrm
                                                : __uint_as_float(r[h][q * 8 + e]);
+            if (GRP) {  // + mean, this head's slice
+              const float4 b0 = *reinterpret_cast<const float4*>(brow + c32 * 32 + q * 8);
+              const float4 b1 = *reinterpret_cast<const float4*>(brow + c32 * 32 + q * 8 + 4);
+              x[0] += b0.x; x[1] += b0.y; x[2] += b0.z; x[3] += b0.w;
+              x[4] += b1.x; x[5] += b1.y; x[6] += b1.z; x[7] += b1.w;
+            }
             const int c16 = (c32 & 1) * 4 + q;
             *reinterpret_cast<uint4*>(dst + ((c16 ^ (row & 7)) << 4)) =
                 make_uint4(pack_out(x[0], x[1], OUT_BF16), pack_out(x[2], x[3], OUT_BF16),
@@ -424,12 +497,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
       fence_proxy_async_smem();  // staging is read by the TMA store (async proxy)
       named_bar_sync(bar_id, gthreads);
-      if (issuer) {  // one head per slot: the slot is the tensor map's (b, h) index
+      if (issuer) {  // the tensor map's (b, h) index: slot * hpg + head
         for (int bx = box0; bx < box0 + nbox_g; ++bx)
-          tma_store_3d(&omap, stg + bx * 16384, bx * 64, blk * kTile, slot);
+          tma_store_3d(&omap, stg + bx * 16384, bx * 64, blk * kTile, slot * HPG + head);
         bulk_commit();
       }
-      if (++blk == tps) { blk = 0; ++slot; }
+      if (++head == HPG) {
+        head = 0;
+        if (MODE == KVC_MODE_CODEBOOK) rn.next();
+        if (++blk == tps) { blk = 0; ++slot; }
+      }
     }
     if (issuer) bulk_wait_read0();  // staging is read before the CTA exits
   }
@@ -447,12 +524,15 @@ PipeKernel pipe_kernel_for(int mode, int out_dtype) {
   const bool bf = out_dtype == KVC_BF16;
   if (mode == KVC_MODE_UNIFORM)
     return bf ? fetch_pipe_kernel<KVC_MODE_UNIFORM, true> : fetch_pipe_kernel<KVC_MODE_UNIFORM, false>;
+  if (mode == KVC_MODE_GROUP)
+    return bf ? fetch_pipe_kernel<KVC_MODE_GROUP, true> : fetch_pipe_kernel<KVC_MODE_GROUP, false>;
   return bf ? fetch_pipe_kernel<KVC_MODE_CODEBOOK, true> : fetch_pipe_kernel<KVC_MODE_CODEBOOK, false>;
 }
 
 }  // namespace
 
-size_t fetch_pipe_smem(int D, int K, int side_bytes, int pmax, int n_bases, FetchPipeShape* sh) {
+size_t fetch_pipe_smem(int D, int K, int side_bytes, int pmax, int n_bases, int min_rs,
+                       FetchPipeShape* sh) {
   const size_t rows = ((size_t)kTile * pmax + 16 + 15) & ~size_t(15);
   const size_t side = ((size_t)kTile * side_bytes + 16 + 15) & ~size_t(15);
   FetchPipeShape z;
@@ -467,7 +547,7 @@ size_t fetch_pipe_smem(int D, int K, int side_bytes, int pmax, int n_bases, Fetc
   z.a_col0 = z.n_acc * D;
   z.n_b = n_bases > 1 ? 2 : 1;
   z.n_stg = 2;
-  z.n_rs = 3;
+  z.n_rs = min_rs;
   auto total = [&](const FetchPipeShape& q) {
     return 1024 + (size_t)q.n_stg * (D / 64) * 16384 + (size_t)q.n_b * D * K * 2 +
            (size_t)q.n_rs * q.rs_bytes + 256 * 2 + (size_t)kNormRing * kTile * 4;
@@ -499,7 +579,7 @@ cudaError_t launch_fetch_pipe(const TcPlan& plan, const Params& p, const FetchAr
   const int total = tiles * p.n_slots;
   const int grid = std::min(total, sm_count());
   const FetchPipeShape& sh = plan.pipe;
-  const PipeArgs t{plan.fetchB, plan.chunks32, plan.slotP, plan.fetch_K, plan.pipe_cols,
+  const PipeArgs t{plan.fetchB, plan.bias, plan.chunks32, plan.slotP, plan.fetch_K, plan.pipe_cols,
                    sh.n_acc, sh.n_a, sh.n_rs, sh.a_col0, sh.a_cols, sh.n_stg, sh.n_b, sh.rs_bytes,
                    f.S, tiles, total};
   k<<<(unsigned)grid, kThreads, plan.pipe_smem, s>>>(p, t, map);

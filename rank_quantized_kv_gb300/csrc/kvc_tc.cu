@@ -760,12 +760,17 @@ kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t
     const float* V = d.V + (size_t)b * din * r;
     const int16_t* order = g.order.data() + (size_t)b * r;
     std::vector<int> kpos(g.n_kept[b]);
+    int gbase = 0;  // group mode: groups of the earlier segments
     for (int s = 0; s < kMaxSeg; ++s) {
       const int32_t* e = &g.seg[((size_t)b * kMaxSeg + s) * 4];
       for (int m = 0; m < e[3]; ++m) kpos[e[2] + m] = koff[(size_t)b * kMaxSeg + s] + m;
-      for (int ci = 0; ci * 8 < e[3]; ++ci)
+      for (int ci = 0; ci * 8 < e[3]; ++ci) {
+        const uint32_t gi =
+            d.mode == KVC_MODE_GROUP ? (uint32_t)(gbase + (8 * ci) / d.group_size) : 0u;
         chunks[(size_t)b * (K / 8) + koff[(size_t)b * kMaxSeg + s] / 8 + ci] =
-            (uint32_t)(e[0] + e[1] * ci) | ((uint32_t)e[1] << 16) | (1u << 31);
+            (uint32_t)(e[0] + e[1] * ci) | ((uint32_t)e[1] << 16) | (gi << 20) | (1u << 31);
+      }
+      if (d.mode == KVC_MODE_GROUP) gbase += (e[3] + d.group_size - 1) / d.group_size;
     }
     for (int nrow = 0; nrow < din; ++nrow) {
       double acc = d.mean && d.mode != KVC_MODE_CODEBOOK ? (double)d.mean[(size_t)b * din + nrow] : 0.0;
@@ -808,14 +813,18 @@ kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t
   plan.fetch_cols = cols;
   plan.fetch_smem = smem;
   plan.fetch_ready = encoder() != nullptr;
-  if (d.heads_per_group == 1 && K <= 256) {
+  const bool grp = d.mode == KVC_MODE_GROUP;
+  // group mode: chunks lie inside one group (group size a multiple of 8), at
+  // most 256 groups (8 bits of the chunk entry)
+  if ((d.heads_per_group == 1 || (grp && d.group_size % 8 == 0 && g.n_groups <= 256)) && K <= 256) {
     // the chunk table again, padded to 32 entries: one 128-byte bulk copy per tile
     std::vector<uint32_t> c32((size_t)nb * 32, 0u);
     for (int b = 0; b < nb; ++b)
       for (int c = 0; c < K / 8; ++c) c32[(size_t)b * 32 + c] = chunks[(size_t)b * (K / 8) + c];
     plan.oChunks32 = put(image, c32.data(), c32.size());
     FetchPipeShape sh;
-    const size_t ps = fetch_pipe_smem(D, K, g.side_bytes, pmax, nb, &sh);
+    // group mode streams the heads' slices of B through two buffers
+    const size_t ps = fetch_pipe_smem(D, K, g.side_bytes, pmax, grp ? 2 : nb, grp ? 2 : 3, &sh);
     if (ps > 0) {
       plan.pipe_ready = plan.fetch_ready;
       int cols_alloc = 32;  // TMEM allocations are powers of two

@@ -48,7 +48,8 @@ struct TcPlan {
   const uint16_t* fetchB = nullptr;  // fp16 [nb][D_in][K] in UMMA no-swizzle K-major order
   const float* bias = nullptr;       // fp32 [nb][D_in]
   const uint32_t* chunks = nullptr;  // [nb][K/8]: first byte | width << 16 | valid << 31;
-                                     // 1 << 30 marks the chunk of ones (bias columns)
+                                     // 1 << 30 marks the chunk of ones (bias columns);
+                                     // group mode: the chunk's group << 20
   bool bias_folded = false;          // B carries the bias (uniform mode)
   const int32_t* slotP = nullptr;    // [n_slots] packed row bytes of each slot
   size_t oChunks32 = 0;
@@ -96,7 +97,8 @@ cudaError_t launch_fetch_tc(const TcPlan& plan, const Params& p, const FetchArgs
 // Warp-specialised persistent fetch (kvc_fetch_pipe.cu); `map` is the output
 // tensor map.  fetch_pipe_smem sizes its rings for D, K, the side bytes, the
 // largest packed row and the number of bases; 0 when they do not fit.
-size_t fetch_pipe_smem(int D, int K, int side_bytes, int pmax, int n_bases, FetchPipeShape* sh);
+size_t fetch_pipe_smem(int D, int K, int side_bytes, int pmax, int n_bases, int min_rs,
+                       FetchPipeShape* sh);
 cudaError_t launch_fetch_pipe(const TcPlan& plan, const Params& p, const FetchArgs& f,
                               const CUtensorMap& map, cudaStream_t s, int* nk);
 // Warp-specialised append (kvc_append_ws.cu): table bytes per basis, one
