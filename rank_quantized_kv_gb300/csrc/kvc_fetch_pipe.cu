@@ -184,8 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* stage = smem;                                  // SS x nbox x 16 KB
   unsigned char* Bs = stage + SS * nbox * 16384;                // NB x [D x K] fp16
   unsigned char* rs = Bs + NB * b_bytes;                        // RS x row stage
-  uint16_t* cbh = reinterpret_cast<uint16_t*>(rs + (size_t)RS * t.rs_bytes);  // [256]
-  float* norm_ring = reinterpret_cast<float*>(cbh + 256);       // kNormRing x [128]
+  // after the row stages: codebook mode the fp16 centroids [256] and the norm
+  // ring [kNormRing][128]; group mode the epilogue groups' mean cache
+  uint16_t* cbh = reinterpret_cast<uint16_t*>(rs + (size_t)RS * t.rs_bytes);
+  float* norm_ring = reinterpret_cast<float*>(cbh + 256);
+  float* mean_c = reinterpret_cast<float*>(rs + (size_t)RS * t.rs_bytes);  // [hpg][D]
   // a row stage: [0, 128) chunk table, then the packed rows, then the side words
   const int side_off = t.rs_bytes - (int)(((size_t)kTile * p.side_bytes + 16 + 15) & ~size_t(15));
 
@@ -447,6 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int box0 = split ? half * (nbox / 2) : 0, nbox_g = split ? nbox / 2 : nbox;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     int slot = first / tps, blk = first % tps, head = 0;
+    float* mean_g = mean_c + (split ? half : 0) * (HPG * (nbox / 2) * 64);  // [hpg][this group's columns]
+    int mean_beta = -1;
     Ring rt(TS), rs_(SS), rn(kNormRing);
     for (int i = 0; i < m * HPG; ++i, rt.next(), rs_.next()) {  // units: tile x head
       const int acc = rt.slot;
@@ -455,9 +460,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         late = late || !mbar_wait_bounded(&norm_full[rn.slot], rn.phase, kWaitNs);
       if (issuer) bulk_wait_read_n(SS - 1);  // this group's store of tile i-SS has left staging
       if (named_bar_or(bar_id, gthreads, late || abort_flag)) { abort_flag = 1; break; }
+      if (GRP) {  // this group's columns of the basis' mean rows, refreshed on a new basis
+        const int beta = p.basis_of[slot];
+        if (beta != mean_beta) {
+          const int per = nbox_g * 64, gt = tid & (gthreads - 1);
+          for (int e = gt; e < HPG * per; e += gthreads) {
+            const int j = e / per, c = box0 * 64 + e % per;
+            mean_g[j * per + (c - box0 * 64)] = t.bias[((size_t)beta * HPG + j) * D + c];
+          }
+          mean_beta = beta;
+          named_bar_sync(bar_id, gthreads);
+        }
+      }
       tc_fence_after();
       const float nrm = MODE == KVC_MODE_CODEBOOK ? norm_ring[rn.slot * kTile + row] : 1.f;
-      const float* brow = GRP ? t.bias + ((size_t)p.basis_of[slot] * HPG + head) * D : nullptr;
+      const float* brow = GRP ? mean_g + head * (nbox_g * 64) - box0 * 64 : nullptr;
       const uint32_t lane_addr = taddr0 + acc * D + lane_off;
       unsigned char* stg = stage + rs_.slot * nbox * 16384;
       for (int j = 0; j < nblk; j += 2) {  // two 32-column loads in flight
@@ -531,8 +548,8 @@ PipeKernel pipe_kernel_for(int mode, int out_dtype) {
 
 }  // namespace
 
-size_t fetch_pipe_smem(int D, int K, int side_bytes, int pmax, int n_bases, int min_rs,
-                       FetchPipeShape* sh) {
+size_t fetch_pipe_smem(int mode, int D, int hpg, int K, int side_bytes, int pmax, int n_bases,
+                       int min_rs, FetchPipeShape* sh) {
   const size_t rows = ((size_t)kTile * pmax + 16 + 15) & ~size_t(15);
   const size_t side = ((size_t)kTile * side_bytes + 16 + 15) & ~size_t(15);
   FetchPipeShape z;
@@ -548,9 +565,12 @@ size_t fetch_pipe_smem(int D, int K, int side_bytes, int pmax, int n_bases, int 
   z.n_b = n_bases > 1 ? 2 : 1;
   z.n_stg = 2;
   z.n_rs = min_rs;
+  const size_t tail = mode == KVC_MODE_CODEBOOK ? 256 * 2 + (size_t)kNormRing * kTile * 4
+                      : mode == KVC_MODE_GROUP  ? (size_t)hpg * D * 4
+                                                : 0;
   auto total = [&](const FetchPipeShape& q) {
     return 1024 + (size_t)q.n_stg * (D / 64) * 16384 + (size_t)q.n_b * D * K * 2 +
-           (size_t)q.n_rs * q.rs_bytes + 256 * 2 + (size_t)kNormRing * kTile * 4;
+           (size_t)q.n_rs * q.rs_bytes + tail;
   };
   const size_t limit = 226 * 1024;
   if (total(z) > limit) return 0;

@@ -97,8 +97,8 @@ cudaError_t launch_fetch_tc(const TcPlan& plan, const Params& p, const FetchArgs
 // Warp-specialised persistent fetch (kvc_fetch_pipe.cu); `map` is the output
 // tensor map.  fetch_pipe_smem sizes its rings for D, K, the side bytes, the
 // largest packed row and the number of bases; 0 when they do not fit.
-size_t fetch_pipe_smem(int D, int K, int side_bytes, int pmax, int n_bases, int min_rs,
-                       FetchPipeShape* sh);
+size_t fetch_pipe_smem(int mode, int D, int hpg, int K, int side_bytes, int pmax, int n_bases,
+                       int min_rs, FetchPipeShape* sh);
 cudaError_t launch_fetch_pipe(const TcPlan& plan, const Params& p, const FetchArgs& f,
                               const CUtensorMap& map, cudaStream_t s, int* nk);
 // Warp-specialised append (kvc_append_ws.cu): table bytes per basis, one
