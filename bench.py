@@ -104,6 +104,15 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+# DRAM traffic (ncu dram__bytes_read.sum + dram__bytes_write.sum) per
+# token-head of a kernel, from the capture named beside it, where the kernel
+# has not changed since.  The roofline's "traffic" scales it to the launch.
+TRAFFIC_PER_UNIT = {
+    # (kind, mode): (bytes per token-head, capture)
+    ("append", "uniform"): (144.9e6 / (64 * 8192), "profiles/append_ws_llama3-8b_S8192.md"),
+}
+
+
 # ----------------------------------------------------------------------------- multi-rank
 
 def max_over_ranks(values, dist=None, device="cpu"):
@@ -332,6 +341,10 @@ def gpu_arm(args, rank, world):
         "traffic": None,
         "algorithmic_bytes_per_launch": nbytes,
     }
+    tr = TRAFFIC_PER_UNIT.get((kind, layers[i].mode))
+    if tr is not None:
+        roof["traffic"] = tr[0] * layers[i].n_slots * S
+        roof["traffic_source"] = tr[1] + " (captured at S = 8192, scaled by tokens)"
     roof["frac"] = roof["achieved"] / roof["peak"]
     launches = sum(c["launches"] for c in counters)
     line = {
