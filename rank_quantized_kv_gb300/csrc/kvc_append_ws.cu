@@ -70,13 +70,13 @@ struct AppendWsArgs {
 //         (A = 2^-s / step, Bc = -(mean . V_k + lo) / step; see the plan);
 //   cff   mean . V_k, iff 1/step (as double-float pairs), lo, vn = ||V_k||
 //         (rounded up);
-//   qk    qmax | chunk-aligned position << 16 (0xFFFF: not kept);
+//   qp    qmax and the chunk-aligned position (not kept: the row's scratch byte);
 // then the pack chunks.
 struct Tab {
   const float4* q4;
   const float2 *cff, *iff;
   const float *lo, *vn;
-  const uint32_t* qk;
+  const int2* qp;
   const uint32_t* chunk;  // [32]: first byte | width << 16 | (codes - 1) << 20 | valid << 31
   __device__ Tab(const unsigned char* base, int rpad)
       : q4(reinterpret_cast<const float4*>(base)),
@@ -84,8 +84,8 @@ struct Tab {
         iff(cff + rpad),
         lo(reinterpret_cast<const float*>(iff + rpad)),
         vn(lo + rpad),
-        qk(reinterpret_cast<const uint32_t*>(vn + rpad)),
-        chunk(qk + rpad) {}
+        qp(reinterpret_cast<const int2*>(vn + rpad)),
+        chunk(reinterpret_cast<const uint32_t*>(qp + rpad)) {}
 };
 
 struct XHdr {  // per x stage, written by the producer
@@ -124,7 +124,7 @@ __device__ void refine_ws(const Params& p, const Tab& tb, const float* Vt, const
                           const unsigned char* xs, unsigned char* codes_s, int ks, __half* side_s,
                           unsigned* nside, int tt, int k, int lane, float uf, float tau) {
   const int D = p.D;
-  const int kp = k == (int)kNormEntry ? 0 : (int)(tb.qk[k] >> 16);
+  const int kp = k == (int)kNormEntry ? 0 : tb.qp[k].y;
   if (MODE == KVC_MODE_UNIFORM) {
     const ff2 z = dot2_ff<BF16, WARP>(xs, tt, D, Vt + (size_t)k * D, lane);
     if (lane == 0) {
@@ -132,7 +132,7 @@ __device__ void refine_ws(const Params& p, const Tab& tb, const float* Vt, const
       const ff2 zl = ff_add(ff_add(z, ff2{-c.x, -c.y}), ff2{-tb.lo[k], 0.f});
       const ff2 u = ff_mul(zl, ff2{iv.x, iv.y});
       const float q = ff_rint(u);
-      const int qmax = (int)(tb.qk[k] & 0xffffu);
+      const int qmax = tb.qp[k].x;
       codes_s[tt * ks + kp] = (uint8_t)(int)fminf(fmaxf(q, 0.f), (float)qmax);
       if (tau > 0.f) atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(
                                                    fabsf(uf - u.hi) / tau));
@@ -171,18 +171,20 @@ __device__ void refine_ws(const Params& p, const Tab& tb, const float* Vt, const
 }
 
 // Uniform fast path: u = (z - mean . V_k - lo) / step as one fma of the
-// table's fused constants, the bound tau on |u - u_exact| (host derivation in
-// append_ws_table), and whether a rounding boundary lies within tau.
-__device__ __forceinline__ int fast_uniform(const Tab& tb, int k, uint32_t qk, float z, float nx,
+// table's fused constants and the code; `near` flags a rounding boundary
+// within the bound tau of u (host derivation in append_ws_table; tau holds for
+// |u| <= qmax + 1, the range of the interior boundaries).  With `exact` the
+// boundary must also be interior (a first pass may flag the outer ones too).
+template <bool EXACT>
+__device__ __forceinline__ int fast_uniform(const Tab& tb, int k, int qmax, float z, float nx,
                                             float& u, float& tau, bool& near) {
-  constexpr float kU4 = 2.384185791015625e-07f;  // 2^-22
   const float4 q = tb.q4[k];
-  const float qmax = (float)(qk & 0xFFFFu);
   u = fmaf(z, q.x, q.y);
-  tau = fmaf(kU4, fabsf(u), fmaf(q.z, nx, q.w));
+  tau = fmaf(q.z, nx, q.w);
   const float hb = floorf(u) + 0.5f;
-  near = hb >= 0.5f && hb <= qmax - 0.5f && fabsf(u - hb) <= tau;
-  return (int)fminf(fmaxf(rintf(u), 0.f), qmax);
+  near = fabsf(u - hb) <= tau;
+  if (EXACT) near = near && hb >= 0.5f && hb <= (float)qmax - 0.5f;
+  return min(max(__float2int_rn(u), 0), qmax);
 }
 
 // Codebook fast path: u = z / ||x||, the nearest centroid by the fp32
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
   __shared__ uint64_t b_full[2], b_empty[2], done_bar;
   __shared__ XHdr hdr[kMaxXS];
   __shared__ uint32_t tmem_base;
-  __shared__ unsigned qcount_g[2], nside_g[2];
+  __shared__ unsigned qcount_g[kQG], nside_g[kQG];
   __shared__ volatile int abort_flag;
 
   constexpr int rpad = kNCB * CW;         // CW: components per thread
@@ -266,8 +268,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
     mbar_init(&done_bar, 1);
     fence_mbar_init();
     abort_flag = 0;
-    qcount_g[0] = qcount_g[1] = 0;
-    nside_g[0] = nside_g[1] = 0;
+    for (int i = 0; i < kQG; ++i) qcount_g[i] = nside_g[i] = 0;
   }
   if (MODE == KVC_MODE_CODEBOOK) {
     for (int j = tid; j < p.cb_levels - 1; j += kThreads) mids_s[j] = p.mids[j];
@@ -488,15 +489,14 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
 #pragma unroll
         for (int j = 0; j < SB; ++j) {
           const int k = cblk * CW + sb * SB + j;  // < rpad; components past r are not kept
-          const uint32_t qk = tb.qk[k];
-          const int kp = (qk >> 16) == 0xFFFFu ? ks - 1 : (int)(qk >> 16);  // not kept: scratch byte
+          const int2 qp = tb.qp[k];  // qmax, position (not kept: the row's scratch byte)
           float uf, tf;
           bool near;
           const int code = MODE == KVC_MODE_UNIFORM
-                               ? fast_uniform(tb, k, qk, z[j], nx, uf, tf, near)
+                               ? fast_uniform<false>(tb, k, qp.x, z[j], nx, uf, tf, near)
                                : fast_codebook(p, tb, k, mids_s, mreg, z[j], rnx, t.gamma, eps_n,
                                                cmax, tiny, uf, tf, near);
-          crow[kp] = (uint8_t)code;
+          crow[qp.y] = (uint8_t)code;
           nmask |= (uint32_t)near << j;
         }
         // queue the near ones (rare); past the queue's end they are decided
@@ -509,11 +509,13 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
             const int k = cblk * CW + sb * SB + j;
             float uf, tf;
             bool near;
-            if (MODE == KVC_MODE_UNIFORM)
-              fast_uniform(tb, k, tb.qk[k], z[j], nx, uf, tf, near);
-            else
+            if (MODE == KVC_MODE_UNIFORM) {
+              fast_uniform<true>(tb, k, tb.qp[k].x, z[j], nx, uf, tf, near);
+              if (!near) continue;  // an outer boundary: the clamped code is certain
+            } else {
               fast_codebook(p, tb, k, mids_s, mreg, z[j], rnx, t.gamma, eps_n, cmax, tiny, uf, tf,
                             near);
+            }
             const unsigned q = atomicAdd(&qcount, 1u);
             if (q < kQueue) {
               queue[q] = ((uint32_t)row << 16) | (uint32_t)k;
@@ -620,7 +622,17 @@ WsKernel ws_kernel_for(int mode, int bf16, int rpad) {
 
 }  // namespace
 
-size_t append_ws_tab_bytes(int rpad) { return ((size_t)rpad * 44 + 128 + 15) & ~size_t(15); }
+size_t append_ws_tab_bytes(int rpad) { return ((size_t)rpad * 48 + 128 + 15) & ~size_t(15); }
+
+int append_ws_chunks(const Geo& g, int b) {
+  int nch = 0;
+  for (int sg = 0; sg < kMaxSeg; ++sg) {
+    const int32_t* e = &g.seg[((size_t)b * kMaxSeg + sg) * 4];
+    if (!e[3]) break;
+    nch += (e[3] + 7) / 8;
+  }
+  return nch;
+}
 
 namespace {
 float round_up_f(double v) {  // the smallest float >= v
@@ -631,15 +643,15 @@ float round_up_f(double v) {  // the smallest float >= v
 }  // namespace
 
 int append_ws_table(const Geo& g, const kvc_layer_desc& d, int rpad, const double* c64,
-                    double inv_scale, double gamma, int b, unsigned char* out) {
+                    double inv_scale, double gamma, int ks, int b, unsigned char* out) {
   const int r = g.r, D = d.D;
   float4* q4 = reinterpret_cast<float4*>(out);
   float2* cff = reinterpret_cast<float2*>(q4 + rpad);
   float2* iff = cff + rpad;
   float* lo = reinterpret_cast<float*>(iff + rpad);
   float* vn = lo + rpad;
-  uint32_t* qk = reinterpret_cast<uint32_t*>(vn + rpad);
-  uint32_t* chunk = qk + rpad;
+  int2* qp = reinterpret_cast<int2*>(vn + rpad);
+  uint32_t* chunk = reinterpret_cast<uint32_t*>(qp + rpad);
   for (int k = 0; k < rpad; ++k) {
     const bool in = k < r;
     const size_t bk = (size_t)b * r + k;
@@ -668,12 +680,14 @@ int append_ws_table(const Geo& g, const kvc_layer_desc& d, int rpad, const doubl
       q4[k].y = (float)(-(c64[bk] + (double)d.qmin[bk]) / st);
       q4[k].z = round_up_f((double)vn[k] / st * (gamma + std::ldexp(1.0, -23)) *
                            (1.0 + std::ldexp(1.0, -20)) * (1.0 + 1e-3));
+      // + 2^-22 (|u| + 1) for |u| <= qmax + 1 (interior boundaries only)
+      const int qm = (1 << g.bits[bk]) - 1;
       q4[k].w = round_up_f((std::fabs(c64[bk]) + std::fabs((double)d.qmin[bk])) / st *
-                           std::ldexp(1.0, -23));
+                               std::ldexp(1.0, -23) +
+                           std::ldexp(1.0, -22) * (qm + 2));
     }
     const int width = in ? g.bits[bk] : 0;
-    qk[k] = (uint32_t)(d.mode == KVC_MODE_UNIFORM ? (width ? (1 << width) - 1 : 0) : 0) |
-            (0xFFFFu << 16);
+    qp[k] = make_int2(d.mode == KVC_MODE_UNIFORM && width ? (1 << width) - 1 : 0, ks - 1);
   }
   // chunk-aligned positions: segment s (packed order) starts on a chunk
   int nch = 0;
@@ -682,7 +696,7 @@ int append_ws_table(const Geo& g, const kvc_layer_desc& d, int rpad, const doubl
     if (!e[3]) break;
     for (int mm = 0; mm < e[3]; ++mm) {
       const int k = g.order[(size_t)b * r + e[2] + mm];
-      qk[k] = (qk[k] & 0xFFFFu) | ((uint32_t)(nch * 8 + mm) << 16);
+      qp[k].y = nch * 8 + mm;
     }
     for (int ci = 0; ci * 8 < e[3]; ++ci) {
       if (nch == 32) return -1;

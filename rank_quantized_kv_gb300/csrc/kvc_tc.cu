@@ -669,11 +669,13 @@ void prepare_append(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>&
   const size_t tab_bytes = append_ws_tab_bytes(rpad);
   std::vector<unsigned char> tab((size_t)nb * tab_bytes, 0);
   int max_chunks = 0;
-  for (int b = 0; b < nb && max_chunks >= 0; ++b) {
-    const int nch = append_ws_table(g, d, rpad, c64.data(), (double)plan.app_inv_scale,
-                                    (double)plan.app_gamma, b, tab.data() + (size_t)b * tab_bytes);
-    max_chunks = nch < 0 ? -1 : std::max(max_chunks, nch);
-  }
+  for (int b = 0; b < nb; ++b) max_chunks = std::max(max_chunks, append_ws_chunks(g, b));
+  if (max_chunks > 32) max_chunks = -1;
+  const int ks = max_chunks * 8 + 8;  // the code staging row (append_ws_plan's)
+  for (int b = 0; b < nb && max_chunks > 0; ++b)
+    if (append_ws_table(g, d, rpad, c64.data(), (double)plan.app_inv_scale, (double)plan.app_gamma,
+                        ks, b, tab.data() + (size_t)b * tab_bytes) < 0)
+      max_chunks = -1;
   AppendWsShape ws;
   const size_t wsm = max_chunks > 0 ? append_ws_plan(D, r, rpad, npieces, pmax, max_chunks, nb, &ws) : 0;
   if (wsm > 0 && plan.append_ready) {

@@ -104,8 +104,9 @@ cudaError_t launch_fetch_pipe(const TcPlan& plan, const Params& p, const FetchAr
 // Warp-specialised append (kvc_append_ws.cu): table bytes per basis, one
 // basis' table, the ring plan (0 when it does not fit), the launcher.
 size_t append_ws_tab_bytes(int rpad);
+int append_ws_chunks(const Geo& g, int b);  // pack chunks of basis b
 int append_ws_table(const Geo& g, const kvc_layer_desc& d, int rpad, const double* c64,
-                    double inv_scale, double gamma, int b,
+                    double inv_scale, double gamma, int ks, int b,
                     unsigned char* out);  // returns the basis' pack chunks, -1 if over 32
 size_t append_ws_plan(int D, int r, int rpad, int npieces, int pmax, int max_chunks, int n_bases,
                       AppendWsShape* sh);
