@@ -603,32 +603,32 @@ __device__ __forceinline__ void load8(const void* x, int dt, int64_t off, float 
   }
 }
 
-// One token row, 16 values per thread: its absmax over the TPR threads, the
-// int8 codes q = rint(v / s), s = max(a / 127, 1e-8), and fp16(s).  Returns
-// the number of codes re-decided.  The fast u = v fl(127 / a) is within
-// 1.5e-5 of 127 v / a (two roundings, |u| <= 127, so no clamp is needed); a
-// code within 3e-5 of a half is decided exactly: for 16-bit inputs 254 |v|
-// and (2k + 1) a are exact in fp32 (at most 19 significant bits each), so the
-// sign of their difference decides it; an exact tie, fp32 inputs, a < 2e-6
-// and a >= 1e30 take the float64 path.
+// One token row, NV = 32 values per thread: its absmax over the TPR threads,
+// the int8 codes q = rint(v / s), s = max(a / 127, 1e-8), and fp16(s).
+// Returns the number of codes re-decided.  The fast u = v fl(127 / a) is
+// within 1.5e-5 of 127 v / a (two roundings, |u| <= 127, so no clamp is
+// needed); a code within 3e-5 of a half is decided exactly: for 16-bit inputs
+// 254 |v| and (2k + 1) a are exact in fp32 (at most 19 significant bits
+// each), so the sign of their difference decides it; an exact tie, fp32
+// inputs, a < 2e-6 and a >= 1e30 take the float64 path.
+constexpr int kI8NV = 32;
 template <int TPR>
 __device__ __forceinline__ unsigned append_int8_row(const Params& p, const AppendArgs& a, int slot,
                                                     int64_t t, int j) {
   const bool valid = t < a.T;
-  float v[16];
+  float v[kI8NV];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = 0.f;
+  for (int i = 0; i < kI8NV; ++i) v[i] = 0.f;
   if (valid) {
     const int b = slot / p.H, h = slot - b * p.H;
-    const int64_t off = (int64_t)b * a.sb + (int64_t)h * a.sh + t * a.st + 16 * j;
-    float (&v0)[8] = *reinterpret_cast<float(*)[8]>(&v[0]);
-    float (&v1)[8] = *reinterpret_cast<float(*)[8]>(&v[8]);
-    load8(a.x, p.in_dtype, off, v0);
-    load8(a.x, p.in_dtype, off + 8, v1);
+    const int64_t off = (int64_t)b * a.sb + (int64_t)h * a.sh + t * a.st + kI8NV * j;
+#pragma unroll
+    for (int c = 0; c < kI8NV / 8; ++c)
+      load8(a.x, p.in_dtype, off + 8 * c, *reinterpret_cast<float(*)[8]>(&v[8 * c]));
   }
   float am = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(v[i]));
+  for (int i = 0; i < kI8NV; ++i) am = fmaxf(am, fabsf(v[i]));
 #pragma unroll
   for (int o = TPR / 2; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(kFull, am, o));
   unsigned nref = 0;
@@ -636,35 +636,54 @@ __device__ __forceinline__ unsigned append_int8_row(const Params& p, const Appen
     const bool slow = !(am > 2e-6f);
     const bool exact16 = p.in_dtype != KVC_F32 && am < 1e30f;  // no overflow in 254 v
     const float inv = slow ? 0.f : 127.f / am;
-    double s64 = -1.0;
-    uint32_t packed[4] = {0u, 0u, 0u, 0u};
+    uint32_t packed[kI8NV / 4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < kI8NV / 4; ++i) packed[i] = 0u;
+    uint32_t flag = 0;  // values within 3e-5 of a half (or a tiny row)
+#pragma unroll
+    for (int i = 0; i < kI8NV; ++i) {
       const float u = v[i] * inv;
-      float q = rintf(u);
-      if (slow || fabsf(u - q) > 0.5f - 3e-5f) {
-        ++nref;
-        const float k = floorf(fabsf(u));
-        const float d = exact16 && !slow ? 254.f * fabsf(v[i]) - (2.f * k + 1.f) * am : 0.f;
-        if (d != 0.f) {
-          q = copysignf(d > 0.f ? k + 1.f : k, v[i]);
-        } else {  // an exact tie, fp32 input or a tiny row: as float64 decides it
-          if (s64 < 0.0) s64 = fmax((double)am / 127.0, 1e-8);
-          q = (float)fmin(fmax(rint((double)v[i] / s64), -127.0), 127.0);
-        }
-      }
+      const float q = rintf(u);
+      flag |= (uint32_t)(fabsf(u - q) > 0.5f - 3e-5f) << i;
       packed[i >> 2] |= ((uint32_t)__float2int_rn(q) & 0xffu) << (8 * (i & 3));
     }
-    uint8_t* dst = p.store + p.pay_off[slot] + (a.t_base + t) * p.D + 16 * j;
-    *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    if (slow) flag = 0xffffffffu;
+    if (flag) {  // rare: re-decide those exactly, then patch their bytes
+      double s64 = fmax((double)am / 127.0, 1e-8);
+      for (uint32_t f = flag; f; f &= f - 1) {
+        const int i = __ffs(f) - 1;
+        ++nref;
+        float vi = 0.f;
+#pragma unroll
+        for (int e = 0; e < kI8NV; ++e) vi = e == i ? v[e] : vi;  // no local-memory indexing
+        const float u = vi * inv;
+        const float k = floorf(fabsf(u));
+        const float d = exact16 && !slow ? 254.f * fabsf(vi) - (2.f * k + 1.f) * am : 0.f;
+        float q;
+        if (d != 0.f) {
+          q = copysignf(d > 0.f ? k + 1.f : k, vi);
+        } else {  // an exact tie, fp32 input or a tiny row: as float64 decides it
+          q = (float)fmin(fmax(rint((double)vi / s64), -127.0), 127.0);
+        }
+        const uint32_t byte = (uint32_t)__float2int_rn(q) & 0xffu;
+#pragma unroll
+        for (int w = 0; w < kI8NV / 4; ++w)
+          if (w == (i >> 2))
+            packed[w] = (packed[w] & ~(0xffu << (8 * (i & 3)))) | (byte << (8 * (i & 3)));
+      }
+    }
+    uint8_t* dst = p.store + p.pay_off[slot] + (a.t_base + t) * p.D + kI8NV * j;
+#pragma unroll
+    for (int w = 0; w < kI8NV / 16; ++w)
+      reinterpret_cast<uint4*>(dst)[w] =
+          make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2], packed[4 * w + 3]);
     if (j == 0) {
       const float s32 = am / 127.f;
       __half s16;
       if (!slow && same_half(s32 * (1.f - 4.f * kU), s32 * (1.f + 4.f * kU))) {
         s16 = __float2half_rn(s32);
       } else {
-        if (s64 < 0.0) s64 = fmax((double)am / 127.0, 1e-8);
-        s16 = __double2half(s64);
+        s16 = __double2half(fmax((double)am / 127.0, 1e-8));
       }
       reinterpret_cast<__half*>(p.store + p.side_off[slot])[a.t_base + t] = s16;
     }
@@ -673,27 +692,21 @@ __device__ __forceinline__ unsigned append_int8_row(const Params& p, const Appen
 }
 
 // Grid: x over blocks of 256 / TPR tokens, y over slots (strided when there
-// are more than 65535), so no thread divides by a runtime value.  Counters
-// are summed per block, then added once.
+// are more than 65535), so no thread divides by a runtime value.  Counters:
+// a warp adds its re-decisions (rarely any); the tokens appended are added
+// once per block of the first slot.
 template <int TPR>
 __global__ void __launch_bounds__(256) append_int8_vec(Params p, AppendArgs a) {
-  __shared__ unsigned blk_ref;
-  if (threadIdx.x == 0) blk_ref = 0;
-  __syncthreads();
   const int j = (int)(threadIdx.x % TPR);
   const int64_t t = (int64_t)blockIdx.x * (256 / TPR) + threadIdx.x / TPR;
   unsigned nref = 0;
   for (int slot = blockIdx.y; slot < p.n_slots; slot += gridDim.y)
     nref += append_int8_row<TPR>(p, a, slot, t, j);
   nref = __reduce_add_sync(kFull, nref);
-  if ((threadIdx.x & 31) == 0 && nref) atomicAdd(&blk_ref, nref);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    if (blk_ref) atomicAdd(&p.counters[0], (unsigned long long)blk_ref);
-    if (blockIdx.y == 0) {  // tokens appended, counted on slot 0
-      const int64_t rows = min((int64_t)(256 / TPR), a.T - (int64_t)blockIdx.x * (256 / TPR));
-      if (rows > 0) atomicAdd(&p.counters[2], (unsigned long long)rows);
-    }
+  if ((threadIdx.x & 31) == 0 && nref) atomicAdd(&p.counters[0], (unsigned long long)nref);
+  if (threadIdx.x == 0 && blockIdx.y == 0) {
+    const int64_t rows = min((int64_t)(256 / TPR), a.T - (int64_t)blockIdx.x * (256 / TPR));
+    if (rows > 0) atomicAdd(&p.counters[2], (unsigned long long)rows);
   }
 }
 
@@ -766,11 +779,11 @@ cudaError_t launch_append_int8(const Params& p, const AppendArgs& a, cudaStream_
                    reinterpret_cast<uintptr_t>(a.x) % 16 == 0 && (a.st * esz) % 16 == 0 &&
                    (a.sh * esz) % 16 == 0 && (a.sb * esz) % 16 == 0;
   if (vec) {
-    const int tpr = p.D / 16;  // 16 values per thread
+    const int tpr = p.D / kI8NV;  // 32 values per thread
     const dim3 grid((unsigned)((a.T * tpr + 255) / 256), (unsigned)std::min(p.n_slots, 65535));
-    if (tpr == 4) append_int8_vec<4><<<grid, 256, 0, s>>>(p, a);
-    else if (tpr == 8) append_int8_vec<8><<<grid, 256, 0, s>>>(p, a);
-    else append_int8_vec<16><<<grid, 256, 0, s>>>(p, a);
+    if (tpr == 2) append_int8_vec<2><<<grid, 256, 0, s>>>(p, a);
+    else if (tpr == 4) append_int8_vec<4><<<grid, 256, 0, s>>>(p, a);
+    else append_int8_vec<8><<<grid, 256, 0, s>>>(p, a);
   } else {
     append_int8_kernel<<<(unsigned)((toks + kI8Warps - 1) / kI8Warps), kI8Warps * 32, 0, s>>>(p, a);
   }
