@@ -188,38 +188,50 @@ __device__ __forceinline__ int fast_uniform(const Tab& tb, int k, int qmax, floa
 }
 
 // Codebook fast path: u = z / ||x||, the nearest centroid by the fp32
-// midpoints, and whether a midpoint lies within the bound of u's error.
-// Up to 8 levels the 7 midpoints sit in registers (+inf past the last): the
-// code is the number of midpoints below u, the distance the nearest one.
+// midpoints, and whether a midpoint lies within the bound tau of u's error:
+// tau = T1_k + |u| e, T1_k = gamma ||V_k|| (1 + 1e-3)(1 + 1e-6) + 2^-22 max|c|
+// (table) and e = eps_n (1 + 1e-6) + 2^-22 (the norm's relative error and the
+// roundings of u and of |u - m|).  Up to 8 levels the 7 midpoints sit in
+// registers (+inf past the last) and a 3-step bisection finds the code and the
+// two bracketing midpoints at once.
 __device__ __forceinline__ int fast_codebook(const Params& p, const Tab& tb, int k,
                                              const float* mids_s, const float (&mreg)[7], float z,
-                                             float rnx, float gamma, float eps_n, float cmax,
-                                             bool tiny, float& u, float& tau, bool& near) {
-  constexpr float kU = 5.9604644775390625e-08f;
+                                             float rnx, float e_u, bool tiny, float& u,
+                                             float& tau, bool& near) {
   const int L = p.cb_levels;
   u = z * rnx;  // rnx = 2^-s fl(1 / ||x||) (0 for a tiny ||x||): two roundings, as z 2^-s / ||x||
-  int lo_i = 0;
-  float dmin = 3.4e38f;
+  int c = 0;
+  float dmin;
   if (L <= 8) {
-#pragma unroll
-    for (int j = 0; j < 7; ++j) {
-      lo_i += mreg[j] < u ? 1 : 0;
-      dmin = fminf(dmin, fabsf(u - mreg[j]));
-    }
+    float lo = -INFINITY, hi = INFINITY;
+    bool g = u > mreg[3];
+    c = g ? 4 : 0;
+    lo = g ? mreg[3] : lo;
+    hi = g ? hi : mreg[3];
+    const float mb = c ? mreg[5] : mreg[1];
+    g = u > mb;
+    c += g ? 2 : 0;
+    lo = g ? mb : lo;
+    hi = g ? hi : mb;
+    const float mc = (c & 4) ? ((c & 2) ? mreg[6] : mreg[4]) : ((c & 2) ? mreg[2] : mreg[0]);
+    g = u > mc;
+    c += g ? 1 : 0;
+    lo = g ? mc : lo;
+    hi = g ? hi : mc;
+    dmin = fminf(u - lo, hi - u);
   } else {
     int hi_i = L - 1;
-    while (lo_i < hi_i) {
-      const int mid = (lo_i + hi_i) >> 1;
-      if (mids_s[mid] < u) lo_i = mid + 1; else hi_i = mid;
+    while (c < hi_i) {
+      const int mid = (c + hi_i) >> 1;
+      if (mids_s[mid] < u) c = mid + 1; else hi_i = mid;
     }
-    if (lo_i > 0) dmin = fminf(dmin, fabsf(u - mids_s[lo_i - 1]));
-    if (lo_i < L - 1) dmin = fminf(dmin, fabsf(u - mids_s[lo_i]));
+    dmin = 3.4e38f;
+    if (c > 0) dmin = fminf(dmin, fabsf(u - mids_s[c - 1]));
+    if (c < L - 1) dmin = fminf(dmin, fabsf(u - mids_s[c]));
   }
-  tau = (gamma * tb.vn[k] * (1.f + 1e-3f) + fabsf(u) * eps_n) * (1.f + 1e-6f) +
-        4.f * kU * (fabsf(u) + cmax);
+  tau = tiny ? 0.f : fmaf(fabsf(u), e_u, tb.q4[k].z);
   near = tiny || dmin <= tau;
-  if (tiny) tau = 0.f;
-  return lo_i;
+  return c;
 }
 
 template <int MODE, bool BF16, int CW>
@@ -395,9 +407,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
     const int ks = t.ks;
     const float kU = 5.9604644775390625e-08f;
     const float eps_n = 0.5f * ((D + 2) * kU) / (1.f - (D + 2) * kU) + 2.f * kU;
-    const float cmax = MODE == KVC_MODE_CODEBOOK
-                           ? fmaxf(fabsf(p.codebook[0]), fabsf(p.codebook[p.cb_levels - 1]))
-                           : 0.f;
+    const float e_u = (eps_n * (1.f + 1e-6f) + 4.f * kU) * (1.f + 1e-6f);  // |u| term of tau
     float mreg[7];
 #pragma unroll
     for (int j = 0; j < 7; ++j)
@@ -494,8 +504,8 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
           bool near;
           const int code = MODE == KVC_MODE_UNIFORM
                                ? fast_uniform<false>(tb, k, qp.x, z[j], nx, uf, tf, near)
-                               : fast_codebook(p, tb, k, mids_s, mreg, z[j], rnx, t.gamma, eps_n,
-                                               cmax, tiny, uf, tf, near);
+                               : fast_codebook(p, tb, k, mids_s, mreg, z[j], rnx, e_u, tiny, uf,
+                                               tf, near);
           crow[qp.y] = (uint8_t)code;
           nmask |= (uint32_t)near << j;
         }
@@ -513,8 +523,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
               fast_uniform<true>(tb, k, tb.qp[k].x, z[j], nx, uf, tf, near);
               if (!near) continue;  // an outer boundary: the clamped code is certain
             } else {
-              fast_codebook(p, tb, k, mids_s, mreg, z[j], rnx, t.gamma, eps_n, cmax, tiny, uf, tf,
-                            near);
+              fast_codebook(p, tb, k, mids_s, mreg, z[j], rnx, e_u, tiny, uf, tf, near);
             }
             const unsigned q = atomicAdd(&qcount, 1u);
             if (q < kQueue) {
@@ -685,6 +694,12 @@ int append_ws_table(const Geo& g, const kvc_layer_desc& d, int rpad, const doubl
       q4[k].w = round_up_f((std::fabs(c64[bk]) + std::fabs((double)d.qmin[bk])) / st *
                                std::ldexp(1.0, -23) +
                            std::ldexp(1.0, -22) * (qm + 2));
+    }
+    if (in && d.mode == KVC_MODE_CODEBOOK) {
+      double cmax = 0.0;
+      for (int j = 0; j < g.cb_levels; ++j) cmax = std::max(cmax, std::fabs((double)d.codebook[j]));
+      q4[k].z = round_up_f(gamma * (double)vn[k] * (1.0 + 1e-3) * (1.0 + 1e-6) +
+                           std::ldexp(1.0, -22) * cmax);
     }
     const int width = in ? g.bits[bk] : 0;
     qp[k] = make_int2(d.mode == KVC_MODE_UNIFORM && width ? (1 << width) - 1 : 0, ks - 1);
