@@ -53,8 +53,8 @@ typedef enum {
   KVC_ECAPACITY = -3, /* the append would exceed the capacity; nothing was written */
   KVC_ECUDA = -4,     /* a CUDA runtime call failed (no device, bad stream, launch error) */
   KVC_ETIMEOUT = -5,  /* a bounded device-side wait gave up (read by kvc_sync_status) */
-  KVC_EDEVICE = -6    /* a kernel met data it cannot encode exactly (e.g. |x| > 65504
-                         on the tensor-core path); read by kvc_sync_status */
+  KVC_EDEVICE = -6    /* reserved for data a kernel cannot encode exactly (read by
+                         kvc_sync_status); no current kernel reports it */
 } kvc_status;
 
 enum {

@@ -259,6 +259,23 @@ def test_cfg5_points(kvc, B, S, r, bits):
     check_fetch(gl.fetch(), gl, rl)
 
 
+@pytest.mark.parametrize("r,choices,budget", [(128, [0, 2, 4, 8], 384), (96, [0, 4, 8], 384)])
+def test_uniform_wide_rank_bf16(kvc, r, choices, budget):
+    """bf16 input, one basis per (b, h), rank above 64: the basis' three 16-bit
+    pieces no longer stack along one MMA N (3 r > 256), so the append takes
+    its one-tile-per-CTA tensor-core kernel.  Several tiles and a ragged tail."""
+    B, H, D, S = 1, 2, 128, 300
+    x = synth.kv_spectral(B, H, S, D, alpha=0.7, seed=7100 + r, tensor=0, dtype="bf16")
+    x64 = x.double().numpy()
+    p = fit_uniform(x64, 256, r, choices, budget)
+    gl, rl = _make(kvc, "uniform", B, H, D, p, "bf16", S, "auto")
+    gl.append(x.to(_dev()))
+    assert gl.sync_status() == 0
+    rl.append(x64)
+    _all_slots_match(gl, rl, x64)
+    check_fetch(gl.fetch(), gl, rl)
+
+
 # ------------------------------------------------------------------------- invariants
 
 @pytest.mark.parametrize("mode", ["uniform", "group", "codebook", "int8"])
