@@ -417,6 +417,12 @@ kvc_status kvc_init_layer(const kvc_layer_desc* d, kvc_layer** out) {
   auto* base = static_cast<uint8_t*>(block);
   kvc::bind_params(L->p, d, g, im, base);
   kvc::tc_bind(L->tc, base);
+  st = kvc::tc_alloc(L->tc, g.n_slots, r);
+  if (st) {
+    cudaFree(block);
+    delete L;
+    return st;
+  }
 
   L->block = block;
   L->device = dev;
@@ -460,6 +466,8 @@ kvc_status kvc_append_strided(kvc_layer* L, const void* x, int64_t T, int64_t sb
     e = kvc::launch_append_int8(L->p, a, s, &nk);
   else if (L->path == KVC_PATH_AUTO && kvc::tc_append_ok(L->tc, L->p, a))
     e = kvc::launch_append_tc(L->tc, L->p, a, s, &nk);
+  else if (L->path == KVC_PATH_AUTO && kvc::tc_group_ok(L->tc, L->p, a))
+    e = kvc::launch_append_group_tc(L->tc, L->p, a, s, &nk);
   else
     e = kvc::launch_append_generic(L->p, a, s, &nk);
   L->launches += nk;

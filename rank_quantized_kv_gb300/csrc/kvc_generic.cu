@@ -170,9 +170,15 @@ __device__ void quant_uniform(const Params& p, int beta, const float* vnorm, con
   if (valid && w > 0) c.codes[k] = (uint8_t)code;
 }
 
+// Error bound of the fp32 latents: |z32 - z| <= gamma n ||V_k|| + ex ||V_k|| + en n,
+// n = ||x - mean||.
+struct QBound {
+  float gamma, ex, en;
+};
+
 // Group: per token and group, s = max(absmax / qmax, 1e-8); q = clip(rint(z / s)).
 __device__ void quant_group(const Params& p, int beta, const float* vnorm, const RowCtx& c,
-                            int gi, int lane, unsigned* nref, unsigned* nside) {
+                            int gi, int lane, unsigned* nref, unsigned* nside, const QBound& qb) {
   const int first = p.groups[gi * 3 + 0];
   const int cnt = p.groups[gi * 3 + 1];
   const int w = p.groups[gi * 3 + 2];
@@ -180,10 +186,10 @@ __device__ void quant_group(const Params& p, int beta, const float* vnorm, const
   const int off = 1 << (w - 1);
   const int k = first + lane;
   const bool valid = lane < cnt;
-  const float gam = proj_gamma(p.d_in);
   const float z = valid ? c.zs[k] : 0.f;
   const float az = fabsf(z);
-  const float tz = valid ? gam * c.nrm * vnorm[k] * (1.f + 1e-3f) : 0.f;
+  const float tz =
+      valid ? (qb.gamma * c.nrm * vnorm[k] + qb.ex * vnorm[k] + qb.en * c.nrm) * (1.f + 1e-3f) : 0.f;
   const float a32 = warp_maxf(valid ? az : 0.f);
   const float tzm = warp_maxf(tz);
   // Too close to zero (or to the 1e-8 floor) to trust the fp32 maximum.
@@ -205,6 +211,7 @@ __device__ void quant_group(const Params& p, int beta, const float* vnorm, const
     // The scale needs the exact maximum: recompute every component that could hold it.
     const bool cand = valid && (full || az + tz >= a32 - tzm);
     unsigned todo = __ballot_sync(kFull, cand) | nmask;
+    const bool redone = (todo >> lane) & 1u;
     if (lane == 0) {
       atomicAdd(nref, (unsigned)__popc(nmask));
       atomicAdd(nside, 1u);
@@ -217,6 +224,10 @@ __device__ void quant_group(const Params& p, int beta, const float* vnorm, const
       const ff2 z2 =
           dot_ff(c.xs, c.mean, p.Vt + ((int64_t)beta * p.r + first + f) * p.d_in, p.d_in, lane);
       if (lane == f) zmine = z2;
+    }
+    if (redone && tz > 0.f) {  // the bound in use against the observed error
+      const float ratio = fabsf((z - zmine.hi) - zmine.lo) / tz;
+      atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(ratio));
     }
     ff2 a2 = cand ? ff_abs(zmine) : ff2{0.f, 0.f};
 #pragma unroll
@@ -306,7 +317,7 @@ constexpr int kAppTT = 8;
 constexpr int kAppThreads = 256;
 
 __global__ void __launch_bounds__(kAppThreads)
-append_generic_kernel(Params p, AppendArgs a) {
+append_generic_kernel(Params p, AppendArgs a, ZIn zin) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int slot = blockIdx.y;
   const int64_t t0 = (int64_t)blockIdx.x * kAppTT;
@@ -352,9 +363,16 @@ append_generic_kernel(Params p, AppendArgs a) {
     acc = warp_sumf(acc);
     if (lane == 0) nrm[t] = sqrtf(acc);  // the bounds below carry their own margin
   }
-  // 3. projection: fp32 fma in blocks of kProjBlk terms, then the block sums
+  // 3. projection: fp32 fma in blocks of kProjBlk terms, then the block sums;
+  // or the latents the tensor-core projection wrote for this tile
+  const bool from_z = zin.z != nullptr && zin.ovf[(int64_t)slot * zin.tps + (t0 >> 7)] == 0;
+  const QBound qb = from_z ? QBound{zin.gamma, zin.ex, zin.en} : QBound{proj_gamma(d_in), 0.f, 0.f};
   const float* V = p.V + (int64_t)beta * d_in * r;
-  for (int k = threadIdx.x; k < r; k += blockDim.x) {
+  if (from_z) {
+    const float* zsrc = zin.z + ((int64_t)slot * zin.Tc + t0) * r;
+    for (int idx = threadIdx.x; idx < n * r; idx += blockDim.x) zs[idx] = zsrc[idx];
+  }
+  for (int k = from_z ? r : threadIdx.x; k < r; k += blockDim.x) {
     float acc[kAppTT];
 #pragma unroll
     for (int t = 0; t < kAppTT; ++t) acc[t] = 0.f;
@@ -396,7 +414,7 @@ append_generic_kernel(Params p, AppendArgs a) {
     for (int item = warp; item < n * p.n_groups; item += nwarps) {
       const int t = item / p.n_groups, gi = item - t * p.n_groups;
       RowCtx c{xs + t * d_in, mean, zs + t * r, nrm[t], codes + t * r, side + t * n_side};
-      quant_group(p, beta, vnorm, c, gi, lane, &s_nref, &s_nside);
+      quant_group(p, beta, vnorm, c, gi, lane, &s_nref, &s_nside, qb);
     }
   } else {
     const int nchunk = (r + 31) / 32;
@@ -741,7 +759,8 @@ __global__ void __launch_bounds__(256) fetch_int8_vec(Params p, FetchArgs f) {
 
 }  // namespace
 
-cudaError_t launch_append_generic(const Params& p, const AppendArgs& a, cudaStream_t s, int* nk) {
+cudaError_t launch_append_generic(const Params& p, const AppendArgs& a, cudaStream_t s, int* nk,
+                                  const ZIn* zin) {
   if (a.T <= 0) return cudaSuccess;
   const int n_side = p.side_bytes / 2;
   const size_t smem = sizeof(float) * (2 * kAppTT * p.d_in + kAppTT * p.r + kAppTT) +
@@ -752,7 +771,7 @@ cudaError_t launch_append_generic(const Params& p, const AppendArgs& a, cudaStre
     if (e != cudaSuccess) return e;
   }
   dim3 grid((unsigned)((a.T + kAppTT - 1) / kAppTT), (unsigned)p.n_slots);
-  append_generic_kernel<<<grid, kAppThreads, smem, s>>>(p, a);
+  append_generic_kernel<<<grid, kAppThreads, smem, s>>>(p, a, zin ? *zin : ZIn{});
   ++*nk;
   return cudaGetLastError();
 }

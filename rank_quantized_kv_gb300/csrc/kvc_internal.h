@@ -65,6 +65,18 @@ struct FetchArgs {
   int64_t S;     // tokens to reconstruct
 };
 
+// Latents projected elsewhere (group mode: the tensor-core projection), read
+// by the CUDA-core append in place of its own projection, with the error bound
+// that projection guarantees:
+//   |z32 - z| <= gamma ||x - mean|| ||V_k|| + ex ||V_k|| + en ||x - mean||.
+struct ZIn {
+  const float* z = nullptr;  // [n_slots][Tc][r] fp32 latents of the call's tokens
+  const int* ovf = nullptr;  // [n_slots][tps]: nonzero where a 128-token tile is not in z
+  int64_t Tc = 0;            // rows per slot in z
+  int tps = 0;               // 128-token tiles per slot
+  float gamma = 0.f, ex = 0.f, en = 0.f;
+};
+
 // Everything derived from a descriptor, on the host (kvc_api.cu).
 struct Geo {
   int d_in = 0, Hg = 0, n_slots = 0, nb = 0, r = 0;
@@ -109,7 +121,8 @@ bool device_ptr_on(const void* ptr, int dev);
 
 // Kernel launchers (kvc_generic.cu).  Return the launch's cudaError_t and add
 // the number of kernels launched to *nk.
-cudaError_t launch_append_generic(const Params& p, const AppendArgs& a, cudaStream_t s, int* nk);
+cudaError_t launch_append_generic(const Params& p, const AppendArgs& a, cudaStream_t s, int* nk,
+                                  const ZIn* zin = nullptr);
 cudaError_t launch_fetch_generic(const Params& p, const FetchArgs& f, cudaStream_t s, int* nk);
 cudaError_t launch_append_int8(const Params& p, const AppendArgs& a, cudaStream_t s, int* nk);
 cudaError_t launch_fetch_int8(const Params& p, const FetchArgs& f, cudaStream_t s, int* nk);

@@ -687,6 +687,80 @@ void prepare_append(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>&
   }
 }
 
+// Group mode: tables of the tensor-core projection (kvc_group_proj.cu).  V is
+// scaled by 2^se (largest entry near 2^14) and split into fp16 hi + lo, cut
+// into [rpad][64] slices per head and 64-column box, each in core-matrix order.
+// The latents' error bound, per unit of ||x - mean|| ||V_k|| (gamma):
+//   the hi accumulator's chain of D terms per head, the truncation model of
+//   the uniform append (the same /8), plus 2^-9 of it for the rest
+//   accumulator (its terms are <= 2^-10 of the hi terms, twice as many);
+//   the epilogue's fp32 sums, gamma_{hpg+2}; the pieces' representation
+//   errors, 2^-22 each for x and V, and the dropped x_lo V_lo, 2^-22;
+//   the rounding of x - mean, 2^-24;
+// absolute parts where a piece is subnormal in fp16 (residual <= 2^-25 in
+// scaled units): ex = 2^-24-sx sqrt(d_in) (times ||V_k||) and
+// en = 2^-24-se sqrt(d_in) (times ||x - mean||).
+constexpr size_t kZScratchBytes = size_t(32) << 20;
+
+void prepare_group(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>& image,
+                   TcPlan& plan) {
+  if (d.mode != KVC_MODE_GROUP || !(d.in_dtype == KVC_BF16 || d.in_dtype == KVC_F16)) return;
+  const int D = d.D, hpg = d.heads_per_group, din = g.d_in, r = g.r, nb = g.nb;
+  int rpad = 32;
+  while (rpad < r) rpad *= 2;
+  if (!(D % 64 == 0 && rpad <= 256) || encoder() == nullptr) return;
+  int n_b = 0;
+  const size_t smem = group_proj_smem(rpad, &n_b);
+  if (smem == 0) return;
+  float vmax = 0.f;
+  for (size_t i = 0; i < (size_t)nb * din * r; ++i) vmax = std::max(vmax, std::fabs(d.V[i]));
+  if (!(vmax > 0.f) || !std::isfinite(vmax)) return;
+  const int se = 14 - (int)std::ceil(std::log2((double)vmax));
+  const int sx = 6;  // x - mean up to 1023 in magnitude; larger tiles fall back
+  const float vscale = std::ldexp(1.f, se);
+  const int nbx = D / 64;
+  std::vector<uint16_t> Bop((size_t)nb * din * 2 * rpad, 0);
+  for (int b = 0; b < nb; ++b) {
+    const float* V = d.V + (size_t)b * din * r;
+    for (int i = 0; i < din; ++i) {
+      const int h = i / D, bx = (i % D) / 64, kk = i % 64;
+      for (int k = 0; k < r; ++k) {
+        const float v = V[(size_t)i * r + k] * vscale;  // exact
+        const uint16_t hi = half_bits(v);
+        const uint16_t lo = half_bits(v - __half2float(__ushort_as_half(hi)));
+        const size_t in_slice = ((size_t)(k / 8) * 8 + kk / 8) * 64 + (k % 8) * 8 + (kk % 8);
+        for (int pc = 0; pc < 2; ++pc) {
+          const size_t slice = (((size_t)b * hpg + h) * nbx + bx) * 2 + pc;
+          Bop[slice * rpad * 64 + in_slice] = pc == 0 ? hi : lo;
+        }
+      }
+    }
+  }
+  const double u = std::ldexp(1.0, -24);
+  const double g_tc =
+      (17.0 * D / 16.0 + 2.0) * std::ldexp(1.0, -23) * (1.0 + std::ldexp(1.0, -7)) / 8.0;
+  const double n_ep = hpg + 2;
+  const double gamma = g_tc * (1.0 + std::ldexp(1.0, -9)) + n_ep * u / (1.0 - n_ep * u) +
+                       3.0 * std::ldexp(1.0, -22) + u;
+  const double root = std::sqrt((double)din);
+  const int64_t per_tok = (int64_t)g.n_slots * r * 4;
+  int64_t Tc = (int64_t)kZScratchBytes / per_tok / kTile * kTile;
+  Tc = std::max<int64_t>(Tc, kTile);
+  Tc = std::min<int64_t>(Tc, (d.capacity + kTile - 1) / kTile * kTile);
+  plan.oGpB = put(image, Bop.data(), Bop.size());
+  plan.gp_bf16 = d.in_dtype == KVC_BF16 ? 1 : 0;
+  plan.gp_rpad = rpad;
+  plan.gp_nb = n_b;
+  plan.gp_smem = smem;
+  plan.gp_xscale = std::ldexp(1.f, sx);
+  plan.gp_zscale = std::ldexp(1.f, -(sx + se));
+  plan.gp_gamma = (float)gamma;
+  plan.gp_ex = (float)(std::ldexp(1.0, -24 - sx) * root);
+  plan.gp_en = (float)(std::ldexp(1.0, -24 - se) * root);
+  plan.gp_Tc = Tc;
+  plan.gp_ready = true;
+}
+
 using AppendKernel = void (*)(const Params, const AppendTc, const CUtensorMap, const AppendArgs, int,
                               int);
 
@@ -721,6 +795,7 @@ kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t
   plan = TcPlan{};
   if (d.mode == KVC_MODE_INT8) return KVC_OK;
   prepare_append(d, g, image, plan);
+  prepare_group(d, g, image, plan);
   const int D = d.D, din = g.d_in, r = g.r, nb = g.nb;
   // K layout: every packed segment starts on an 8-value chunk boundary, so a
   // chunk of A is decoded from consecutive bytes of one segment; the gaps are
@@ -853,9 +928,28 @@ void tc_bind(TcPlan& plan, uint8_t* base) {
     plan.c64 = reinterpret_cast<const double*>(base + plan.oC64);
     if (plan.ws_ready) plan.wsTab = reinterpret_cast<const unsigned char*>(base + plan.oWsTab);
   }
+  if (plan.gp_ready) plan.gpB = reinterpret_cast<const uint16_t*>(base + plan.oGpB);
 }
 
-void tc_release(TcPlan&) {}
+kvc_status tc_alloc(TcPlan& plan, int n_slots, int r) {
+  if (!plan.gp_ready) return KVC_OK;
+  const size_t zb = align_up((size_t)n_slots * plan.gp_Tc * r * sizeof(float), 256);
+  const size_t ob = (size_t)n_slots * (plan.gp_Tc / kTile) * sizeof(int);
+  void* mem = nullptr;
+  if (cudaMalloc(&mem, zb + ob) != cudaSuccess) {
+    cudaGetLastError();
+    return set_error(KVC_ECUDA, "cudaMalloc(group projection scratch) failed");
+  }
+  plan.zbuf = static_cast<float*>(mem);
+  plan.zovf = reinterpret_cast<int*>(static_cast<uint8_t*>(mem) + zb);
+  return KVC_OK;
+}
+
+void tc_release(TcPlan& plan) {
+  if (plan.zbuf) cudaFree(plan.zbuf);
+  plan.zbuf = nullptr;
+  plan.zovf = nullptr;
+}
 
 bool tc_fetch_ok(const TcPlan& plan, const Params&, const FetchArgs& f) {
   return plan.fetch_ready && (reinterpret_cast<uintptr_t>(f.out) % 16 == 0) && f.S > 0 &&
@@ -891,6 +985,55 @@ bool tc_append_ok(const TcPlan& plan, const Params& p, const AppendArgs& a) {
   return plan.append_ready && (reinterpret_cast<uintptr_t>(a.x) % 16 == 0) && a.T > 0 &&
          a.T < (int64_t(1) << 31) && a.st % 8 == 0 && a.sh % 8 == 0 && a.sb % 8 == 0 &&
          a.st >= p.D && (p.H == 1 || a.sh > 0) && (p.B == 1 || a.sb > 0);
+}
+
+// x as a 4D tensor map (D, tokens, heads, batch), boxes of 64 x 128 x 1 x 1
+// with 128-byte swizzle.
+CUresult encode_x_map(CUtensorMap* map, const Params& p, const AppendArgs& a, bool bf16) {
+  const cuuint64_t dims[4] = {(cuuint64_t)p.D, (cuuint64_t)a.T, (cuuint64_t)p.H, (cuuint64_t)p.B};
+  const cuuint64_t strides[3] = {(cuuint64_t)a.st * 2,
+                                 (cuuint64_t)(p.H > 1 ? a.sh : a.T * a.st) * 2,
+                                 (cuuint64_t)(p.B > 1 ? a.sb : p.H * a.T * a.st) * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)kTile, 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return encoder()(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                   4, const_cast<void*>(a.x), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+bool tc_group_ok(const TcPlan& plan, const Params& p, const AppendArgs& a) {
+  // TMA needs a 16-byte aligned base and strides that are multiples of 16 bytes
+  return plan.gp_ready && plan.zbuf && (reinterpret_cast<uintptr_t>(a.x) % 16 == 0) && a.T > 0 &&
+         a.T < (int64_t(1) << 31) && a.st % 8 == 0 && a.sh % 8 == 0 && a.sb % 8 == 0 &&
+         a.st >= p.D && (p.H == 1 || a.sh > 0) && (p.B == 1 || a.sb > 0);
+}
+
+// Chunks of gp_Tc tokens: the projection into the scratch, then the CUDA-core
+// quantiser and packer reading it.
+cudaError_t launch_append_group_tc(const TcPlan& plan, const Params& p, const AppendArgs& a,
+                                   cudaStream_t s, int* nk) {
+  for (int64_t c0 = 0; c0 < a.T; c0 += plan.gp_Tc) {
+    AppendArgs ac = a;
+    ac.x = static_cast<const uint16_t*>(a.x) + c0 * a.st;
+    ac.T = std::min(plan.gp_Tc, a.T - c0);
+    ac.t_base = a.t_base + c0;
+    CUtensorMap map;
+    if (encode_x_map(&map, p, ac, plan.gp_bf16 != 0) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    cudaError_t e = launch_group_proj(plan, p, ac, map, s, nk);
+    if (e != cudaSuccess) return e;
+    ZIn zin;
+    zin.z = plan.zbuf;
+    zin.ovf = plan.zovf;
+    zin.Tc = plan.gp_Tc;
+    zin.tps = (int)((ac.T + kTile - 1) / kTile);
+    zin.gamma = plan.gp_gamma;
+    zin.ex = plan.gp_ex;
+    zin.en = plan.gp_en;
+    e = launch_append_generic(p, ac, s, nk, &zin);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_append_tc(const TcPlan& plan, const Params& p, const AppendArgs& a,

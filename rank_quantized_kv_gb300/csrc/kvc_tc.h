@@ -80,11 +80,28 @@ struct TcPlan {
   int ws_pmax = 0;                   // largest packed row
   size_t oWsTab = 0;
   const unsigned char* wsTab = nullptr;  // [nb][tab_bytes] quantiser tables
+
+  // group mode: z = (x - mean) V on the tensor cores (kvc_group_proj.cu) into a
+  // scratch the CUDA-core quantiser reads, in chunks of gp_Tc tokens
+  bool gp_ready = false;
+  int gp_bf16 = 0;             // x is bf16 (else fp16)
+  int gp_rpad = 0;             // N of the MMA: r rounded up to a power of two >= 32
+  int gp_nb = 0;               // basis slice stages
+  size_t gp_smem = 0;
+  float gp_xscale = 1.f;       // 2^sx applied to x - mean before the fp16 split
+  float gp_zscale = 1.f;       // 2^-(sx + se)
+  float gp_gamma = 0.f, gp_ex = 0.f, gp_en = 0.f;  // the latents' error bound (ZIn)
+  int64_t gp_Tc = 0;           // tokens per chunk
+  size_t oGpB = 0;
+  const uint16_t* gpB = nullptr;  // [nb][hpg][D/64][2][rpad][64] fp16 slices, core-matrix order
+  float* zbuf = nullptr;          // [n_slots][gp_Tc][r], owned (tc_alloc / tc_release)
+  int* zovf = nullptr;            // [n_slots][gp_Tc / 128]
 };
 
 kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>& image,
                       TcPlan& plan);
 void tc_bind(TcPlan& plan, uint8_t* block_base);
+kvc_status tc_alloc(TcPlan& plan, int n_slots, int r);  // device scratch the plan needs
 void tc_release(TcPlan& plan);
 
 bool tc_append_ok(const TcPlan& plan, const Params& p, const AppendArgs& a);
@@ -93,6 +110,9 @@ cudaError_t launch_append_tc(const TcPlan& plan, const Params& p, const AppendAr
                              cudaStream_t s, int* nk);
 cudaError_t launch_fetch_tc(const TcPlan& plan, const Params& p, const FetchArgs& f,
                             cudaStream_t s, int* nk);
+bool tc_group_ok(const TcPlan& plan, const Params& p, const AppendArgs& a);
+cudaError_t launch_append_group_tc(const TcPlan& plan, const Params& p, const AppendArgs& a,
+                                   cudaStream_t s, int* nk);
 
 // Warp-specialised persistent fetch (kvc_fetch_pipe.cu); `map` is the output
 // tensor map.  fetch_pipe_smem sizes its rings for D, K, the side bytes, the
@@ -112,6 +132,12 @@ size_t append_ws_plan(int D, int r, int rpad, int npieces, int pmax, int max_chu
                       AppendWsShape* sh);
 cudaError_t launch_append_ws(const TcPlan& plan, const Params& p, const AppendArgs& a,
                              const CUtensorMap& xmap, cudaStream_t s, int* nk);
+// Group-mode projection (kvc_group_proj.cu): shared memory for N = rpad and
+// the basis slice stages it leaves room for (0 when two do not fit); the
+// launcher for one chunk of tokens (`map` covers exactly that chunk).
+size_t group_proj_smem(int rpad, int* n_b);
+cudaError_t launch_group_proj(const TcPlan& plan, const Params& p, const AppendArgs& a,
+                              const CUtensorMap& map, cudaStream_t s, int* nk);
 int sm_count();
 
 }  // namespace kvc

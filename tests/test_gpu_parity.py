@@ -171,6 +171,65 @@ def test_cfg3_full_sampled(kvc):
     print(f"cfg3 full: counters {gl.counters()}")
 
 
+def _same_store(ga, gb, n_slots):
+    for s in range(n_slots):
+        ra, sa = ga.slot_rows(s)
+        rb, sb = gb.slot_rows(s)
+        assert torch.equal(ra, rb), f"slot {s}: packed rows differ"
+        assert torch.equal(sa, sb), f"slot {s}: side words differ"
+
+
+def test_group_tensor_core_projection_chunks(kvc):
+    """Group mode with the tensor-core projection in two chunks (16 slots, r = 256:
+    2048 tokens per chunk, then a ragged 452).  Codes against the oracle on two
+    slots; the whole store equal to the CUDA-core projection's (both decide every
+    code exactly)."""
+    B, H, S, hpg = 8, 16, 2500, 8
+    x, x64 = _cfg3_inputs(B, H, S, hpg, 0)
+    params = fit_group(x64[:, :, :512], hpg, 256)
+    ga, rl = _make(kvc, "group", B, H, 128, params, "bf16", S, "auto")
+    gg, _ = _make(kvc, "group", B, H, 128, params, "bf16", S, "generic")
+    xd = x.to(_dev())
+    ga.append(xd)
+    gg.append(xd)
+    assert ga.sync_status() == 0 and gg.sync_status() == 0
+    c = ga.counters()
+    assert c["launches"] == 4, c  # per chunk: the projection, then the quantiser
+    assert c["max_error_ratio"] < 1.0, c
+    _same_store(ga, gg, rl.n_slots)
+    n = mism = 0
+    for s in (0, rl.n_slots - 1):
+        rows, side = ga.slot_rows(s)
+        cc, m = compare_codes(rows.cpu().numpy(), side.cpu().numpy(), rl, s, rl.slot_rows(x64, s))
+        n, mism = n + cc, mism + m
+    assert mism <= MISMATCH_RATE * n
+    print(f"group tensor-core projection: counters {c}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_group_tile_beyond_split_range(kvc, dtype):
+    """Tokens with |x - mean| in the thousands, beyond the fp16 split the
+    tensor-core projection uses: their 128-token tiles are projected on the CUDA
+    cores instead, and every code still matches the oracle (bf16 and fp16 x)."""
+    B, H, S, hpg = 1, 16, 300, 8
+    x, x64 = _cfg3_inputs(B, H, S, hpg, 1)
+    params = fit_group(x64, hpg, 256)
+    x[0, 3, 150, 5] = 3000.0
+    x[0, 9, 20, 100] = -2500.0
+    if dtype == "f16":
+        x = x.to(torch.float16)
+    x64 = x.double().numpy()
+    gl, rl = _make(kvc, "group", B, H, 128, params, dtype, S, "auto")
+    gg, _ = _make(kvc, "group", B, H, 128, params, dtype, S, "generic")
+    gl.append(x.to(_dev()))
+    gg.append(x.to(_dev()))
+    assert gl.sync_status() == 0 and gg.sync_status() == 0
+    rl.append(x64)
+    _all_slots_match(gl, rl, x64)
+    _same_store(gl, gg, rl.n_slots)
+    check_fetch(gl.fetch(), gl, rl)
+
+
 # ------------------------------------------------------------------------- config 4
 
 @pytest.mark.parametrize("path", PATHS)
