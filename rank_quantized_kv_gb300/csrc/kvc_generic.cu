@@ -77,19 +77,48 @@ __device__ __forceinline__ double dot64(const float* x, const float* m, const fl
 
 // sum_i (x_i - m_i) * w_i as a double-float (compensated fp32: x - m and each
 // product split exactly, TwoSum accumulation), one warp, on every lane.
+__device__ __forceinline__ void dot_ff_term(float xi, float mi, float wi, float& S, float& C) {
+  float dh, dl;
+  two_sum(xi, -mi, dh, dl);
+  const float pr = dh * wi;
+  const float pe = fmaf(dh, wi, -pr);
+  float s, e;
+  two_sum(S, pr, s, e);
+  S = s;
+  C += pe + e + dl * wi;
+}
+
 __device__ __forceinline__ ff2 dot_ff(const float* x, const float* m, const float* w, int n,
                                       int lane) {
   float S = 0.f, C = 0.f;
-  for (int i = lane; i < n; i += 32) {
-    float dh, dl;
-    two_sum(x[i], -m[i], dh, dl);
-    const float wi = w[i];
-    const float pr = dh * wi;
-    const float pe = fmaf(dh, wi, -pr);
-    float s, e;
-    two_sum(S, pr, s, e);
-    S = s;
-    C += pe + e + dl * wi;
+  if ((n & 3) == 0) {  // 4 consecutive terms per lane and load (16-byte aligned rows)
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    const float4* m4 = reinterpret_cast<const float4*>(m);
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    const int n4 = n >> 2;
+    int j = lane;
+    for (; j + 96 < n4; j += 128) {  // four loads of w in flight per lane
+      float4 wv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) wv[u] = __ldg(w4 + j + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 xv = x4[j + 32 * u], mv = m4[j + 32 * u];
+        dot_ff_term(xv.x, mv.x, wv[u].x, S, C);
+        dot_ff_term(xv.y, mv.y, wv[u].y, S, C);
+        dot_ff_term(xv.z, mv.z, wv[u].z, S, C);
+        dot_ff_term(xv.w, mv.w, wv[u].w, S, C);
+      }
+    }
+    for (; j < n4; j += 32) {
+      const float4 xv = x4[j], mv = m4[j], wv = __ldg(w4 + j);
+      dot_ff_term(xv.x, mv.x, wv.x, S, C);
+      dot_ff_term(xv.y, mv.y, wv.y, S, C);
+      dot_ff_term(xv.z, mv.z, wv.z, S, C);
+      dot_ff_term(xv.w, mv.w, wv.w, S, C);
+    }
+  } else {
+    for (int i = lane; i < n; i += 32) dot_ff_term(x[i], m[i], w[i], S, C);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -316,7 +345,7 @@ __device__ void quant_codebook(const Params& p, int beta, const float* vnorm, co
 constexpr int kAppTT = 8;
 constexpr int kAppThreads = 256;
 
-__global__ void __launch_bounds__(kAppThreads)
+__global__ void __launch_bounds__(kAppThreads, 4)
 append_generic_kernel(Params p, AppendArgs a, ZIn zin) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int slot = blockIdx.y;
@@ -326,9 +355,13 @@ append_generic_kernel(Params p, AppendArgs a, ZIn zin) {
   const int d_in = p.d_in, r = p.r;
   const int b = slot / p.Hg, g = slot % p.Hg;
 
+  // With latents from the tensor-core projection the centred rows are not
+  // kept (they are recomputed where needed: the same fp32 subtraction), so
+  // the block needs half the shared memory and more of them fit on an SM.
+  const bool has_xc = zin.z == nullptr;
   float* xs = reinterpret_cast<float*>(smem);      // [TT][d_in]
-  float* xc = xs + kAppTT * d_in;                  // [TT][d_in] fl(x - mean)
-  float* zs = xc + kAppTT * d_in;                  // [TT][r]
+  float* xc = has_xc ? xs + kAppTT * d_in : nullptr;  // [TT][d_in] fl(x - mean)
+  float* zs = xs + (has_xc ? 2 : 1) * kAppTT * d_in;  // [TT][r]
   float* nrm = zs + kAppTT * r;                    // [TT]
   __half* side = reinterpret_cast<__half*>(nrm + kAppTT);  // [TT][n_side]
   const int n_side = p.side_bytes / 2;
@@ -339,16 +372,49 @@ append_generic_kernel(Params p, AppendArgs a, ZIn zin) {
   const float* vnorm = p.vnorm + (int64_t)beta * r;
   if (threadIdx.x == 0) { s_nref = 0; s_nside = 0; }
 
-  // 1. token rows -> fp32 (exact for f32 / f16 / bf16 inputs)
-  for (int idx = threadIdx.x; idx < kAppTT * d_in; idx += blockDim.x) {
-    const int t = idx / d_in, i = idx - t * d_in;
-    float v = 0.f;
-    if (t < n) {
-      const int h = g * p.hpg + i / p.D, dd = i % p.D;
-      v = load_in(a.x, p.in_dtype, (int64_t)b * a.sb + (int64_t)h * a.sh + (t0 + t) * a.st + dd);
+  // 1. token rows -> fp32 (exact for f32 / f16 / bf16 inputs); 16-bit inputs
+  // with 16-byte aligned rows and head slices load 8 values at a time
+  const bool vec8 = p.in_dtype != KVC_F32 && p.D % 8 == 0 &&
+                    (reinterpret_cast<uintptr_t>(a.x) & 15) == 0 &&
+                    ((a.sb | a.sh | a.st) & 7) == 0;
+  if (vec8) {
+    for (int e = threadIdx.x * 8; e < kAppTT * d_in; e += blockDim.x * 8) {
+      const int t = e / d_in, i = e - t * d_in;
+      float v[8];
+      if (t < n) {
+        const int h = g * p.hpg + i / p.D, dd = i % p.D;
+        const uint4 raw = *reinterpret_cast<const uint4*>(
+            static_cast<const uint16_t*>(a.x) + (int64_t)b * a.sb + (int64_t)h * a.sh +
+            (t0 + t) * a.st + dd);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint16_t bits = (uint16_t)(w[q >> 1] >> (16 * (q & 1)));
+          v[q] = p.in_dtype == KVC_F16 ? __half2float(__ushort_as_half(bits))
+                                        : __uint_as_float((uint32_t)bits << 16);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = 0.f;
+      }
+      *reinterpret_cast<float4*>(xs + e) = make_float4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<float4*>(xs + e + 4) = make_float4(v[4], v[5], v[6], v[7]);
+      if (has_xc) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xc[e + q] = t < n ? v[q] - mean[i + q] : 0.f;
+      }
     }
-    xs[idx] = v;
-    xc[idx] = t < n ? v - mean[i] : 0.f;  // the projection's one rounding of x - mean
+  } else {
+    for (int idx = threadIdx.x; idx < kAppTT * d_in; idx += blockDim.x) {
+      const int t = idx / d_in, i = idx - t * d_in;
+      float v = 0.f;
+      if (t < n) {
+        const int h = g * p.hpg + i / p.D, dd = i % p.D;
+        v = load_in(a.x, p.in_dtype, (int64_t)b * a.sb + (int64_t)h * a.sh + (t0 + t) * a.st + dd);
+      }
+      xs[idx] = v;
+      if (has_xc) xc[idx] = t < n ? v - mean[i] : 0.f;  // the projection's one rounding of x - mean
+    }
   }
   __syncthreads();
 
@@ -357,7 +423,7 @@ append_generic_kernel(Params p, AppendArgs a, ZIn zin) {
   for (int t = warp; t < kAppTT; t += nwarps) {
     float acc = 0.f;
     for (int i = lane; i < d_in; i += 32) {
-      const float d = xc[t * d_in + i];
+      const float d = has_xc ? xc[t * d_in + i] : xs[t * d_in + i] - mean[i];
       acc = fmaf(d, d, acc);
     }
     acc = warp_sumf(acc);
@@ -384,7 +450,8 @@ append_generic_kernel(Params p, AppendArgs a, ZIn zin) {
         for (int i = i0; i < min(i0 + kProjBlk, d_in); ++i) {
           const float v = V[(int64_t)i * r + k];
 #pragma unroll
-          for (int t = 0; t < kAppTT; ++t) blk[t] = fmaf(xc[t * d_in + i], v, blk[t]);
+          for (int t = 0; t < kAppTT; ++t)
+            blk[t] = fmaf(has_xc ? xc[t * d_in + i] : xs[t * d_in + i] - mean[i], v, blk[t]);
         }
       } else {  // whole block, 4 columns per 128-bit load
 #pragma unroll 2
@@ -393,7 +460,14 @@ append_generic_kernel(Params p, AppendArgs a, ZIn zin) {
         const float v2 = V[(int64_t)(i + 2) * r + k], v3 = V[(int64_t)(i + 3) * r + k];
 #pragma unroll
         for (int t = 0; t < kAppTT; ++t) {
-          const float4 c4 = *reinterpret_cast<const float4*>(xc + t * d_in + i);
+          float4 c4;
+          if (has_xc) {
+            c4 = *reinterpret_cast<const float4*>(xc + t * d_in + i);
+          } else {
+            const float4 x4 = *reinterpret_cast<const float4*>(xs + t * d_in + i);
+            const float4 m4 = *reinterpret_cast<const float4*>(mean + i);
+            c4 = make_float4(x4.x - m4.x, x4.y - m4.y, x4.z - m4.z, x4.w - m4.w);
+          }
           blk[t] = fmaf(c4.x, v0, blk[t]);
           blk[t] = fmaf(c4.y, v1, blk[t]);
           blk[t] = fmaf(c4.z, v2, blk[t]);
@@ -763,7 +837,7 @@ cudaError_t launch_append_generic(const Params& p, const AppendArgs& a, cudaStre
                                   const ZIn* zin) {
   if (a.T <= 0) return cudaSuccess;
   const int n_side = p.side_bytes / 2;
-  const size_t smem = sizeof(float) * (2 * kAppTT * p.d_in + kAppTT * p.r + kAppTT) +
+  const size_t smem = sizeof(float) * ((zin ? 1 : 2) * kAppTT * p.d_in + kAppTT * p.r + kAppTT) +
                       sizeof(__half) * kAppTT * (n_side > 0 ? n_side : 1) + kAppTT * p.r + 16;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(append_generic_kernel,

@@ -22,10 +22,11 @@
 //                       swizzle) into four 32 KB stages, basis slices
 //                       (rpad x 64 fp16, bulk copies) into a ring;
 //   MMA (warp 17)       per box 12 MMAs of M = 128, N = rpad, K = 16;
-//   warps 0-15          split the next head's boxes in place (x_hi over the
-//                       raw tile, x_lo beside it), then drain this head's
-//                       accumulators: warp w reads TMEM lanes 32 (w % 4)..
-//                       (its tokens) and the w / 4-th quarter of the columns.
+//   warps 0-15          drain this head's accumulators (warp w reads TMEM
+//                       lanes 32 (w % 4).. (its tokens) and the w / 4-th
+//                       quarter of the columns), then split the boxes of the
+//                       head two ahead in place (x_hi over the raw tile, x_lo
+//                       beside it).
 // A tile holding a value the split cannot represent (|xc 2^sx| >= 65504, or
 // not finite) is flagged; the quantiser projects that tile itself.
 #include <cuda_fp16.h>
@@ -285,7 +286,10 @@ __global__ void __launch_bounds__(kThr, 1)
       }
     };
 
+    // Two heads are split ahead: the MMA of head j + 1 starts as soon as head
+    // j is drained, and splitting head j + 2 overlaps it.
     if (m > 0) split_head();
+    if (ci < m) split_head();
     int es = first / tps, eb = first % tps;
     uint32_t heads = 0;
     for (int i = 0; i < m; ++i) {
@@ -293,7 +297,6 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
       for (int j = 0; j < CPT; ++j) zacc[j] = 0.f;
       for (int h = 0; h < hpg; ++h, ++heads) {
-        if (ci < m) split_head();
         if (!abort_flag && !mbar_wait_bounded(&acc_full, heads & 1u, kWaitNs)) abort_flag = 1;
         tc_fence_after();
 #pragma unroll
@@ -309,6 +312,7 @@ __global__ void __launch_bounds__(kThr, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty);
+        if (ci < m) split_head();
       }
       const int64_t t = (int64_t)eb * kTile + row;
       if (t < a.T) {
