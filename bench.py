@@ -108,8 +108,8 @@ class ClockSampler:
 # token-head of a kernel, from the capture named beside it, where the kernel
 # has not changed since.  The roofline's "traffic" scales it to the launch.
 TRAFFIC_PER_UNIT = {
-    # (kind, mode): (bytes per token-head, capture)
-    ("append", "uniform"): (144.9e6 / (64 * 8192), "profiles/append_ws_llama3-8b_S8192.md"),
+    # (kind, mode): (DRAM bytes per token-head of one launch, capture)
+    ("append", "uniform"): (70.27e6 / (64 * 4096), "profiles/append_ws_llama3-8b_S4096.md"),
 }
 
 
@@ -367,7 +367,7 @@ def gpu_arm(args, rank, world):
     tr = TRAFFIC_PER_UNIT.get((kind, layers[i].mode))
     if tr is not None:
         roof["traffic"] = tr[0] * layers[i].n_slots * S
-        roof["traffic_source"] = tr[1] + " (captured at S = 8192, scaled by tokens)"
+        roof["traffic_source"] = tr[1] + " (per token-head, times the launch's token-heads)"
     roof["frac"] = roof["achieved"] / roof["peak"]
     launches = sum(c["launches"] for c in counters)
     line = {
