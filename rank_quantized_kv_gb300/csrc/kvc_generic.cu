@@ -52,6 +52,12 @@ __device__ __forceinline__ float warp_maxf(float v) {
   return v;
 }
 
+// q / d for 0 <= q < 2^21 without an integer division: (q + 1/2) / d lies at
+// least 1/(2d) from an integer, and the two float roundings move it by less.
+__device__ __forceinline__ int small_div(int q, float inv_d) {
+  return __float2int_rd(((float)q + 0.5f) * inv_d);
+}
+
 // gamma_n = n u / (1 - n u)
 __device__ __forceinline__ float gamma_n(int n) {
   const float nu = n * kU;
@@ -377,12 +383,14 @@ append_generic_kernel(Params p, AppendArgs a, ZIn zin) {
   const bool vec8 = p.in_dtype != KVC_F32 && p.D % 8 == 0 &&
                     (reinterpret_cast<uintptr_t>(a.x) & 15) == 0 &&
                     ((a.sb | a.sh | a.st) & 7) == 0;
+  const float inv_din = 1.f / (float)d_in, inv_D = 1.f / (float)p.D;
   if (vec8) {
     for (int e = threadIdx.x * 8; e < kAppTT * d_in; e += blockDim.x * 8) {
-      const int t = e / d_in, i = e - t * d_in;
+      const int t = small_div(e, inv_din), i = e - t * d_in;
       float v[8];
       if (t < n) {
-        const int h = g * p.hpg + i / p.D, dd = i % p.D;
+        const int hh = small_div(i, inv_D);
+        const int h = g * p.hpg + hh, dd = i - hh * p.D;
         const uint4 raw = *reinterpret_cast<const uint4*>(
             static_cast<const uint16_t*>(a.x) + (int64_t)b * a.sb + (int64_t)h * a.sh +
             (t0 + t) * a.st + dd);
@@ -508,13 +516,15 @@ append_generic_kernel(Params p, AppendArgs a, ZIn zin) {
   const int16_t* order = p.order + (int64_t)beta * r;
   const int32_t* seg = p.seg + (int64_t)beta * kMaxSeg * 4;
   uint8_t* dst = p.store + p.pay_off[slot] + (a.t_base + t0) * P;
+  const float inv_P = 1.f / (float)P;
   for (int idx = threadIdx.x; idx < n * P; idx += blockDim.x) {
-    const int t = idx / P, j = idx - t * P;
+    const int t = small_div(idx, inv_P), j = idx - t * P;
     int s = 0;
     while (s + 1 < kMaxSeg && seg[(s + 1) * 4 + 3] > 0 && seg[(s + 1) * 4 + 0] <= j) ++s;
     const int start = seg[s * 4 + 0], w = seg[s * 4 + 1], m0 = seg[s * 4 + 2], cntm = seg[s * 4 + 3];
     const int q0 = 8 * (j - start);
-    int mlo = q0 / w, mhi = (q0 + 7) / w;
+    const float inv_w = 1.f / (float)w;  // w in {1, 2, 3, 4, 8}
+    int mlo = small_div(q0, inv_w), mhi = small_div(q0 + 7, inv_w);
     if (mhi > cntm - 1) mhi = cntm - 1;
     unsigned v = 0;
     for (int mm = mlo; mm <= mhi; ++mm) {
