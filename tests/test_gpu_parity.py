@@ -230,6 +230,38 @@ def test_group_tile_beyond_split_range(kvc, dtype):
     check_fetch(gl.fetch(), gl, rl)
 
 
+@pytest.mark.parametrize("D, dtype", [(80, "bf16"), (36, "f16")])
+def test_uniform_odd_shapes(kvc, D, dtype):
+    """Head sizes that are not multiples of 64 (the CUDA-core kernels; D = 36 is
+    not a multiple of 8 either, so x loads one value at a time), 3 heads, r = 20,
+    widths {0,1,2,3,4,8} with 3-bit codes straddling bytes, a ragged 77 tokens."""
+    B, H, S = 2, 3, 77
+    x = synth.kv_spectral(B, H, S, D, alpha=0.9, seed=7100, tensor=0, dtype=dtype)
+    x64 = x.double().numpy()
+    params = fit_uniform(x64, S, 20, [0, 1, 2, 3, 4, 8], 53)
+    gl, rl = _make(kvc, "uniform", B, H, D, params, dtype, S, "auto")
+    gl.append(x.to(_dev()))
+    assert gl.sync_status() == 0
+    rl.append(x64)
+    _all_slots_match(gl, rl, x64)
+    check_fetch(gl.fetch(), gl, rl)
+
+
+def test_group_odd_shapes(kvc):
+    """Group mode with 3 heads of D = 40 per group (D_in = 120, not a power of
+    two), r = 48 (a full and a half 32-component group), fp16 input, 150 tokens."""
+    B, H, S, D, hpg = 2, 6, 150, 40, 3
+    x = synth.group_spectral(B, H, S, D, hpg, alpha=1.0, seed=7200, tensor=0, dtype="f16")
+    x64 = x.double().numpy()
+    params = fit_group(x64, hpg, 48)
+    gl, rl = _make(kvc, "group", B, H, D, params, "f16", S, "auto")
+    gl.append(x.to(_dev()))
+    assert gl.sync_status() == 0
+    rl.append(x64)
+    _all_slots_match(gl, rl, x64)
+    check_fetch(gl.fetch(), gl, rl)
+
+
 # ------------------------------------------------------------------------- config 4
 
 @pytest.mark.parametrize("path", PATHS)
