@@ -1,0 +1,27 @@
+"""The reference arm of bench.py (the oracle timed on the host cores) keeps the
+JSON-line contract; it needs no GPU."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_one_contract_line():
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2",
+                          "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.strip()]
+    line = json.loads(lines[-1])
+    assert line["impl"] == "reference"
+    assert line["value"] > 0 and line["unit"] == "KV tokens/s"
+    assert line["higher_is_better"] is True and line["n_gpus"] == 1
+    assert line["steps"] == 2 and line["warmup"] == 3
+    assert line["config"]["workload"] == "llama3-8b"
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
+    assert cb["sample"]
