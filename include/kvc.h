@@ -22,8 +22,10 @@
  * device; every pointer named "host" is ordinary host memory read during the
  * call only.  The caller owns the store, the inputs and the outputs.  The
  * library owns one small block of device memory per layer (its frozen
- * parameters in kernel layouts, plus an error word and counters), allocated
- * in kvc_init_layer and freed in kvc_destroy; no other call allocates.
+ * parameters in kernel layouts, plus an error word and counters) and, in
+ * group mode with 16-bit inputs and D a multiple of 64, a scratch of at most
+ * 32 MiB for the tensor-core projection's fp32 latents; both are allocated in
+ * kvc_init_layer and freed in kvc_destroy; no other call allocates.
  *
  * Errors: every call returns a kvc_status.  Arguments are checked on the host
  * before any launch; on error nothing is launched and the layer is unchanged.
@@ -225,7 +227,7 @@ kvc_status kvc_sync_status(kvc_layer *layer, void *stream);
  * margin), [5] reserved (0).  With reset != 0 the counters are then zeroed. */
 kvc_status kvc_counters(kvc_layer *layer, int64_t out[6], int32_t reset, void *stream);
 
-/* Free the layer's parameter block (synchronises the device first).  NULL is a no-op. */
+/* Free the layer's device memory (synchronises the device first).  NULL is a no-op. */
 void kvc_destroy(kvc_layer *layer);
 
 /* Append without allocating any device memory.  The pages have no
