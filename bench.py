@@ -7,6 +7,7 @@ context in one call (project + quantise + bit-pack), fetch it back
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload llama3-8b|palu-group|turboquant|sweep] [--path auto|generic]
+    python bench.py --sweep [--steps K]     # the Llama-3-70B-like grid, one line per point
 
 Prints one JSON line (rank 0).  ``value`` is KV tokens per second over all
 ranks, a KV token being one (batch, kv-head, position): its key row and its
@@ -45,6 +46,13 @@ WORKLOADS = {
     # Llama-3-70B-like KV shape, uniform all-b allocation (one sweep point)
     "sweep": dict(B=8, H=8, D=128, S=8192, r=32, bits=4, mode="uniform", dtype="bf16"),
 }
+
+
+# Llama-3-70B-like KV throughput grid (H_kv = 8, D = 128): per rank r and
+# uniform width, per batch and context, the fetch of the whole context and the
+# append of one token; batch x context bounded by the fp16 output's bytes.
+SWEEP = dict(H=8, D=128, B=(1, 8, 32, 64), S=(1024, 8192, 32768, 131072), r=(32, 64),
+             bits=(2, 4), max_out_bytes=180e9, chunk=8192)
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -521,6 +529,109 @@ def reference_arm(args, rank, world):
 
 # ----------------------------------------------------------------------------- main
 
+def _timed_ms(fn, reps, flush):
+    """Mean CUDA-event time of fn() after two untimed calls, L2 flushed before each."""
+    import torch
+
+    fn()
+    fn()
+    total = 0.0
+    for _ in range(reps):
+        flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        e1.synchronize()
+        total += e0.elapsed_time(e1)
+    return total / reps
+
+
+def sweep_arm(args):
+    """The throughput grid: one JSON line per (r, bits, B, S), then a summary line.
+
+    The cache of each point is filled with S tokens (appended in chunks of the
+    same seeded rows); then the fetch of all S tokens and the append of one
+    more token (after dropping the last, so the length stays S) are timed.
+    """
+    import torch
+
+    import rank_quantized_kv_gb300 as kvc
+    import synth
+    from rank_quantized_kv_gb300 import calib
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    H, D, chunk = SWEEP["H"], SWEEP["D"], SWEEP["chunk"]
+    reps = max(3, min(args.steps, 20))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    f32 = torch.float32
+    x_fit = synth.kv_spectral(1, H, 4096, D, alpha=1.0, seed=5000, tensor=0, dtype="bf16",
+                              device=dev, work_dtype=f32)
+    src = synth.kv_spectral(1, H, chunk, D, alpha=1.0, seed=5001, tensor=0, dtype="bf16",
+                            device=dev, work_dtype=f32)
+    sampler = ClockSampler(dev.index).start()
+    points = []
+    for r in SWEEP["r"]:
+        for bits in SWEEP["bits"]:
+            params = calib.fit_uniform_shared(x_fit, r, bits)
+            for B in SWEEP["B"]:
+                xin = src.repeat(B, 1, 1, 1)
+                params["basis_of"] = np.array([h for _ in range(B) for h in range(H)],
+                                              dtype=np.int32)
+                for S in SWEEP["S"]:
+                    out_bytes = B * H * S * D * 2
+                    if out_bytes > SWEEP["max_out_bytes"]:
+                        continue
+                    L = kvc.KVCacheLayer("uniform", B, H, D, in_dtype="bf16", capacity=S,
+                                         device=dev, **params)
+                    for c0 in range(0, S, chunk):
+                        L.append(xin[:, :, :min(chunk, S - c0)])
+                    out = torch.empty(B, H, S, D, dtype=torch.float16, device=dev)
+                    fetch_ms = _timed_ms(lambda: L.fetch(out=out), reps, flush)
+                    x1 = xin[:, :, :1]
+
+                    def append_one():
+                        L.trim(1)
+                        L.append(x1)
+
+                    app_ms = _timed_ms(append_one, reps, flush)
+                    if L.sync_status() != 0:
+                        raise RuntimeError(f"device error at r={r} bits={bits} B={B} S={S}")
+                    P = L.slot_layout(0)["row_bytes"]
+                    fetch_bytes = B * H * S * (P + D * 2)
+                    fetch_flops = 2.0 * B * H * S * D * r
+                    t_roof = max(fetch_bytes / (peaks["hbm_gbs"] * 1e9),
+                                 fetch_flops / (peaks["bf16_tflops"] * 1e12))
+                    line = {"r": r, "bits": bits, "B": B, "S": S, "row_bytes": P,
+                            "fetch_us": fetch_ms * 1e3,
+                            "fetch_tokens_per_s": B * H * S / (fetch_ms * 1e-3),
+                            "fetch_gbs": fetch_bytes / (fetch_ms * 1e-3) / 1e9,
+                            "fetch_roofline_frac": t_roof / (fetch_ms * 1e-3),
+                            "append_one_us": app_ms * 1e3,
+                            "append_one_bytes": B * H * (D * 2 + P)}
+                    print(json.dumps(line), flush=True)
+                    points.append(line)
+                    del out
+                    L.close()
+                del xin
+    clocks = sampler.stop()
+    best = max(points, key=lambda q: q["fetch_roofline_frac"])
+    big = [q for q in points if q["B"] * q["S"] >= 8 * 131072]
+    print(json.dumps({
+        "sweep": "llama3-70b-like kv grid", "points": len(points), "unit": "KV tokens/s",
+        "peak_hbm_gbs": peaks["hbm_gbs"], "peak_source": peaks["source"],
+        "fetch_roofline_frac_best": best["fetch_roofline_frac"],
+        "best_point": {k: best[k] for k in ("r", "bits", "B", "S")},
+        "fetch_roofline_frac_min_at_B_S_ge_1M": min((q["fetch_roofline_frac"] for q in big),
+                                                     default=None),
+        "append_one_us_range": [min(q["append_one_us"] for q in points),
+                                max(q["append_one_us"] for q in points)],
+        "l2": "flushed before every timed call", "clocks": clocks}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -533,7 +644,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--seq", type=int, default=0,
                     help="tokens per (b, h) instead of the workload's S (profiling captures)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the Llama-3-70B-like throughput grid (one GPU), one line per point")
     args = ap.parse_args()
+    if args.sweep:
+        sweep_arm(args)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     rank = int(os.environ.get("RANK", 0))
