@@ -32,7 +32,9 @@
  * kvc_last_error() returns a message for the last failure on this thread.
  * Work is asynchronous on the given stream (a cudaStream_t passed as void*;
  * NULL is the legacy default stream); device-side conditions surface through
- * kvc_sync_status.
+ * kvc_sync_status.  Calls on one layer write its store (and scratch) and must
+ * be ordered: issue them on one stream, or order the streams with events.
+ * Different layers are independent.
  */
 #ifndef KVC_H
 #define KVC_H
