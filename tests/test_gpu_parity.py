@@ -230,6 +230,30 @@ def test_group_tile_beyond_split_range(kvc, dtype):
     check_fetch(gl.fetch(), gl, rl)
 
 
+@pytest.mark.parametrize("hpg, r, dtype", [(2, 20, "bf16"), (4, 128, "f16")])
+def test_group_tensor_core_ranks(kvc, hpg, r, dtype):
+    """The tensor-core group projection at other ranks: r = 20 (N padded to 32,
+    the padding columns never written) and r = 128 (32 components per epilogue
+    thread); D = 64, 200 tokens.  Codes against the oracle, and the same store as
+    the CUDA-core projection."""
+    B, S, D = 2, 200, 64
+    H = 2 * hpg
+    x = synth.group_spectral(B, H, S, D, hpg, alpha=1.0, seed=7300 + r, tensor=0, dtype=dtype)
+    x64 = x.double().numpy()
+    params = fit_group(x64, hpg, r)
+    ga, rl = _make(kvc, "group", B, H, D, params, dtype, S, "auto")
+    gg, _ = _make(kvc, "group", B, H, D, params, dtype, S, "generic")
+    xd = x.to(_dev())
+    ga.append(xd)
+    gg.append(xd)
+    assert ga.sync_status() == 0 and gg.sync_status() == 0
+    assert ga.counters()["launches"] == 2  # the projection, then the quantiser
+    rl.append(x64)
+    _all_slots_match(ga, rl, x64)
+    _same_store(ga, gg, rl.n_slots)
+    check_fetch(ga.fetch(), ga, rl)
+
+
 @pytest.mark.parametrize("D, dtype", [(80, "bf16"), (36, "f16")])
 def test_uniform_odd_shapes(kvc, D, dtype):
     """Head sizes that are not multiples of 64 (the CUDA-core kernels; D = 36 is
