@@ -295,6 +295,31 @@ def test_group_dominant_entry_and_zero_group():
     assert zhat[1, 4] == -float(scales[1, 1]) and zhat[0, 0] == 7 * float(scales[0, 0])
 
 
+def test_group_codes_symmetric_and_within_half_scale():
+    """Random latents at mixed widths: every code lies in [1, 2^b - 1] (symmetric
+    around 2^(b-1)); each group's largest |z| takes the extreme code; and the
+    decode is within half a scale of z plus the fp16 rounding of the scale,
+    |zhat - z| <= s/2 + qmax |fp16(s) - s| (q is taken with the unrounded s)."""
+    rng = np.random.default_rng(13)
+    bits = [4] * 12 + [2] * 36
+    z = rng.standard_normal((300, 48)) * np.linspace(3.0, 0.05, 48)
+    codes, scales = codec.quantize_group(z, bits, 16)
+    zhat = codec.dequantize_group(codes, scales, bits, 16)
+    for g, (w, comps) in enumerate(codec.group_ranges(bits, 16)):
+        qmax, off = (1 << (w - 1)) - 1, 1 << (w - 1)
+        c = codes[:, comps].astype(np.int64)
+        assert c.min() >= off - qmax and c.max() <= off + qmax
+        zg = z[:, comps]
+        s = np.maximum(np.abs(zg).max(axis=1) / qmax, 1e-8)
+        s16 = np.asarray(scales[:, g], dtype=np.float64)
+        assert np.array_equal(s16, s.astype(np.float16).astype(np.float64))
+        top = np.argmax(np.abs(zg), axis=1)
+        q_top = c[np.arange(len(top)), top] - off
+        assert np.array_equal(q_top, np.sign(zg[np.arange(len(top)), top]).astype(np.int64) * qmax)
+        bound = s / 2 + qmax * np.abs(s16 - s)
+        assert np.all(np.abs(zhat[:, comps] - zg) <= bound[:, None] * (1 + 1e-12))
+
+
 def test_group_ranges_cfg3_split():
     bits = fit.palu_bits(256, 4, 2, 0.25)
     g = codec.group_ranges(bits, 32)
