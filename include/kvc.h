@@ -135,10 +135,15 @@ typedef struct {
  *              P = sum over widths b of ceil(r_b * b / 8) (INT8: D).
  *  side        per-token fp16 side words: GROUP 2 * n_groups, CODEBOOK 2 (norm),
  *              INT8 2 (scale), UNIFORM 0 -- times length, summed over slots.
- *  fixed       frozen parameters a decoder needs, counted as fp32 values and
- *              1-byte widths: UNIFORM n_bases * (4 D_in r + 4 D_in + 8 r + r);
- *              GROUP n_bases * (4 D_in r + 4 D_in + r); CODEBOOK 4 D r + 4 * 2^cb_bits;
- *              INT8 0.
+ *  fixed       frozen parameters counted beside the codes, as the pages count
+ *              them: UNIFORM n_bases * (4 D_in r + 4 D_in + r) + 8 * (kept
+ *              components over all bases) -- basis and mean in fp32, a width
+ *              byte per component, an fp32 minimum and step per kept
+ *              component (kvtc_cache page, "Byte accounting" and
+ *              _TensorKVTC._requantize); GROUP n_bases * (4 D_in r + 4 D_in),
+ *              V_g and mu_g in fp32 (palu_cache page, projection_bytes);
+ *              CODEBOOK and INT8 0 (turboquant_cache page, memory_bytes counts
+ *              per-token bytes only: the rotation follows from the seed).
  *  fp16_equiv  B * H * length * D * 2, the uncompressed fp16 size. */
 typedef struct {
   int64_t payload;
@@ -252,7 +257,10 @@ void kvc_destroy(kvc_layer *layer);
  * whose work overlaps on the GPU (other streams, other threads) race and
  * corrupt each other's tables: order them on one stream.  The first call on
  * a device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.
+ * that device current; make that first call before any stream capture.  The
+ * address is that of the CUDA runtime's primary context of the device: call
+ * this entry point from the runtime's context, not from a context created
+ * with the driver API.
  *
  * Errors: KVC_EINVAL for a bad descriptor or pointers, or when the tables
  * exceed 8 MiB (e.g. many bases of a large D_in x r); KVC_ECAPACITY if

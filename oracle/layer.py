@@ -166,15 +166,26 @@ class OracleLayer:
         return n
 
     def param_bytes(self) -> int:
-        """Bytes of the frozen parameters a decoder needs (fp32 values, 1-byte widths)."""
-        if self.mode == "int8":
+        """Bytes of the frozen parameters the stored bytes carry beside the codes.
+
+        uniform: kvtc_cache page, "Byte accounting" (the stored size carries
+        the projection basis) and ``_TensorKVTC._requantize`` (a minimum and a
+        scale for each surviving component, with the per-component bit
+        allocation): per basis V and mean in fp32, one width byte per
+        component, and an fp32 minimum and step per kept component.
+        group: palu_cache page, ``projection_bytes`` (V_g and mu_g in fp32 per
+        head group); the widths are the cache's configuration, not stored.
+        codebook and int8: turboquant_cache page, ``memory_bytes`` counts only
+        per-token bytes (the rotation and codebook follow from the seed and
+        the width).
+        """
+        if self.mode in ("int8", "codebook"):
             return 0
-        if self.mode == "codebook":
-            return self.n_bases * 4 * self.d_in * self.r + 4 * self.codebook.shape[0]
-        per = 4 * self.d_in * self.r + 4 * self.d_in + self.r
-        if self.mode == "uniform":
-            per += 8 * self.r
-        return self.n_bases * per
+        per = 4 * self.d_in * self.r + 4 * self.d_in
+        if self.mode == "group":
+            return self.n_bases * per
+        kept = int(np.sum(self.bits > 0))
+        return self.n_bases * (per + self.r) + 8 * kept
 
     def nbytes(self) -> dict:
         """Stored-byte accounting (kvtc_cache page "Byte accounting"; turboquant_cache

@@ -210,10 +210,17 @@ kvc_status build_geo(const kvc_layer_desc* d, Geo& g) {
   g.store_total = align_up(cur, 256);
 
   const int64_t din = g.d_in, r = g.r, nb = g.nb;
+  // frozen parameters counted beside the codes: the basis and mean (fp32) of
+  // every basis; uniform mode adds a width byte per component and an fp32
+  // minimum and step per kept component; codebook and int8 modes count none
   switch (d->mode) {
-    case KVC_MODE_UNIFORM: g.fixed = nb * (4 * din * r + 4 * din + 8 * r + r); break;
-    case KVC_MODE_GROUP: g.fixed = nb * (4 * din * r + 4 * din + r); break;
-    case KVC_MODE_CODEBOOK: g.fixed = nb * 4 * din * r + 4 * (int64_t)g.cb_levels; break;
+    case KVC_MODE_UNIFORM: {
+      int64_t kept = 0;
+      for (int b = 0; b < g.nb; ++b) kept += g.n_kept[b];
+      g.fixed = nb * (4 * din * r + 4 * din + r) + 8 * kept;
+      break;
+    }
+    case KVC_MODE_GROUP: g.fixed = nb * (4 * din * r + 4 * din); break;
     default: g.fixed = 0;
   }
   return KVC_OK;

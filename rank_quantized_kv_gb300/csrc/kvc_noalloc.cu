@@ -27,7 +27,10 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_noalloc_scratch on device `dev` (the current device).
-// Looked up once per device; the name itself is only a host-side stand-in.
+// Looked up once per device, in the CUDA runtime's primary context of that
+// device (the context every runtime call uses); the name itself is only a
+// host-side stand-in.  Callers that bind a context of their own with the
+// driver API are not supported.
 kvc_status scratch_address(int dev, void** out) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (dev < 0 || dev >= kMaxDevices) return kvc::set_error(KVC_ECUDA, "device index out of range");
@@ -89,6 +92,11 @@ extern "C" kvc_status kvc_append_noalloc(const kvc_layer_desc* desc, int64_t len
   kvc::bind_params(p, desc, g, im, static_cast<uint8_t*>(scratch));
   const kvc::AppendArgs a{x, stride_b, stride_h, stride_t, T, length};
   int nk = 0;
+  // The error word and counters in the array cannot be read back through this
+  // entry point, so only kernels that report nothing through them may run
+  // here: the CUDA-core append kernels have no bounded waits and no device
+  // error paths.  A kernel that reports a time-out or a range error must not
+  // be launched from this call.
   e = desc->mode == KVC_MODE_INT8 ? kvc::launch_append_int8(p, a, s, &nk)
                                   : kvc::launch_append_generic(p, a, s, &nk);
   if (e != cudaSuccess) return kvc::set_error(KVC_ECUDA, "append launch failed");

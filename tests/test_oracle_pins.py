@@ -230,6 +230,75 @@ def test_rotation_orthogonal_and_qr_unique():
 
 # ---------------------------------------------------------------- quantisers
 
+def test_uniform_params_hand_worked():
+    """Frozen minimum and step of the fit rows (kvtc_cache page,
+    ``_TensorKVTC._requantize``: ``quantize_component`` gives each surviving
+    component a minimum and a scale).  Worked by hand: the minimum of each
+    column, and (max - min) / (2^b - 1) as the step; a constant column takes
+    the 1e-8 floor; a dropped column takes nothing."""
+    Z = np.array([[1.0, -2.0, 5.0, 7.0],
+                  [3.0, 0.0, 5.0, 1.0],
+                  [2.0, 4.0, 5.0, -3.0]])
+    lo, step = fit.uniform_params(Z, [2, 1, 3, 0])
+    assert lo.tolist() == [1.0, -2.0, 5.0, 0.0]
+    assert step[0] == 2.0 / 3.0           # (3 - 1) / (2^2 - 1)
+    assert step[1] == 6.0                 # (4 - (-2)) / (2^1 - 1)
+    assert step[2] == 1e-8                # constant column: the floor
+    assert step[3] == 0.0                 # 0 bits: not stored
+    lo8, step8 = fit.uniform_params(Z[:, :1], [8])
+    assert lo8[0] == 1.0 and step8[0] == 2.0 / 255.0
+
+
+@pytest.mark.parametrize("b", [1, 2, 3, 4, 8])
+def test_uniform_params_span_the_code_range(b):
+    """On its own fit rows the frozen quantiser uses every end of the code
+    range: the row holding a column's minimum gets code 0, the row holding its
+    maximum gets 2^b - 1, and every fit row decodes within half a step.  A step
+    of (max - min) / 2^b, or a minimum off by a row, fails one of these."""
+    rng = np.random.default_rng(40 + b)
+    Z = rng.standard_normal((300, 5)) * np.array([3.0, 1.0, 0.2, 7.0, 0.01]) + 2.0
+    bits = [b] * 5
+    lo, step = fit.uniform_params(Z, bits)
+    codes = codec.quantize_uniform(Z, lo, step, bits)
+    qmax = (1 << b) - 1
+    for k in range(5):
+        assert codes[np.argmin(Z[:, k]), k] == 0
+        assert codes[np.argmax(Z[:, k]), k] == qmax
+        assert codes[:, k].min() == 0 and codes[:, k].max() == qmax
+    zhat = codec.dequantize_uniform(codes, lo, step, bits)
+    assert np.all(np.abs(zhat - Z) <= step / 2 * (1 + 1e-12))
+
+
+def test_fixed_bytes_golden():
+    """The frozen-parameter bytes the stored size carries, against values worked
+    by hand from the pages' byte accounting (tests/golden/fixed_bytes.json)."""
+    rng = np.random.default_rng(5)
+    for case in _golden("fixed_bytes.json")["cases"]:
+        mode, d_in = case["mode"], case["d_in"]
+        if mode == "int8":
+            L = OracleLayer("int8", 1, 2, d_in)
+        elif mode == "codebook":
+            L = OracleLayer("codebook", 1, 2, d_in, V=np.eye(d_in),
+                            codebook=[-1.0, -0.3, 0.3, 1.0])
+        elif mode == "group":
+            hpg = case["hpg"]
+            nb, r = case["n_bases"], case["r"]
+            D = d_in // hpg
+            L = OracleLayer("group", 1, nb * hpg, D, heads_per_group=hpg,
+                            V=np.zeros((nb, d_in, r)), mean=np.zeros((nb, d_in)),
+                            bits=[[4] * (r // 4) + [2] * (r - r // 4)] * nb, group_size=32,
+                            basis_of=np.arange(nb))
+        else:
+            nb, r = case["n_bases"], case["r"]
+            bits = np.array(case["bits"])
+            L = OracleLayer("uniform", 1, nb, d_in, V=rng.standard_normal((nb, d_in, r)),
+                            mean=rng.standard_normal((nb, d_in)), bits=bits,
+                            qmin=np.zeros((nb, r)), qstep=np.ones((nb, r)),
+                            basis_of=np.arange(nb))
+        assert L.param_bytes() == case["fixed"], case["why"]
+        assert L.nbytes()["fixed"] == case["fixed"]
+
+
 def test_uniform_ties_round_half_to_even():
     lo, step = np.array([0.0]), np.array([0.25])         # exact binary fractions
     z = (np.arange(16) + 0.5)[:, None] * 0.25
