@@ -17,11 +17,14 @@ name the three documentation pages of the VeloxQuant-MLX caches):
   scale, scalar codebook), the per-token int8 value quantiser, LSB-first
   bit packing into byte-aligned segments and reconstruction;
 * ``layer`` -- a cache layer with the append / fetch / trim / nbytes
-  semantics of the C ABI, built from the two modules above.
+  semantics of the C ABI, built from the two modules above;
+* ``attend`` -- decode attention of one query per (batch, query head) over
+  the decoded keys and values of two layers (softmax of the scaled scores,
+  weighted sum of the values).
 
 Parity pins (tests/test_oracle_*.py) tie every function to something other
 than itself: the bit layouts the turboquant_cache page prints, closed forms,
 Max's 1960 table, brute force and invariants.  No function here is
 "parity unpinned".
 """
-from . import fit, codec, layer  # noqa: F401
+from . import fit, codec, layer, attend  # noqa: F401
