@@ -20,11 +20,13 @@ name the three documentation pages of the VeloxQuant-MLX caches):
   semantics of the C ABI, built from the two modules above;
 * ``attend`` -- decode attention of one query per (batch, query head) over
   the decoded keys and values of two layers (softmax of the scaled scores,
-  weighted sum of the values).
+  weighted sum of the values);
+* ``entropy`` -- order-0 Huffman byte accounting of the stored codes with
+  the fixed-width fallback and the entropy-coding gain.
 
 Parity pins (tests/test_oracle_*.py) tie every function to something other
 than itself: the bit layouts the turboquant_cache page prints, closed forms,
 Max's 1960 table, brute force and invariants.  No function here is
 "parity unpinned".
 """
-from . import fit, codec, layer, attend  # noqa: F401
+from . import fit, codec, layer, attend, entropy  # noqa: F401
