@@ -6,15 +6,21 @@ context in one call (project + quantise + bit-pack), fetch it back
 (unpack + dequantise + reconstruct to fp16 [B, H, S, D]).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload llama3-8b|palu-group|turboquant|sweep] [--path auto|generic]
+                    [--workload turboquant|llama3-8b|palu-group|kvtc-tiny|sweep]
+                    [--path auto|generic] [--no-configs]
     python bench.py --sweep [--steps K]     # the Llama-3-70B-like grid, one line per point
 
 Prints one JSON line (rank 0).  ``value`` is KV tokens per second over all
 ranks, a KV token being one (batch, kv-head, position): its key row and its
-value row are each appended and fetched once per step.  Inputs are resident
-in HBM; L2 is flushed (a 256 MiB write) between timed steps.  ``e2e`` times
-the same step through the public API with the inputs copied from pinned host
-memory and the fetched rows copied back, every step.
+value row are each appended and fetched once per step.  The default workload
+is the largest single-GPU configuration, the TurboQuant-style one (B 16,
+H_kv 8, S 16384: codebook keys, int8 values).  ``configs`` adds the other
+configurations measured in the same run (the tiny KVTC-style case as
+latencies, the Llama-3-8B-like and the PALU-style workloads, and the
+one-token append).  Inputs are resident in HBM; L2 is flushed (a 256 MiB
+write) between timed steps.  ``e2e`` times the same step through the public
+API with the inputs copied from pinned host memory and the fetched rows
+copied back, every step.
 """
 from __future__ import annotations
 
@@ -36,16 +42,21 @@ METRIC = "KV tokens/s for fetch (unpack+reconstruct) and append; % of HBM/tensor
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 
 WORKLOADS = {
-    # Llama-3-8B-like decode layer: KVTC-style uniform mode, local PCA per (b, h)
-    "llama3-8b": dict(B=8, H=8, D=128, S=4096, fit=512, r=32, choices=(0, 2, 4, 8),
-                      budget=128, mode="uniform", dtype="bf16"),
-    # PALU-style group-head mode: 4 groups of 8 heads (D_in = 1024 -> r = 256)
-    "palu-group": dict(B=4, H=32, D=128, S=8192, hpg=8, r=256, mode="group", dtype="bf16"),
     # TurboQuant-MSE-style: rotation + 3-bit codebook keys, int8 values
     "turboquant": dict(B=16, H=8, D=128, S=16384, mode="codebook", dtype="f16"),
+    # Llama-3-8B-like decode layer: KVTC-style uniform mode, local PCA per (b, h)
+    "llama3-8b": dict(B=8, H=8, D=128, S=4096, fit=512, r=32, choices=(0, 2, 4, 8),
+                      budget=128, mode="uniform", dtype="bf16", alpha=1.0, seed=2000,
+                      outliers=3),
+    # PALU-style group-head mode: 4 groups of 8 heads (D_in = 1024 -> r = 256)
+    "palu-group": dict(B=4, H=32, D=128, S=8192, hpg=8, r=256, mode="group", dtype="bf16"),
+    # tiny KVTC-style correctness case: fp32, prefill 64 then 16 single-token appends
+    "kvtc-tiny": dict(B=1, H=2, D=64, S=80, fit=64, r=16, choices=(0, 1, 2, 4, 8), budget=48,
+                      mode="uniform", dtype="f32", alpha=0.8, seed=1000, outliers=0),
     # Llama-3-70B-like KV shape, uniform all-b allocation (one sweep point)
     "sweep": dict(B=8, H=8, D=128, S=8192, r=32, bits=4, mode="uniform", dtype="bf16"),
 }
+DEFAULT_WORKLOAD = "turboquant"
 
 
 # Llama-3-70B-like KV throughput grid (H_kv = 8, D = 128): per rank r and
@@ -113,12 +124,11 @@ class ClockSampler:
 
 
 # DRAM traffic (ncu dram__bytes_read.sum + dram__bytes_write.sum) per
-# token-head of a kernel, from the capture named beside it, where the kernel
-# has not changed since.  The roofline's "traffic" scales it to the launch.
-TRAFFIC_PER_UNIT = {
-    # (kind, mode): (DRAM bytes per token-head of one launch, capture)
-    ("append", "uniform"): (70.27e6 / (64 * 4096), "profiles/append_ws_llama3-8b_S4096.md"),
-}
+# token-head of a kernel, from one capture of the kernel as it stands (the
+# capture and its command are recorded with the ncu summaries); an entry is
+# removed whenever its kernel changes.  The roofline's "traffic" scales it to
+# the launch.
+TRAFFIC_PER_UNIT = {}
 
 
 # ----------------------------------------------------------------------------- multi-rank
@@ -172,16 +182,18 @@ def build_layers(wl, dev):
                                       device=dev, work_dtype=f32)
                 L = kvc.KVCacheLayer("int8", B, H, D, in_dtype="f16", capacity=S, device=dev)
         else:
-            x = synth.kv_spectral(B, H, S, D, alpha=1.0, seed=2000 if "fit" in wl else 5000,
-                                  tensor=tensor, n_outliers=3 if "fit" in wl else 0,
-                                  dtype="bf16", device=dev, work_dtype=f32)
-            if "fit" in wl:
+            fitted = "fit" in wl
+            x = synth.kv_spectral(B, H, S, D, alpha=wl.get("alpha", 1.0),
+                                  seed=wl.get("seed", 5000), tensor=tensor,
+                                  n_outliers=wl.get("outliers", 0), dtype=wl["dtype"], device=dev,
+                                  work_dtype=f32)
+            if fitted:
                 params = calib.fit_uniform(x[:, :, :wl["fit"]], wl["r"], wl["choices"],
                                            wl["budget"])
             else:
                 params = calib.fit_uniform_shared(x[:, :, :min(S, 4096)], wl["r"], wl["bits"])
-            L = kvc.KVCacheLayer("uniform", B, H, D, in_dtype="bf16", capacity=S, device=dev,
-                                 **params)
+            L = kvc.KVCacheLayer("uniform", B, H, D, in_dtype=wl["dtype"], capacity=S,
+                                 device=dev, **params)
         layers.append(L)
         inputs.append(x.contiguous())
     return layers, inputs
@@ -207,6 +219,192 @@ def algorithmic(wl, layers):
     return out
 
 
+def _event_ms(fn, reps, flush):
+    """Mean CUDA-event time (ms) of fn() on the current stream, L2 flushed before each."""
+    import torch
+
+    total = 0.0
+    for _ in range(reps):
+        flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        e1.synchronize()
+        total += e0.elapsed_time(e1)
+    return total / reps
+
+
+def launch_floor_us(flush, reps=50):
+    """Event-timed launch of a trivial kernel: the floor under any one-launch latency."""
+    tiny = flush[:16]
+    tiny.zero_()
+    return _event_ms(lambda: tiny.zero_(), reps, flush) * 1e3
+
+
+def tensor_name(i, L):
+    return ("keys" if i == 0 else "values") + f"/{L.mode}"
+
+
+def time_steps(layers, inputs, outs, steps, flush):
+    """K timed steps (trim, append S, fetch S per tensor): per-step ms and
+    per-tensor summed append / fetch ms, all from CUDA events."""
+    import torch
+
+    nten = len(layers)
+    step_ms, app_ms, fet_ms = [], np.zeros(nten), np.zeros(nten)
+    for _ in range(steps):
+        flush.fill_(1)                       # L2 flush, outside the timed events
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nten)]
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for i, (L, x, o) in enumerate(zip(layers, inputs, outs)):
+            L.trim(len(L))
+            ev[i][0].record()
+            L.append(x)
+            ev[i][1].record()
+            L.fetch(out=o)
+            ev[i][2].record()
+        s1.record()
+        s1.synchronize()
+        step_ms.append(s0.elapsed_time(s1))
+        for i in range(nten):
+            app_ms[i] += ev[i][0].elapsed_time(ev[i][1])
+            fet_ms[i] += ev[i][1].elapsed_time(ev[i][2])
+    return step_ms, app_ms, fet_ms
+
+
+def op_table(wl, layers, app_ms, fet_ms, steps, peaks):
+    """Per tensor: append / fetch time, tokens/s and roofline fraction."""
+    B, H, S = wl["B"], wl["H"], wl["S"]
+    hbm = peaks["hbm_gbs"] * 1e9
+    tflops = peaks["bf16_tflops"] * 1e12
+    alg = algorithmic(wl, layers)
+    ops = {}
+    for i, L in enumerate(layers):
+        fb, ab, fl = alg[i]
+        ta, tf = app_ms[i] / steps / 1e3, fet_ms[i] / steps / 1e3
+        ops[tensor_name(i, L)] = {
+            "append_us": ta * 1e6, "fetch_us": tf * 1e6,
+            "append_tokens_per_s": B * H * S / ta, "fetch_tokens_per_s": B * H * S / tf,
+            "append_roofline_frac": max(ab / hbm, fl / tflops) / ta,
+            "fetch_roofline_frac": max(fb / hbm, fl / tflops) / tf,
+            "append_bytes": ab, "fetch_bytes": fb, "flops": fl,
+        }
+    return ops
+
+
+def attend_op(layers, flush, peaks, reps, rep=4):
+    """Decode attention on the stored codes (kvc_attend): one query per
+    (batch, query head), rep query heads per key/value head, over every
+    stored token.  Bytes: the key and value rows and side words, read once."""
+    import torch
+
+    import rank_quantized_kv_gb300 as kvc
+
+    K, V = layers
+    dev = K.device
+    q = torch.randn(K.B, K.H * rep, K.D, device=dev,
+                    generator=torch.Generator(device=dev).manual_seed(11))
+    out = torch.empty(K.B, K.H * rep, K.D, dtype=torch.float16, device=dev)
+    ws = torch.empty(kvc.attend_workspace_bytes(K, V, K.H * rep), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        kvc.attend(K, V, q, out=out, workspace=ws)
+    ms = _event_ms(lambda: kvc.attend(K, V, q, out=out, workspace=ws), reps, flush)
+    S = len(K)
+    nbytes = 0
+    for L in layers:
+        lay = L.slot_layout(0)
+        nbytes += L.n_slots * S * (lay["row_bytes"] + lay["side_bytes"])
+    t = ms / 1e3
+    return {"us": ms * 1e3, "query_heads_per_kv_head": rep, "tokens": S,
+            "kv_tokens_per_s": K.B * K.H * S / t, "bytes": nbytes,
+            "roofline_frac": nbytes / (peaks["hbm_gbs"] * 1e9) / t,
+            "what": "softmax(scale q . k_hat) v_hat from the codes, keys and values never "
+                    "reconstructed"}
+
+
+def extra_configs(dev, flush, peaks, steps):
+    """The configurations beside the headline, measured in the same run: the
+    tiny KVTC-style case (latencies: a 64-token prefill append, single-token
+    appends, the fetch of all 80 tokens), the Llama-3-8B-like layer (bulk
+    append and fetch, and the one-token decode append at S = 4096) and the
+    PALU-style group workload (bulk append and fetch)."""
+    import torch
+
+    res = {"launch_floor_us": launch_floor_us(flush)}
+    # tiny KVTC-style case, as latencies
+    wl = WORKLOADS["kvtc-tiny"]
+    layers, inputs = build_layers(wl, dev)
+    tiny = {}
+    for i, (L, x) in enumerate(zip(layers, inputs)):
+        pre = x[:, :, :wl["fit"]].contiguous()
+        one = [x[:, :, t:t + 1].contiguous() for t in range(wl["fit"], wl["S"])]
+        out = torch.empty(wl["B"], wl["H"], wl["S"], wl["D"], dtype=torch.float16, device=dev)
+
+        def prefill():
+            L.trim(len(L))
+            L.append(pre)
+
+        def decode_all():
+            L.trim(len(L) - wl["fit"])
+            for xt in one:
+                L.append(xt)
+
+        for _ in range(3):
+            prefill()
+            decode_all()
+            L.fetch(out=out)
+        reps = max(5, min(steps, 50))
+        t_pre = _event_ms(prefill, reps, flush)
+        decode_all()
+        t_dec = _event_ms(decode_all, reps, flush) / len(one)
+        t_fet = _event_ms(lambda: L.fetch(out=out), reps, flush)
+        if L.sync_status() != 0:
+            raise RuntimeError("device error in the tiny case")
+        tiny[tensor_name(i, L)] = {"prefill_append_64_us": t_pre * 1e3,
+                                   "single_token_append_us": t_dec * 1e3,
+                                   "fetch_80_us": t_fet * 1e3}
+    res["kvtc-tiny"] = {"shape": "B 1, H 2, D 64, fp32, r 16, {0,1,2,4,8}, 48 bits",
+                        "latency": tiny,
+                        "note": "160 token-heads: launch-latency bound; compare with "
+                                "launch_floor_us, not with a roofline"}
+    del layers, inputs
+    # Llama-3-8B-like layer and the PALU-style group workload, bulk
+    for name in ("llama3-8b", "palu-group"):
+        wl = WORKLOADS[name]
+        layers, inputs = build_layers(wl, dev)
+        outs = [torch.empty(wl["B"], wl["H"], wl["S"], wl["D"], dtype=torch.float16, device=dev)
+                for _ in layers]
+        time_steps(layers, inputs, outs, 3, flush)
+        n = max(3, min(steps, 20))
+        _, app_ms, fet_ms = time_steps(layers, inputs, outs, n, flush)
+        entry = {"ops": op_table(wl, layers, app_ms, fet_ms, n, peaks), "steps": n}
+        if name == "llama3-8b":
+            one = []
+            for L, x in zip(layers, inputs):
+                x1 = x[:, :, :1]
+
+                def append_one():
+                    L.trim(1)
+                    L.append(x1)
+
+                one.append(_event_ms(append_one, n, flush) * 1e3)
+            entry["one_token_append_us"] = {tensor_name(i, L): one[i]
+                                            for i, L in enumerate(layers)}
+            entry["one_token_note"] = ("one token appended to each of the 64 (b, h) at S = 4096: "
+                                       "launch-latency bound, compare with launch_floor_us")
+        for L in layers:
+            if L.sync_status() != 0:
+                raise RuntimeError(f"device error in {name}")
+        res[name] = entry
+        del layers, inputs, outs
+        torch.cuda.empty_cache()
+    return res
+
+
 def gpu_arm(args, rank, world):
     import torch
 
@@ -223,20 +421,7 @@ def gpu_arm(args, rank, world):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     alg = algorithmic(wl, layers)
 
-    def step(ev=None):
-        for i, (L, x, o) in enumerate(zip(layers, inputs, outs)):
-            L.trim(len(L))
-            if ev is not None:
-                ev[i][0].record()
-            L.append(x)
-            if ev is not None:
-                ev[i][1].record()
-            L.fetch(out=o)
-            if ev is not None:
-                ev[i][2].record()
-
-    for _ in range(args.warmup):
-        step()
+    time_steps(layers, inputs, outs, args.warmup, flush)
     torch.cuda.synchronize()
     for L in layers:
         if L.sync_status() != 0:
@@ -248,25 +433,11 @@ def gpu_arm(args, rank, world):
         import torch.distributed as dist
     sampler = ClockSampler(dev.index).start() if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
-    nten = len(layers)
-    step_ms, app_ms, fet_ms = [], np.zeros(nten), np.zeros(nten)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    for _ in range(args.steps):
-        flush.fill_(1)                       # L2 flush, outside the timed events
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nten)]
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record()
-        step(ev)
-        s1.record()
-        s1.synchronize()
-        step_ms.append(s0.elapsed_time(s1))
-        for i in range(nten):
-            app_ms[i] += ev[i][0].elapsed_time(ev[i][1])
-            fet_ms[i] += ev[i][1].elapsed_time(ev[i][2])
+    step_ms, app_ms, fet_ms = time_steps(layers, inputs, outs, args.steps, flush)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -335,24 +506,14 @@ def gpu_arm(args, rank, world):
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms /= e2e_steps
     e2e_ms, = max_over_ranks([e2e_ms], dist, dev)
+    del hosts_in, hosts_out
     if rank != 0:
         return None
 
     peaks = load_peaks()
     hbm = peaks["hbm_gbs"] * 1e9
     tflops = peaks["bf16_tflops"] * 1e12
-    ops = {}
-    for i, L in enumerate(layers):
-        name = ("keys" if i == 0 else "values") + f"/{L.mode}"
-        fb, ab, fl = alg[i]
-        ta, tf = app_ms[i] / args.steps / 1e3, fet_ms[i] / args.steps / 1e3
-        ops[name] = {
-            "append_us": ta * 1e6, "fetch_us": tf * 1e6,
-            "append_tokens_per_s": B * H * S / ta, "fetch_tokens_per_s": B * H * S / tf,
-            "append_roofline_frac": max(ab / hbm, fl / tflops) / ta,
-            "fetch_roofline_frac": max(fb / hbm, fl / tflops) / tf,
-            "append_bytes": ab, "fetch_bytes": fb, "flops": fl,
-        }
+    ops = op_table(wl, layers, app_ms, fet_ms, args.steps, peaks)
     # dominant kernel: the op with the largest time per launch
     cand = []
     for i, L in enumerate(layers):
@@ -371,11 +532,11 @@ def gpu_arm(args, rank, world):
         "peak_source": peaks["source"],
         "traffic": None,
         "algorithmic_bytes_per_launch": nbytes,
+        "launch_us": t * 1e6,
     }
     tr = TRAFFIC_PER_UNIT.get((kind, layers[i].mode))
-    if tr is not None:
-        roof["traffic"] = tr[0] * layers[i].n_slots * S
-        roof["traffic_source"] = tr[1] + " (per token-head, times the launch's token-heads)"
+    if tr is not None and not args.seq:
+        roof["traffic"] = tr * layers[i].n_slots * S
     roof["frac"] = roof["achieved"] / roof["peak"]
     launches = sum(c["launches"] for c in counters)
     line = {
@@ -388,7 +549,10 @@ def gpu_arm(args, rank, world):
                    "parallelism": f"replicas{world}", "l2": "flushed between timed steps",
                    "step": "per tensor (K, V): trim all, append S tokens, fetch S tokens"},
         "e2e": {"value": job_throughput(world, units, e2e_ms), "unit": "KV tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "how": ("public API calls on one stream; the step's inputs uploaded from pinned "
+                        "host memory and its fetched rows downloaded by torch copies on two "
+                        "side streams, ordered by events and pipelined across steps")},
         "gpu_launches": launches,
         "roofline": roof,
         "ops": ops,
@@ -396,8 +560,14 @@ def gpu_arm(args, rank, world):
         "clocks": clocks,
         "wall_s_timed": wall,
     }
+    if len(layers) == 2 and layers[0].mode in ("uniform", "codebook") and \
+            layers[1].mode in ("int8", "uniform"):
+        line["attend"] = attend_op(layers, flush, peaks, max(3, min(args.steps, 50)))
+    if not args.no_configs and world == 1 and not args.seq:
+        line["configs"] = extra_configs(dev, flush, peaks, args.steps)
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds,
+                                            workload=None if args.seq else args.workload)
     return line
 
 
@@ -439,8 +609,9 @@ def _oracle_sample(wl, n_slots_sample):
             x64 = x.double().numpy()
         else:
             fit_len = wl.get("fit", min(S, 4096))
-            x = synth.kv_spectral(1, n_slots_sample, S, D, alpha=1.0, seed=2000, tensor=tensor,
-                                  n_outliers=3 if "fit" in wl else 0, dtype="bf16")
+            x = synth.kv_spectral(1, n_slots_sample, S, D, alpha=wl.get("alpha", 1.0),
+                                  seed=wl.get("seed", 5000), tensor=tensor,
+                                  n_outliers=wl.get("outliers", 0), dtype=wl["dtype"])
             x64 = x.double().numpy()
             Vs, ms, bs, los, sts = [], [], [], [], []
             for h in range(n_slots_sample):
@@ -481,8 +652,9 @@ def _oracle_once(jobs):
     return x0.shape[0] * x0.shape[1] * x0.shape[2]
 
 
-def cpu_baseline(wl, budget_s=12.0):
-    """The float64 oracle, as it stands, on a bounded sample of the workload."""
+def _oracle_rate(wl, budget_s):
+    """KV tokens/s of the oracle, as it stands, on a bounded sample of the
+    workload: (rate, seconds, KV heads sampled)."""
     n_sample = 2 if wl["mode"] != "group" else wl["hpg"]
     jobs = _oracle_sample(wl, n_sample)
     t0 = time.perf_counter()
@@ -492,10 +664,36 @@ def cpu_baseline(wl, budget_s=12.0):
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
+    return done / dt, dt, n_sample
+
+
+_ONE_THREAD_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+                   "VECLIB_MAXIMUM_THREADS": "1", "NUMEXPR_NUM_THREADS": "1",
+                   "CUDA_VISIBLE_DEVICES": ""}
+
+
+def _oracle_single_thread(workload, budget_s):
+    """The same oracle timing in a child process whose BLAS and torch use one thread."""
+    env = dict(os.environ, **_ONE_THREAD_ENV)
+    res = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-single-thread",
+                          workload, "--cpu-seconds", str(budget_s)], env=env, capture_output=True,
+                         text=True, timeout=600)
+    if res.returncode:
+        return {"error": res.stderr.strip().splitlines()[-1:] or ["failed"]}
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(wl, budget_s=12.0, workload=None):
+    """The float64 oracle, as it stands, on a bounded sample of the workload:
+    on all host cores (BLAS threads) and on one thread."""
+    rate, dt, n_sample = _oracle_rate(wl, budget_s / 2)
     sample = (f"{n_sample} of the workload's KV heads x {wl['S']} tokens (K and V), "
               f"appended and fetched repeatedly for {dt:.1f} s")
-    return {"value": done / dt, "unit": "KV tokens/s", "cores": _cores_used(), "kind": "oracle",
-            "sample": sample}
+    out = {"value": rate, "unit": "KV tokens/s", "cores": _cores_used(), "kind": "oracle",
+           "sample": sample, "host_cpus": os.cpu_count()}
+    if workload is not None:
+        out["single_thread"] = _oracle_single_thread(workload, budget_s / 2)
+    return out
 
 
 def reference_arm(args, rank, world):
@@ -638,7 +836,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(WORKLOADS), default="llama3-8b")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--path", choices=["auto", "generic"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -646,7 +844,22 @@ def main():
                     help="tokens per (b, h) instead of the workload's S (profiling captures)")
     ap.add_argument("--sweep", action="store_true",
                     help="the Llama-3-70B-like throughput grid (one GPU), one line per point")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configurations measured beside the headline")
+    ap.add_argument("--oracle-single-thread", metavar="WORKLOAD", default=None,
+                    help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_single_thread:
+        # child of cpu_baseline: the oracle with one BLAS / torch thread, no GPU
+        import torch
+
+        torch.set_num_threads(1)
+        rate, dt, n = _oracle_rate(WORKLOADS[args.oracle_single_thread], args.cpu_seconds)
+        print(json.dumps({"value": rate, "unit": "KV tokens/s", "cores": 1,
+                          "blas_threads_reported": _cores_used(), "seconds": dt,
+                          "sample": f"{n} KV heads x {WORKLOADS[args.oracle_single_thread]['S']} "
+                                    f"tokens (K and V), repeatedly for {dt:.1f} s"}))
+        return
     if args.sweep:
         sweep_arm(args)
         return

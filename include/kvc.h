@@ -220,6 +220,87 @@ kvc_status kvc_get_slot_layout(const kvc_layer *layer, int32_t slot, kvc_slot_la
 /* Choose the kernels used by later calls (KVC_PATH_*).  Host-only. */
 kvc_status kvc_set_path(kvc_layer *layer, int32_t path);
 
+/* Decode attention on the stored codes (turboquant_cache page,
+ * TurboQuantKVCache.attend: the query's score against every stored key,
+ * softmax of the scaled scores, weighted sum of the decoded values;
+ * palu_cache page, module docstring: the latents are reconstructed only at
+ * attend time).  For every batch entry b and query head hq, over all
+ * `length` stored tokens t of key/value head h = hq / (Hq / H):
+ *   out[b, hq] = sum_t softmax_t(scale * q[b, hq] . k_hat[b, h, t]) v_hat[b, h, t],
+ * with k_hat and v_hat the rows kvc_fetch would reconstruct, but computed
+ * from the codes without reconstructing them: uniform keys through the
+ * per-query weights (V^T q)_k step_k, codebook keys through (R^T q)_k times
+ * the centroids and the norm; int8 values as q8 * scale, uniform values as
+ * the weighted mean latent projected once.
+ *
+ *  keys       a KVC_MODE_UNIFORM or KVC_MODE_CODEBOOK layer, heads_per_group 1.
+ *  values     a KVC_MODE_INT8 or KVC_MODE_UNIFORM layer with the keys' B, H, D,
+ *             device and length; D is 64, 128 or 256.
+ *  q          device fp32 [B, Hq, D]; Hq / H is 1, 2, 4 or 8.
+ *  scale      the score scale; 0 means 1 / sqrt(D), the pages' scale.
+ *  out        device [B, Hq, D] in the value layer's out_dtype.
+ *  workspace  device, 256-byte aligned, at least kvc_attend_workspace_bytes()
+ *             bytes; caller-owned scratch, overwritten by the call.
+ * With length 0 the output is zero.  Asynchronous on `stream`.  Returns
+ * KVC_EINVAL for unsupported modes or shapes, mismatched layers, host
+ * pointers or a short workspace; nothing is launched then. */
+kvc_status kvc_attend(const kvc_layer *keys, const kvc_layer *values, const float *q, int32_t Hq,
+                      float scale, void *out, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+/* Workspace bytes kvc_attend needs for these layers at their current length
+ * and Hq query heads (host-only). */
+kvc_status kvc_attend_workspace_bytes(const kvc_layer *keys, const kvc_layer *values, int32_t Hq,
+                                      size_t *out);
+
+/* Order-0 Huffman accounting of the stored codes (kvtc_cache page, module
+ * docstring "Byte accounting" and KVTCKVCache.entropy_coding_gain).  Not on
+ * the hot path: the store stays fixed width; these calls report what an
+ * entropy-coded store would take.  Each kept component of a slot gets its
+ * own Huffman code over the values it takes across the slot's tokens; its
+ * table costs one byte per symbol of its 2^b alphabet; a slot stores
+ * min(ceil(payload bits / 8) + tables, fixed-width bytes).
+ *  pre_entropy     fixed-width payload bytes (sum over slots of length * P)
+ *  stored_payload  payload after entropy coding and the fixed-width fallback
+ *  params          the layer's frozen parameter bytes (kvc_bytes.fixed)
+ *  gain            pre_entropy / (stored_payload + params); below 1 when the
+ *                  parameters dominate, as the page notes. */
+typedef struct {
+  int64_t pre_entropy;
+  int64_t stored_payload;
+  int64_t params;
+  double gain;
+} kvc_entropy;
+
+/* Bytes of the code histogram of a coded layer: n_slots * NC * 256 uint32
+ * counts, NC the basis' largest number of chunk-aligned packed positions
+ * (every width segment starts on a multiple of 8).  Host-only.  KVC_EINVAL
+ * for an int8 layer. */
+kvc_status kvc_code_histogram_bytes(const kvc_layer *layer, size_t *out);
+
+/* Count the stored codes: counts (device, caller-owned, 4-byte aligned, at
+ * least kvc_code_histogram_bytes) receives, for slot s and packed position j
+ * (segments in descending width, components ascending, each segment starting
+ * on a multiple of 8), how many of the slot's tokens hold code v at
+ * [(s * NC + j) * 256 + v].  Asynchronous on `stream` (the counts are zeroed
+ * first on the same stream). */
+kvc_status kvc_code_histogram(kvc_layer *layer, uint32_t *counts, size_t counts_bytes,
+                              void *stream);
+
+/* The Huffman byte accounting from a histogram copied to host memory
+ * (counts: host, as kvc_code_histogram wrote it for the current length). */
+kvc_status kvc_entropy_bytes(const kvc_layer *layer, const uint32_t *counts, kvc_entropy *out);
+
+/* Limit, in nanoseconds, of the waits inside the warp-specialised tensor-core
+ * append kernel (one role waiting for another: a tile loaded, an accumulator
+ * written or released).  A kernel whose wait runs out stops its work, waits
+ * for its copies and tensor-core work already in flight (up to 2 s), frees its
+ * tensor memory and returns; kvc_sync_status then reports KVC_ETIMEOUT and the
+ * rows of that call are undefined.  ns == 0 restores the default of 2 s; a
+ * limit shorter than a kernel's normal waits makes every call time out.
+ * Host-only.  KVC_EINVAL if ns < 0. */
+kvc_status kvc_set_wait_limit(kvc_layer *layer, int64_t ns);
+
 /* Synchronise `stream`, then read and clear the layer's device error word:
  * KVC_OK, KVC_ETIMEOUT (a bounded wait gave up) or KVC_EDEVICE (data the kernel
  * cannot encode exactly).  KVC_ECUDA if the synchronisation itself failed. */

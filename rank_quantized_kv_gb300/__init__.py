@@ -20,7 +20,7 @@ from ctypes import POINTER, byref, c_float, c_int32, c_int64, c_size_t, c_uint8,
 import numpy as np
 
 __all__ = ["KVCacheLayer", "load_library", "library_path", "KvcError", "MODES", "DTYPES",
-           "EXPORTED_SYMBOLS", "store_bytes"]
+           "EXPORTED_SYMBOLS", "store_bytes", "attend", "attend_workspace_bytes"]
 
 MODES = {"uniform": 0, "group": 1, "codebook": 2, "int8": 3}
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
@@ -33,7 +33,8 @@ EXPORTED_SYMBOLS = (
     "kvc_abi_version", "kvc_last_error", "kvc_store_bytes", "kvc_init_layer", "kvc_append",
     "kvc_append_strided", "kvc_fetch", "kvc_trim", "kvc_length", "kvc_nbytes",
     "kvc_get_slot_layout", "kvc_set_path", "kvc_sync_status", "kvc_counters", "kvc_destroy",
-    "kvc_append_noalloc",
+    "kvc_append_noalloc", "kvc_set_wait_limit", "kvc_attend", "kvc_attend_workspace_bytes",
+    "kvc_code_histogram_bytes", "kvc_code_histogram", "kvc_entropy_bytes",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -47,6 +48,11 @@ class KvcError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS.get(status, status)}: {message}")
         self.status = status
+
+
+class _Entropy(ctypes.Structure):
+    _fields_ = [("pre_entropy", c_int64), ("stored_payload", c_int64), ("params", c_int64),
+                ("gain", ctypes.c_double)]
 
 
 class _Desc(ctypes.Structure):
@@ -104,6 +110,12 @@ def load_library():
             "kvc_nbytes": (c_int32, [P, POINTER(_Bytes)]),
             "kvc_get_slot_layout": (c_int32, [P, c_int32, POINTER(_SlotLayout)]),
             "kvc_set_path": (c_int32, [P, c_int32]),
+            "kvc_set_wait_limit": (c_int32, [P, c_int64]),
+            "kvc_attend": (c_int32, [P, P, P, c_int32, ctypes.c_float, P, P, c_size_t, P]),
+            "kvc_attend_workspace_bytes": (c_int32, [P, P, c_int32, POINTER(c_size_t)]),
+            "kvc_code_histogram_bytes": (c_int32, [P, POINTER(c_size_t)]),
+            "kvc_code_histogram": (c_int32, [P, P, c_size_t, P]),
+            "kvc_entropy_bytes": (c_int32, [P, P, POINTER(_Entropy)]),
             "kvc_sync_status": (c_int32, [P, P]),
             "kvc_counters": (c_int32, [P, POINTER(c_int64), c_int32, P]),
             "kvc_destroy": (None, [P]),
@@ -322,6 +334,32 @@ class KVCacheLayer:
     def set_path(self, path: str):
         _check(self._lib.kvc_set_path(self._h, PATHS[path]))
 
+    def code_histogram(self, stream=None):
+        """Per (slot, packed position, code value) counts of the stored codes,
+        a device uint32 tensor [n_slots, NC, 256] (kvc_code_histogram)."""
+        import torch
+
+        n = c_size_t()
+        _check(self._lib.kvc_code_histogram_bytes(self._h, byref(n)))
+        counts = torch.empty(int(n.value) // 4, dtype=torch.int32, device=self.device)
+        _check(self._lib.kvc_code_histogram(self._h, c_void_p(counts.data_ptr()), n.value,
+                                            _stream_ptr(stream, self.device)))
+        return counts.view(self.n_slots, -1, 256)
+
+    def entropy_bytes(self, stream=None) -> dict:
+        """Order-0 Huffman accounting of the stored codes (kvc_entropy_bytes)."""
+        import torch
+
+        counts = self.code_histogram(stream).cpu().contiguous()
+        e = _Entropy()
+        _check(self._lib.kvc_entropy_bytes(self._h, c_void_p(counts.data_ptr()), byref(e)))
+        return {"pre_entropy": e.pre_entropy, "stored_payload": e.stored_payload,
+                "params": e.params, "gain": e.gain}
+
+    def set_wait_limit(self, ns: int):
+        """Limit (ns) of the append kernel's waits; 0 restores the default (2 s)."""
+        _check(self._lib.kvc_set_wait_limit(self._h, int(ns)))
+
     def sync_status(self, stream=None) -> int:
         """Synchronise and return the device status (0 = ok); clears it."""
         return int(self._lib.kvc_sync_status(self._h, _stream_ptr(stream, self.device)))
@@ -343,3 +381,35 @@ class KVCacheLayer:
             self.close()
         except Exception:
             pass
+
+
+def attend_workspace_bytes(keys: "KVCacheLayer", values: "KVCacheLayer", Hq: int) -> int:
+    """Device workspace bytes kvc_attend needs at the layers' current length."""
+    n = c_size_t()
+    _check(load_library().kvc_attend_workspace_bytes(keys._h, values._h, int(Hq), byref(n)))
+    return int(n.value)
+
+
+def attend(keys: "KVCacheLayer", values: "KVCacheLayer", q, scale: float = 0.0, out=None,
+           workspace=None, stream=None):
+    """Decode attention on the stored codes: q [B, Hq, D] fp32 (device) over
+    every stored token of ``keys`` and ``values`` (kvc_attend).  Returns out
+    [B, Hq, D] in the value layer's out_dtype; the workspace (device bytes) is
+    allocated when not given."""
+    import torch
+
+    lib = load_library()
+    if q.dtype != torch.float32 or not q.is_contiguous() or q.dim() != 3:
+        raise ValueError("q must be a contiguous fp32 [B, Hq, D] tensor")
+    Hq = q.shape[1]
+    n = c_size_t()
+    _check(lib.kvc_attend_workspace_bytes(keys._h, values._h, Hq, byref(n)))
+    if workspace is None:
+        workspace = torch.empty(max(int(n.value), 256), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty(q.shape, dtype=_torch_dtypes()[values.out_dtype], device=q.device)
+    _check(lib.kvc_attend(keys._h, values._h, c_void_p(q.data_ptr()), Hq, float(scale),
+                          c_void_p(out.data_ptr()), c_void_p(workspace.data_ptr()),
+                          workspace.numel() * workspace.element_size(),
+                          _stream_ptr(stream, q.device)))
+    return out

@@ -13,6 +13,8 @@
 
 using kvc::Params;
 
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
 struct kvc_layer {
   Params p{};
   void* block = nullptr;  // device parameter block (owned)
@@ -20,13 +22,17 @@ struct kvc_layer {
   int64_t len = 0;
   int64_t capacity = 0;
   int32_t path = KVC_PATH_AUTO;
+  uint64_t wait_ns = kDefaultWaitNs;  // limit of the kernels' loop waits
   int64_t launches = 0;              // kernels launched by this layer (host count)
   int mode = 0, B = 0, H = 0, D = 0, hpg = 1, r = 0, n_bases = 0, n_slots = 0;
   int side_bytes = 0;
+  int ncpos = 0;                     // largest chunk-aligned packed positions of a basis
+  int pmax = 0;                      // largest packed row
   int64_t fixed_bytes = 0;
   std::vector<int32_t> P_host;       // per basis
   std::vector<int32_t> basis_host;   // per slot
   std::vector<int64_t> pay_host, side_host;
+  std::vector<int32_t> seg_host;     // [nb][kMaxSeg][4] width segments
   kvc::TcPlan tc{};                  // tensor-core path tables (kvc_tc.cu)
 };
 
@@ -443,10 +449,18 @@ kvc_status kvc_init_layer(const kvc_layer_desc* d, kvc_layer** out) {
   L->n_bases = nb;
   L->n_slots = g.n_slots;
   L->side_bytes = g.side_bytes;
+  for (int b = 0; b < nb; ++b) {
+    int pos = 0;
+    for (int sg = 0; sg < kvc::kMaxSeg; ++sg) pos += (g.seg[((size_t)b * kvc::kMaxSeg + sg) * 4 + 3] + 7) / 8 * 8;
+    L->ncpos = std::max(L->ncpos, pos);
+    L->pmax = std::max(L->pmax, g.P[b]);
+  }
+  if (d->mode == KVC_MODE_INT8) L->pmax = d->D;
   L->fixed_bytes = g.fixed;
   L->P_host = g.P;
   L->basis_host = g.basis;
   L->pay_host = g.pay_off;
+  L->seg_host = g.seg;
   L->side_host = g.side_off;
   *out = L;
   return succeed();
@@ -472,7 +486,7 @@ kvc_status kvc_append_strided(kvc_layer* L, const void* x, int64_t T, int64_t sb
   if (L->mode == KVC_MODE_INT8)
     e = kvc::launch_append_int8(L->p, a, s, &nk);
   else if (L->path == KVC_PATH_AUTO && kvc::tc_append_ok(L->tc, L->p, a))
-    e = kvc::launch_append_tc(L->tc, L->p, a, s, &nk);
+    e = kvc::launch_append_tc(L->tc, L->p, a, L->wait_ns, s, &nk);
   else if (L->path == KVC_PATH_AUTO && kvc::tc_group_ok(L->tc, L->p, a))
     e = kvc::launch_append_group_tc(L->tc, L->p, a, s, &nk);
   else
@@ -556,6 +570,164 @@ kvc_status kvc_set_path(kvc_layer* L, int32_t path) {
   if (!L) return fail(KVC_ESTATE, "layer is NULL");
   if (path != KVC_PATH_AUTO && path != KVC_PATH_GENERIC) return fail(KVC_EINVAL, "unknown path %d", path);
   L->path = path;
+  return succeed();
+}
+
+}  // extern "C"
+
+namespace {
+
+// Checks shared by the attention entry points; fills the shape fields of a.
+kvc_status attend_check(const kvc_layer* K, const kvc_layer* V, int32_t Hq, kvc::AttendArgs& a,
+                        size_t* ws_bytes) {
+  if (!K || !V) return fail(KVC_ESTATE, "key or value layer is NULL");
+  if (K->mode != KVC_MODE_UNIFORM && K->mode != KVC_MODE_CODEBOOK)
+    return fail(KVC_EINVAL, "keys must be a uniform or codebook layer");
+  if (V->mode != KVC_MODE_INT8 && V->mode != KVC_MODE_UNIFORM)
+    return fail(KVC_EINVAL, "values must be an int8 or uniform layer");
+  if (K->hpg != 1 || V->hpg != 1) return fail(KVC_EINVAL, "head groups are not supported here");
+  if (K->B != V->B || K->H != V->H || K->D != V->D)
+    return fail(KVC_EINVAL, "key and value layers differ in B, H or D");
+  if (K->device != V->device) return fail(KVC_EINVAL, "key and value layers are on different devices");
+  if (K->len != V->len) return fail(KVC_EINVAL, "key and value layers hold different lengths");
+  if (!(K->D == 64 || K->D == 128 || K->D == 256)) return fail(KVC_EINVAL, "D must be 64, 128 or 256");
+  if (Hq < K->H || Hq % K->H) return fail(KVC_EINVAL, "Hq must be a multiple of H");
+  const int rep = Hq / K->H;
+  if (!(rep == 1 || rep == 2 || rep == 4 || rep == 8))
+    return fail(KVC_EINVAL, "Hq / H must be 1, 2, 4 or 8");
+  if (K->ncpos > 256 || (V->mode == KVC_MODE_UNIFORM && V->ncpos > 256))
+    return fail(KVC_EINVAL, "more than 256 packed positions");
+  a.Hq = Hq;
+  a.rep = rep;
+  a.S = K->len;
+  a.NCk = std::max(8, K->ncpos);
+  a.Dv = V->mode == KVC_MODE_INT8 ? V->D : std::max(8, V->ncpos);
+  a.Pk_max = K->pmax;
+  a.Pv_max = V->pmax;
+  a.out_bf16 = V->p.out_dtype == KVC_BF16 ? 1 : 0;
+  int sms = 1;
+  {
+    DeviceGuard dg(K->device);
+    sms = kvc::sm_count();
+  }
+  *ws_bytes = kvc::attend_plan(K->B, Hq, K->n_slots, rep, std::max<int64_t>(K->len, 1), a.NCk,
+                               a.Dv, sms, &a.splits, &a.span);
+  return KVC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvc_status kvc_attend_workspace_bytes(const kvc_layer* K, const kvc_layer* V, int32_t Hq,
+                                      size_t* out) {
+  if (!out) return fail(KVC_EINVAL, "out is NULL");
+  kvc::AttendArgs a;
+  size_t n = 0;
+  kvc_status st = attend_check(K, V, Hq, a, &n);
+  if (st) return st;
+  *out = n;
+  return succeed();
+}
+
+kvc_status kvc_attend(const kvc_layer* K, const kvc_layer* V, const float* q, int32_t Hq,
+                      float scale, void* out, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  kvc::AttendArgs a;
+  size_t need = 0;
+  kvc_status st = attend_check(K, V, Hq, a, &need);
+  if (st) return st;
+  if (!(scale >= 0.f) || !std::isfinite(scale)) return fail(KVC_EINVAL, "scale must be finite and >= 0");
+  if (!q || !out) return fail(KVC_EINVAL, "q or out is NULL");
+  DeviceGuard dg(K->device);
+  if (!dg.ok) return fail(KVC_ECUDA, "cannot select the layer's device");
+  if (!is_device_ptr(q, K->device) || !is_device_ptr(out, K->device))
+    return fail(KVC_EINVAL, "q and out must be device memory of the layers' device");
+  auto s = static_cast<cudaStream_t>(stream);
+  if (K->len == 0) {  // no stored token: the output is zero
+    const cudaError_t e = cudaMemsetAsync(out, 0, (size_t)K->B * Hq * K->D * 2, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(out)");
+    return succeed();
+  }
+  if (!workspace || workspace_bytes < need)
+    return fail(KVC_EINVAL, "workspace is NULL or below kvc_attend_workspace_bytes()");
+  if (!is_device_ptr(workspace, K->device)) return fail(KVC_EINVAL, "workspace is not device memory");
+  if ((uintptr_t)workspace % 256) return fail(KVC_EINVAL, "workspace must be 256-byte aligned");
+  a.q = q;
+  a.out = out;
+  const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)K->D);
+  a.scale_log2 = (float)(sc * 1.4426950408889634);
+  int nk = 0;
+  const cudaError_t e = kvc::launch_attend(K->p, V->p, a, workspace, s, &nk);
+  const_cast<kvc_layer*>(K)->launches += nk;
+  if (e != cudaSuccess) return cuda_fail(e, "attend launch");
+  return succeed();
+}
+
+kvc_status kvc_code_histogram_bytes(const kvc_layer* L, size_t* out) {
+  if (!L) return fail(KVC_ESTATE, "layer is NULL");
+  if (!out) return fail(KVC_EINVAL, "out is NULL");
+  if (L->mode == KVC_MODE_INT8) return fail(KVC_EINVAL, "int8 layers store no codes");
+  *out = kvc::histogram_bytes(L->n_slots, std::max(8, L->ncpos));
+  return succeed();
+}
+
+kvc_status kvc_code_histogram(kvc_layer* L, uint32_t* counts, size_t counts_bytes, void* stream) {
+  size_t need = 0;
+  kvc_status st = kvc_code_histogram_bytes(L, &need);
+  if (st) return st;
+  if (!counts || counts_bytes < need) return fail(KVC_EINVAL, "counts is NULL or too small");
+  DeviceGuard dg(L->device);
+  if (!dg.ok) return fail(KVC_ECUDA, "cannot select the layer's device");
+  if (!is_device_ptr(counts, L->device)) return fail(KVC_EINVAL, "counts is not device memory");
+  if ((uintptr_t)counts % 4) return fail(KVC_EINVAL, "counts must be 4-byte aligned");
+  int nk = 0;
+  const cudaError_t e = kvc::launch_code_histogram(L->p, counts, std::max(8, L->ncpos), L->len,
+                                                   static_cast<cudaStream_t>(stream), &nk);
+  L->launches += nk;
+  if (e != cudaSuccess) return cuda_fail(e, "histogram launch");
+  return succeed();
+}
+
+kvc_status kvc_entropy_bytes(const kvc_layer* L, const uint32_t* counts, kvc_entropy* out) {
+  if (!L) return fail(KVC_ESTATE, "layer is NULL");
+  if (!counts || !out) return fail(KVC_EINVAL, "counts or out is NULL");
+  if (L->mode == KVC_MODE_INT8) return fail(KVC_EINVAL, "int8 layers store no codes");
+  const int NC = std::max(8, L->ncpos);
+  int64_t pre = 0, stored = 0;
+  for (int s = 0; s < L->n_slots; ++s) {
+    const int b = L->basis_host[s];
+    const int64_t fixed = L->len * L->P_host[b];
+    int64_t bits = 0, table = 0;
+    int nch = 0;
+    for (int sg = 0; sg < kvc::kMaxSeg; ++sg) {
+      const int32_t* e = &L->seg_host[((size_t)b * kvc::kMaxSeg + sg) * 4];
+      if (!e[3]) break;
+      const int w = e[1], n = 1 << w;
+      for (int m = 0; m < e[3]; ++m) {
+        const uint32_t* c = counts + ((size_t)s * NC + nch * 8 + m) * 256;
+        const std::vector<int> len = kvc::huffman_code_lengths(c, n);
+        for (int v = 0; v < n; ++v) bits += (int64_t)c[v] * len[v];
+        table += n;
+      }
+      nch += (e[3] + 7) / 8;
+    }
+    const int64_t coded = L->len ? (bits + 7) / 8 + table : 0;
+    pre += fixed;
+    stored += std::min(fixed, coded);
+  }
+  out->pre_entropy = pre;
+  out->stored_payload = stored;
+  out->params = L->fixed_bytes;
+  const int64_t total = stored + L->fixed_bytes;
+  out->gain = total ? (double)pre / (double)total : 1.0;
+  return succeed();
+}
+
+kvc_status kvc_set_wait_limit(kvc_layer* L, int64_t ns) {
+  if (!L) return fail(KVC_ESTATE, "layer is NULL");
+  if (ns < 0) return fail(KVC_EINVAL, "wait limit must be >= 0");
+  L->wait_ns = ns == 0 ? kDefaultWaitNs : (uint64_t)ns;
   return succeed();
 }
 

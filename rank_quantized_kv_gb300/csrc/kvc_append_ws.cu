@@ -63,6 +63,7 @@ struct AppendWsArgs {
   int vt_smem;              // each group keeps its basis' V^T in shared memory
   float inv_scale, gamma;
   int tiles_per_slot, total_tiles;
+  unsigned long long wait_ns;  // limit of the loop waits (the drains keep kWaitNs)
 };
 
 // Per-basis quantiser table (host layout in append_ws_table), per component:
@@ -94,6 +95,20 @@ struct XHdr {  // per x stage, written by the producer
   long long row0;           // store row of the tile's first token
   long long pay, side;      // the slot's payload and side-word offsets in the store
 };
+
+// Wait for phase `parity` of `bar`; false after `ns` of wall time, or as soon
+// as another role has given up (*abort set), so that one time-out unwinds
+// every role promptly.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t ns,
+                                              volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > ns) return false;
+  }
+}
 
 // Position in a ring of n buffers: the buffer of the current use and the
 // parity of its barriers' phase; next() moves on one use.
@@ -315,12 +330,12 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       for (int i = 0; i < m; ++i, rx.next()) {
         const int s = rx.slot;
         // the quantiser of tile i - XS released this stage
-        if (i >= XS && !mbar_wait_bounded(&x_empty[s], rx.phase ^ 1u, kWaitNs)) { abort_flag = 1; break; }
+        if (i >= XS && !wait_or_abort(&x_empty[s], rx.phase ^ 1u, t.wait_ns, &abort_flag)) { abort_flag = 1; break; }
         int first_use = 0;
         if (beta != cur_beta) {
           bslot = NB == 2 ? bslot ^ 1 : 0;
           if (bload[bslot] > 0 &&
-              !mbar_wait_bounded(&b_empty[bslot], (bload[bslot] - 1) & 1, kWaitNs)) { abort_flag = 1; break; }
+              !wait_or_abort(&b_empty[bslot], (bload[bslot] - 1) & 1, t.wait_ns, &abort_flag)) { abort_flag = 1; break; }
           mbar_arrive_expect_tx(&b_full[bslot], (uint32_t)b_bytes);
           bulk_load(Bs + bslot * b_bytes, t.B + (size_t)beta * (b_bytes / 2), (uint32_t)b_bytes,
                     &b_full[bslot]);
@@ -363,15 +378,15 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       Ring rx(XS), rt(TS);
       for (int i = 0; i < m; ++i, rx.next(), rt.next()) {
         const int s = rx.slot, acc = rt.slot;
-        if (!mbar_wait_bounded(&x_full[s], rx.phase, kWaitNs)) { abort_flag = 1; break; }
+        if (!wait_or_abort(&x_full[s], rx.phase, t.wait_ns, &abort_flag)) { abort_flag = 1; break; }
         const int info = hdr[s].info, bs = info & 1;
         if (info & 2) {  // first tile on a newly loaded B: the other buffer is free when
           if (i > 0) umma_commit(&b_empty[NB == 2 ? bs ^ 1 : 0]);  // the MMAs issued so far finish
-          if (!mbar_wait_bounded(&b_full[bs], buse[bs] & 1, kWaitNs)) { abort_flag = 1; break; }
+          if (!wait_or_abort(&b_full[bs], buse[bs] & 1, t.wait_ns, &abort_flag)) { abort_flag = 1; break; }
           ++buse[bs];
         }
         // the quantiser of tile i - TS released this accumulator
-        if (i >= TS && !mbar_wait_bounded(&acc_empty[acc], rt.phase ^ 1u, kWaitNs)) { abort_flag = 1; break; }
+        if (i >= TS && !wait_or_abort(&acc_empty[acc], rt.phase ^ 1u, t.wait_ns, &abort_flag)) { abort_flag = 1; break; }
         tc_fence_after();
         const uint32_t xa = smem_u32(xst + (size_t)s * t.x_stage);
         const uint32_t b0 = smem_u32(Bs + bs * b_bytes);
@@ -418,8 +433,8 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       if (i > g)
         for (int j = 0; j < QG; ++j) { rx.next(); rt.next(); }
       const int s = rx.slot, acc = rt.slot;
-      bool late = !mbar_wait_bounded(&x_full[s], rx.phase, kWaitNs);
-      late = late || !mbar_wait_bounded(&acc_full[acc], rt.phase, kWaitNs);
+      bool late = !wait_or_abort(&x_full[s], rx.phase, t.wait_ns, &abort_flag);
+      late = late || !wait_or_abort(&acc_full[acc], rt.phase, t.wait_ns, &abort_flag);
       const unsigned char* xs = xst + (size_t)s * t.x_stage;
       const Tab tb(xs + tab_off, rpad);
       const XHdr hd = hdr[s];
@@ -755,7 +770,7 @@ size_t append_ws_plan(int D, int r, int rpad, int npieces, int pmax, int max_chu
 }
 
 cudaError_t launch_append_ws(const TcPlan& plan, const Params& p, const AppendArgs& a,
-                             const CUtensorMap& xmap, cudaStream_t s, int* nk) {
+                             const CUtensorMap& xmap, uint64_t wait_ns, cudaStream_t s, int* nk) {
   WsKernel k = ws_kernel_for(p.mode, plan.app_bf16, plan.app_rpad);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)plan.ws_smem);
@@ -767,7 +782,7 @@ cudaError_t launch_append_ws(const TcPlan& plan, const Params& p, const AppendAr
   const AppendWsArgs t{plan.appB,    plan.c64,     plan.wsTab,   plan.app_rpad,      plan.app_pieces,
                        sh.acc_stride, sh.cols,      sh.n_acc,     sh.n_x,             sh.n_b,
                        sh.x_stage,    sh.tab_bytes, plan.ws_pmax, sh.ks,              sh.vt_smem,
-                       plan.app_inv_scale, plan.app_gamma, tiles, total};
+                       plan.app_inv_scale, plan.app_gamma, tiles, total, wait_ns};
   k<<<(unsigned)grid, kThreadsWs, plan.ws_smem, s>>>(p, t, xmap, a);
   ++*nk;
   return cudaGetLastError();

@@ -77,6 +77,36 @@ struct ZIn {
   float gamma = 0.f, ex = 0.f, en = 0.f;
 };
 
+// Decode attention over a key layer and a value layer (kvc_attend.cu).
+struct AttendArgs {
+  const float* q = nullptr;  // [B][Hq][D] fp32
+  void* out = nullptr;       // [B][Hq][D] fp16 or bf16
+  int Hq = 0, rep = 0;       // query heads; query heads per key/value head
+  float scale_log2 = 0.f;    // score scale times log2(e)
+  int out_bf16 = 0;
+  int64_t S = 0;             // stored tokens
+  int splits = 0;            // token splits per slot
+  int64_t span = 0;          // tokens per split (a multiple of 128)
+  int NCk = 0;               // packed positions of the key codes (chunk-aligned)
+  int Dv = 0;                // accumulator width: D (int8 values) or the value positions
+  int Pk_max = 0, Pv_max = 0;  // largest packed key / value row
+  float* w = nullptr;        // workspace: [B Hq][NCk] key weights
+  float* c1 = nullptr;       // workspace: [B Hq] score offsets
+  float* part = nullptr;     // workspace: [n_slots][splits][rep][2 + Dv] partials
+};
+// Workspace bytes (and the split) of an attention call; the launcher.
+size_t attend_plan(int B, int Hq, int n_slots, int rep, int64_t S, int NCk, int Dv, int sms,
+                   int* splits, int64_t* span);
+cudaError_t launch_attend(const Params& kp, const Params& vp, AttendArgs a, void* workspace,
+                          cudaStream_t s, int* nk);
+
+// Code histogram of the store (kvc_entropy.cu): counts [n_slots][NC][256]
+// (NC chunk-aligned positions); Huffman code lengths of n symbol counts.
+size_t histogram_bytes(int n_slots, int NC);
+cudaError_t launch_code_histogram(const Params& p, uint32_t* counts, int NC, int64_t S,
+                                  cudaStream_t s, int* nk);
+std::vector<int> huffman_code_lengths(const uint32_t* counts, int n);
+
 // Everything derived from a descriptor, on the host (kvc_api.cu).
 struct Geo {
   int d_in = 0, Hg = 0, n_slots = 0, nb = 0, r = 0;

@@ -107,7 +107,7 @@ void tc_release(TcPlan& plan);
 bool tc_append_ok(const TcPlan& plan, const Params& p, const AppendArgs& a);
 bool tc_fetch_ok(const TcPlan& plan, const Params& p, const FetchArgs& f);
 cudaError_t launch_append_tc(const TcPlan& plan, const Params& p, const AppendArgs& a,
-                             cudaStream_t s, int* nk);
+                             uint64_t wait_ns, cudaStream_t s, int* nk);
 cudaError_t launch_fetch_tc(const TcPlan& plan, const Params& p, const FetchArgs& f,
                             cudaStream_t s, int* nk);
 bool tc_group_ok(const TcPlan& plan, const Params& p, const AppendArgs& a);
@@ -131,7 +131,7 @@ int append_ws_table(const Geo& g, const kvc_layer_desc& d, int rpad, const doubl
 size_t append_ws_plan(int D, int r, int rpad, int npieces, int pmax, int max_chunks, int n_bases,
                       AppendWsShape* sh);
 cudaError_t launch_append_ws(const TcPlan& plan, const Params& p, const AppendArgs& a,
-                             const CUtensorMap& xmap, cudaStream_t s, int* nk);
+                             const CUtensorMap& xmap, uint64_t wait_ns, cudaStream_t s, int* nk);
 // Group-mode projection (kvc_group_proj.cu): shared memory for N = rpad and
 // the basis slice stages it leaves room for (0 when two do not fit); the
 // launcher for one chunk of tokens (`map` covers exactly that chunk).

@@ -93,6 +93,7 @@ def test_null_layer_calls_fail_cleanly(kvc):
     assert lib.kvc_length(None, ctypes.byref(n)) == -2
     assert lib.kvc_append(None, None, 1, None) == -2
     assert lib.kvc_fetch(None, None, 1, None, None) == -2
+    assert lib.kvc_set_wait_limit(None, 1000) == -2
     lib.kvc_destroy(None)
     assert b"NULL" in lib.kvc_last_error()
 

@@ -18,7 +18,9 @@ def test_reference_arm_prints_one_contract_line():
     assert line["value"] > 0 and line["unit"] == "KV tokens/s"
     assert line["higher_is_better"] is True and line["n_gpus"] == 1
     assert line["steps"] == 2 and line["warmup"] == 3
-    assert line["config"]["workload"] == "llama3-8b"
+    import bench
+
+    assert line["config"]["workload"] == bench.DEFAULT_WORKLOAD
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
