@@ -128,7 +128,10 @@ class ClockSampler:
 # capture and its command are recorded with the ncu summaries); an entry is
 # removed whenever its kernel changes.  The roofline's "traffic" scales it to
 # the launch.
-TRAFFIC_PER_UNIT = {}
+TRAFFIC_PER_UNIT = {
+    # codebook append: 269.06 MB read + 41.39 MB written for 16 x 8 x 8192 token-heads
+    ("append", "codebook"): (269.06e6 + 41.39e6) / (16 * 8 * 8192),
+}
 
 
 # ----------------------------------------------------------------------------- multi-rank

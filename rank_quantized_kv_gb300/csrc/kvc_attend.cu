@@ -85,6 +85,24 @@ __device__ __forceinline__ uint32_t chunk_code(uint2 b, int w, int e) {
   return (b.x >> (w * e)) & ((1u << w) - 1u);
 }
 
+// REP consecutive fp32 weights from shared memory in as few vector loads as
+// possible (16-byte aligned for REP >= 4).
+template <int REP>
+__device__ __forceinline__ void load_w(const float* src, float (&w)[REP]) {
+  if constexpr (REP >= 4) {
+#pragma unroll
+    for (int q = 0; q < REP / 4; ++q) {
+      const float4 v = reinterpret_cast<const float4*>(src)[q];
+      w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+    }
+  } else if constexpr (REP == 2) {
+    const float2 v = *reinterpret_cast<const float2*>(src);
+    w[0] = v.x; w[1] = v.y;
+  } else {
+    w[0] = src[0];
+  }
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
@@ -118,9 +136,15 @@ __global__ void attend_prep_kernel(const Params kp, const AttendArgs a) {
   for (int j = tid; j < a.NCk; j += blockDim.x) {
     const int k = position_component(kp, beta, j);
     if (k < 0) continue;
-    const float* vt = kp.Vt + ((size_t)beta * kp.r + k) * D;
-    float qv = 0.f;
-    for (int i = 0; i < D; ++i) qv = fmaf(qs[i], vt[i], qv);
+    // (V^T q)_k: the threads of a warp read one row of V [D_in][r] at their
+    // columns; four partial sums keep the dependent chain short
+    const float* vc = kp.V + (size_t)beta * D * kp.r + k;
+    float q4[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int i = 0; i < D; i += 4) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) q4[e] = fmaf(qs[i + e], vc[(size_t)(i + e) * kp.r], q4[e]);
+    }
+    const float qv = (q4[0] + q4[1]) + (q4[2] + q4[3]);
     const size_t bk = (size_t)beta * kp.r + k;
     w[j] = a.scale_log2 * qv * (uniform ? kp.step[bk] : 1.f);
     if (uniform) part = fmaf(qv, kp.lo[bk], part);
@@ -175,8 +199,8 @@ __global__ void __launch_bounds__(kMainThreads)
   }
   if (KMODE == KVC_MODE_CODEBOOK)
     for (int j = tid; j < kp.cb_levels; j += kMainThreads) cbv[j] = kp.codebook[j];
-  for (int e = tid; e < REP * NCk; e += kMainThreads) {
-    const int g = e / NCk, j = e - g * NCk;
+  for (int e = tid; e < REP * NCk; e += kMainThreads) {  // ws[j][g]: one vector load per position
+    const int j = e / REP, g = e - j * REP;
     ws[e] = a.w[(size_t)(bq0 + g) * NCk + j];
   }
   if (tid < REP) c1s[tid] = KMODE == KVC_MODE_UNIFORM ? a.c1[bq0 + tid] : 0.f;
@@ -235,8 +259,10 @@ __global__ void __launch_bounds__(kMainThreads)
         for (int e = 0; e < 8; ++e) {
           const uint32_t code = chunk_code(bits, w, e);
           const float v = KMODE == KVC_MODE_CODEBOOK ? cbv[code] : (float)code;
+          float wv[REP];
+          load_w<REP>(ws + (8 * c + e) * REP, wv);
 #pragma unroll
-          for (int g = 0; g < REP; ++g) sc[g] = fmaf(ws[g * NCk + 8 * c + e], v, sc[g]);
+          for (int g = 0; g < REP; ++g) sc[g] = fmaf(wv[g], v, sc[g]);
         }
       }
       if (KMODE == KVC_MODE_CODEBOOK) {
