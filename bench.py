@@ -399,6 +399,17 @@ def extra_configs(dev, flush, peaks, steps):
                                             for i, L in enumerate(layers)}
             entry["one_token_note"] = ("one token appended to each of the 64 (b, h) at S = 4096: "
                                        "launch-latency bound, compare with launch_floor_us")
+            import rank_quantized_kv_gb300 as kvc
+
+            xf = inputs[0][:, :, :wl["fit"]]
+            kvc.fit_uniform(xf, wl["fit"], wl["r"], wl["choices"], wl["budget"])
+            fit_ms = _event_ms(lambda: kvc.fit_uniform(xf, wl["fit"], wl["r"], wl["choices"],
+                                                       wl["budget"]), 3, flush)
+            entry["prefill_fit_us"] = fit_ms * 1e3
+            entry["prefill_fit_note"] = (
+                "kvc_fit_uniform over the 64 (b, h) slots' first 512 key rows: covariance, "
+                "Jacobi eigendecomposition, DP allocation and min/step in float64, four "
+                "launches; once per layer before the hot path")
         for L in layers:
             if L.sync_status() != 0:
                 raise RuntimeError(f"device error in {name}")

@@ -291,6 +291,64 @@ kvc_status kvc_code_histogram(kvc_layer *layer, uint32_t *counts, size_t counts_
  * (counts: host, as kvc_code_histogram wrote it for the current length). */
 kvc_status kvc_entropy_bytes(const kvc_layer *layer, const uint32_t *counts, kvc_entropy *out);
 
+/* On-device prefill fit of the KVC_MODE_UNIFORM parameters (kvtc_cache page:
+ * module docstring "Design", prefill step 1, a local PCA per (b, h) fitted
+ * in one batched call by KVTCKVCache.update_and_fetch; the module
+ * docstring's DP-optimal discrete allocation under a bit budget, 0 bits
+ * dropping a component; _TensorKVTC._requantize, a minimum and a step per
+ * kept component, frozen here at fit time).  For every slot (b, h), over its
+ * first S_fit rows X (float64 throughout, rounded to fp32 at the end):
+ *   mean = the column means of X;  C = (X - mean)^T (X - mean) / S_fit;
+ *   C = U diag(lam) U^T (cyclic Jacobi), eigenpairs ordered largest first,
+ *   ties by index, each vector's sign such that its first largest-magnitude
+ *   entry is positive;  V = the first r columns of U in fp32;
+ *   bits = argmin sum_k lam_k 2^(-2 b_k) over b_k in bit_choices with
+ *   sum_k b_k <= bit_budget (dynamic programme; the smaller width wins a tie);
+ *   qmin_k = min_t z_tk, qstep_k = max((max_t z_tk - qmin_k) / (2^b_k - 1), 1e-8)
+ *   over z = (x - fp32 mean) V in float64, rounded to fp32 (0 for dropped
+ *   components).
+ * The outputs are what kvc_layer_desc takes for a UNIFORM layer with one
+ * basis per slot (n_bases = B * H, basis_of = identity), in device memory.
+ *
+ *  x            device [.., D] rows in in_dtype; row t of head h of batch b
+ *               starts at x + b*stride_b + h*stride_h + t*stride_t (elements).
+ *  S_fit        fit rows per slot (>= 2; the pages fit on the prefill).
+ *  D            8 .. 128, a multiple of 8.  r: 1 .. D.
+ *  bit_choices  host int32 [n_choices], 1 .. 8 distinct widths from
+ *               {0,1,2,3,4,8}; some allocation must fit the budget
+ *               (min(bit_choices) * r <= bit_budget).
+ *  outputs      device, written for every slot: V fp32 [B*H][D][r], mean fp32
+ *               [B*H][D], bits uint8 [B*H][r], qmin and qstep fp32 [B*H][r];
+ *               lam float64 [B*H][D] (the sorted eigenvalues) may be NULL. */
+typedef struct {
+  const void *x;
+  int32_t in_dtype;
+  int32_t B, H, D;
+  int64_t S_fit;
+  int64_t stride_b, stride_h, stride_t;
+  int32_t r;
+  const int32_t *bit_choices;
+  int32_t n_choices;
+  int32_t bit_budget;
+  float *V;
+  float *mean;
+  uint8_t *bits;
+  float *qmin;
+  float *qstep;
+  double *lam;
+} kvc_fit_desc;
+
+/* Workspace bytes kvc_fit_uniform needs for this descriptor (host-only;
+ * float64 covariance, eigenvectors and DP tables of every slot). */
+kvc_status kvc_fit_uniform_workspace_bytes(const kvc_fit_desc *desc, size_t *out);
+
+/* Run the fit on the current device, asynchronously on `stream` (four kernel
+ * launches).  workspace: device, 256-byte aligned, at least
+ * kvc_fit_uniform_workspace_bytes() bytes, overwritten.  KVC_EINVAL for a bad
+ * field, host pointers or a short workspace; nothing is launched then. */
+kvc_status kvc_fit_uniform(const kvc_fit_desc *desc, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
 /* Limit, in nanoseconds, of the waits inside the warp-specialised tensor-core
  * append kernel (one role waiting for another: a tile loaded, an accumulator
  * written or released).  A kernel whose wait runs out stops its work, waits

@@ -20,7 +20,7 @@ from ctypes import POINTER, byref, c_float, c_int32, c_int64, c_size_t, c_uint8,
 import numpy as np
 
 __all__ = ["KVCacheLayer", "load_library", "library_path", "KvcError", "MODES", "DTYPES",
-           "EXPORTED_SYMBOLS", "store_bytes", "attend", "attend_workspace_bytes"]
+           "EXPORTED_SYMBOLS", "store_bytes", "attend", "attend_workspace_bytes", "fit_uniform"]
 
 MODES = {"uniform": 0, "group": 1, "codebook": 2, "int8": 3}
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
@@ -35,6 +35,7 @@ EXPORTED_SYMBOLS = (
     "kvc_get_slot_layout", "kvc_set_path", "kvc_sync_status", "kvc_counters", "kvc_destroy",
     "kvc_append_noalloc", "kvc_set_wait_limit", "kvc_attend", "kvc_attend_workspace_bytes",
     "kvc_code_histogram_bytes", "kvc_code_histogram", "kvc_entropy_bytes",
+    "kvc_fit_uniform_workspace_bytes", "kvc_fit_uniform",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -64,6 +65,16 @@ class _Desc(ctypes.Structure):
         ("group_size", c_int32), ("codebook", POINTER(c_float)), ("cb_bits", c_int32),
         ("in_dtype", c_int32), ("out_dtype", c_int32), ("capacity", c_int64),
         ("store", c_void_p), ("store_bytes", c_size_t),
+    ]
+
+
+class _FitDesc(ctypes.Structure):
+    _fields_ = [
+        ("x", c_void_p), ("in_dtype", c_int32), ("B", c_int32), ("H", c_int32), ("D", c_int32),
+        ("S_fit", c_int64), ("stride_b", c_int64), ("stride_h", c_int64), ("stride_t", c_int64),
+        ("r", c_int32), ("bit_choices", POINTER(c_int32)), ("n_choices", c_int32),
+        ("bit_budget", c_int32), ("V", c_void_p), ("mean", c_void_p), ("bits", c_void_p),
+        ("qmin", c_void_p), ("qstep", c_void_p), ("lam", c_void_p),
     ]
 
 
@@ -116,6 +127,8 @@ def load_library():
             "kvc_code_histogram_bytes": (c_int32, [P, POINTER(c_size_t)]),
             "kvc_code_histogram": (c_int32, [P, P, c_size_t, P]),
             "kvc_entropy_bytes": (c_int32, [P, P, POINTER(_Entropy)]),
+            "kvc_fit_uniform_workspace_bytes": (c_int32, [POINTER(_FitDesc), POINTER(c_size_t)]),
+            "kvc_fit_uniform": (c_int32, [POINTER(_FitDesc), P, c_size_t, P]),
             "kvc_sync_status": (c_int32, [P, P]),
             "kvc_counters": (c_int32, [P, POINTER(c_int64), c_int32, P]),
             "kvc_destroy": (None, [P]),
@@ -412,4 +425,47 @@ def attend(keys: "KVCacheLayer", values: "KVCacheLayer", q, scale: float = 0.0, 
                           c_void_p(out.data_ptr()), c_void_p(workspace.data_ptr()),
                           workspace.numel() * workspace.element_size(),
                           _stream_ptr(stream, q.device)))
+    return out
+
+
+def fit_uniform(x, S_fit: int, r: int, choices, budget: int, stream=None):
+    """On-device prefill fit of the uniform mode (kvc_fit_uniform): per (b, h)
+    of x [B, H, T, D] (device; fp32, fp16 or bf16; last dimension contiguous),
+    over its first S_fit rows: the local PCA, the DP bit allocation and the
+    frozen minimum and step.  Returns a dict of device tensors V [B*H, D, r]
+    fp32, mean [B*H, D] fp32, bits [B*H, r] uint8, qmin and qstep [B*H, r]
+    fp32 and lam [B*H, D] float64 (the sorted eigenvalues); V, mean, bits,
+    qmin and qstep are the uniform layer's parameters with one basis per slot."""
+    import torch
+
+    lib = load_library()
+    rev = {v: k for k, v in _torch_dtypes().items()}
+    if x.dim() != 4 or x.dtype not in rev or x.stride(3) != 1:
+        raise ValueError("x must be [B, H, T, D] fp32/fp16/bf16 with a contiguous last dimension")
+    B, H, T, D = x.shape
+    if S_fit > T:
+        raise ValueError("S_fit exceeds the rows of x")
+    # outputs on x's GPU; rows in host memory reach the library, which rejects them
+    dev = x.device if x.is_cuda else torch.device("cuda", torch.cuda.current_device())
+    ns = B * H
+    out = dict(V=torch.empty(ns, D, r, dtype=torch.float32, device=dev),
+               mean=torch.empty(ns, D, dtype=torch.float32, device=dev),
+               bits=torch.empty(ns, r, dtype=torch.uint8, device=dev),
+               qmin=torch.empty(ns, r, dtype=torch.float32, device=dev),
+               qstep=torch.empty(ns, r, dtype=torch.float32, device=dev),
+               lam=torch.empty(ns, D, dtype=torch.float64, device=dev))
+    ch = (c_int32 * len(choices))(*[int(c) for c in choices])
+    d = _FitDesc(x=x.data_ptr(), in_dtype=DTYPES[rev[x.dtype]], B=B, H=H, D=D, S_fit=int(S_fit),
+                 stride_b=x.stride(0), stride_h=x.stride(1), stride_t=x.stride(2), r=int(r),
+                 bit_choices=ch, n_choices=len(choices), bit_budget=int(budget),
+                 V=out["V"].data_ptr(), mean=out["mean"].data_ptr(), bits=out["bits"].data_ptr(),
+                 qmin=out["qmin"].data_ptr(), qstep=out["qstep"].data_ptr(),
+                 lam=out["lam"].data_ptr())
+    n = c_size_t()
+    _check(lib.kvc_fit_uniform_workspace_bytes(byref(d), byref(n)))
+    ws = torch.empty(max(int(n.value), 256), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.kvc_fit_uniform(byref(d), c_void_p(ws.data_ptr()), int(n.value),
+                                   _stream_ptr(stream, dev)))
+    out["workspace"] = ws  # kept alive until the caller synchronises
     return out

@@ -2,9 +2,11 @@
 
 This runs once per layer before the hot path (the kvtc_cache page fits the
 local PCA basis and the bit allocation on the first call and freezes them;
-the palu_cache page fits one projection per head group at prefill).  It uses
-PyTorch linear algebra in float64 on whatever device the rows are on; the
-hot path itself (append / fetch) runs only in libkvc's kernels.
+the palu_cache page fits one projection per head group at prefill).  The
+per-(b, h) uniform fit runs on the GPU in libkvc (kvc_fit_uniform); the
+shared and head-group fits, whose pooled rows reach D_in = 1024, use PyTorch
+linear algebra in float64.  The hot path itself (append / fetch) runs only in
+libkvc's kernels.
 
     params = fit_uniform(x[:, :, :512], r=32, choices=(0, 2, 4, 8), budget=128)
     layer = KVCacheLayer("uniform", B, H, D, capacity=S, **params)
@@ -16,7 +18,7 @@ import math
 import numpy as np
 import torch
 
-__all__ = ["pca", "allocate_bits", "fit_uniform", "fit_uniform_shared", "fit_group",
+__all__ = ["pca", "fit_uniform", "fit_uniform_shared", "fit_group",
            "rotation", "gaussian_codebook"]
 
 
@@ -37,40 +39,6 @@ def pca(rows: torch.Tensor):
     return mean, lam, U * sign
 
 
-def allocate_bits(lam, choices, budget: int) -> np.ndarray:
-    """Bit widths minimising sum_k lam_k 4^-b_k under sum_k b_k <= budget.
-
-    Forward dynamic programme over the bits spent so far: best[c] is the
-    least distortion of the components seen so far using exactly c bits.
-    """
-    lam = np.asarray(lam, dtype=np.float64)
-    choices = sorted(set(int(c) for c in choices))
-    r = lam.shape[0]
-    best = np.full(budget + 1, np.inf)
-    best[0] = 0.0
-    pick = np.zeros((r, budget + 1), dtype=np.int64)
-    for k in range(r):
-        nxt = np.full(budget + 1, np.inf)
-        arg = np.zeros(budget + 1, dtype=np.int64)
-        for b in reversed(choices):
-            if b > budget:
-                continue
-            cand = np.full(budget + 1, np.inf)
-            cand[b:] = best[: budget + 1 - b] + lam[k] * 4.0 ** (-b)
-            better = cand <= nxt
-            nxt = np.where(better, cand, nxt)
-            arg = np.where(better, b, arg)
-        best, pick[k] = nxt, arg
-    c = int(np.argmin(best))
-    if not np.isfinite(best[c]):
-        raise ValueError("no allocation fits the budget")
-    bits = np.zeros(r, dtype=np.int64)
-    for k in range(r - 1, -1, -1):
-        bits[k] = pick[k, c]
-        c -= bits[k]
-    return bits
-
-
 def _min_step(Z: torch.Tensor, bits: np.ndarray):
     lo = Z.min(dim=0).values
     hi = Z.max(dim=0).values
@@ -81,24 +49,18 @@ def _min_step(Z: torch.Tensor, bits: np.ndarray):
 
 
 def fit_uniform(x_fit: torch.Tensor, r: int, choices, budget: int) -> dict:
-    """One basis per (b, h) from prefill rows x_fit [B, H, S_fit, D]."""
+    """One basis per (b, h) from prefill rows x_fit [B, H, S_fit, D] (device),
+    fitted on the GPU by libkvc's kvc_fit_uniform (covariance, Jacobi
+    eigendecomposition, DP allocation, frozen minimum and step, in float64);
+    returns the uniform layer's parameters as host arrays."""
+    from . import fit_uniform as device_fit
+
     B, H, S, D = x_fit.shape
-    if S < 2:
-        raise ValueError("the fit needs at least two prefill rows")
-    mean, lam, U = pca(x_fit.reshape(B * H, S, D))
-    V32 = U[:, :, :r].to(torch.float32)
-    m32 = mean.to(torch.float32)
-    out_bits, out_lo, out_st = [], [], []
-    for n in range(B * H):
-        bits = allocate_bits(lam[n, :r].cpu().numpy(), choices, budget)
-        Z = (x_fit.reshape(B * H, S, D)[n].to(torch.float64) - m32[n].double()) @ V32[n].double()
-        lo, st = _min_step(Z, bits)
-        out_bits.append(bits), out_lo.append(lo), out_st.append(st)
-    return dict(V=V32.cpu().numpy(), mean=m32.cpu().numpy(),
-                bits=np.stack(out_bits).astype(np.uint8),
-                qmin=torch.stack(out_lo).to(torch.float32).cpu().numpy(),
-                qstep=torch.stack(out_st).to(torch.float32).cpu().numpy(),
-                basis_of=np.arange(B * H, dtype=np.int32))
+    out = device_fit(x_fit, S, r, choices, budget)
+    torch.cuda.synchronize(x_fit.device)
+    return dict(V=out["V"].cpu().numpy(), mean=out["mean"].cpu().numpy(),
+                bits=out["bits"].cpu().numpy(), qmin=out["qmin"].cpu().numpy(),
+                qstep=out["qstep"].cpu().numpy(), basis_of=np.arange(B * H, dtype=np.int32))
 
 
 def fit_uniform_shared(x_fit: torch.Tensor, r: int, bits_each: int) -> dict:

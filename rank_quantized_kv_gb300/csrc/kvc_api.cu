@@ -724,6 +724,84 @@ kvc_status kvc_entropy_bytes(const kvc_layer* L, const uint32_t* counts, kvc_ent
   return succeed();
 }
 
+// Validate a fit descriptor into FitArgs (choices sorted and distinct, the
+// budget clamped to max(choices) * r, beyond which the allocation is the same).
+static kvc_status fit_check(const kvc_fit_desc* d, kvc::FitArgs& f) {
+  if (!d) return fail(KVC_EINVAL, "descriptor is NULL");
+  if (d->in_dtype != KVC_F32 && d->in_dtype != KVC_F16 && d->in_dtype != KVC_BF16)
+    return fail(KVC_EINVAL, "in_dtype must be KVC_F32, KVC_F16 or KVC_BF16");
+  if (d->B < 1 || d->H < 1) return fail(KVC_EINVAL, "B and H must be >= 1");
+  if (d->D < 8 || d->D > kvc::kFitMaxD || d->D % 8)
+    return fail(KVC_EINVAL, "D must be a multiple of 8 in [8, %d]", kvc::kFitMaxD);
+  if (d->S_fit < 2) return fail(KVC_EINVAL, "the fit needs S_fit >= 2 rows");
+  if (d->r < 1 || d->r > d->D) return fail(KVC_EINVAL, "r must be in [1, D]");
+  if (!d->bit_choices || d->n_choices < 1 || d->n_choices > kvc::kFitMaxChoices)
+    return fail(KVC_EINVAL, "bit_choices must hold 1 .. %d widths", kvc::kFitMaxChoices);
+  std::vector<int> ch(d->bit_choices, d->bit_choices + d->n_choices);
+  for (int b : ch)
+    if (b < 0 || b > 8 || b == 5 || b == 6 || b == 7)
+      return fail(KVC_EINVAL, "bit widths must be in {0,1,2,3,4,8}");
+  std::sort(ch.begin(), ch.end());
+  ch.erase(std::unique(ch.begin(), ch.end()), ch.end());
+  if (d->bit_budget < 0 || (int64_t)ch.front() * d->r > d->bit_budget)
+    return fail(KVC_EINVAL, "no allocation fits bit_budget with these widths");
+  f.x = d->x;
+  f.dtype = d->in_dtype;
+  f.B = d->B;
+  f.H = d->H;
+  f.D = d->D;
+  f.r = d->r;
+  f.S = d->S_fit;
+  f.sb = d->stride_b;
+  f.sh = d->stride_h;
+  f.st = d->stride_t;
+  f.n_choices = (int)ch.size();
+  for (size_t i = 0; i < ch.size(); ++i) f.choices[i] = ch[i];
+  f.budget = (int)std::min<int64_t>(d->bit_budget, (int64_t)ch.back() * d->r);
+  f.V = d->V;
+  f.mean = d->mean;
+  f.bits = d->bits;
+  f.qmin = d->qmin;
+  f.qstep = d->qstep;
+  f.lam_out = d->lam;
+  return KVC_OK;
+}
+
+kvc_status kvc_fit_uniform_workspace_bytes(const kvc_fit_desc* d, size_t* out) {
+  kvc::FitArgs f;
+  const kvc_status st = fit_check(d, f);
+  if (st) return st;
+  if (!out) return fail(KVC_EINVAL, "out is NULL");
+  *out = kvc::fit_workspace_bytes(f.B * f.H, f.D, f.r, f.budget);
+  return succeed();
+}
+
+kvc_status kvc_fit_uniform(const kvc_fit_desc* d, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  kvc::FitArgs f;
+  const kvc_status st = fit_check(d, f);
+  if (st) return st;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const void* dev_ptrs[] = {f.x, f.V, f.mean, f.bits, f.qmin, f.qstep, workspace};
+  for (const void* p : dev_ptrs)
+    if (!p || !is_device_ptr(p, dev))
+      return fail(KVC_EINVAL, "x, the outputs and the workspace must be device memory of the current device");
+  if (f.lam_out && !is_device_ptr(f.lam_out, dev)) return fail(KVC_EINVAL, "lam is not device memory");
+  if ((uintptr_t)f.V % 4 || (uintptr_t)f.mean % 4 || (uintptr_t)f.qmin % 4 ||
+      (uintptr_t)f.qstep % 4 || (uintptr_t)f.lam_out % 8 ||
+      (uintptr_t)f.x % (f.dtype == KVC_F32 ? 4 : 2))
+    return fail(KVC_EINVAL, "an array is not aligned to its element size");
+  if ((uintptr_t)workspace % 256) return fail(KVC_EINVAL, "workspace must be 256-byte aligned");
+  if (workspace_bytes < kvc::fit_workspace_bytes(f.B * f.H, f.D, f.r, f.budget))
+    return fail(KVC_EINVAL, "workspace is below kvc_fit_uniform_workspace_bytes()");
+  int nk = 0;
+  e = kvc::launch_fit_uniform(f, workspace, static_cast<cudaStream_t>(stream), &nk);
+  if (e != cudaSuccess) return cuda_fail(e, "fit launch");
+  return succeed();
+}
+
 kvc_status kvc_set_wait_limit(kvc_layer* L, int64_t ns) {
   if (!L) return fail(KVC_ESTATE, "layer is NULL");
   if (ns < 0) return fail(KVC_EINVAL, "wait limit must be >= 0");

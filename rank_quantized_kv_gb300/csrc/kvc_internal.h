@@ -100,6 +100,32 @@ size_t attend_plan(int B, int Hq, int n_slots, int rep, int64_t S, int NCk, int 
 cudaError_t launch_attend(const Params& kp, const Params& vp, AttendArgs a, void* workspace,
                           cudaStream_t s, int* nk);
 
+// On-device prefill fit of the uniform mode (kvc_fit.cu).  Every pointer is
+// device memory; the float64 scratch lives in the caller's workspace.
+constexpr int kFitMaxD = 128;
+constexpr int kFitMaxChoices = 8;
+struct FitArgs {
+  const void* x = nullptr;
+  int dtype = 0;
+  int B = 0, H = 0, D = 0, r = 0;
+  int64_t S = 0;                // fit rows per slot
+  int64_t sb = 0, sh = 0, st = 0;  // element strides of batch, head, token
+  int n_choices = 0;
+  int choices[kFitMaxChoices] = {};  // ascending, distinct
+  int budget = 0;               // bits per token, at most max(choices) * r
+  float* V = nullptr;           // [n_slots][D][r]
+  float* mean = nullptr;        // [n_slots][D]
+  uint8_t* bits = nullptr;      // [n_slots][r]
+  float* qmin = nullptr;        // [n_slots][r]
+  float* qstep = nullptr;       // [n_slots][r]
+  double* lam_out = nullptr;    // [n_slots][D] sorted eigenvalues (may be null)
+  // workspace
+  double *mean64 = nullptr, *lam = nullptr, *lam_sorted = nullptr, *cov = nullptr,
+         *vec = nullptr, *dp = nullptr;
+};
+size_t fit_workspace_bytes(int n_slots, int D, int r, int budget);
+cudaError_t launch_fit_uniform(FitArgs f, void* workspace, cudaStream_t s, int* nk);
+
 // Code histogram of the store (kvc_entropy.cu): counts [n_slots][NC][256]
 // (NC chunk-aligned positions); Huffman code lengths of n symbol counts.
 size_t histogram_bytes(int n_slots, int NC);

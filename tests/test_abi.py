@@ -116,3 +116,36 @@ def test_init_without_device_memory_is_an_error(kvc):
     h = ctypes.c_void_p()
     st = lib.kvc_init_layer(ctypes.byref(desc), ctypes.byref(h))
     assert st in (-1, -4) and not h.value
+
+
+def _fit_desc(kvc, **kw):
+    a = dict(in_dtype=0, B=2, H=3, D=64, S_fit=16, stride_b=3 * 16 * 64, stride_h=16 * 64,
+             stride_t=64, r=8, choices=(0, 2, 4), bit_budget=16)
+    a.update(kw)
+    ch = a.pop("choices")
+    arr = (ctypes.c_int32 * max(len(ch), 1))(*ch)
+    d = kvc._FitDesc(**a, bit_choices=arr, n_choices=len(ch))
+    return d, arr
+
+
+def test_fit_workspace_bytes_and_host_validation(kvc):
+    """kvc_fit_uniform_workspace_bytes validates the descriptor on the host:
+    float64 mean, two eigenvalue arrays, covariance and eigenvectors per slot,
+    plus the DP table of (r + 1) x (budget + 1) entries (the budget clamped at
+    max(choices) * r, beyond which the allocation no longer changes)."""
+    lib = kvc.load_library()
+    n = ctypes.c_size_t()
+    d, keep = _fit_desc(kvc)
+    assert lib.kvc_fit_uniform_workspace_bytes(ctypes.byref(d), ctypes.byref(n)) == 0
+    al = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    ns, D, r, W = 6, 64, 8, 17
+    assert n.value == 3 * al(ns * D * 8) + 2 * al(ns * D * D * 8) + al(ns * (r + 1) * W * 8)
+    d, keep = _fit_desc(kvc, bit_budget=10_000)
+    assert lib.kvc_fit_uniform_workspace_bytes(ctypes.byref(d), ctypes.byref(n)) == 0
+    assert n.value == 3 * al(ns * D * 8) + 2 * al(ns * D * D * 8) + al(ns * (r + 1) * 33 * 8)
+    for bad in (dict(S_fit=1), dict(D=136), dict(D=60), dict(r=0), dict(r=65), dict(in_dtype=3),
+                dict(choices=(5,)), dict(choices=()), dict(choices=(2, 4), bit_budget=15),
+                dict(bit_budget=-1), dict(B=0)):
+        d, keep = _fit_desc(kvc, **bad)
+        assert lib.kvc_fit_uniform_workspace_bytes(ctypes.byref(d), ctypes.byref(n)) == -1, bad
+    assert lib.kvc_fit_uniform_workspace_bytes(None, ctypes.byref(n)) == -1
