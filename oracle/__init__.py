@@ -22,11 +22,14 @@ name the three documentation pages of the VeloxQuant-MLX caches):
   the decoded keys and values of two layers (softmax of the scaled scores,
   weighted sum of the values);
 * ``entropy`` -- order-0 Huffman byte accounting of the stored codes with
-  the fixed-width fallback and the entropy-coding gain.
+  the fixed-width fallback and the entropy-coding gain;
+* ``prod`` -- the TurboQuantProd residual sketch (QJL sign bits and an fp16
+  residual norm over the MSE stage) and the outlier two-stream key store,
+  their decode, score estimate and attention.
 
 Parity pins (tests/test_oracle_*.py) tie every function to something other
 than itself: the bit layouts the turboquant_cache page prints, closed forms,
 Max's 1960 table, brute force and invariants.  No function here is
 "parity unpinned".
 """
-from . import fit, codec, layer, attend, entropy  # noqa: F401
+from . import fit, codec, layer, attend, entropy, prod  # noqa: F401
