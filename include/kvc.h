@@ -291,6 +291,56 @@ kvc_status kvc_code_histogram(kvc_layer *layer, uint32_t *counts, size_t counts_
  * (counts: host, as kvc_code_histogram wrote it for the current length). */
 kvc_status kvc_entropy_bytes(const kvc_layer *layer, const uint32_t *counts, kvc_entropy *out);
 
+/* Residual sketch and outlier two-stream store of a KVC_MODE_CODEBOOK key
+ * layer (turboquant_cache page: the class docstring -- indices at b_mse bits
+ * and QJL sign bits at one bit each; __init__ -- ceil(m / 8) sign bytes, an
+ * fp16 residual norm, the outlier detector's n_outliers channels after
+ * n_calib keys with an int8 row and fp16 scale per key; append_key;
+ * _unpack_signs_block; attend; memory_bytes).  For key t of slot (b, h):
+ *   if n_outliers > 0 and t >= split_from: o = x[channels] is stored as int8
+ *     codes rint(o / s) with s = max(max|o| / 127, 1e-8) and fp16(s), and
+ *     those channels of x are set to 0 (earlier keys: codes 0, scale 0);
+ *   the codebook mode's indices and fp16 norm n16 of (the rest of) x, with
+ *     desc->cb_bits = b_mse (b - 1 bits for a b-bit prod quantiser);
+ *   if m > 0: r = x - n16 R c[idx]; sign bit j = [(S r)_j > 0]; fp16 ||r||.
+ * kvc_fetch returns n16 R c[idx] + sqrt(pi/2)/m ||r||16 S^T (2 bits - 1) plus
+ * the outlier channels' int8 decode; kvc_attend scores with the same sum.
+ * A stored row is [indices | ceil(m/8) sign bytes | n_outliers int8 codes];
+ * its side words are fp16 [n16, ||r|| (m > 0), s (n_outliers > 0)].
+ *
+ *  m            sketch rows (the pages' jl_dim): 0, or a multiple of 16 up to 128.
+ *  S            host fp32 [m][D]: the sketch (seeded N(0, 1) entries, the
+ *               caller's draw).  NULL when m == 0.
+ *  n_outliers   outlier channels per slot: 0 .. min(32, D - 1).
+ *  channels     host int32 [B*H][n_outliers], ascending and distinct in [0, D).
+ *  split_from   first key index that is split (n_calib - 1: the key that
+ *               completes the calibration is split), >= 0.
+ * The key layer must have heads_per_group 1, n_bases 1 and D in {32, 64, 128}. */
+typedef struct {
+  int32_t m;
+  const float *S;
+  int32_t n_outliers;
+  const int32_t *channels;
+  int64_t split_from;
+} kvc_prod_desc;
+
+/* kvc_store_bytes / kvc_init_layer for a codebook key layer with a residual
+ * sketch and/or an outlier stream (prod may not be NULL). */
+kvc_status kvc_store_bytes_prod(const kvc_layer_desc *desc, const kvc_prod_desc *prod,
+                                size_t *out);
+kvc_status kvc_init_layer_prod(const kvc_layer_desc *desc, const kvc_prod_desc *prod,
+                               kvc_layer **out);
+
+/* The outlier channels of every slot from its first n_calib keys (device
+ * work): the n_outliers channels of largest mean |x| (the lower channel first
+ * among equals), ascending, into channels (device int32 [B*H][n_outliers]).
+ * x, in_dtype and strides as for kvc_append_strided; n_calib >= 1;
+ * 1 <= n_outliers <= min(32, D - 1); D <= 256.  Asynchronous on `stream`. */
+kvc_status kvc_fit_outliers(const void *x, int32_t in_dtype, int32_t B, int32_t H, int32_t D,
+                            int64_t n_calib, int64_t stride_b, int64_t stride_h,
+                            int64_t stride_t, int32_t n_outliers, int32_t *channels,
+                            void *stream);
+
 /* On-device prefill fit of the KVC_MODE_UNIFORM parameters (kvtc_cache page:
  * module docstring "Design", prefill step 1, a local PCA per (b, h) fitted
  * in one batched call by KVTCKVCache.update_and_fetch; the module

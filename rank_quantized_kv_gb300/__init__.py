@@ -20,7 +20,8 @@ from ctypes import POINTER, byref, c_float, c_int32, c_int64, c_size_t, c_uint8,
 import numpy as np
 
 __all__ = ["KVCacheLayer", "load_library", "library_path", "KvcError", "MODES", "DTYPES",
-           "EXPORTED_SYMBOLS", "store_bytes", "attend", "attend_workspace_bytes", "fit_uniform"]
+           "EXPORTED_SYMBOLS", "store_bytes", "attend", "attend_workspace_bytes", "fit_uniform",
+           "fit_outliers"]
 
 MODES = {"uniform": 0, "group": 1, "codebook": 2, "int8": 3}
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
@@ -35,7 +36,8 @@ EXPORTED_SYMBOLS = (
     "kvc_get_slot_layout", "kvc_set_path", "kvc_sync_status", "kvc_counters", "kvc_destroy",
     "kvc_append_noalloc", "kvc_set_wait_limit", "kvc_attend", "kvc_attend_workspace_bytes",
     "kvc_code_histogram_bytes", "kvc_code_histogram", "kvc_entropy_bytes",
-    "kvc_fit_uniform_workspace_bytes", "kvc_fit_uniform",
+    "kvc_fit_uniform_workspace_bytes", "kvc_fit_uniform", "kvc_store_bytes_prod",
+    "kvc_init_layer_prod", "kvc_fit_outliers",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -76,6 +78,11 @@ class _FitDesc(ctypes.Structure):
         ("bit_budget", c_int32), ("V", c_void_p), ("mean", c_void_p), ("bits", c_void_p),
         ("qmin", c_void_p), ("qstep", c_void_p), ("lam", c_void_p),
     ]
+
+
+class _ProdDesc(ctypes.Structure):
+    _fields_ = [("m", c_int32), ("S", POINTER(c_float)), ("n_outliers", c_int32),
+                ("channels", POINTER(c_int32)), ("split_from", c_int64)]
 
 
 class _Bytes(ctypes.Structure):
@@ -129,6 +136,11 @@ def load_library():
             "kvc_entropy_bytes": (c_int32, [P, P, POINTER(_Entropy)]),
             "kvc_fit_uniform_workspace_bytes": (c_int32, [POINTER(_FitDesc), POINTER(c_size_t)]),
             "kvc_fit_uniform": (c_int32, [POINTER(_FitDesc), P, c_size_t, P]),
+            "kvc_store_bytes_prod": (c_int32, [POINTER(_Desc), POINTER(_ProdDesc),
+                                               POINTER(c_size_t)]),
+            "kvc_init_layer_prod": (c_int32, [POINTER(_Desc), POINTER(_ProdDesc), POINTER(c_void_p)]),
+            "kvc_fit_outliers": (c_int32, [P, c_int32, c_int32, c_int32, c_int32, c_int64, c_int64,
+                                           c_int64, c_int64, c_int32, P, P]),
             "kvc_sync_status": (c_int32, [P, P]),
             "kvc_counters": (c_int32, [P, POINTER(c_int64), c_int32, P]),
             "kvc_destroy": (None, [P]),
@@ -252,7 +264,8 @@ class KVCacheLayer:
 
     def __init__(self, mode, B, H, D, *, capacity, r=None, V=None, mean=None, bits=None,
                  qmin=None, qstep=None, basis_of=None, heads_per_group=1, group_size=32,
-                 codebook=None, in_dtype="bf16", out_dtype="f16", device=None, path="auto"):
+                 codebook=None, in_dtype="bf16", out_dtype="f16", device=None, path="auto",
+                 sketch=None, outlier_channels=None, split_from=0):
         import torch
 
         lib = load_library()
@@ -268,14 +281,35 @@ class KVCacheLayer:
         desc, keep = _build_desc(mode, B, H, D, r, V, mean, bits, qmin, qstep, basis_of,
                                  heads_per_group, group_size, codebook, in_dtype, out_dtype,
                                  capacity)
+        # codebook keys with a residual sketch S [m, D] and/or outlier channels
+        # [B*H, n_outliers] (kvc_init_layer_prod)
+        self.prod = sketch is not None or outlier_channels is not None
+        pd = None
+        if self.prod:
+            pd = _ProdDesc()
+            if sketch is not None:
+                keep["S"] = _f32(sketch)
+                pd.m = keep["S"].shape[0]
+                pd.S = _ptr(keep["S"], c_float)
+            if outlier_channels is not None:
+                keep["channels"] = np.ascontiguousarray(np.asarray(outlier_channels, dtype=np.int32))
+                pd.n_outliers = keep["channels"].shape[-1]
+                pd.channels = _ptr(keep["channels"], c_int32)
+            pd.split_from = int(split_from)
         n = c_size_t()
-        _check(lib.kvc_store_bytes(byref(desc), byref(n)))
+        if pd is None:
+            _check(lib.kvc_store_bytes(byref(desc), byref(n)))
+        else:
+            _check(lib.kvc_store_bytes_prod(byref(desc), byref(pd), byref(n)))
         self.store = torch.zeros(int(n.value), dtype=torch.uint8, device=self.device)
         desc.store = c_void_p(self.store.data_ptr())
         desc.store_bytes = n.value
         handle = c_void_p()
         with torch.cuda.device(self.device):
-            _check(lib.kvc_init_layer(byref(desc), byref(handle)))
+            if pd is None:
+                _check(lib.kvc_init_layer(byref(desc), byref(handle)))
+            else:
+                _check(lib.kvc_init_layer_prod(byref(desc), byref(pd), byref(handle)))
         self._h = handle
         self._lib = lib
         self.set_path(path)
@@ -468,4 +502,25 @@ def fit_uniform(x, S_fit: int, r: int, choices, budget: int, stream=None):
         _check(lib.kvc_fit_uniform(byref(d), c_void_p(ws.data_ptr()), int(n.value),
                                    _stream_ptr(stream, dev)))
     out["workspace"] = ws  # kept alive until the caller synchronises
+    return out
+
+
+def fit_outliers(x, n_calib: int, n_outliers: int, stream=None):
+    """Outlier channels of every (b, h) from the first n_calib rows of x
+    [B, H, T, D] (kvc_fit_outliers): device int32 [B*H, n_outliers], the
+    channels of largest mean |x| in ascending order."""
+    import torch
+
+    lib = load_library()
+    rev = {v: k for k, v in _torch_dtypes().items()}
+    if x.dim() != 4 or x.dtype not in rev or (x.shape[2] and x.stride(3) != 1):
+        raise ValueError("x must be [B, H, T, D] fp32/fp16/bf16 with a contiguous last dimension")
+    B, H, T, D = x.shape
+    dev = x.device if x.is_cuda else torch.device("cuda", torch.cuda.current_device())
+    out = torch.empty(B * H, n_outliers, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib.kvc_fit_outliers(c_void_p(x.data_ptr()), DTYPES[rev[x.dtype]], B, H, D,
+                                    int(n_calib), x.stride(0), x.stride(1), x.stride(2),
+                                    int(n_outliers), c_void_p(out.data_ptr()),
+                                    _stream_ptr(stream, dev)))
     return out

@@ -67,6 +67,24 @@ bool valid_width(int b) { return b == 0 || b == 1 || b == 2 || b == 3 || b == 4 
 
 namespace kvc {
 
+// Store layout: per slot, payload rows then side words, 256-byte aligned, each
+// region with 16 bytes of slack for vector over-reads.
+static void layout_store(const kvc_layer_desc* d, Geo& g) {
+  g.pay_off.assign(g.n_slots, 0);
+  g.side_off.assign(g.n_slots, 0);
+  int64_t cur = 0;
+  for (int s = 0; s < g.n_slots; ++s) {
+    const int64_t P = d->mode == KVC_MODE_INT8 ? d->D : g.P[g.basis[s]];
+    cur = align_up(cur, 256);
+    g.pay_off[s] = cur;
+    cur += d->capacity * P + 16;
+    cur = align_up(cur, 256);
+    g.side_off[s] = cur;
+    cur += d->capacity * g.side_bytes + 16;
+  }
+  g.store_total = align_up(cur, 256);
+}
+
 kvc_status build_geo(const kvc_layer_desc* d, Geo& g) {
   if (!d) return fail(KVC_EINVAL, "descriptor is NULL");
   if (d->mode < KVC_MODE_UNIFORM || d->mode > KVC_MODE_INT8)
@@ -199,21 +217,7 @@ kvc_status build_geo(const kvc_layer_desc* d, Geo& g) {
     }
   }
 
-  // store layout: per slot, payload rows then side words, 256-byte aligned,
-  // each region with 16 bytes of slack for vector over-reads
-  g.pay_off.assign(g.n_slots, 0);
-  g.side_off.assign(g.n_slots, 0);
-  int64_t cur = 0;
-  for (int s = 0; s < g.n_slots; ++s) {
-    const int64_t P = d->mode == KVC_MODE_INT8 ? d->D : g.P[g.basis[s]];
-    cur = align_up(cur, 256);
-    g.pay_off[s] = cur;
-    cur += d->capacity * P + 16;
-    cur = align_up(cur, 256);
-    g.side_off[s] = cur;
-    cur += d->capacity * g.side_bytes + 16;
-  }
-  g.store_total = align_up(cur, 256);
+  layout_store(d, g);
 
   const int64_t din = g.d_in, r = g.r, nb = g.nb;
   // frozen parameters counted beside the codes: the basis and mean (fp32) of
@@ -229,6 +233,49 @@ kvc_status build_geo(const kvc_layer_desc* d, Geo& g) {
     case KVC_MODE_GROUP: g.fixed = nb * (4 * din * r + 4 * din); break;
     default: g.fixed = 0;
   }
+  return KVC_OK;
+}
+
+// A codebook key layer with a residual sketch and/or an outlier stream: the
+// codebook geometry, then rows [indices | sign bytes | outlier codes] and side
+// words [norm, residual norm, outlier scale].
+kvc_status build_geo_prod(const kvc_layer_desc* d, const kvc_prod_desc* pd, Geo& g) {
+  kvc_status st = build_geo(d, g);
+  if (st) return st;
+  if (!pd) return fail(KVC_EINVAL, "prod descriptor is NULL");
+  if (d->mode != KVC_MODE_CODEBOOK) return fail(KVC_EINVAL, "the residual sketch needs KVC_MODE_CODEBOOK");
+  if (g.nb != 1) return fail(KVC_EINVAL, "the residual sketch needs n_bases == 1");
+  if (d->D != 32 && d->D != 64 && d->D != 128) return fail(KVC_EINVAL, "the residual sketch needs D in {32, 64, 128}");
+  if (pd->m < 0 || pd->m > kProdMaxM || pd->m % 16)
+    return fail(KVC_EINVAL, "m must be a multiple of 16 in [0, %d]", kProdMaxM);
+  if (pd->m && !pd->S) return fail(KVC_EINVAL, "S is NULL");
+  if (pd->n_outliers < 0 || pd->n_outliers > kProdMaxOut || pd->n_outliers >= d->D)
+    return fail(KVC_EINVAL, "n_outliers must be in [0, min(%d, D - 1)]", kProdMaxOut);
+  if (pd->n_outliers && !pd->channels) return fail(KVC_EINVAL, "channels is NULL");
+  if (pd->split_from < 0) return fail(KVC_EINVAL, "split_from must be >= 0");
+  g.S.assign((size_t)pd->m * d->D, 0.f);
+  for (size_t i = 0; i < g.S.size(); ++i) {
+    if (!std::isfinite(pd->S[i])) return fail(KVC_EINVAL, "S has a non-finite entry");
+    g.S[i] = pd->S[i];
+  }
+  g.channels.assign((size_t)g.n_slots * pd->n_outliers, 0);
+  for (int s = 0; s < g.n_slots; ++s)
+    for (int l = 0; l < pd->n_outliers; ++l) {
+      const int32_t c = pd->channels[(size_t)s * pd->n_outliers + l];
+      if (c < 0 || c >= d->D || (l && c <= pd->channels[(size_t)s * pd->n_outliers + l - 1]))
+        return fail(KVC_EINVAL, "channels of slot %d must be ascending and distinct in [0, D)", s);
+      g.channels[(size_t)s * pd->n_outliers + l] = c;
+    }
+  g.prod = 1;
+  g.m = pd->m;
+  g.n_out = pd->n_outliers;
+  g.split_from = pd->split_from;
+  g.code_bytes = g.P[0];
+  g.sign_bytes = (pd->m + 7) / 8;
+  g.P[0] = g.code_bytes + g.sign_bytes + g.n_out;
+  g.side_bytes = 2 * (1 + (g.m > 0) + (g.n_out > 0));
+  layout_store(d, g);
+  g.fixed = 0;
   return KVC_OK;
 }
 
@@ -290,6 +337,43 @@ void build_param_image(const kvc_layer_desc* d, const Geo& g, ParamImage& im) {
   im.oSide = im.put(g.side_off.data(), g.side_off.size());
   im.oErr = im.zeros(sizeof(int));
   im.oCnt = im.zeros(4 * sizeof(unsigned long long));
+  if (g.prod) {
+    // W1 = [R | 0 | S^T from column 128], (S R)^T, W3 = [R^T ; S], row norms
+    // rounded up; S R is formed in float64 and rounded once
+    const int D = d->D, m = g.m;
+    const float* R = d->V;
+    std::vector<float> W1((size_t)D * 256, 0.f), SRt((size_t)D * 128, 0.f),
+        W3((size_t)(D + m) * D, 0.f), sn(std::max(m, 1), 0.f), srn(std::max(m, 1), 0.f);
+    for (int i = 0; i < D; ++i)
+      for (int k = 0; k < D; ++k) {
+        W1[(size_t)i * 256 + k] = R[(size_t)i * D + k];
+        W3[(size_t)k * D + i] = R[(size_t)i * D + k];
+      }
+    for (int j = 0; j < m; ++j) {
+      double s2 = 0.0, sr2 = 0.0;
+      for (int i = 0; i < D; ++i) {
+        const float v = g.S[(size_t)j * D + i];
+        W1[(size_t)i * 256 + 128 + j] = v;
+        W3[(size_t)(D + j) * D + i] = v;
+        s2 += (double)v * v;
+      }
+      for (int k = 0; k < D; ++k) {
+        double acc = 0.0;
+        for (int i = 0; i < D; ++i) acc += (double)g.S[(size_t)j * D + i] * (double)R[(size_t)i * D + k];
+        const float f = (float)acc;
+        SRt[(size_t)k * 128 + j] = f;
+        sr2 += (double)f * f;
+      }
+      sn[j] = std::nextafter((float)(std::sqrt(s2) * (1.0 + 1e-12)), INFINITY);
+      srn[j] = std::nextafter((float)(std::sqrt(sr2) * (1.0 + 1e-12)), INFINITY);
+    }
+    im.oW1 = im.put(W1.data(), W1.size());
+    im.oSRt = im.put(SRt.data(), SRt.size());
+    im.oW3 = im.put(W3.data(), W3.size());
+    im.oSn = im.put(sn.data(), sn.size());
+    im.oSRn = im.put(srn.data(), srn.size());
+    im.oCh = im.put(g.channels.data(), g.channels.size());
+  }
 }
 
 // Device pointers of a parameter block uploaded from `im` at `base`.
@@ -333,6 +417,20 @@ void bind_params(Params& p, const kvc_layer_desc* d, const Geo& g, const ParamIm
   p.side_off = reinterpret_cast<const int64_t*>(base + im.oSide);
   p.err = reinterpret_cast<int*>(base + im.oErr);
   p.counters = reinterpret_cast<unsigned long long*>(base + im.oCnt);
+  if (g.prod) {
+    p.prod = 1;
+    p.m = g.m;
+    p.n_out = g.n_out;
+    p.code_bytes = g.code_bytes;
+    p.sign_bytes = g.sign_bytes;
+    p.split_from = g.split_from;
+    p.W1 = reinterpret_cast<const float*>(base + im.oW1);
+    p.SRt = reinterpret_cast<const float*>(base + im.oSRt);
+    p.W3 = reinterpret_cast<const float*>(base + im.oW3);
+    p.s_norm = reinterpret_cast<const float*>(base + im.oSn);
+    p.sr_norm = reinterpret_cast<const float*>(base + im.oSRn);
+    p.channels = reinterpret_cast<const int32_t*>(base + im.oCh);
+  }
 }
 
 kvc_status set_error(kvc_status s, const char* msg) { return fail(s, "%s", msg); }
@@ -387,12 +485,37 @@ kvc_status kvc_store_bytes(const kvc_layer_desc* desc, size_t* out) {
   return succeed();
 }
 
+static kvc_status init_from_geo(const kvc_layer_desc* d, Geo& g, kvc_layer** out);
+
 kvc_status kvc_init_layer(const kvc_layer_desc* d, kvc_layer** out) {
   if (!out) return fail(KVC_EINVAL, "out is NULL");
   *out = nullptr;
   Geo g;
   kvc_status st = kvc::build_geo(d, g);
   if (st) return st;
+  return init_from_geo(d, g, out);
+}
+
+kvc_status kvc_store_bytes_prod(const kvc_layer_desc* desc, const kvc_prod_desc* prod, size_t* out) {
+  if (!out) return fail(KVC_EINVAL, "out is NULL");
+  Geo g;
+  kvc_status st = kvc::build_geo_prod(desc, prod, g);
+  if (st) return st;
+  *out = (size_t)g.store_total;
+  return succeed();
+}
+
+kvc_status kvc_init_layer_prod(const kvc_layer_desc* d, const kvc_prod_desc* prod, kvc_layer** out) {
+  if (!out) return fail(KVC_EINVAL, "out is NULL");
+  *out = nullptr;
+  Geo g;
+  kvc_status st = kvc::build_geo_prod(d, prod, g);
+  if (st) return st;
+  return init_from_geo(d, g, out);
+}
+
+static kvc_status init_from_geo(const kvc_layer_desc* d, Geo& g, kvc_layer** out) {
+  kvc_status st;
   if (!d->store) return fail(KVC_EINVAL, "store is NULL");
   if ((uintptr_t)d->store % 256) return fail(KVC_EINVAL, "store must be 256-byte aligned");
   if (d->store_bytes < (size_t)g.store_total)
@@ -409,7 +532,7 @@ kvc_status kvc_init_layer(const kvc_layer_desc* d, kvc_layer** out) {
 
   kvc_layer* L = new kvc_layer();
   L->tc = kvc::TcPlan{};
-  st = kvc::tc_prepare(*d, g, im.bytes, L->tc);
+  st = g.prod ? KVC_OK : kvc::tc_prepare(*d, g, im.bytes, L->tc);
   if (st) {
     delete L;
     return st;
@@ -485,6 +608,8 @@ kvc_status kvc_append_strided(kvc_layer* L, const void* x, int64_t T, int64_t sb
   int nk = 0;
   if (L->mode == KVC_MODE_INT8)
     e = kvc::launch_append_int8(L->p, a, s, &nk);
+  else if (L->p.prod)
+    e = kvc::launch_append_prod(L->p, a, s, &nk);
   else if (L->path == KVC_PATH_AUTO && kvc::tc_append_ok(L->tc, L->p, a))
     e = kvc::launch_append_tc(L->tc, L->p, a, L->wait_ns, s, &nk);
   else if (L->path == KVC_PATH_AUTO && kvc::tc_group_ok(L->tc, L->p, a))
@@ -517,6 +642,8 @@ kvc_status kvc_fetch(kvc_layer* L, void* out, int64_t ld_s, int64_t* S_out, void
   int nk = 0;
   if (L->mode == KVC_MODE_INT8)
     e = kvc::launch_fetch_int8(L->p, f, s, &nk);
+  else if (L->p.prod)
+    e = kvc::launch_fetch_prod(L->p, f, s, &nk);
   else if (L->path == KVC_PATH_AUTO && kvc::tc_fetch_ok(L->tc, L->p, f))
     e = kvc::launch_fetch_tc(L->tc, L->p, f, s, &nk);
   else
@@ -586,6 +713,7 @@ kvc_status attend_check(const kvc_layer* K, const kvc_layer* V, int32_t Hq, kvc:
   if (V->mode != KVC_MODE_INT8 && V->mode != KVC_MODE_UNIFORM)
     return fail(KVC_EINVAL, "values must be an int8 or uniform layer");
   if (K->hpg != 1 || V->hpg != 1) return fail(KVC_EINVAL, "head groups are not supported here");
+  if (V->p.prod) return fail(KVC_EINVAL, "values must be an int8 or uniform layer");
   if (K->B != V->B || K->H != V->H || K->D != V->D)
     return fail(KVC_EINVAL, "key and value layers differ in B, H or D");
   if (K->device != V->device) return fail(KVC_EINVAL, "key and value layers are on different devices");
@@ -610,8 +738,15 @@ kvc_status attend_check(const kvc_layer* K, const kvc_layer* V, int32_t Hq, kvc:
     DeviceGuard dg(K->device);
     sms = kvc::sm_count();
   }
+  if (K->p.prod) {
+    a.prod = 1;
+    a.m = K->p.m;
+    a.n_out = K->p.n_out;
+    a.kcode = K->p.code_bytes;
+    a.knw = K->side_bytes / 2;
+  }
   *ws_bytes = kvc::attend_plan(K->B, Hq, K->n_slots, rep, std::max<int64_t>(K->len, 1), a.NCk,
-                               a.Dv, sms, &a.splits, &a.span);
+                               a.Dv, sms, a.m + a.n_out, &a.splits, &a.span);
   return KVC_OK;
 }
 
@@ -668,6 +803,7 @@ kvc_status kvc_code_histogram_bytes(const kvc_layer* L, size_t* out) {
   if (!L) return fail(KVC_ESTATE, "layer is NULL");
   if (!out) return fail(KVC_EINVAL, "out is NULL");
   if (L->mode == KVC_MODE_INT8) return fail(KVC_EINVAL, "int8 layers store no codes");
+  if (L->p.prod) return fail(KVC_EINVAL, "the code histogram takes layers without a sketch or outlier stream");
   *out = kvc::histogram_bytes(L->n_slots, std::max(8, L->ncpos));
   return succeed();
 }
@@ -693,6 +829,7 @@ kvc_status kvc_entropy_bytes(const kvc_layer* L, const uint32_t* counts, kvc_ent
   if (!L) return fail(KVC_ESTATE, "layer is NULL");
   if (!counts || !out) return fail(KVC_EINVAL, "counts or out is NULL");
   if (L->mode == KVC_MODE_INT8) return fail(KVC_EINVAL, "int8 layers store no codes");
+  if (L->p.prod) return fail(KVC_EINVAL, "the code histogram takes layers without a sketch or outlier stream");
   const int NC = std::max(8, L->ncpos);
   int64_t pre = 0, stored = 0;
   for (int s = 0; s < L->n_slots; ++s) {
@@ -799,6 +936,27 @@ kvc_status kvc_fit_uniform(const kvc_fit_desc* d, void* workspace, size_t worksp
   int nk = 0;
   e = kvc::launch_fit_uniform(f, workspace, static_cast<cudaStream_t>(stream), &nk);
   if (e != cudaSuccess) return cuda_fail(e, "fit launch");
+  return succeed();
+}
+
+kvc_status kvc_fit_outliers(const void* x, int32_t in_dtype, int32_t B, int32_t H, int32_t D,
+                            int64_t n_calib, int64_t sb, int64_t sh, int64_t st, int32_t n_out,
+                            int32_t* channels, void* stream) {
+  if (in_dtype != KVC_F32 && in_dtype != KVC_F16 && in_dtype != KVC_BF16)
+    return fail(KVC_EINVAL, "in_dtype must be KVC_F32, KVC_F16 or KVC_BF16");
+  if (B < 1 || H < 1 || D < 2 || D > 256) return fail(KVC_EINVAL, "need B, H >= 1 and 2 <= D <= 256");
+  if (n_calib < 1) return fail(KVC_EINVAL, "n_calib must be >= 1");
+  if (n_out < 1 || n_out > kvc::kProdMaxOut || n_out >= D)
+    return fail(KVC_EINVAL, "n_outliers must be in [1, min(%d, D - 1)]", kvc::kProdMaxOut);
+  if (sb < 0 || sh < 0 || st < 0) return fail(KVC_EINVAL, "strides must be >= 0");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (!x || !channels || !is_device_ptr(x, dev) || !is_device_ptr(channels, dev))
+    return fail(KVC_EINVAL, "x and channels must be device memory of the current device");
+  e = kvc::launch_fit_outliers(x, in_dtype, B, H, D, n_calib, sb, sh, st, n_out, channels,
+                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "outlier fit launch");
   return succeed();
 }
 

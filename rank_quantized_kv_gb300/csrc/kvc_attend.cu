@@ -9,6 +9,10 @@
 //                           q . k_hat = sum_j w_j code_j + c1 with
 //                           w_j = (V^T q)_k step_k and c1 = (V^T q) . lo + q . mean;
 //            codebook keys  k_hat = n R c[idx], so q . k_hat = n sum_k (R^T q)_k c[idx_k];
+//                           with a residual sketch (turboquant_cache page,
+//                           estimate_inner_product) plus
+//                           sqrt(pi/2)/m ||r|| sum_j (S q)_j (2 bit_j - 1), and
+//                           with an outlier stream plus s sum_l q_{ch_l} o8_l;
 //   weights  softmax over the tokens, online and in base 2 (scale log2(e)
 //            folded into w and c1);
 //   output   int8 values    sum_t p_t s_t q8_t;
@@ -149,6 +153,18 @@ __global__ void attend_prep_kernel(const Params kp, const AttendArgs a) {
     w[j] = a.scale_log2 * qv * (uniform ? kp.step[bk] : 1.f);
     if (uniform) part = fmaf(qv, kp.lo[bk], part);
   }
+  if (a.prod) {  // sketch weights sqrt(pi/2)/m (S q)_j, outlier weights q[ch_l]
+    float* wx = a.wx + (size_t)bq * (a.m + a.n_out);
+    const float coef = a.m ? 1.2533141373155003f / (float)a.m : 0.f;
+    for (int j = tid; j < a.m; j += blockDim.x) {
+      const float* srow = kp.W3 + (size_t)(D + j) * D;
+      float sq = 0.f;
+      for (int i = 0; i < D; ++i) sq = fmaf(srow[i], qs[i], sq);
+      wx[j] = a.scale_log2 * coef * sq;
+    }
+    for (int l = tid; l < a.n_out; l += blockDim.x)
+      wx[a.m + l] = a.scale_log2 * qs[kp.channels[(size_t)slot * a.n_out + l]];
+  }
   if (uniform)
     for (int i = tid; i < D; i += blockDim.x) part = fmaf(qs[i], kp.mean[(size_t)beta * D + i], part);
   part = warp_sum(part);
@@ -175,6 +191,7 @@ __global__ void __launch_bounds__(kMainThreads)
   __shared__ uint32_t kch[32], vch[32];
   __shared__ float cbv[256];
   __shared__ float c1s[REP];
+  __shared__ float wxs[(kProdMaxM + kProdMaxOut) * REP];  // sketch, outlier weights [j][g]
   constexpr bool VU = VMODE == KVC_MODE_UNIFORM;
   constexpr int ACC = VU ? 8 : DPL;  // accumulator values per lane and query head
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -204,6 +221,12 @@ __global__ void __launch_bounds__(kMainThreads)
     ws[e] = a.w[(size_t)(bq0 + g) * NCk + j];
   }
   if (tid < REP) c1s[tid] = KMODE == KVC_MODE_UNIFORM ? a.c1[bq0 + tid] : 0.f;
+  const int nx = a.m + a.n_out;
+  if (KMODE == KVC_MODE_CODEBOOK && a.prod)
+    for (int e = tid; e < REP * nx; e += kMainThreads) {
+      const int j = e / REP, g = e - j * REP;
+      wxs[e] = a.wx[(size_t)(bq0 + g) * nx + j];
+    }
   __syncthreads();
   int nchk = 0, nchv = 0;
   while (nchk < 32 && (kch[nchk] >> 31)) ++nchk;
@@ -266,9 +289,44 @@ __global__ void __launch_bounds__(kMainThreads)
         }
       }
       if (KMODE == KVC_MODE_CODEBOOK) {
-        const float n = __half2float(knorm[tb + lane]);
+        const int64_t sw = (tb + lane) * a.knw;  // the key's side words
+        const float n = __half2float(knorm[sw]);
 #pragma unroll
         for (int g = 0; g < REP; ++g) sc[g] *= n;
+        if (a.prod) {
+          if (a.m) {  // + ||r|| sum_j w_j (2 bit_j - 1)
+            const unsigned char* sb = krow + row + a.kcode;
+            float qj[REP];
+#pragma unroll
+            for (int g = 0; g < REP; ++g) qj[g] = 0.f;
+            for (int j8 = 0; j8 < (a.m >> 3); ++j8) {
+              const uint32_t byte = sb[j8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float f = (byte >> e) & 1u ? 1.f : -1.f;
+#pragma unroll
+                for (int g = 0; g < REP; ++g) qj[g] = fmaf(wxs[(8 * j8 + e) * REP + g], f, qj[g]);
+              }
+            }
+            const float gam = __half2float(knorm[sw + 1]);
+#pragma unroll
+            for (int g = 0; g < REP; ++g) sc[g] = fmaf(gam, qj[g], sc[g]);
+          }
+          if (a.n_out) {  // + s sum_l q[ch_l] o8_l
+            const int8_t* o8 = reinterpret_cast<const int8_t*>(krow + row + a.kcode + (a.m >> 3));
+            float qo[REP];
+#pragma unroll
+            for (int g = 0; g < REP; ++g) qo[g] = 0.f;
+            for (int l = 0; l < a.n_out; ++l) {
+              const float v = (float)o8[l];
+#pragma unroll
+              for (int g = 0; g < REP; ++g) qo[g] = fmaf(wxs[(a.m + l) * REP + g], v, qo[g]);
+            }
+            const float os = __half2float(knorm[sw + a.knw - 1]);
+#pragma unroll
+            for (int g = 0; g < REP; ++g) sc[g] = fmaf(os, qo[g], sc[g]);
+          }
+        }
       }
     } else {
 #pragma unroll
@@ -470,7 +528,7 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 }  // namespace
 
 size_t attend_plan(int B, int Hq, int n_slots, int rep, int64_t S, int NCk, int Dv, int sms,
-                   int* splits, int64_t* span) {
+                   int extra, int* splits, int64_t* span) {
   // enough CTAs for about four per SM, at least 128 tokens each (a multiple of
   // 128 so that every warp's 32-token blocks start at a multiple of 32)
   const int64_t max_splits = std::max<int64_t>(1, (S + 127) / 128);
@@ -483,7 +541,8 @@ size_t attend_plan(int B, int Hq, int n_slots, int rep, int64_t S, int NCk, int 
   const size_t w = align256((size_t)B * Hq * NCk * 4);
   const size_t c1 = align256((size_t)B * Hq * 4);
   const size_t part = align256((size_t)n_slots * (*splits) * rep * (2 + Dv) * 4);
-  return w + c1 + part;
+  const size_t wx = align256((size_t)B * Hq * extra * 4);
+  return w + c1 + part + wx;
 }
 
 cudaError_t launch_attend(const Params& kp, const Params& vp, AttendArgs a, void* workspace,
@@ -493,6 +552,8 @@ cudaError_t launch_attend(const Params& kp, const Params& vp, AttendArgs a, void
   a.w = static_cast<float*>(workspace);
   a.c1 = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + wbytes);
   a.part = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + wbytes + cbytes);
+  const size_t pbytes = align256((size_t)kp.n_slots * a.splits * a.rep * (2 + a.Dv) * 4);
+  a.wx = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + wbytes + cbytes + pbytes);
   attend_prep_kernel<<<(unsigned)(kp.B * a.Hq), 128, 0, s>>>(kp, a);
   ++*nk;
   cudaError_t e = cudaGetLastError();

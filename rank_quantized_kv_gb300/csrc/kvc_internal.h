@@ -50,6 +50,18 @@ struct Params {
 
   int* err;                        // device error word
   unsigned long long* counters;    // [4]
+
+  // Residual sketch and outlier stream of a codebook key layer (kvc_prod.cu);
+  // prod == 0 elsewhere.  Row: [codes | sign bits | outlier int8]; side words
+  // [norm, residual norm (m > 0), outlier scale (n_out > 0)] in fp16.
+  int prod = 0, m = 0, n_out = 0, code_bytes = 0, sign_bytes = 0;
+  int64_t split_from = 0;
+  const float* W1 = nullptr;       // [D][256]: R | S^T | 0
+  const float* SRt = nullptr;      // [D][128]: (S R)^T, zero columns beyond m
+  const float* W3 = nullptr;       // [D + m][D]: R^T over S
+  const float* s_norm = nullptr;   // [m] ||S_j||_2, rounded up
+  const float* sr_norm = nullptr;  // [m] ||(S R)_j||_2, rounded up
+  const int32_t* channels = nullptr;  // [n_slots][n_out] ascending
 };
 
 struct AppendArgs {
@@ -93,10 +105,16 @@ struct AttendArgs {
   float* w = nullptr;        // workspace: [B Hq][NCk] key weights
   float* c1 = nullptr;       // workspace: [B Hq] score offsets
   float* part = nullptr;     // workspace: [n_slots][splits][rep][2 + Dv] partials
+  // keys with a residual sketch and/or an outlier stream
+  int prod = 0, m = 0, n_out = 0;
+  int kcode = 0;             // code bytes of a key row (the sign bytes follow)
+  int knw = 1;               // fp16 side words per key
+  float* wx = nullptr;       // workspace: [B Hq][m + n_out] sketch and outlier weights
 };
 // Workspace bytes (and the split) of an attention call; the launcher.
+// extra: sketch rows plus outlier channels of the keys (0 without them).
 size_t attend_plan(int B, int Hq, int n_slots, int rep, int64_t S, int NCk, int Dv, int sms,
-                   int* splits, int64_t* span);
+                   int extra, int* splits, int64_t* span);
 cudaError_t launch_attend(const Params& kp, const Params& vp, AttendArgs a, void* workspace,
                           cudaStream_t s, int* nk);
 
@@ -126,6 +144,16 @@ struct FitArgs {
 size_t fit_workspace_bytes(int n_slots, int D, int r, int budget);
 cudaError_t launch_fit_uniform(FitArgs f, void* workspace, cudaStream_t s, int* nk);
 
+// Residual-sketch / outlier-stream codebook keys (kvc_prod.cu).
+constexpr int kProdMaxD = 128;
+constexpr int kProdMaxM = 128;
+constexpr int kProdMaxOut = 32;
+cudaError_t launch_append_prod(const Params& p, const AppendArgs& a, cudaStream_t s, int* nk);
+cudaError_t launch_fetch_prod(const Params& p, const FetchArgs& f, cudaStream_t s, int* nk);
+cudaError_t launch_fit_outliers(const void* x, int dt, int B, int H, int D, int64_t n, int64_t sb,
+                                int64_t sh, int64_t st, int n_out, int32_t* channels,
+                                cudaStream_t s);
+
 // Code histogram of the store (kvc_entropy.cu): counts [n_slots][NC][256]
 // (NC chunk-aligned positions); Huffman code lengths of n symbol counts.
 size_t histogram_bytes(int n_slots, int NC);
@@ -143,6 +171,11 @@ struct Geo {
   std::vector<int64_t> pay_off, side_off;
   int64_t store_total = 0;
   int64_t fixed = 0;
+  // residual sketch / outlier stream (kvc_init_layer_prod)
+  int prod = 0, m = 0, n_out = 0, code_bytes = 0, sign_bytes = 0;
+  int64_t split_from = 0;
+  std::vector<float> S;             // [m][D]
+  std::vector<int32_t> channels;    // [n_slots][n_out]
 };
 
 // Host image of a layer's parameter block: arrays appended at 256-byte
@@ -151,7 +184,8 @@ struct ParamImage {
   std::vector<uint8_t> bytes;
   size_t oV = 0, oVt = 0, oMean = 0, oLo = 0, oStep = 0, oInv = 0, oVn = 0, oBits = 0,
          oOrder = 0, oSeg = 0, oP = 0, oKept = 0, oGroups = 0, oCb = 0, oMids = 0, oBasis = 0,
-         oPay = 0, oSide = 0, oErr = 0, oCnt = 0;
+         oPay = 0, oSide = 0, oErr = 0, oCnt = 0, oW1 = 0, oSRt = 0, oW3 = 0, oSn = 0, oSRn = 0,
+         oCh = 0;
   template <class T>
   size_t put(const T* src, size_t n) {
     const size_t off = (bytes.size() + 255) / 256 * 256;
@@ -169,6 +203,7 @@ struct ParamImage {
 // Validate a descriptor and derive its layout; on failure the message is
 // available from kvc_last_error().
 kvc_status build_geo(const kvc_layer_desc* d, Geo& g);
+kvc_status build_geo_prod(const kvc_layer_desc* d, const kvc_prod_desc* pd, Geo& g);
 void build_param_image(const kvc_layer_desc* d, const Geo& g, ParamImage& im);
 void bind_params(Params& p, const kvc_layer_desc* d, const Geo& g, const ParamImage& im,
                  uint8_t* base);

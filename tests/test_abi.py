@@ -149,3 +149,43 @@ def test_fit_workspace_bytes_and_host_validation(kvc):
         d, keep = _fit_desc(kvc, **bad)
         assert lib.kvc_fit_uniform_workspace_bytes(ctypes.byref(d), ctypes.byref(n)) == -1, bad
     assert lib.kvc_fit_uniform_workspace_bytes(None, ctypes.byref(n)) == -1
+
+
+def test_prod_descriptor_host_validation(kvc):
+    """kvc_store_bytes_prod sizes rows [indices | sign bytes | outlier codes]
+    and fp16 side words [norm, residual norm, outlier scale], and rejects bad
+    sketch or outlier fields before anything touches a device."""
+    lib = kvc.load_library()
+    rng = np.random.default_rng(5)
+    D, B, H, cap = 64, 1, 2, 10
+    R = np.linalg.qr(rng.standard_normal((D, D)))[0].astype(np.float32)
+    cb = np.array([-0.2, -0.05, 0.05, 0.2], dtype=np.float32)
+    desc, keep = kvc._build_desc("codebook", B, H, D, None, R, None, None, None, None, None, 1,
+                                 32, cb, "f16", "f16", cap)
+    S = rng.standard_normal((32, D)).astype(np.float32)
+    ch = np.array([[3, 9, 40], [0, 1, 63]], dtype=np.int32)
+
+    def prod_desc(m=32, S=S, n_out=3, ch=ch, split=0):
+        pd = kvc._ProdDesc()
+        pd.m, pd.n_outliers, pd.split_from = m, n_out, split
+        pd.S = S.ctypes.data_as(ctypes.POINTER(ctypes.c_float)) if S is not None else None
+        pd.channels = ch.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if ch is not None else None
+        return pd
+
+    n = ctypes.c_size_t()
+    pd = prod_desc()
+    assert lib.kvc_store_bytes_prod(ctypes.byref(desc), ctypes.byref(pd), ctypes.byref(n)) == 0
+    P = D * 2 // 8 + 32 // 8 + 3
+    al = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    per_slot = al(cap * P + 16) + al(cap * 6 + 16)
+    assert n.value == B * H * per_slot
+    bad = [prod_desc(m=24), prod_desc(m=144), prod_desc(S=None), prod_desc(n_out=64),
+           prod_desc(ch=np.array([[3, 3, 40], [0, 1, 63]], dtype=np.int32)),
+           prod_desc(ch=np.array([[3, 9, 64], [0, 1, 63]], dtype=np.int32)), prod_desc(split=-1)]
+    for pd in bad:
+        assert lib.kvc_store_bytes_prod(ctypes.byref(desc), ctypes.byref(pd), ctypes.byref(n)) == -1
+    assert lib.kvc_store_bytes_prod(ctypes.byref(desc), None, ctypes.byref(n)) == -1
+    udesc, ukeep = kvc._build_desc("uniform", B, H, D, None, R[:, :8], None, np.full(8, 2),
+                                   np.zeros(8), np.ones(8), None, 1, 32, None, "f16", "f16", cap)
+    pd = prod_desc()
+    assert lib.kvc_store_bytes_prod(ctypes.byref(udesc), ctypes.byref(pd), ctypes.byref(n)) == -1
