@@ -53,6 +53,11 @@ WORKLOADS = {
     # tiny KVTC-style correctness case: fp32, prefill 64 then 16 single-token appends
     "kvtc-tiny": dict(B=1, H=2, D=64, S=80, fit=64, r=16, choices=(0, 1, 2, 4, 8), budget=48,
                       mode="uniform", dtype="f32", alpha=0.8, seed=1000, outliers=0),
+    # the TurboQuant workload with the prod quantiser's keys: b = 3 bits split as
+    # 2-bit codebook indices plus a 128-row residual sketch, and 8 outlier
+    # channels per (b, h) calibrated on the first 128 keys
+    "turboquant-prod": dict(B=16, H=8, D=128, S=16384, mode="codebook", dtype="f16",
+                            prod=dict(b_mse=2, m=128, n_out=8, n_calib=128)),
     # Llama-3-70B-like KV shape, uniform all-b allocation (one sweep point)
     "sweep": dict(B=8, H=8, D=128, S=8192, r=32, bits=4, mode="uniform", dtype="bf16"),
 }
@@ -175,7 +180,18 @@ def build_layers(wl, dev):
             L = kvc.KVCacheLayer("group", B, H, D, in_dtype="bf16", capacity=S, device=dev,
                                  **params)
         elif wl["mode"] == "codebook":
-            if tensor == 0:
+            pr = wl.get("prod")
+            if tensor == 0 and pr:
+                x = synth.heavy_tailed_keys(B, H, S, D, seed=4000, dtype="f16", device=dev)
+                ch = kvc.fit_outliers(x, pr["n_calib"], pr["n_out"]).cpu().numpy()
+                sketch = np.random.default_rng(1235).standard_normal((pr["m"], D)).astype(
+                    np.float32)
+                L = kvc.KVCacheLayer(
+                    "codebook", B, H, D, in_dtype="f16", capacity=S, device=dev,
+                    V=calib.rotation(D, 1234),
+                    codebook=calib.gaussian_codebook(pr["b_mse"], 1 / math.sqrt(D)),
+                    sketch=sketch, outlier_channels=ch, split_from=pr["n_calib"] - 1)
+            elif tensor == 0:
                 x = synth.heavy_tailed_keys(B, H, S, D, seed=4000, dtype="f16", device=dev)
                 L = kvc.KVCacheLayer("codebook", B, H, D, in_dtype="f16", capacity=S, device=dev,
                                      V=calib.rotation(D, 1234),
@@ -416,7 +432,46 @@ def extra_configs(dev, flush, peaks, steps):
         res[name] = entry
         del layers, inputs, outs
         torch.cuda.empty_cache()
+    res["turboquant-prod"] = prod_config(dev, flush, peaks, steps)
     return res
+
+
+def prod_config(dev, flush, peaks, steps):
+    """The TurboQuant workload with residual-sketch / outlier-stream keys: bulk
+    append and fetch of both tensors, and decode attention on the codes.  The
+    key kernels run on the CUDA cores: their roofline is the fp32 FMA rate
+    (152 SMs x 128 lanes x 2 flops x the SM clock)."""
+    import torch
+
+    wl = WORKLOADS["turboquant-prod"]
+    pr = wl["prod"]
+    B, H, D, S = wl["B"], wl["H"], wl["D"], wl["S"]
+    layers, inputs = build_layers(wl, dev)
+    outs = [torch.empty(B, H, S, D, dtype=torch.float16, device=dev) for _ in layers]
+    time_steps(layers, inputs, outs, 3, flush)
+    n = max(3, min(steps, 20))
+    _, app_ms, fet_ms = time_steps(layers, inputs, outs, n, flush)
+    entry = {"ops": op_table(wl, layers, app_ms, fet_ms, n, peaks), "steps": n}
+    sm_mhz = max((c for c in [peaks.get("sm_mhz")] if c), default=2070.0)
+    alu = 152 * 128 * 2 * sm_mhz * 1e6
+    tokens = B * H * S
+    m = pr["m"]
+    fl_app = 2.0 * tokens * (D * (128 + 128) + D * 128)   # x W1 (padded), c (S R)^T
+    fl_fet = 2.0 * tokens * (D + m) * D                   # A [R^T ; S]
+    ta, tf = app_ms[0] / n / 1e3, fet_ms[0] / n / 1e3
+    entry["keys_alu"] = {
+        "bound": "alu", "peak_tflops": alu / 1e12, "peak_source": "152 SMs x 128 fp32 lanes x 2 "
+        "flops x SM clock", "append_flops": fl_app, "fetch_flops": fl_fet,
+        "append_frac": fl_app / ta / alu, "fetch_frac": fl_fet / tf / alu}
+    entry["attend"] = attend_op(layers, flush, peaks, reps=max(5, min(steps, 20)))
+    for L in layers:
+        if L.sync_status() != 0:
+            raise RuntimeError("device error in turboquant-prod")
+    entry["shape"] = (f"B {B}, H {H}, D {D}, S {S}; keys: 2-bit indices, {m}-row sketch, "
+                      f"{pr['n_out']} outlier channels after {pr['n_calib']} keys; values int8")
+    del layers, inputs, outs
+    torch.cuda.empty_cache()
+    return entry
 
 
 def gpu_arm(args, rank, world):
@@ -610,7 +665,21 @@ def _oracle_sample(wl, n_slots_sample):
                 np.float32).astype(np.float64), mean=mean.astype(np.float32).astype(np.float64),
                 bits=bits, group_size=32)
         elif wl["mode"] == "codebook":
-            if tensor == 0:
+            pr = wl.get("prod")
+            if tensor == 0 and pr:
+                from oracle import prod
+
+                x = synth.heavy_tailed_keys(1, n_slots_sample, S, D, seed=4000, dtype="f16")
+                x64 = x.double().numpy()
+                ch = np.stack([prod.outlier_channels(x64[0, h, :pr["n_calib"]], pr["n_out"])
+                               for h in range(n_slots_sample)])
+                L = prod.ProdKeyLayer(
+                    1, n_slots_sample, D, R=fit.seeded_rotation(D, 1234).astype(np.float32),
+                    centroids=fit.lloyd_max_gaussian(1 << pr["b_mse"], 1 / math.sqrt(D)).astype(
+                        np.float32),
+                    S=np.random.default_rng(1235).standard_normal((pr["m"], D)).astype(np.float32),
+                    channels=ch, split_from=pr["n_calib"] - 1)
+            elif tensor == 0:
                 x = synth.heavy_tailed_keys(1, n_slots_sample, S, D, seed=4000, dtype="f16")
                 L = OracleLayer("codebook", 1, n_slots_sample, D,
                                 V=fit.seeded_rotation(D, 1234).astype(np.float32),

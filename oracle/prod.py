@@ -213,6 +213,17 @@ class ProdKeyLayer:
         self.len += x.shape[2]
         return self.len
 
+    def trim(self, n: int) -> int:
+        """Drop the n most recent keys (clamped to the length); the sketch,
+        channels and split point stay, as ``OracleLayer.trim`` keeps its fit."""
+        n = min(self.len, int(n))
+        if n <= 0:
+            return 0
+        self.len -= n
+        self.enc = [None if e is None or self.len == 0 else {k: v[: self.len] for k, v in e.items()}
+                    for e in self.enc]
+        return n
+
     def rows(self, s):
         """Packed rows [len, row_bytes] uint8 and side words [len, k] fp16 of slot s (P6)."""
         e = self.enc[s]

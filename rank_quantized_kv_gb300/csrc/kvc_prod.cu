@@ -117,24 +117,91 @@ __device__ __forceinline__ void gemm_rows(const float* As, int lda, const float*
   }
 }
 
+// The same product with B staged through shared memory in chunks of kBlk
+// rows (Bs: kBlk x NC floats, NC the columns staged, a multiple of 8), the
+// next chunk's global loads in flight while the current one is used.  The
+// thread's 8 columns are c0 .. c0 + 3 and NC/2 + c0 .. NC/2 + c0 + 3 (c0 a
+// multiple of 4), so a warp's 16-byte reads of a B row are contiguous.  Every
+// thread of the CTA calls it (it synchronises).
+template <int TM, int NC>
+__device__ __forceinline__ void gemm_staged(const float* As, int lda, const float* __restrict__ B,
+                                            int ldb, int K, float* Bs, int r0, int c0,
+                                            float (&acc)[TM][8]) {
+  constexpr int kVec = kBlk * NC / 4;                    // float4s per chunk
+  constexpr int kPer = (kVec + kPThreads - 1) / kPThreads;
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  float4 pre[kPer];
+  auto fetch = [&](int k0) {
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int v = tid + q * kPThreads;
+      if (v < kVec) {
+        const int rr = v / (NC / 4), cc = v - rr * (NC / 4);
+        pre[q] = __ldg(reinterpret_cast<const float4*>(B + (size_t)(k0 + rr) * ldb) + cc);
+      }
+    }
+  };
+  fetch(0);
+  for (int k0 = 0; k0 < K; k0 += kBlk) {
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int v = tid + q * kPThreads;
+      if (v < kVec) reinterpret_cast<float4*>(Bs)[v] = pre[q];
+    }
+    __syncthreads();
+    if (k0 + kBlk < K) fetch(k0 + kBlk);
+    float part[TM][8];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) part[i][j] = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < kBlk; ++k) {
+      const float4 b0 = *reinterpret_cast<const float4*>(Bs + k * NC + c0);
+      const float4 b1 = *reinterpret_cast<const float4*>(Bs + k * NC + NC / 2 + c0);
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < TM; ++i) {
+        const float a = As[(r0 + i) * lda + k0 + k];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) part[i][j] = fmaf(a, bv[j], part[i][j]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] += part[i][j];
+    __syncthreads();  // the chunk is overwritten next
+  }
+}
+
 // Shared-memory layout of the append tile (floats unless noted).
 struct AppSmem {
   static constexpr int xs = 0;                          // [kTT][D] x with outliers zeroed
   static constexpr int zy = xs + kTT * kProdMaxD;       // [kTT][kW1] z | S x; (S R) c over z
-  static constexpr int cs = zy + kTT * kW1;             // [kTT][D] c[idx]
-  static constexpr int tok = cs + kTT * kProdMaxD;      // [kTT][8] per-token scalars
-  static constexpr int rr = tok + kTT * 8;              // [8 warps][2][D] residual (hi, lo)
-  static constexpr int nfloats = rr + 8 * 2 * kProdMaxD;
+  static constexpr int cs = zy + kTT * kW1;             // [kTT][D + 4] c[idx] (padded rows)
+  static constexpr int tok = cs + kTT * (kProdMaxD + 4);  // [kTT][8] per-token scalars
+  // scratch: the staged B chunks of the products, then the residuals of the
+  // exact sign decisions ([8 warps][2][D]) and the sign queue (int [kTT m + 1])
+  static constexpr int scr = tok + kTT * 8;
+  static constexpr int rr = scr;
+  static constexpr int nscr = 8 * 2 * kProdMaxD + (kTT * kProdMaxM + 1);
+  static constexpr int nfloats = scr + (nscr > kBlk * kW1 ? nscr : kBlk * kW1);
   static constexpr int idx_b = nfloats * 4;             // bytes: [kTT][D] centroid indices
   static constexpr int sgn_b = idx_b + kTT * kProdMaxD;  // [kTT][m] sign bits
   static constexpr int o8_b = sgn_b + kTT * kProdMaxM;  // [kTT][n_out] outlier codes
-  static constexpr int q_b = o8_b + kTT * kProdMaxOut;  // int [kTT * kProdMaxM + 1] sign queue
-  static constexpr int row_b = q_b + 4 * (kTT * kProdMaxM + 1);  // [kTT][P] staged rows
+  static constexpr int q_b = (rr + 8 * 2 * kProdMaxD) * 4;  // the sign queue, inside scr
+  static constexpr int row_b = o8_b + kTT * kProdMaxOut;  // [kTT][P] staged rows
   static constexpr int bytes(int P) { return row_b + kTT * P + 16; }
 };
 // per-token scalars in AppSmem::tok
 enum { kN32 = 0, kN16, kNB, kCN, kZC, kG16, kOS, kValid };
 
+template <int D>
 __global__ void __launch_bounds__(kPThreads, 2) append_prod_kernel(const Params p, const AppendArgs a) {
   extern __shared__ __align__(16) unsigned char sm[];
   float* fsm = reinterpret_cast<float*>(sm);
@@ -148,22 +215,26 @@ __global__ void __launch_bounds__(kPThreads, 2) append_prod_kernel(const Params 
   int* queue = reinterpret_cast<int*>(sm + AppSmem::q_b);
   uint8_t* row_s = sm + AppSmem::row_b;
 
-  const int D = p.D, m = p.m, nout = p.n_out, L = p.cb_levels;
+  constexpr int CS = D + 4;  // row stride of cs: rows 2 apart fall in different banks
+  const int m = p.m, nout = p.n_out, L = p.cb_levels;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slot = blockIdx.y;
   const int64_t t0 = (int64_t)blockIdx.x * kTT;
   const int nt = (int)min((int64_t)kTT, a.T - t0);
   const int b = slot / p.H, h = slot - b * p.H;
   const int64_t xbase = (int64_t)b * a.sb + (int64_t)h * a.sh;
-  const float* cb = p.codebook;
-  const float* mids = p.mids;
+  __shared__ float cb[256], mids[256], vn[kProdMaxD];
+  for (int j = tid; j < L; j += kPThreads) {
+    cb[j] = p.codebook[j];
+    if (j + 1 < L) mids[j] = p.mids[j];
+  }
+  for (int k = tid; k < D; k += kPThreads) vn[k] = p.vnorm[k];
 
   // 1. rows (fp32; rows past the call's end are zero)
   for (int e = tid; e < kTT * D; e += kPThreads) {
     const int t = e / D, i = e - t * D;
     xs[t * D + i] = t < nt ? load_in(a.x, p.in_dtype, xbase + (t0 + t) * a.st + i) : 0.f;
   }
-  if (tid == 0) queue[kTT * kProdMaxM] = 0;
   __syncthreads();
 
   // 2. outlier split and 3. norms, one warp per token
@@ -180,22 +251,35 @@ __global__ void __launch_bounds__(kPThreads, 2) append_prod_kernel(const Params 
         v = split ? x[ch] : 0.f;
       }
       const float amax = warp_maxf(fabsf(v));
-      double s64 = 0.0;
+      // s = max(amax / 127, 1e-8) as float64 computes it; amax < 2e-6 (the
+      // floor, subnormal scales) takes float64 throughout
+      const bool tiny_o = amax < 2e-6f;
+      float s16 = 0.f;
       if (split) {
-        s64 = fmax((double)amax / 127.0, 1e-8);
-        const float inv = (float)(1.0 / s64);
-        const float u = v * inv;  // within 1.5e-5 of v / s
-        const float au = fabsf(u);
-        float q = rintf(u);
-        if (fabsf(au - floorf(au) - 0.5f) < 1e-4f || amax < 2e-6f) q = (float)rint((double)v / s64);
+        float q;
+        if (tiny_o) {
+          q = (float)rint((double)v / fmax((double)amax / 127.0, 1e-8));
+        } else {
+          const float u = v * (127.f / amax);  // within 1.5e-5 of v / s
+          const float au = fabsf(u);
+          q = rintf(u);
+          if (fabsf(au - floorf(au) - 0.5f) < 1e-4f) q = (float)rint((double)v / ((double)amax / 127.0));
+        }
         if (lane < nout) o8_s[t * kProdMaxOut + lane] = (int8_t)fminf(fmaxf(q, -127.f), 127.f);
+        // fp16(s): fl32(amax / 127) and float64's value both lie within 2u of
+        // amax / 127, so one fp16 for that interval decides it
+        const float s32 = amax / 127.f;
+        if (!tiny_o && same_half(s32 * (1.f - 2.f * kU), s32 * (1.f + 2.f * kU)))
+          s16 = __half2float(__float2half_rn(s32));
+        else
+          s16 = __half2float(__double2half(fmax((double)amax / 127.0, 1e-8)));
       } else if (lane < nout) {
         o8_s[t * kProdMaxOut + lane] = 0;
       }
       __syncwarp();
       if (split && lane < nout) x[ch] = 0.f;
       __syncwarp();
-      if (lane == 0) tk[t * 8 + kOS] = split ? __half2float(__double2half(s64)) : 0.f;
+      if (lane == 0) tk[t * 8 + kOS] = s16;
     }
     // ||x||: lane-sequential sums and a 5-level tree: |error| <= gamma_{D/32+5} ||x||^2
     float s2 = 0.f;
@@ -226,11 +310,13 @@ __global__ void __launch_bounds__(kPThreads, 2) append_prod_kernel(const Params 
   {
     const int tx = tid & 31, ty = tid >> 5;
     float acc[4][8];
-    gemm_rows<4>(xs, D, p.W1, kW1, D, 4 * ty, 8 * tx, acc);
+    gemm_staged<4, kW1>(xs, D, p.W1, kW1, D, fsm + AppSmem::scr, 4 * ty, 4 * tx, acc);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) zy[(4 * ty + i) * kW1 + 8 * tx + j] = acc[i][j];
+    for (int i = 0; i < 4; ++i) {
+      float* o = zy + (4 * ty + i) * kW1 + 4 * tx;
+      *reinterpret_cast<float4*>(o) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      *reinterpret_cast<float4*>(o + kW1 / 2) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    }
   }
   __syncthreads();
 
@@ -251,7 +337,7 @@ __global__ void __launch_bounds__(kPThreads, 2) append_prod_kernel(const Params 
     }
     int idx = lo;
     // |u32 - z / ||x|| | <= gamma_z ||R_k|| + (gamma_n / 2 + 2u) |u32|
-    const float del = 1.02f * (gz * p.vnorm[k] + (0.5f * gn + 2.f * kU) * fabsf(u)) + 1e-30f;
+    const float del = 1.02f * (gz * vn[k] + (0.5f * gn + 2.f * kU) * fabsf(u)) + 1e-30f;
     const bool near = (idx > 0 && u - mids[idx - 1] <= del) || (idx < L - 1 && mids[idx] - u <= del);
     if ((near || tiny) && tk[t * 8 + kValid] != 0.f) {
       // float64: z and ||x|| summed in float64, then the oracle's comparison
@@ -259,7 +345,7 @@ __global__ void __launch_bounds__(kPThreads, 2) append_prod_kernel(const Params 
       const float* x = xs + t * D;
       double z64 = 0.0, n2 = 0.0;
       for (int i = 0; i < D; ++i) {
-        z64 = fma((double)x[i], (double)p.V[(size_t)i * D + k], z64);
+        z64 = fma((double)x[i], (double)p.Vt[(size_t)k * D + i], z64);
         n2 = fma((double)x[i], (double)x[i], n2);
       }
       const double u64 = n2 > 0.0 ? z64 / sqrt(n2) : 0.0;
@@ -276,7 +362,7 @@ __global__ void __launch_bounds__(kPThreads, 2) append_prod_kernel(const Params 
       ++n_ref_code;
     }
     idx_s[t * kProdMaxD + k] = (uint8_t)idx;
-    cs[t * D + k] = cb[idx];
+    cs[t * CS + k] = cb[idx];
   }
   __syncthreads();
 
@@ -286,7 +372,7 @@ __global__ void __launch_bounds__(kPThreads, 2) append_prod_kernel(const Params 
   for (int t = warp; t < kTT; t += kPThreads / 32) {
     float c2 = 0.f, zc = 0.f, x2 = 0.f;
     for (int k = lane; k < D; k += 32) {
-      const float c = cs[t * D + k];
+      const float c = cs[t * CS + k];
       c2 = fmaf(c, c, c2);
       zc = fmaf(zy[t * kW1 + k], c, zc);
       x2 = fmaf(xs[t * D + k], xs[t * D + k], x2);
@@ -307,19 +393,22 @@ __global__ void __launch_bounds__(kPThreads, 2) append_prod_kernel(const Params 
   if (m) {
     const int tx = tid & 15, ty = tid >> 4;  // tokens 2 ty, 2 ty + 1; columns 8 tx ..
     float acc[2][8];
-    gemm_rows<2>(cs, D, p.SRt, kW2, D, 2 * ty, 8 * tx, acc);
-    __syncthreads();
+    gemm_staged<2, kW2>(cs, CS, p.SRt, kW2, D, fsm + AppSmem::scr, 2 * ty, 4 * tx, acc);
+    if (tid == 0) queue[kTT * kProdMaxM] = 0;  // the scratch holds the queue from here
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) zy[(2 * ty + i) * kW1 + 8 * tx + j] = acc[i][j];
+    for (int i = 0; i < 2; ++i) {
+      float* o = zy + (2 * ty + i) * kW1 + 4 * tx;
+      *reinterpret_cast<float4*>(o) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      *reinterpret_cast<float4*>(o + kW2 / 2) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    }
     __syncthreads();
 
     // 8. sign bits: s_j = (S x)_j - n16 ((S R) c)_j, with
     //    |s32 - s| <= gamma_z ||S_j|| ||x|| + n16 (gamma_z + 2u) ||(S R)_j|| ||c||
     //                 + u n16 |(S R c)_j| + u |s32|
-    for (int e = tid; e < kTT * m; e += kPThreads) {
-      const int t = e / m, j = e - t * m;
+    for (int e = tid; e < kTT * kProdMaxM; e += kPThreads) {
+      const int t = e >> 7, j = e & (kProdMaxM - 1);
+      if (j >= m) continue;
       const float y = zy[t * kW1 + kY + j], tq = zy[t * kW1 + j];
       const float n16 = tk[t * 8 + kN16];
       const float s = fmaf(-n16, tq, y);
@@ -329,7 +418,7 @@ __global__ void __launch_bounds__(kPThreads, 2) append_prod_kernel(const Params 
       uint8_t bit = s > 0.f ? 1 : 0;
       if (fabsf(s) <= tau && tk[t * 8 + kValid] != 0.f) {
         const int qi = atomicAdd(&queue[kTT * kProdMaxM], 1);
-        queue[qi] = e;
+        queue[qi] = t * m + j;
       }
       sgn_s[t * kProdMaxM + j] = bit;
     }
@@ -349,7 +438,7 @@ __global__ void __launch_bounds__(kPThreads, 2) append_prod_kernel(const Params 
         __syncwarp();
         for (int i = lane; i < D; i += 32) {
           ff2 w{0.f, 0.f};
-          for (int k = 0; k < D; ++k) w = ff_add(w, ff_mul(ff2{p.V[(size_t)i * D + k], 0.f}, ff2{cs[t * D + k], 0.f}));
+          for (int k = 0; k < D; ++k) w = ff_add(w, ff_mul(ff2{p.Vt[(size_t)k * D + i], 0.f}, ff2{cs[t * CS + k], 0.f}));
           const ff2 r = ff_add(ff2{xs[t * D + i], 0.f}, ff_mul(ff2{-n16, 0.f}, w));
           rh[i] = r.hi;
           rl[i] = r.lo;
@@ -374,10 +463,13 @@ __global__ void __launch_bounds__(kPThreads, 2) append_prod_kernel(const Params 
     const int t = e / P, c = e - t * P;
     uint32_t v = 0;
     if (c < cbytes) {
-      for (int q = 0; q < 8; ++q) {
-        const int pos = 8 * c + q, k = pos / bw;
-        if (k < D) v |= (uint32_t)((idx_s[t * kProdMaxD + k] >> (pos - k * bw)) & 1u) << q;
+      // codes k with bits [k bw, k bw + bw) meeting [8 c, 8 c + 8)
+      for (int k = (8 * c) / bw; k < D && k * bw < 8 * c + 8; ++k) {
+        const int sh = k * bw - 8 * c;
+        const uint32_t code = idx_s[t * kProdMaxD + k];
+        v |= sh >= 0 ? code << sh : code >> -sh;
       }
+      v &= 0xffu;
     } else if (c < cbytes + sbytes) {
       const int j0 = 8 * (c - cbytes);
       for (int q = 0; q < 8 && j0 + q < m; ++q) v |= (uint32_t)sgn_s[t * kProdMaxM + j0 + q] << q;
@@ -412,10 +504,11 @@ template <int D>
 __global__ void __launch_bounds__(kPThreads) fetch_prod_kernel(const Params p, const FetchArgs f) {
   constexpr int TX = D / 8, TY = kPThreads / TX, TM = kFT / TY;
   extern __shared__ __align__(16) unsigned char sm[];
-  const int m = p.m, nout = p.n_out, K = D + m;
-  float* A = reinterpret_cast<float*>(sm);           // [kFT][K]
-  float* osc = A + kFT * (D + kProdMaxM);            // [kFT]
-  uint8_t* rows = reinterpret_cast<uint8_t*>(osc + kFT);  // [kFT][P]
+  const int m = p.m, nout = p.n_out, K = D + m, KA = K + 4;  // KA: padded row stride of A
+  float* A = reinterpret_cast<float*>(sm);           // [kFT][KA]
+  float* osc = A + kFT * (D + kProdMaxM + 4);        // [kFT]
+  float* Bs = osc + kFT;                             // [kBlk][D] staged rows of W3
+  uint8_t* rows = reinterpret_cast<uint8_t*>(Bs + kBlk * D);  // [kFT][P]
   const int tid = threadIdx.x;
   const int slot = blockIdx.y;
   const int64_t t0 = (int64_t)blockIdx.x * kFT;
@@ -443,7 +536,7 @@ __global__ void __launch_bounds__(kPThreads) fetch_prod_kernel(const Params p, c
         v = coef * __half2float(side[(t0 + t) * nw + 1]) * (bit ? 1.f : -1.f);
       }
     }
-    A[t * K + k] = v;
+    A[t * KA + k] = v;
   }
   if (nout)
     for (int t = tid; t < kFT; t += kPThreads)
@@ -451,39 +544,43 @@ __global__ void __launch_bounds__(kPThreads) fetch_prod_kernel(const Params p, c
   __syncthreads();
   const int tx = tid % TX, ty = tid / TX;
   float acc[TM][8];
-  gemm_rows<TM>(A, K, p.W3, D, K, TM * ty, 8 * tx, acc);
+  gemm_staged<TM, D>(A, KA, p.W3, D, K, Bs, TM * ty, 4 * tx, acc);
   const int b = slot / p.H, h = slot - b * p.H;
 #pragma unroll
   for (int i = 0; i < TM; ++i) {
     const int t = TM * ty + i;
     if (t >= nt) continue;
-    float v[8];
+    float v[8];  // columns 4 tx .. 4 tx + 3 and D/2 + 4 tx .. D/2 + 4 tx + 3
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = acc[i][j];
     if (nout) {
       const int8_t* o8 = reinterpret_cast<const int8_t*>(rows + t * P + cbytes + p.sign_bytes);
       const int32_t* ch = p.channels + (size_t)slot * nout;
       for (int l = 0; l < nout; ++l) {
-        const int c = ch[l] - 8 * tx;
-        if (c >= 0 && c < 8) {
+        const int c = ch[l];
+        const int j = c - 4 * tx >= 0 && c - 4 * tx < 4 ? c - 4 * tx
+                      : (c - D / 2 - 4 * tx >= 0 && c - D / 2 - 4 * tx < 4 ? 4 + c - D / 2 - 4 * tx : -1);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (j == c) v[j] += (float)o8[l] * osc[t];
-        }
+        for (int q = 0; q < 8; ++q)
+          if (q == j) v[q] += (float)o8[l] * osc[t];
       }
     }
-    const int64_t base = (((int64_t)b * p.H + h) * f.ld_s + t0 + t) * D + 8 * tx;
-    if (p.out_dtype == KVC_F16) {
-      __align__(16) __half o[8];
+    const int64_t row0 = (((int64_t)b * p.H + h) * f.ld_s + t0 + t) * D;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) o[j] = __float2half_rn(v[j]);
-      *reinterpret_cast<uint4*>(static_cast<__half*>(f.out) + base) = *reinterpret_cast<const uint4*>(o);
-    } else {
-      __align__(16) __nv_bfloat16 o[8];
+    for (int half = 0; half < 2; ++half) {
+      const int64_t base = row0 + half * (D / 2) + 4 * tx;
+      if (p.out_dtype == KVC_F16) {
+        __align__(8) __half o[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) o[j] = __float2bfloat16_rn(v[j]);
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(f.out) + base) =
-          *reinterpret_cast<const uint4*>(o);
+        for (int j = 0; j < 4; ++j) o[j] = __float2half_rn(v[4 * half + j]);
+        *reinterpret_cast<uint2*>(static_cast<__half*>(f.out) + base) = *reinterpret_cast<const uint2*>(o);
+      } else {
+        __align__(8) __nv_bfloat16 o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = __float2bfloat16_rn(v[4 * half + j]);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(f.out) + base) =
+            *reinterpret_cast<const uint2*>(o);
+      }
     }
   }
 }
@@ -529,22 +626,33 @@ cudaError_t launch_fit_outliers(const void* x, int dt, int B, int H, int D, int6
   return cudaGetLastError();
 }
 
-cudaError_t launch_append_prod(const Params& p, const AppendArgs& a, cudaStream_t s, int* nk) {
+template <int D>
+static cudaError_t launch_append_prod_d(const Params& p, const AppendArgs& a, cudaStream_t s) {
   const int P = p.code_bytes + p.sign_bytes + p.n_out;
   const size_t smem = (size_t)AppSmem::bytes(P);
-  cudaError_t e = cudaFuncSetAttribute(append_prod_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(append_prod_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((a.T + kTT - 1) / kTT), (unsigned)p.n_slots);
-  append_prod_kernel<<<grid, kPThreads, smem, s>>>(p, a);
-  ++*nk;
+  append_prod_kernel<D><<<grid, kPThreads, smem, s>>>(p, a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_append_prod(const Params& p, const AppendArgs& a, cudaStream_t s, int* nk) {
+  ++*nk;
+  switch (p.D) {
+    case 32: return launch_append_prod_d<32>(p, a, s);
+    case 64: return launch_append_prod_d<64>(p, a, s);
+    case 128: return launch_append_prod_d<128>(p, a, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int D>
 static cudaError_t launch_fetch_prod_d(const Params& p, const FetchArgs& f, cudaStream_t s) {
   const int P = p.code_bytes + p.sign_bytes + p.n_out;
-  const size_t smem = (size_t)kFT * (D + kProdMaxM) * 4 + kFT * 4 + (size_t)kFT * P + 16;
+  const size_t smem = (size_t)kFT * (D + kProdMaxM + 4) * 4 + kFT * 4 + (size_t)kBlk * D * 4 +
+                      (size_t)kFT * P + 16;
   cudaError_t e = cudaFuncSetAttribute(fetch_prod_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;

@@ -230,3 +230,23 @@ def test_attend_scores_equal_the_decoded_keys():
                                atol=1e-12)
             ref = attend_rows(q[b, hq], K[b, h], V[b, h], 1 / math.sqrt(D))
             assert np.allclose(out[b, hq], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_trim_then_append_equals_appending_the_kept_keys():
+    rng = np.random.default_rng(31)
+    B, H, D, m = 1, 1, 16, 16
+    R = fit.seeded_rotation(D, 32)
+    cb = fit.lloyd_max_gaussian(4, 1 / math.sqrt(D))
+    S = rng.standard_normal((m, D))
+    x = rng.standard_normal((B, H, 12, D))
+    ch = np.array([prod.outlier_channels(x[0, 0, :4], 2)])
+    a = prod.ProdKeyLayer(B, H, D, R=R, centroids=cb, S=S, channels=ch, split_from=3)
+    b = prod.ProdKeyLayer(B, H, D, R=R, centroids=cb, S=S, channels=ch, split_from=3)
+    a.append(x)
+    assert a.trim(5) == 5 and a.len == 7 and a.trim(-1) == 0
+    a.append(x[:, :, 7:])
+    b.append(x)
+    ra, sa = a.rows(0)
+    rb, sb = b.rows(0)
+    assert np.array_equal(ra, rb) and np.array_equal(sa.view(np.uint16), sb.view(np.uint16))
+    assert a.trim(100) == 12 and a.len == 0
