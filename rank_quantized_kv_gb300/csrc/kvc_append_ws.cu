@@ -453,11 +453,11 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
         }
         Vt = vt_s;
       }
-      // partial ||x||^2 over this warp's half of the row
+      // partial ||x||^2 over this warp's share of the row
       {
         float sq = 0.f;
-        const int c0 = cblk * (D / 2);
-        for (int c = c0; c < c0 + D / 2; c += 8) {
+        const int c0 = cblk * (D / kNCB);
+        for (int c = c0; c < c0 + D / kNCB; c += 8) {
           const uint4 v = *reinterpret_cast<const uint4*>(
               xs + (c >> 6) * 16384 + row * 128 + ((((c & 63) >> 3) ^ (row & 7)) << 4));
           const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
@@ -481,7 +481,10 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       if (named_bar_or(qbar, kQThreads, late || abort_flag)) { abort_flag = 1; break; }
       // the first tile on a new B buffer: the other buffer's last reader was the
       // previous tile, finished now
-      const float nx = sqrtf(nsq_s[row] + nsq_s[kTile + row]);
+      float nsq = nsq_s[row];
+#pragma unroll
+      for (int cb = 1; cb < kNCB; ++cb) nsq += nsq_s[cb * kTile + row];
+      const float nx = sqrtf(nsq);
       const bool tiny = MODE == KVC_MODE_CODEBOOK && nx < 1e-18f;
       const float rnx = MODE == KVC_MODE_CODEBOOK && !tiny ? t.inv_scale * (1.f / nx) : 0.f;
       const bool live = row < n;
@@ -629,12 +632,12 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
 using WsKernel = void (*)(const Params, const AppendWsArgs, const CUtensorMap, const AppendArgs);
 
 template <int MODE, bool BF16>
-WsKernel ws_for(int rpad) {
+WsKernel ws_for(int rpad) {  // CW = rpad / kNCB components per thread
   switch (rpad) {
-    case 16: return append_ws_kernel<MODE, BF16, 8>;
-    case 32: return append_ws_kernel<MODE, BF16, 16>;
-    case 64: return append_ws_kernel<MODE, BF16, 32>;
-    default: return append_ws_kernel<MODE, BF16, 64>;
+    case 16: return append_ws_kernel<MODE, BF16, 16 / kNCB>;
+    case 32: return append_ws_kernel<MODE, BF16, 32 / kNCB>;
+    case 64: return append_ws_kernel<MODE, BF16, 64 / kNCB>;
+    default: return append_ws_kernel<MODE, BF16, 128 / kNCB>;
   }
 }
 

@@ -16,6 +16,7 @@
 
 #include "kvc_ff.cuh"
 #include "kvc_internal.h"
+#include "kvc_tc.h"
 
 namespace kvc {
 namespace {
@@ -715,6 +716,11 @@ __device__ __forceinline__ void load8(const void* x, int dt, int64_t off, float 
 // inputs, a < 2e-6 and a >= 1e30 take the float64 path.
 constexpr int kI8NV = 32;
 template <int TPR>
+__device__ __forceinline__ unsigned append_int8_vals(const Params& p, const AppendArgs& a, int slot,
+                                                     int64_t t, int j, bool valid,
+                                                     float (&v)[kI8NV]);
+
+template <int TPR>
 __device__ __forceinline__ unsigned append_int8_row(const Params& p, const AppendArgs& a, int slot,
                                                     int64_t t, int j) {
   const bool valid = t < a.T;
@@ -728,6 +734,13 @@ __device__ __forceinline__ unsigned append_int8_row(const Params& p, const Appen
     for (int c = 0; c < kI8NV / 8; ++c)
       load8(a.x, p.in_dtype, off + 8 * c, *reinterpret_cast<float(*)[8]>(&v[8 * c]));
   }
+  return append_int8_vals<TPR>(p, a, slot, t, j, valid, v);
+}
+
+template <int TPR>
+__device__ __forceinline__ unsigned append_int8_vals(const Params& p, const AppendArgs& a, int slot,
+                                                     int64_t t, int j, bool valid,
+                                                     float (&v)[kI8NV]) {
   float am = 0.f;
 #pragma unroll
   for (int i = 0; i < kI8NV; ++i) am = fmaxf(am, fabsf(v[i]));
@@ -812,6 +825,86 @@ __global__ void __launch_bounds__(256) append_int8_vec(Params p, AppendArgs a) {
   }
 }
 
+// Pipelined int8 append: a persistent grid walks the rows (slot-major, 256 /
+// TPR rows per block step); each thread copies its own 32 values of the rows
+// kI8Stages - 1 steps ahead into shared memory with cp.async (16 bytes each,
+// one commit group per step) and waits for its oldest group with
+// cp.async.wait_group, so HBM sees kI8Stages - 1 rows per thread in flight.
+// A thread reads back only what it copied: no barrier is needed.  ESZ: the
+// input element bytes (2 or 4).
+constexpr int kI8Stages = 4;
+template <int TPR, int ESZ>
+__global__ void __launch_bounds__(256, 3) append_int8_pipe(Params p, AppendArgs a) {
+  constexpr int Q = kI8NV * ESZ / 16;  // 16-byte pieces of a thread's values
+  constexpr int RPB = 256 / TPR;       // rows per block step
+  extern __shared__ uint4 stage_buf[];  // [kI8Stages][Q][256]
+  const int tid = threadIdx.x, j = tid % TPR;
+  const int64_t total = (int64_t)p.n_slots * a.T;
+  const int64_t step = (int64_t)gridDim.x * RPB;
+  const int64_t r0 = (int64_t)blockIdx.x * RPB + tid / TPR;
+  auto issue = [&](int64_t r, int st) {
+    if (r < total) {
+      const int slot = (int)(r / a.T);
+      const int64_t t = r - (int64_t)slot * a.T;
+      const int b = slot / p.H, h = slot - b * p.H;
+      const char* src = static_cast<const char*>(a.x) +
+                        ((int64_t)b * a.sb + (int64_t)h * a.sh + t * a.st + kI8NV * j) * ESZ;
+#pragma unroll
+      for (int q = 0; q < Q; ++q) {
+        const uint32_t dst =
+            (uint32_t)__cvta_generic_to_shared(&stage_buf[((size_t)st * Q + q) * 256 + tid]);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src + 16 * q)
+                     : "memory");
+      }
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  };
+#pragma unroll
+  for (int s0 = 0; s0 < kI8Stages - 1; ++s0) issue(r0 + s0 * step, s0);
+  unsigned nref = 0, rows0 = 0;
+  for (int64_t k = 0;; ++k) {
+    const int64_t r = r0 + k * step;
+    if (r - (int64_t)(tid / TPR) >= total) break;  // the whole block step is past the end
+    issue(r + (kI8Stages - 1) * step, (int)((k + kI8Stages - 1) % kI8Stages));
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(kI8Stages - 1) : "memory");
+    const int st = (int)(k % kI8Stages);
+    float v[kI8NV];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      const uint4 w = stage_buf[((size_t)st * Q + q) * 256 + tid];
+      if (ESZ == 4) {
+        v[4 * q] = __uint_as_float(w.x);
+        v[4 * q + 1] = __uint_as_float(w.y);
+        v[4 * q + 2] = __uint_as_float(w.z);
+        v[4 * q + 3] = __uint_as_float(w.w);
+      } else {
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint16_t lo = (uint16_t)(ww[e] & 0xffffu), hi = (uint16_t)(ww[e] >> 16);
+          if (p.in_dtype == KVC_F16) {
+            v[8 * q + 2 * e] = __half2float(__ushort_as_half(lo));
+            v[8 * q + 2 * e + 1] = __half2float(__ushort_as_half(hi));
+          } else {
+            v[8 * q + 2 * e] = __bfloat162float(__ushort_as_bfloat16(lo));
+            v[8 * q + 2 * e + 1] = __bfloat162float(__ushort_as_bfloat16(hi));
+          }
+        }
+      }
+    }
+    const bool valid = r < total;
+    const int slot = valid ? (int)(r / a.T) : 0;
+    const int64_t t = valid ? r - (int64_t)slot * a.T : a.T;
+    nref += append_int8_vals<TPR>(p, a, slot, t, j, valid, v);
+    rows0 += (valid && slot == 0 && j == 0) ? 1u : 0u;
+  }
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  nref = __reduce_add_sync(kFull, nref);
+  rows0 = __reduce_add_sync(kFull, rows0);
+  if ((tid & 31) == 0 && nref) atomicAdd(&p.counters[0], (unsigned long long)nref);
+  if ((tid & 31) == 0 && rows0) atomicAdd(&p.counters[2], (unsigned long long)rows0);
+}
+
 // Grid as append_int8_vec.
 template <int TPR>
 __global__ void __launch_bounds__(256) fetch_int8_vec(Params p, FetchArgs f) {
@@ -881,7 +974,26 @@ cudaError_t launch_append_int8(const Params& p, const AppendArgs& a, cudaStream_
   const bool vec = (p.D == 64 || p.D == 128 || p.D == 256) &&
                    reinterpret_cast<uintptr_t>(a.x) % 16 == 0 && (a.st * esz) % 16 == 0 &&
                    (a.sh * esz) % 16 == 0 && (a.sb * esz) % 16 == 0;
-  if (vec) {
+  if (vec && toks >= 4096) {
+    // persistent, pipelined: three blocks per SM, or fewer for a small call
+    const int tpr = p.D / kI8NV;
+    const int rpb = 256 / tpr;
+    const int64_t steps = (toks + rpb - 1) / rpb;
+    const unsigned grid = (unsigned)std::min<int64_t>(steps, 3 * (int64_t)sm_count());
+    const size_t smem = (size_t)kI8Stages * kI8NV * esz * 256;
+    cudaError_t e = cudaSuccess;
+#define KVC_I8_PIPE(T, E)                                                                     \
+  e = cudaFuncSetAttribute(append_int8_pipe<T, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                           (int)smem);                                                         \
+  if (e == cudaSuccess) append_int8_pipe<T, E><<<grid, 256, smem, s>>>(p, a);
+    if (esz == 2) {
+      if (tpr == 2) { KVC_I8_PIPE(2, 2) } else if (tpr == 4) { KVC_I8_PIPE(4, 2) } else { KVC_I8_PIPE(8, 2) }
+    } else {
+      if (tpr == 2) { KVC_I8_PIPE(2, 4) } else if (tpr == 4) { KVC_I8_PIPE(4, 4) } else { KVC_I8_PIPE(8, 4) }
+    }
+#undef KVC_I8_PIPE
+    if (e != cudaSuccess) return e;
+  } else if (vec) {
     const int tpr = p.D / kI8NV;  // 32 values per thread
     const dim3 grid((unsigned)((a.T * tpr + 255) / 256), (unsigned)std::min(p.n_slots, 65535));
     if (tpr == 2) append_int8_vec<2><<<grid, 256, 0, s>>>(p, a);

@@ -487,3 +487,19 @@ def test_host_pointer_is_rejected(kvc):
     with pytest.raises(kvc.KvcError) as e:
         gl.append(torch.zeros(B, H, 2, D, dtype=torch.float16))     # CPU tensor
     assert e.value.status == -1 and len(gl) == 0
+
+
+@pytest.mark.parametrize("dtype", ["f16", "f32"])
+def test_int8_values_pipelined_many_steps(kvc, dtype):
+    """Enough rows (4 x 8 x 3001, ragged) that every block of the persistent,
+    pipelined int8 append walks several steps; rows read through strides."""
+    B, H, S, D = 4, 8, 3001, 128
+    x = synth.kv_spectral(B, H, S, D, alpha=1.0, seed=4200, tensor=1, dtype=dtype)
+    x64 = x.double().numpy()
+    gl, rl = _make(kvc, "int8", B, H, D, {}, dtype, S, "auto")
+    xs = x.permute(0, 2, 1, 3).contiguous().to(_dev()).permute(0, 2, 1, 3)
+    gl.append(xs)
+    assert gl.sync_status() == 0
+    rl.append(x64)
+    _all_slots_match(gl, rl, x64)
+    assert gl.counters()["appended"] == S
