@@ -209,10 +209,10 @@ __device__ __forceinline__ int fast_uniform(const Tab& tb, int k, int qmax, floa
 // roundings of u and of |u - m|).  Up to 8 levels the 7 midpoints sit in
 // registers (+inf past the last) and a 3-step bisection finds the code and the
 // two bracketing midpoints at once.
-__device__ __forceinline__ int fast_codebook(const Params& p, const Tab& tb, int k,
-                                             const float* mids_s, const float (&mreg)[7], float z,
-                                             float rnx, float e_u, bool tiny, float& u,
-                                             float& tau, bool& near) {
+__device__ __forceinline__ int fast_codebook(const Params& p, float t1, const float* mids_s,
+                                             const float (&mreg)[7], float z, float rnx,
+                                             float e_u, bool tiny, float& u, float& tau,
+                                             bool& near) {
   const int L = p.cb_levels;
   u = z * rnx;  // rnx = 2^-s fl(1 / ||x||) (0 for a tiny ||x||): two roundings, as z 2^-s / ||x||
   int c = 0;
@@ -244,7 +244,7 @@ __device__ __forceinline__ int fast_codebook(const Params& p, const Tab& tb, int
     if (c > 0) dmin = fminf(dmin, fabsf(u - mids_s[c - 1]));
     if (c < L - 1) dmin = fminf(dmin, fabsf(u - mids_s[c]));
   }
-  tau = tiny ? 0.f : fmaf(fabsf(u), e_u, tb.q4[k].z);
+  tau = tiny ? 0.f : fmaf(fabsf(u), e_u, t1);
   near = tiny || dmin <= tau;
   return c;
 }
@@ -437,6 +437,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       late = late || !wait_or_abort(&acc_full[acc], rt.phase, t.wait_ns, &abort_flag);
       const unsigned char* xs = xst + (size_t)s * t.x_stage;
       const Tab tb(xs + tab_off, rpad);
+      const float t1 = MODE == KVC_MODE_CODEBOOK ? tb.q4[0].z : 0.f;  // the codebook bound's base
       const XHdr hd = hdr[s];
       const int n = hd.n;
       // V^T for the re-decision: beside B (visible: the MMA waited for B before
@@ -517,14 +518,21 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
 #pragma unroll
         for (int j = 0; j < SB; ++j) {
           const int k = cblk * CW + sb * SB + j;  // < rpad; components past r are not kept
-          const int2 qp = tb.qp[k];  // qmax, position (not kept: the row's scratch byte)
+          // position (not kept: the row's scratch byte) and qmax; a codebook's
+          // one segment keeps the components in order from position 0
+          int pos = k < r ? k : ks - 1, qmax = 0;
+          if (MODE == KVC_MODE_UNIFORM) {
+            const int2 qp = tb.qp[k];
+            qmax = qp.x;
+            pos = qp.y;
+          }
           float uf, tf;
           bool near;
           const int code = MODE == KVC_MODE_UNIFORM
-                               ? fast_uniform<false>(tb, k, qp.x, z[j], nx, uf, tf, near)
-                               : fast_codebook(p, tb, k, mids_s, mreg, z[j], rnx, e_u, tiny, uf,
-                                               tf, near);
-          crow[qp.y] = (uint8_t)code;
+                               ? fast_uniform<false>(tb, k, qmax, z[j], nx, uf, tf, near)
+                               : fast_codebook(p, t1, mids_s, mreg, z[j], rnx, e_u, tiny, uf, tf,
+                                               near);
+          crow[pos] = (uint8_t)code;
           nmask |= (uint32_t)near << j;
         }
         // queue the near ones (rare); past the queue's end they are decided
@@ -541,7 +549,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
               fast_uniform<true>(tb, k, tb.qp[k].x, z[j], nx, uf, tf, near);
               if (!near) continue;  // an outer boundary: the clamped code is certain
             } else {
-              fast_codebook(p, tb, k, mids_s, mreg, z[j], rnx, e_u, tiny, uf, tf, near);
+              fast_codebook(p, t1, mids_s, mreg, z[j], rnx, e_u, tiny, uf, tf, near);
             }
             const unsigned q = atomicAdd(&qcount, 1u);
             if (q < kQueue) {
@@ -612,7 +620,14 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&x_empty[s]);
       unsigned char* dst = p.store + hd.pay + hd.row0 * P;
-      for (int idx = qt; idx < n * P; idx += kQThreads) dst[idx] = out_s[idx];
+      if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0) {  // 16-byte copies, then the tail
+        const int nv = (n * P) >> 4;
+        for (int v = qt; v < nv; v += kQThreads)
+          reinterpret_cast<uint4*>(dst)[v] = reinterpret_cast<const uint4*>(out_s)[v];
+        for (int idx = 16 * nv + qt; idx < n * P; idx += kQThreads) dst[idx] = out_s[idx];
+      } else {
+        for (int idx = qt; idx < n * P; idx += kQThreads) dst[idx] = out_s[idx];
+      }
       if (MODE == KVC_MODE_CODEBOOK && qt < n)
         reinterpret_cast<__half*>(p.store + hd.side)[hd.row0 + qt] = side_s[qt];
       if (qt == 0) {  // the next tile starts with an empty queue (read above, before B3)
@@ -679,6 +694,15 @@ int append_ws_table(const Geo& g, const kvc_layer_desc& d, int rpad, const doubl
   float* vn = lo + rpad;
   int2* qp = reinterpret_cast<int2*>(vn + rpad);
   uint32_t* chunk = reinterpret_cast<uint32_t*>(qp + rpad);
+  double vmax = 0.0;  // the largest ||V_k||, rounded up as below
+  for (int k = 0; k < r; ++k) {
+    double ss = 0.0;
+    for (int i = 0; i < D; ++i) {
+      const double v = d.V[((size_t)b * D + i) * r + k];
+      ss += v * v;
+    }
+    vmax = std::max(vmax, (double)std::nextafter((float)std::sqrt(ss), INFINITY));
+  }
   for (int k = 0; k < rpad; ++k) {
     const bool in = k < r;
     const size_t bk = (size_t)b * r + k;
@@ -714,10 +738,11 @@ int append_ws_table(const Geo& g, const kvc_layer_desc& d, int rpad, const doubl
                            std::ldexp(1.0, -22) * (qm + 2));
     }
     if (in && d.mode == KVC_MODE_CODEBOOK) {
+      // one bound for every component (the quantiser reads it once per tile):
+      // the basis' largest ||V_k||
       double cmax = 0.0;
       for (int j = 0; j < g.cb_levels; ++j) cmax = std::max(cmax, std::fabs((double)d.codebook[j]));
-      q4[k].z = round_up_f(gamma * (double)vn[k] * (1.0 + 1e-3) * (1.0 + 1e-6) +
-                           std::ldexp(1.0, -22) * cmax);
+      q4[k].z = round_up_f(gamma * vmax * (1.0 + 1e-3) * (1.0 + 1e-6) + std::ldexp(1.0, -22) * cmax);
     }
     const int width = in ? g.bits[bk] : 0;
     qp[k] = make_int2(d.mode == KVC_MODE_UNIFORM && width ? (1 << width) - 1 : 0, ks - 1);
