@@ -202,6 +202,48 @@ __device__ __forceinline__ int fast_uniform(const Tab& tb, int k, int qmax, floa
   return min(max(__float2int_rn(u), 0), qmax);
 }
 
+// The packed bytes of 32 consecutive W-bit codes (in: 32 code bytes as 8
+// words, LSB-first) as W 32-bit words, LSB-first.
+template <int W>
+__device__ __forceinline__ void pack32(const uint32_t (&in)[8], uint32_t (&out)[W]) {
+  uint64_t acc = 0;
+  int nb = 0, o = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    acc |= (uint64_t)((in[j >> 2] >> (8 * (j & 3))) & 0xffu) << nb;
+    nb += W;
+    if (nb >= 32) {
+      out[o++] = (uint32_t)acc;
+      acc >>= 32;
+      nb -= 32;
+    }
+  }
+}
+
+// Codebook rows (one segment of D codes, D a multiple of 32): one thread per
+// (token, 32 codes), 8-byte loads of the codes, W 4-byte stores of the bits.
+template <int W>
+__device__ __forceinline__ void pack_codebook(int qt, int n, int D, const unsigned char* codes_s,
+                                              int ks, unsigned char* out_s, int P) {
+  const int ng = D / 32;
+  for (int item = qt; item < n * ng; item += kQThreads) {
+    const int tt = item / ng, g4 = item - tt * ng;
+    const uint2* src = reinterpret_cast<const uint2*>(codes_s + tt * ks + 32 * g4);
+    uint32_t in[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint2 v = src[q];
+      in[2 * q] = v.x;
+      in[2 * q + 1] = v.y;
+    }
+    uint32_t out[W];
+    pack32<W>(in, out);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(out_s + tt * P + 4 * W * g4);
+#pragma unroll
+    for (int q = 0; q < W; ++q) dst[q] = out[q];
+  }
+}
+
 // Codebook fast path: u = z / ||x||, the nearest centroid by the fp32
 // midpoints, and whether a midpoint lies within the bound tau of u's error:
 // tau = T1_k + |u| e, T1_k = gamma ||V_k|| (1 + 1e-3)(1 + 1e-6) + 2^-22 max|c|
@@ -210,7 +252,7 @@ __device__ __forceinline__ int fast_uniform(const Tab& tb, int k, int qmax, floa
 // registers (+inf past the last) and a 3-step bisection finds the code and the
 // two bracketing midpoints at once.
 __device__ __forceinline__ int fast_codebook(const Params& p, float t1, const float* mids_s,
-                                             const float (&mreg)[7], float z, float rnx,
+                                             const float* mpad, float m3, float z, float rnx,
                                              float e_u, bool tiny, float& u, float& tau,
                                              bool& near) {
   const int L = p.cb_levels;
@@ -218,22 +260,12 @@ __device__ __forceinline__ int fast_codebook(const Params& p, float t1, const fl
   int c = 0;
   float dmin;
   if (L <= 8) {
-    float lo = -INFINITY, hi = INFINITY;
-    bool g = u > mreg[3];
-    c = g ? 4 : 0;
-    lo = g ? mreg[3] : lo;
-    hi = g ? hi : mreg[3];
-    const float mb = c ? mreg[5] : mreg[1];
-    g = u > mb;
-    c += g ? 2 : 0;
-    lo = g ? mb : lo;
-    hi = g ? hi : mb;
-    const float mc = (c & 4) ? ((c & 2) ? mreg[6] : mreg[4]) : ((c & 2) ? mreg[2] : mreg[0]);
-    g = u > mc;
-    c += g ? 1 : 0;
-    lo = g ? mc : lo;
-    hi = g ? hi : mc;
-    dmin = fminf(u - lo, hi - u);
+    // mpad = [-inf, m_0 .. m_6, +inf] (+inf past the last midpoint): a 3-step
+    // bisection, then the bracketing midpoints mpad[c] < u <= mpad[c + 1]
+    c = u > m3 ? 4 : 0;
+    c += u > mpad[c + 2] ? 2 : 0;
+    c += u > mpad[c + 1] ? 1 : 0;
+    dmin = fminf(u - mpad[c], mpad[c + 1] - u);
   } else {
     int hi_i = L - 1;
     while (c < hi_i) {
@@ -285,6 +317,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
   float* vt0 = reinterpret_cast<float*>(grp0 + QG * ws_group_bytes(t.ks, t.pmax));  // QG x V^T
   float* mids_s = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(vt0) + QG * vt_bytes);
   float* cb_s = mids_s + 256;                                       // [256]
+  __shared__ float mpad[9];  // codebooks of <= 8 levels: -inf, the midpoints, +inf
   const int tab_off = nbox * 16384;                                 // table after the x boxes
 
   if (warp == kMmaWarp) tmem_alloc(&tmem_base, t.cols);
@@ -299,6 +332,8 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
   }
   if (MODE == KVC_MODE_CODEBOOK) {
     for (int j = tid; j < p.cb_levels - 1; j += kThreads) mids_s[j] = p.mids[j];
+    if (tid < 9)
+      mpad[tid] = tid == 0 ? -INFINITY : (tid < p.cb_levels ? p.mids[tid - 1] : INFINITY);
     for (int j = tid; j < p.cb_levels; j += kThreads) cb_s[j] = p.codebook[j];
   }
   tc_fence_before();
@@ -423,10 +458,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
     const float kU = 5.9604644775390625e-08f;
     const float eps_n = 0.5f * ((D + 2) * kU) / (1.f - (D + 2) * kU) + 2.f * kU;
     const float e_u = (eps_n * (1.f + 1e-6f) + 4.f * kU) * (1.f + 1e-6f);  // |u| term of tau
-    float mreg[7];
-#pragma unroll
-    for (int j = 0; j < 7; ++j)
-      mreg[j] = MODE == KVC_MODE_CODEBOOK && j < p.cb_levels - 1 ? mids_s[j] : INFINITY;
+    const float m3 = MODE == KVC_MODE_CODEBOOK ? mpad[4] : 0.f;  // the first bisection step
     Ring rx(XS), rt(TS);
     for (int j = 0; j < g; ++j) { rx.next(); rt.next(); }
     for (int i = g; i < m; i += QG) {
@@ -530,8 +562,8 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
           bool near;
           const int code = MODE == KVC_MODE_UNIFORM
                                ? fast_uniform<false>(tb, k, qmax, z[j], nx, uf, tf, near)
-                               : fast_codebook(p, t1, mids_s, mreg, z[j], rnx, e_u, tiny, uf, tf,
-                                               near);
+                               : fast_codebook(p, t1, mids_s, mpad, m3, z[j], rnx, e_u, tiny, uf,
+                                               tf, near);
           crow[pos] = (uint8_t)code;
           nmask |= (uint32_t)near << j;
         }
@@ -549,7 +581,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
               fast_uniform<true>(tb, k, tb.qp[k].x, z[j], nx, uf, tf, near);
               if (!near) continue;  // an outer boundary: the clamped code is certain
             } else {
-              fast_codebook(p, t1, mids_s, mreg, z[j], rnx, e_u, tiny, uf, tf, near);
+              fast_codebook(p, t1, mids_s, mpad, m3, z[j], rnx, e_u, tiny, uf, tf, near);
             }
             const unsigned q = atomicAdd(&qcount, 1u);
             if (q < kQueue) {
@@ -599,8 +631,18 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
         if (nside) atomicAdd(&p.counters[1], (unsigned long long)nside);
         if (hd.slot == 0) atomicAdd(&p.counters[2], (unsigned long long)n);
       }
-      // pack: one thread per (token, 8-code chunk) -> w bytes, LSB-first
+      // pack: one thread per (token, 8-code chunk) -> w bytes, LSB-first; a
+      // codebook's single segment 32 codes at a time
       const int P = hd.P;
+      if (MODE == KVC_MODE_CODEBOOK && D % 32 == 0) {
+        switch (p.cb_bits) {
+          case 1: pack_codebook<1>(qt, n, D, codes_s, ks, out_s, P); break;
+          case 2: pack_codebook<2>(qt, n, D, codes_s, ks, out_s, P); break;
+          case 3: pack_codebook<3>(qt, n, D, codes_s, ks, out_s, P); break;
+          case 4: pack_codebook<4>(qt, n, D, codes_s, ks, out_s, P); break;
+          default: pack_codebook<8>(qt, n, D, codes_s, ks, out_s, P); break;
+        }
+      } else
       for (int item = qt; item < kTile * 32; item += kQThreads) {
         const int tt = item & (kTile - 1), c = item >> 7;
         const uint32_t ent = tb.chunk[c];
