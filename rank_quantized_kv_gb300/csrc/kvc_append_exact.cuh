@@ -88,6 +88,52 @@ __device__ ff2 dot2_ff(const unsigned char* xs, int t, int D, const float* w, in
   return ff2{s, e};
 }
 
+// The same dots by a group of GL lanes (GL divides 32; the shuffles stay
+// inside the group): x_t . x_t and, when w is not null, x_t . w in one pass
+// over the row.  Every lane of the warp must call it; the results are on every
+// lane of the group.
+template <bool BF16, int GL>
+__device__ __forceinline__ void dot2_ff_group(const unsigned char* xs, int t, int D,
+                                              const float* w, int sub, ff2& xx, ff2& xw) {
+  float S1 = 0.f, C1 = 0.f, S2 = 0.f, C2 = 0.f;
+  for (int i = sub; i < D; i += GL) {
+    const unsigned char* src =
+        xs + (i >> 6) * 16384 + t * 128 + ((((i & 63) >> 3) ^ (t & 7)) << 4) + (i & 7) * 2;
+    const uint16_t raw = *reinterpret_cast<const uint16_t*>(src);
+    const float xv = BF16 ? __bfloat162float(__ushort_as_bfloat16(raw))
+                          : __half2float(__ushort_as_half(raw));
+    float s, e;
+    const float p1 = xv * xv, e1 = fmaf(xv, xv, -p1);
+    two_sum(S1, p1, s, e);
+    S1 = s;
+    C1 += e1 + e;
+    if (w) {
+      const float wv = w[i];
+      const float p2 = xv * wv, e2 = fmaf(xv, wv, -p2);
+      two_sum(S2, p2, s, e);
+      S2 = s;
+      C2 += e2 + e;
+    }
+  }
+#pragma unroll
+  for (int o = GL / 2; o > 0; o >>= 1) {
+    float s, e;
+    const float So1 = __shfl_xor_sync(0xffffffffu, S1, o), Co1 = __shfl_xor_sync(0xffffffffu, C1, o);
+    two_sum(S1, So1, s, e);
+    S1 = s;
+    C1 = C1 + Co1 + e;
+    const float So2 = __shfl_xor_sync(0xffffffffu, S2, o), Co2 = __shfl_xor_sync(0xffffffffu, C2, o);
+    two_sum(S2, So2, s, e);
+    S2 = s;
+    C2 = C2 + Co2 + e;
+  }
+  float s, e;
+  two_sum(S1, C1, s, e);
+  xx = ff2{s, e};
+  two_sum(S2, C2, s, e);
+  xw = ff2{s, e};
+}
+
 template <bool BF16, bool WARP>
 __device__ double dot2_row(const unsigned char* xs, int t, int D, const float* w, int lane) {
   const ff2 v = dot2_ff<BF16, WARP>(xs, t, D, w, lane);

@@ -185,6 +185,56 @@ __device__ void refine_ws(const Params& p, const Tab& tb, const float* Vt, const
   }
 }
 
+// The same decisions by a group of GL lanes, several groups of a warp each
+// deciding its own queue entry (act: the group has one; every lane calls).
+// A codebook code takes ||x||^2 and x . V_k from one pass over the row.
+template <int MODE, bool BF16, int GL>
+__device__ __forceinline__ void refine_group(const Params& p, const Tab& tb, const float* Vt,
+                                             const float* cb_s, const unsigned char* xs,
+                                             unsigned char* codes_s, int ks, __half* side_s,
+                                             unsigned* nside, int tt, int k, int sub, bool act,
+                                             float uf, float tau) {
+  const int D = p.D;
+  const bool norm_entry = k == (int)kNormEntry;
+  const int kk = norm_entry ? 0 : k;
+  ff2 xx, z;
+  dot2_ff_group<BF16, GL>(xs, tt, D, norm_entry ? nullptr : Vt + (size_t)kk * D, sub, xx, z);
+  if (!act || sub != 0) return;
+  const int kp = norm_entry ? 0 : tb.qp[k].y;
+  if (MODE == KVC_MODE_UNIFORM) {
+    const float2 c = tb.cff[k], iv = tb.iff[k];
+    const ff2 zl = ff_add(ff_add(z, ff2{-c.x, -c.y}), ff2{-tb.lo[k], 0.f});
+    const ff2 u = ff_mul(zl, ff2{iv.x, iv.y});
+    const float q = ff_rint(u);
+    const int qmax = tb.qp[k].x;
+    codes_s[tt * ks + kp] = (uint8_t)(int)fminf(fmaxf(q, 0.f), (float)qmax);
+    if (tau > 0.f)
+      atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(fabsf(uf - u.hi) / tau));
+    return;
+  }
+  const ff2 nrm = ff_sqrt(xx);
+  if (norm_entry) {
+    side_s[tt] = ff_to_half(nrm);
+    atomicAdd(nside, 1u);
+    return;
+  }
+  // nearest centroid, ties to the lower one: the number of exact midpoints m
+  // (double-float, from the fp32 centroids) with m ||x|| < z; ||x|| = 0: u = 0
+  const bool zero = nrm.hi == 0.f;
+  int lo_i = 0, hi_i = p.cb_levels - 1;
+  while (lo_i < hi_i) {
+    const int mid = (lo_i + hi_i) >> 1;
+    float ms, me;
+    two_sum(cb_s[mid], cb_s[mid + 1], ms, me);
+    const ff2 m{0.5f * ms, 0.5f * me};
+    const bool below = zero ? m.hi < 0.f : ff_less(ff_mul(m, nrm), z);
+    if (below) lo_i = mid + 1; else hi_i = mid;
+  }
+  codes_s[tt * ks + kp] = (uint8_t)lo_i;
+  if (tau > 0.f && !zero)
+    atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(fabsf(uf - z.hi / nrm.hi) / tau));
+}
+
 // Uniform fast path: u = (z - mean . V_k - lo) / step as one fma of the
 // table's fused constants and the code; `near` flags a rounding boundary
 // within the bound tau of u (host derivation in append_ws_table; tau holds for
@@ -619,11 +669,18 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       }
       named_bar_sync(qbar, kQThreads);  // B2: fast-path codes and the queue complete
       const unsigned nq = qcount;
-      for (unsigned e = wq; e < min(nq, (unsigned)kQueue); e += kQWarps) {
-        const uint32_t ent = queue[e];
-        const float2 ax = aux[e];
-        refine_ws<MODE, BF16, true>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside,
-                                    (int)(ent >> 16), (int)(ent & 0xffffu), lane, ax.x, ax.y);
+      {  // four entries per warp at a time, eight lanes each
+        constexpr int GL = 8, PER = 32 / GL;
+        const unsigned nqe = min(nq, (unsigned)kQueue);
+        for (unsigned e0 = wq * PER; e0 < nqe; e0 += kQWarps * PER) {
+          const unsigned e = e0 + lane / GL;
+          const bool act = e < nqe;
+          const uint32_t ent = queue[act ? e : e0];
+          const float2 ax = aux[act ? e : e0];
+          refine_group<MODE, BF16, GL>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside,
+                                       (int)(ent >> 16), (int)(ent & 0xffffu), lane & (GL - 1),
+                                       act, ax.x, ax.y);
+        }
       }
       named_bar_sync(qbar, kQThreads);  // B3: every code decided
       if (qt == 0) {
