@@ -137,7 +137,8 @@ __host__ __device__ constexpr size_t ws_group_bytes(int ks, int pmax) {
 template <int MODE, bool BF16, bool WARP>
 __device__ void refine_ws(const Params& p, const Tab& tb, const float* Vt, const float* cb_s,
                           const unsigned char* xs, unsigned char* codes_s, int ks, __half* side_s,
-                          unsigned* nside, int tt, int k, int lane, float uf, float tau) {
+                          unsigned* nside, unsigned long long* cnt, int tt, int k, int lane,
+                          float uf, float tau) {
   const int D = p.D;
   const int kp = k == (int)kNormEntry ? 0 : tb.qp[k].y;
   if (MODE == KVC_MODE_UNIFORM) {
@@ -149,7 +150,7 @@ __device__ void refine_ws(const Params& p, const Tab& tb, const float* Vt, const
       const float q = ff_rint(u);
       const int qmax = tb.qp[k].x;
       codes_s[tt * ks + kp] = (uint8_t)(int)fminf(fmaxf(q, 0.f), (float)qmax);
-      if (tau > 0.f) atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(
+      if (tau > 0.f) atomicMax(&cnt[3], (unsigned long long)__float_as_uint(
                                                    fabsf(uf - u.hi) / tau));
     }
   } else {
@@ -178,7 +179,7 @@ __device__ void refine_ws(const Params& p, const Tab& tb, const float* Vt, const
         }
         codes_s[tt * ks + kp] = (uint8_t)lo_i;
         if (tau > 0.f && !zero)
-          atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(
+          atomicMax(&cnt[3], (unsigned long long)__float_as_uint(
                                         fabsf(uf - z.hi / nrm.hi) / tau));
       }
     }
@@ -192,8 +193,8 @@ template <int MODE, bool BF16, int GL>
 __device__ __forceinline__ void refine_group(const Params& p, const Tab& tb, const float* Vt,
                                              const float* cb_s, const unsigned char* xs,
                                              unsigned char* codes_s, int ks, __half* side_s,
-                                             unsigned* nside, int tt, int k, int sub, bool act,
-                                             float uf, float tau) {
+                                             unsigned* nside, unsigned long long* cnt, int tt,
+                                             int k, int sub, bool act, float uf, float tau) {
   const int D = p.D;
   const bool norm_entry = k == (int)kNormEntry;
   const int kk = norm_entry ? 0 : k;
@@ -209,7 +210,7 @@ __device__ __forceinline__ void refine_group(const Params& p, const Tab& tb, con
     const int qmax = tb.qp[k].x;
     codes_s[tt * ks + kp] = (uint8_t)(int)fminf(fmaxf(q, 0.f), (float)qmax);
     if (tau > 0.f)
-      atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(fabsf(uf - u.hi) / tau));
+      atomicMax(&cnt[3], (unsigned long long)__float_as_uint(fabsf(uf - u.hi) / tau));
     return;
   }
   const ff2 nrm = ff_sqrt(xx);
@@ -232,7 +233,7 @@ __device__ __forceinline__ void refine_group(const Params& p, const Tab& tb, con
   }
   codes_s[tt * ks + kp] = (uint8_t)lo_i;
   if (tau > 0.f && !zero)
-    atomicMax(&p.counters[3], (unsigned long long)__float_as_uint(fabsf(uf - z.hi / nrm.hi) / tau));
+    atomicMax(&cnt[3], (unsigned long long)__float_as_uint(fabsf(uf - z.hi / nrm.hi) / tau));
 }
 
 // Uniform fast path: u = (z - mean . V_k - lo) / step as one fma of the
@@ -368,6 +369,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
   float* mids_s = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(vt0) + QG * vt_bytes);
   float* cb_s = mids_s + 256;                                       // [256]
   __shared__ float mpad[9];  // codebooks of <= 8 levels: -inf, the midpoints, +inf
+  __shared__ unsigned long long cnt_s[4];  // this CTA's counters, added to p.counters at exit
   const int tab_off = nbox * 16384;                                 // table after the x boxes
 
   if (warp == kMmaWarp) tmem_alloc(&tmem_base, t.cols);
@@ -379,6 +381,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
     fence_mbar_init();
     abort_flag = 0;
     for (int i = 0; i < kQG; ++i) qcount_g[i] = nside_g[i] = 0;
+    for (int i = 0; i < 4; ++i) cnt_s[i] = 0ull;
   }
   if (MODE == KVC_MODE_CODEBOOK) {
     for (int j = tid; j < p.cb_levels - 1; j += kThreads) mids_s[j] = p.mids[j];
@@ -584,6 +587,14 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
           uint32_t rr[SB];
 #pragma unroll
           for (int j = 0; j < SB; ++j) z[j] = 0.f;
+          if (t.npieces == 2) {  // both pieces loaded before one wait
+            uint32_t r1[SB];
+            tmem_ld_n<SB>(la + rpad, r1);
+            tmem_ld_n<SB>(la, rr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < SB; ++j) z[j] = __uint_as_float(rr[j]) + __uint_as_float(r1[j]);
+          } else {
           for (int pc = t.npieces - 1; pc >= 1; --pc) {
             tmem_ld_n<SB>(la + pc * rpad, rr);
             tmem_wait_ld();
@@ -594,6 +605,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < SB; ++j) z[j] = __uint_as_float(rr[j]) + z[j];
+          }
         }
         if (!live) continue;
         uint32_t nmask = 0;
@@ -644,7 +656,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
         }
         for (; ovf; ovf &= ovf - 1) {
           const int k = cblk * CW + sb * SB + (__ffs(ovf) - 1);
-          refine_ws<MODE, BF16, false>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside, row, k, 0,
+          refine_ws<MODE, BF16, false>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside, cnt_s, row, k, 0,
                                        0.f, 0.f);
         }
       }
@@ -659,7 +671,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
               queue[q] = ((uint32_t)row << 16) | kNormEntry;
               aux[q] = make_float2(0.f, 0.f);
             } else {
-              refine_ws<MODE, BF16, false>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside, row,
+              refine_ws<MODE, BF16, false>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside, cnt_s, row,
                                            (int)kNormEntry, 0, 0.f, 0.f);
             }
           } else {
@@ -669,24 +681,24 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       }
       named_bar_sync(qbar, kQThreads);  // B2: fast-path codes and the queue complete
       const unsigned nq = qcount;
-      {  // four entries per warp at a time, eight lanes each
-        constexpr int GL = 8, PER = 32 / GL;
+      {  // two entries per warp at a time, sixteen lanes each
+        constexpr int GL = 16, PER = 32 / GL;
         const unsigned nqe = min(nq, (unsigned)kQueue);
         for (unsigned e0 = wq * PER; e0 < nqe; e0 += kQWarps * PER) {
           const unsigned e = e0 + lane / GL;
           const bool act = e < nqe;
           const uint32_t ent = queue[act ? e : e0];
           const float2 ax = aux[act ? e : e0];
-          refine_group<MODE, BF16, GL>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside,
+          refine_group<MODE, BF16, GL>(p, tb, Vt, cb_s, xs, codes_s, ks, side_s, &nside, cnt_s,
                                        (int)(ent >> 16), (int)(ent & 0xffffu), lane & (GL - 1),
                                        act, ax.x, ax.y);
         }
       }
       named_bar_sync(qbar, kQThreads);  // B3: every code decided
       if (qt == 0) {
-        if (nq > nside) atomicAdd(&p.counters[0], (unsigned long long)(nq - nside));
-        if (nside) atomicAdd(&p.counters[1], (unsigned long long)nside);
-        if (hd.slot == 0) atomicAdd(&p.counters[2], (unsigned long long)n);
+        if (nq > nside) atomicAdd(&cnt_s[0], (unsigned long long)(nq - nside));
+        if (nside) atomicAdd(&cnt_s[1], (unsigned long long)nside);
+        if (hd.slot == 0) atomicAdd(&cnt_s[2], (unsigned long long)n);
       }
       // pack: one thread per (token, 8-code chunk) -> w bytes, LSB-first; a
       // codebook's single segment 32 codes at a time
@@ -737,6 +749,8 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
   }
   __syncthreads();
   if (abort_flag && tid == 0) atomicCAS(p.err, 0, kErrTimeout);
+  if (tid < 3 && cnt_s[tid]) atomicAdd(&p.counters[tid], cnt_s[tid]);  // once per CTA
+  if (tid == 3 && cnt_s[3]) atomicMax(&p.counters[3], cnt_s[3]);
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(taddr0, t.cols);
