@@ -154,6 +154,17 @@ __device__ __forceinline__ uint4 decode_codebook(uint2 b, int w, const uint16_t*
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// The same for widths w <= 4 through a table of code pairs: entry c0 | c1 << w
+// holds the fp16 centroids of (c0, c1) as one half2 word.
+__device__ __forceinline__ uint4 decode_codebook_pairs(uint2 b, int w, const uint32_t* cb2) {
+  const uint64_t bits = (uint64_t)b.x | ((uint64_t)b.y << 32);
+  const uint32_t mask2 = (1u << (2 * w)) - 1u;
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) o[q] = cb2[(uint32_t)(bits >> (2 * w * q)) & mask2];
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 template <int MODE, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fetch_pipe_kernel(const Params p, const PipeArgs t, const __grid_constant__ CUtensorMap omap) {
@@ -184,10 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* stage = smem;                                  // SS x nbox x 16 KB
   unsigned char* Bs = stage + SS * nbox * 16384;                // NB x [D x K] fp16
   unsigned char* rs = Bs + NB * b_bytes;                        // RS x row stage
-  // after the row stages: codebook mode the fp16 centroids [256] and the norm
-  // ring [kNormRing][128]; group mode the epilogue groups' mean cache
+  // after the row stages: codebook mode the fp16 centroids [256], the norm
+  // ring [kNormRing][128] and the centroid pairs [256]; group mode the
+  // epilogue groups' mean cache
   uint16_t* cbh = reinterpret_cast<uint16_t*>(rs + (size_t)RS * t.rs_bytes);
   float* norm_ring = reinterpret_cast<float*>(cbh + 256);
+  uint32_t* cb2 = reinterpret_cast<uint32_t*>(norm_ring + kNormRing * kTile);  // [256] pairs
   float* mean_c = reinterpret_cast<float*>(rs + (size_t)RS * t.rs_bytes);  // [hpg][D]
   // a row stage: [0, 128) chunk table, then the packed rows, then the side words
   const int side_off = t.rs_bytes - (int)(((size_t)kTile * p.side_bytes + 16 + 15) & ~size_t(15));
@@ -205,9 +218,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     abort_flag = 0;
   }
-  if (MODE == KVC_MODE_CODEBOOK)
+  if (MODE == KVC_MODE_CODEBOOK) {
     for (int j = tid; j < p.cb_levels; j += kThreads)
       cbh[j] = __half_as_ushort(__float2half_rn(p.codebook[j]));
+    if (p.cb_bits <= 4)
+      for (int j = tid; j < p.cb_levels * p.cb_levels; j += kThreads) {
+        const int c0 = j & (p.cb_levels - 1), c1 = j >> p.cb_bits;
+        cb2[j] = (uint32_t)__half_as_ushort(__float2half_rn(p.codebook[c0])) |
+                 ((uint32_t)__half_as_ushort(__float2half_rn(p.codebook[c1])) << 16);
+      }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -397,8 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (live) {
               const int w = (int)((ent[u] >> 16) & 0xfu);
               if (ent[u] >> 31) {
-                v = MODE == KVC_MODE_CODEBOOK ? decode_codebook(bits[u], w, cbh)
-                                              : decode_uniform(bits[u], w);
+                v = MODE == KVC_MODE_CODEBOOK
+                        ? (w <= 4 ? decode_codebook_pairs(bits[u], w, cb2)
+                                  : decode_codebook(bits[u], w, cbh))
+                        : decode_uniform(bits[u], w);
                 if (GRP) {  // (code - 2^(w-1)) * s, one fp16 rounding; s: the chunk's group scale
                   const uint32_t sg = (uint32_t)reinterpret_cast<const uint16_t*>(
                       st_base + side_off)[tt * n_groups + (int)((ent[u] >> 20) & 0xffu)];
@@ -565,7 +587,7 @@ size_t fetch_pipe_smem(int mode, int D, int hpg, int K, int side_bytes, int pmax
   z.n_b = n_bases > 1 ? 2 : 1;
   z.n_stg = 2;
   z.n_rs = min_rs;
-  const size_t tail = mode == KVC_MODE_CODEBOOK ? 256 * 2 + (size_t)kNormRing * kTile * 4
+  const size_t tail = mode == KVC_MODE_CODEBOOK ? 256 * 2 + (size_t)kNormRing * kTile * 4 + 256 * 4
                       : mode == KVC_MODE_GROUP  ? (size_t)hpg * D * 4
                                                 : 0;
   auto total = [&](const FetchPipeShape& q) {
