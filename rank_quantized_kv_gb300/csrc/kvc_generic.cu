@@ -842,32 +842,51 @@ __global__ void __launch_bounds__(256, 3) append_int8_pipe(Params p, AppendArgs 
   const int64_t total = (int64_t)p.n_slots * a.T;
   const int64_t step = (int64_t)gridDim.x * RPB;
   const int64_t r0 = (int64_t)blockIdx.x * RPB + tid / TPR;
-  auto issue = [&](int64_t r, int st) {
-    if (r < total) {
-      const int slot = (int)(r / a.T);
-      const int64_t t = r - (int64_t)slot * a.T;
+  // (slot, token) of a row, advanced by one step without dividing: a step is
+  // sq slots and st_rem tokens
+  const int64_t sq = step / a.T, st_rem = step - sq * a.T;
+  struct Pos {
+    int64_t slot, t;
+  };
+  auto advance = [&](Pos& q) {
+    q.slot += sq;
+    q.t += st_rem;
+    if (q.t >= a.T) {
+      q.t -= a.T;
+      ++q.slot;
+    }
+  };
+  Pos pi{r0 / a.T, 0}, pp;
+  pi.t = r0 - pi.slot * a.T;
+  pp = pi;
+  auto issue = [&](const Pos& q, int st) {
+    if (q.slot < p.n_slots) {
+      const int slot = (int)q.slot;
       const int b = slot / p.H, h = slot - b * p.H;
       const char* src = static_cast<const char*>(a.x) +
-                        ((int64_t)b * a.sb + (int64_t)h * a.sh + t * a.st + kI8NV * j) * ESZ;
+                        ((int64_t)b * a.sb + (int64_t)h * a.sh + q.t * a.st + kI8NV * j) * ESZ;
 #pragma unroll
-      for (int q = 0; q < Q; ++q) {
+      for (int qq = 0; qq < Q; ++qq) {
         const uint32_t dst =
-            (uint32_t)__cvta_generic_to_shared(&stage_buf[((size_t)st * Q + q) * 256 + tid]);
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src + 16 * q)
+            (uint32_t)__cvta_generic_to_shared(&stage_buf[((size_t)st * Q + qq) * 256 + tid]);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src + 16 * qq)
                      : "memory");
       }
     }
     asm volatile("cp.async.commit_group;\n" ::: "memory");
   };
 #pragma unroll
-  for (int s0 = 0; s0 < kI8Stages - 1; ++s0) issue(r0 + s0 * step, s0);
+  for (int s0 = 0; s0 < kI8Stages - 1; ++s0) {
+    issue(pi, s0);
+    advance(pi);
+  }
   unsigned nref = 0, rows0 = 0;
-  for (int64_t k = 0;; ++k) {
-    const int64_t r = r0 + k * step;
-    if (r - (int64_t)(tid / TPR) >= total) break;  // the whole block step is past the end
-    issue(r + (kI8Stages - 1) * step, (int)((k + kI8Stages - 1) % kI8Stages));
+  int64_t rb = (int64_t)blockIdx.x * RPB;  // the block's first row of the step
+  for (int k = 0; rb < total; ++k, rb += step) {
+    issue(pi, (k + kI8Stages - 1) % kI8Stages);
+    advance(pi);
     asm volatile("cp.async.wait_group %0;\n" ::"n"(kI8Stages - 1) : "memory");
-    const int st = (int)(k % kI8Stages);
+    const int st = k % kI8Stages;
     float v[kI8NV];
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
@@ -892,11 +911,11 @@ __global__ void __launch_bounds__(256, 3) append_int8_pipe(Params p, AppendArgs 
         }
       }
     }
-    const bool valid = r < total;
-    const int slot = valid ? (int)(r / a.T) : 0;
-    const int64_t t = valid ? r - (int64_t)slot * a.T : a.T;
-    nref += append_int8_vals<TPR>(p, a, slot, t, j, valid, v);
+    const bool valid = pp.slot < p.n_slots;
+    const int slot = valid ? (int)pp.slot : 0;
+    nref += append_int8_vals<TPR>(p, a, slot, valid ? pp.t : a.T, j, valid, v);
     rows0 += (valid && slot == 0 && j == 0) ? 1u : 0u;
+    advance(pp);
   }
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
   nref = __reduce_add_sync(kFull, nref);
