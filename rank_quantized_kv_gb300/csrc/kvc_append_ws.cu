@@ -272,7 +272,8 @@ __device__ __forceinline__ void pack32(const uint32_t (&in)[8], uint32_t (&out)[
 }
 
 // Codebook rows (one segment of D codes, D a multiple of 32): one thread per
-// (token, 32 codes), 8-byte loads of the codes, W 4-byte stores of the bits.
+// (token, 32 codes), 8-byte loads of the codes, W 4-byte stores of the bits to
+// out (rows P bytes apart, 4-byte aligned).
 template <int W>
 __device__ __forceinline__ void pack_codebook(int qt, int n, int D, const unsigned char* codes_s,
                                               int ks, unsigned char* out_s, int P) {
@@ -700,18 +701,23 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
         if (nside) atomicAdd(&cnt_s[1], (unsigned long long)nside);
         if (hd.slot == 0) atomicAdd(&cnt_s[2], (unsigned long long)n);
       }
-      // pack: one thread per (token, 8-code chunk) -> w bytes, LSB-first; a
-      // codebook's single segment 32 codes at a time
       const int P = hd.P;
       if (MODE == KVC_MODE_CODEBOOK && D % 32 == 0) {
+        // a codebook's single segment, 32 codes at a time, written straight to
+        // the store: every re-decision is done (B3), so the x stage is free and
+        // no staging or second barrier is needed
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&x_empty[s]);
+        unsigned char* dst = p.store + hd.pay + hd.row0 * P;
         switch (p.cb_bits) {
-          case 1: pack_codebook<1>(qt, n, D, codes_s, ks, out_s, P); break;
-          case 2: pack_codebook<2>(qt, n, D, codes_s, ks, out_s, P); break;
-          case 3: pack_codebook<3>(qt, n, D, codes_s, ks, out_s, P); break;
-          case 4: pack_codebook<4>(qt, n, D, codes_s, ks, out_s, P); break;
-          default: pack_codebook<8>(qt, n, D, codes_s, ks, out_s, P); break;
+          case 1: pack_codebook<1>(qt, n, D, codes_s, ks, dst, P); break;
+          case 2: pack_codebook<2>(qt, n, D, codes_s, ks, dst, P); break;
+          case 3: pack_codebook<3>(qt, n, D, codes_s, ks, dst, P); break;
+          case 4: pack_codebook<4>(qt, n, D, codes_s, ks, dst, P); break;
+          default: pack_codebook<8>(qt, n, D, codes_s, ks, dst, P); break;
         }
-      } else
+      } else {
+      // pack: one thread per (token, 8-code chunk) -> w bytes, LSB-first
       for (int item = qt; item < kTile * 32; item += kQThreads) {
         const int tt = item & (kTile - 1), c = item >> 7;
         const uint32_t ent = tb.chunk[c];
@@ -738,6 +744,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
         for (int idx = 16 * nv + qt; idx < n * P; idx += kQThreads) dst[idx] = out_s[idx];
       } else {
         for (int idx = qt; idx < n * P; idx += kQThreads) dst[idx] = out_s[idx];
+      }
       }
       if (MODE == KVC_MODE_CODEBOOK && qt < n)
         reinterpret_cast<__half*>(p.store + hd.side)[hd.row0 + qt] = side_s[qt];
