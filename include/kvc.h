@@ -446,13 +446,15 @@ void kvc_destroy(kvc_layer *layer);
  * whose work overlaps on the GPU (other streams, other threads) race and
  * corrupt each other's tables: order them on one stream.  The first call on
  * a device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.  The
+ * that device current.  The call cannot be captured into a CUDA graph (the
+ * upload reads a host buffer that is freed on return): while `stream` is
+ * capturing it returns KVC_EINVAL and enqueues nothing.  The
  * address is that of the CUDA runtime's primary context of the device: call
  * this entry point from the runtime's context, not from a context created
  * with the driver API.
  *
- * Errors: KVC_EINVAL for a bad descriptor or pointers, or when the tables
- * exceed 8 MiB (e.g. many bases of a large D_in x r); KVC_ECAPACITY if
+ * Errors: KVC_EINVAL for a bad descriptor or pointers, under stream capture,
+ * or when the tables exceed 8 MiB (e.g. many bases of a large D_in x r); KVC_ECAPACITY if
  * length + T > capacity; KVC_ECUDA on a CUDA error.  Nothing is written on
  * error.  Calls no cudaMalloc or cudaFree. */
 kvc_status kvc_append_noalloc(const kvc_layer_desc *desc, int64_t length, const void *x,

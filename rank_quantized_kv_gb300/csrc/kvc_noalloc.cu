@@ -73,8 +73,20 @@ extern "C" kvc_status kvc_append_noalloc(const kvc_layer_desc* desc, int64_t len
   if (T == 0) return KVC_OK;
   if (!x) return kvc::set_error(KVC_EINVAL, "x is NULL");
 
+  // The tables are uploaded from a host vector that is freed on return, so
+  // the call cannot be recorded into a CUDA graph: a replay would upload
+  // whatever then occupies that memory.
+  auto s = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cap);
+  if (e != cudaSuccess) return kvc::set_error(KVC_ECUDA, "cudaStreamIsCapturing failed");
+  if (cap != cudaStreamCaptureStatusNone)
+    return kvc::set_error(KVC_EINVAL,
+                          "kvc_append_noalloc cannot run under stream capture; call it "
+                          "outside the captured region");
+
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return kvc::set_error(KVC_ECUDA, "cudaGetDevice failed");
   if (!kvc::device_ptr_on(desc->store, dev) || !kvc::device_ptr_on(x, dev))
     return kvc::set_error(KVC_EINVAL, "store and x must be device memory of the current device");
@@ -84,7 +96,6 @@ extern "C" kvc_status kvc_append_noalloc(const kvc_layer_desc* desc, int64_t len
 
   // The image carries a zeroed error word and zeroed counters, so every call
   // starts them from zero; the tables overwrite the previous call's.
-  auto s = static_cast<cudaStream_t>(stream);
   e = cudaMemcpyAsync(scratch, im.bytes.data(), im.bytes.size(), cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return kvc::set_error(KVC_ECUDA, "upload of the parameter tables failed");
 

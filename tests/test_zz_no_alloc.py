@@ -99,3 +99,38 @@ def test_noalloc_rejects_tables_beyond_its_limit(kvc):
     assert st == -1 and b"8 MiB" in lib.kvc_last_error()
     torch.cuda.synchronize()
     assert int(store.count_nonzero()) == 0
+
+
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
+def test_noalloc_refuses_stream_capture(kvc):
+    # The tables are uploaded from a host buffer freed on return, so a captured
+    # call would replay a stale upload: the call must refuse and enqueue nothing.
+    B, H, D = 1, 8, 128
+    x = synth.kv_spectral(B, H, 40, D, alpha=1.0, seed=9400, tensor=0, dtype="bf16")
+    params = fit_uniform(x.double().numpy(), 256, 32, [0, 2, 4, 8], 128)
+    desc, keep = kvc._build_desc("uniform", B, H, D, None, params["V"], params["mean"],
+                                 params["bits"], params["qmin"], params["qstep"],
+                                 params.get("basis_of"), 1, 32, None, "bf16", "f16", 64)
+    n = kvc.store_bytes("uniform", B, H, D, capacity=64, V=params["V"], bits=params["bits"],
+                        qmin=params["qmin"], qstep=params["qstep"],
+                        basis_of=params.get("basis_of"))
+    store = torch.zeros(n, dtype=torch.uint8, device="cuda:0")
+    desc.store = ctypes.c_void_p(store.data_ptr())
+    desc.store_bytes = n
+    xd = x.to("cuda:0")
+    lib = kvc.load_library()
+    sb, sh, st_, _ = xd.stride()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=side):
+        cur = torch.cuda.current_stream().cuda_stream
+        status = lib.kvc_append_noalloc(ctypes.byref(desc), 0, ctypes.c_void_p(xd.data_ptr()),
+                                        xd.shape[2], sb, sh, st_, ctypes.c_void_p(cur))
+    assert status == -1 and b"capture" in lib.kvc_last_error()
+    torch.cuda.synchronize()
+    assert int(store.count_nonzero()) == 0
+    # Outside the capture the same call succeeds.
+    _noalloc(kvc, desc, 0, xd)
+    torch.cuda.synchronize()
+    assert int(store.count_nonzero()) > 0
