@@ -751,27 +751,49 @@ __device__ __forceinline__ unsigned append_int8_vals(const Params& p, const Appe
     const bool slow = !(am > 2e-6f);
     const bool exact16 = p.in_dtype != KVC_F32 && am < 1e30f;  // no overflow in 254 v
     const float inv = slow ? 0.f : 127.f / am;
+    // Rounding by adding 1.5 2^23 (half to even for |u| < 2^22) leaves the
+    // code in the low byte of the sum, two's complement, so four codes are
+    // packed by byte permutes: no float-to-int conversions on this path.
+    constexpr float kMagic = 12582912.f;
     uint32_t packed[kI8NV / 4];
+    bool any_near = slow;  // a value within 3e-5 of a half, a NaN, or a tiny row
 #pragma unroll
-    for (int i = 0; i < kI8NV / 4; ++i) packed[i] = 0u;
-    uint32_t flag = 0;  // values within 3e-5 of a half (or a tiny row)
+    for (int i = 0; i < kI8NV; i += 4) {
+      uint32_t tb[4];
 #pragma unroll
-    for (int i = 0; i < kI8NV; ++i) {
-      const float u = v[i] * inv;
-      const float q = rintf(u);
-      flag |= (uint32_t)(fabsf(u - q) > 0.5f - 3e-5f) << i;
-      packed[i >> 2] |= ((uint32_t)__float2int_rn(q) & 0xffu) << (8 * (i & 3));
+      for (int e = 0; e < 4; ++e) {
+        const float u = __fmul_rn(v[i + e], inv);
+        const float t = __fadd_rn(u, kMagic);
+        any_near |= !(fabsf(__fsub_rn(u, __fsub_rn(t, kMagic))) <= 0.5f - 3e-5f);
+        tb[e] = __float_as_uint(t);
+      }
+      packed[i >> 2] =
+          __byte_perm(__byte_perm(tb[0], tb[1], 0x0040), __byte_perm(tb[2], tb[3], 0x0040), 0x5410);
     }
-    if (slow) flag = 0xffffffffu;
+    uint32_t flag = 0;
+    if (any_near) {
+#pragma unroll
+      for (int i = 0; i < kI8NV; ++i) {
+        const float u = v[i] * inv;
+        flag |= (uint32_t)!(fabsf(u - rintf(u)) <= 0.5f - 3e-5f) << i;
+      }
+      if (slow) flag = 0xffffffffu;
+    }
     if (flag) {  // rare: re-decide those exactly, then patch their bytes
       double s64 = fmax((double)am / 127.0, 1e-8);
       for (uint32_t f = flag; f; f &= f - 1) {
         const int i = __ffs(f) - 1;
-        ++nref;
         float vi = 0.f;
 #pragma unroll
         for (int e = 0; e < kI8NV; ++e) vi = e == i ? v[e] : vi;  // no local-memory indexing
         const float u = vi * inv;
+        if (!slow && u != u) {  // a NaN (or an infinity times 0): code 0
+#pragma unroll
+          for (int w = 0; w < kI8NV / 4; ++w)
+            if (w == (i >> 2)) packed[w] &= ~(0xffu << (8 * (i & 3)));
+          continue;
+        }
+        ++nref;
         const float k = floorf(fabsf(u));
         const float d = exact16 && !slow ? 254.f * fabsf(vi) - (2.f * k + 1.f) * am : 0.f;
         float q;
@@ -933,18 +955,25 @@ __global__ void __launch_bounds__(256) fetch_int8_vec(Params p, FetchArgs f) {
   for (int slot = blockIdx.y; slot < p.n_slots; slot += gridDim.y) {
   const int b = slot / p.H, h = slot - b * p.H;
   const uint2 q = *reinterpret_cast<const uint2*>(p.store + p.pay_off[slot] + t * p.D + 8 * j);
-  const float s = __half2float(reinterpret_cast<const __half*>(p.store + p.side_off[slot])[t]);
-  const uint32_t w[2] = {q.x, q.y};
+  const __half sh = reinterpret_cast<const __half*>(p.store + p.side_off[slot])[t];
+  // Code byte b + 128 placed in the low mantissa bits of fp16 1024 gives
+  // 1024 + 128 + b exactly; subtracting 1152 leaves b as an fp16 integer.  No
+  // int-to-float conversions.  b s is exact in fp32 (8 by 11 significant
+  // bits), so one fp16 product rounds exactly as fp16(float(b) s) does.
+  const uint32_t w[2] = {q.x ^ 0x80808080u, q.y ^ 0x80808080u};
+  const __half2 bias = __float2half2_rn(-1152.f);
   uint32_t o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float v0 = (float)(int8_t)((w[i >> 1] >> (16 * (i & 1))) & 0xffu) * s;
-    const float v1 = (float)(int8_t)((w[i >> 1] >> (16 * (i & 1) + 8)) & 0xffu) * s;
+    const uint32_t hb = __byte_perm(w[i >> 1], 0x64646464u, (i & 1) ? 0x4342 : 0x4140);
+    const __half2 b2 = __hadd2(*reinterpret_cast<const __half2*>(&hb), bias);
     if (p.out_dtype == KVC_F16) {
-      const __half2 hv = __floats2half2_rn(v0, v1);
+      const __half2 hv = __hmul2(b2, __half2half2(sh));
       o[i] = *reinterpret_cast<const uint32_t*>(&hv);
     } else {
-      const __nv_bfloat162 hv = __floats2bfloat162_rn(v0, v1);
+      const float2 f = __half22float2(b2);
+      const float s = __half2float(sh);
+      const __nv_bfloat162 hv = __floats2bfloat162_rn(f.x * s, f.y * s);
       o[i] = *reinterpret_cast<const uint32_t*>(&hv);
     }
   }
