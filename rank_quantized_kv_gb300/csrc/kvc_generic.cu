@@ -715,7 +715,7 @@ __device__ __forceinline__ void load8(const void* x, int dt, int64_t off, float 
 // each), so the sign of their difference decides it; an exact tie, fp32
 // inputs, a < 2e-6 and a >= 1e30 take the float64 path.
 constexpr int kI8NV = 32;
-template <int TPR>
+template <int TPR, bool IL = false>
 __device__ __forceinline__ unsigned append_int8_vals(const Params& p, const AppendArgs& a, int slot,
                                                      int64_t t, int j, bool valid,
                                                      float (&v)[kI8NV]);
@@ -737,7 +737,9 @@ __device__ __forceinline__ unsigned append_int8_row(const Params& p, const Appen
   return append_int8_vals<TPR>(p, a, slot, t, j, valid, v);
 }
 
-template <int TPR>
+// IL (interleaved): the thread's values are the row's 8-value groups
+// j, j + TPR, j + 2 TPR, j + 3 TPR instead of 32 consecutive values.
+template <int TPR, bool IL>
 __device__ __forceinline__ unsigned append_int8_vals(const Params& p, const AppendArgs& a, int slot,
                                                      int64_t t, int j, bool valid,
                                                      float (&v)[kI8NV]) {
@@ -809,11 +811,18 @@ __device__ __forceinline__ unsigned append_int8_vals(const Params& p, const Appe
             packed[w] = (packed[w] & ~(0xffu << (8 * (i & 3)))) | (byte << (8 * (i & 3)));
       }
     }
-    uint8_t* dst = p.store + p.pay_off[slot] + (a.t_base + t) * p.D + kI8NV * j;
+    if (IL) {
+      uint8_t* dst = p.store + p.pay_off[slot] + (a.t_base + t) * p.D + 8 * j;
 #pragma unroll
-    for (int w = 0; w < kI8NV / 16; ++w)
-      reinterpret_cast<uint4*>(dst)[w] =
-          make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2], packed[4 * w + 3]);
+      for (int g = 0; g < kI8NV / 8; ++g)
+        reinterpret_cast<uint2*>(dst + 8 * TPR * g)[0] = make_uint2(packed[2 * g], packed[2 * g + 1]);
+    } else {
+      uint8_t* dst = p.store + p.pay_off[slot] + (a.t_base + t) * p.D + kI8NV * j;
+#pragma unroll
+      for (int w = 0; w < kI8NV / 16; ++w)
+        reinterpret_cast<uint4*>(dst)[w] =
+            make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2], packed[4 * w + 3]);
+    }
     if (j == 0) {
       const float s32 = am / 127.f;
       __half s16;
@@ -858,6 +867,7 @@ constexpr int kI8Stages = 4;
 template <int TPR, int ESZ>
 __global__ void __launch_bounds__(256, 3) append_int8_pipe(Params p, AppendArgs a) {
   constexpr int Q = kI8NV * ESZ / 16;  // 16-byte pieces of a thread's values
+  constexpr bool IL = ESZ == 2;
   constexpr int RPB = 256 / TPR;       // rows per block step
   extern __shared__ uint4 stage_buf[];  // [kI8Stages][Q][256]
   const int tid = threadIdx.x, j = tid % TPR;
@@ -885,13 +895,17 @@ __global__ void __launch_bounds__(256, 3) append_int8_pipe(Params p, AppendArgs 
     if (q.slot < p.n_slots) {
       const int slot = (int)q.slot;
       const int b = slot / p.H, h = slot - b * p.H;
+      // 16-bit inputs: piece qq is the row's 16-byte piece TPR qq + j, so
+      // each copy instruction of a warp reads whole 32-byte sectors
       const char* src = static_cast<const char*>(a.x) +
-                        ((int64_t)b * a.sb + (int64_t)h * a.sh + q.t * a.st + kI8NV * j) * ESZ;
+                        ((int64_t)b * a.sb + (int64_t)h * a.sh + q.t * a.st +
+                         (IL ? 8 * j : kI8NV * j)) * ESZ;
 #pragma unroll
       for (int qq = 0; qq < Q; ++qq) {
         const uint32_t dst =
             (uint32_t)__cvta_generic_to_shared(&stage_buf[((size_t)st * Q + qq) * 256 + tid]);
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src + 16 * qq)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst),
+                     "l"(src + 16 * (IL ? TPR * qq : qq))
                      : "memory");
       }
     }
@@ -935,7 +949,7 @@ __global__ void __launch_bounds__(256, 3) append_int8_pipe(Params p, AppendArgs 
     }
     const bool valid = pp.slot < p.n_slots;
     const int slot = valid ? (int)pp.slot : 0;
-    nref += append_int8_vals<TPR>(p, a, slot, valid ? pp.t : a.T, j, valid, v);
+    nref += append_int8_vals<TPR, IL>(p, a, slot, valid ? pp.t : a.T, j, valid, v);
     rows0 += (valid && slot == 0 && j == 0) ? 1u : 0u;
     advance(pp);
   }
