@@ -240,16 +240,19 @@ __device__ __forceinline__ void refine_group(const Params& p, const Tab& tb, con
 // table's fused constants and the code; `near` flags a rounding boundary
 // within the bound tau of u (host derivation in append_ws_table; tau holds for
 // |u| <= qmax + 1, the range of the interior boundaries).  With `exact` the
-// boundary must also be interior (a first pass may flag the outer ones too).
+// boundary is the nearest interior one (a first pass may flag outer ones too).
 template <bool EXACT>
 __device__ __forceinline__ int fast_uniform(const Tab& tb, int k, int qmax, float z, float nx,
                                             float& u, float& tau, bool& near) {
   const float4 q = tb.q4[k];
   u = fmaf(z, q.x, q.y);
   tau = fmaf(q.z, nx, q.w);
-  const float hb = floorf(u) + 0.5f;
+  // the interior boundary nearest u (0.5 .. qmax - 0.5); a first pass may
+  // take the nearest half-integer, never farther than that one, so it flags a
+  // superset (checked again with `exact`)
+  const float hb0 = floorf(u) + 0.5f;
+  const float hb = EXACT ? fminf(fmaxf(hb0, 0.5f), (float)qmax - 0.5f) : hb0;
   near = fabsf(u - hb) <= tau;
-  if (EXACT) near = near && hb >= 0.5f && hb <= (float)qmax - 0.5f;
   return min(max(__float2int_rn(u), 0), qmax);
 }
 

@@ -141,6 +141,55 @@ __device__ __forceinline__ ff2 dot_ff(const float* x, const float* m, const floa
   return ff2{s, e};
 }
 
+// sum_i (x_i - m_i) * w_i in fp32, one warp, on every lane: each lane keeps
+// four fma chains (one per component of its 16-byte loads), so no chain is
+// longer than L = ceil(n / 128) terms (ceil(n / 32) for rows that are not
+// 16-byte multiples); the chains and the lanes are then added with TwoSum
+// into a double-float.  Error bound, u = 2^-24:
+//   |result - sum (x_i - m_i) w_i| <= (gamma_L (1 + u) + u + 2^-40) sum |x_i - m_i| |w_i|
+// (gamma_L for the chains, u for the rounding of x - m, 2^-40 for the
+// compensated sums).  mid_gamma(n) is that factor.
+__device__ __forceinline__ float mid_gamma(int n) {
+  const int L = (n & 3) == 0 ? (n + 127) / 128 : (n + 31) / 32;
+  return gamma_n(L) * (1.f + kU) + kU + 1e-12f;
+}
+
+__device__ __forceinline__ ff2 dot_mid(const float* x, const float* m, const float* w, int n,
+                                       int lane) {
+  float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+  if ((n & 3) == 0) {
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    const float4* m4 = reinterpret_cast<const float4*>(m);
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    const int n4 = n >> 2;
+#pragma unroll 4
+    for (int j = lane; j < n4; j += 32) {
+      const float4 xv = x4[j], mv = m4[j], wv = __ldg(w4 + j);
+      c0 = fmaf(xv.x - mv.x, wv.x, c0);
+      c1 = fmaf(xv.y - mv.y, wv.y, c1);
+      c2 = fmaf(xv.z - mv.z, wv.z, c2);
+      c3 = fmaf(xv.w - mv.w, wv.w, c3);
+    }
+  } else {
+    for (int i = lane; i < n; i += 32) c0 = fmaf(x[i] - m[i], w[i], c0);
+  }
+  float S, C, e;
+  two_sum(c0, c1, S, C);
+  two_sum(S, c2, S, e);
+  C += e;
+  two_sum(S, c3, S, e);
+  C += e;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float So = __shfl_xor_sync(kFull, S, o);
+    const float Co = __shfl_xor_sync(kFull, C, o);
+    two_sum(S, So, S, e);
+    C = C + Co + e;
+  }
+  two_sum(S, C, S, e);
+  return ff2{S, e};
+}
+
 // sum_i x_i^2 in double precision, one warp.
 __device__ __forceinline__ double sumsq64(const float* x, int n, int lane) {
   double acc = 0.0;
@@ -186,8 +235,10 @@ __device__ void quant_uniform(const Params& p, int beta, const float* vnorm, con
     const float tau_z = gam * c.nrm * vnorm[k] * (1.f + 1e-3f);
     const float tau_u = tau_z * inv * (1.f + 1e-6f) + 4.f * kU * (fabsf(u) + 1.f);
     qmax = (1 << w) - 1;
-    const float hb = floorf(u) + 0.5f;
-    near = (hb >= 0.5f) && (hb <= (float)qmax - 0.5f) && (fabsf(u - hb) <= tau_u);
+    // the interior boundary nearest u (0.5 .. qmax - 0.5): with a wide tau
+    // the one below a clamped u counts too
+    const float hb = fminf(fmaxf(floorf(u) + 0.5f, 0.5f), (float)qmax - 0.5f);
+    near = fabsf(u - hb) <= tau_u;
     code = (int)fminf(fmaxf(rintf(u), 0.f), (float)qmax);
   }
   unsigned m = __ballot_sync(kFull, near);
@@ -236,22 +287,72 @@ __device__ void quant_group(const Params& p, int beta, const float* vnorm, const
   float u = full ? 0.f : z / s32;
   const float au = fabsf(u);
   const float tau_u = full ? 0.f : (tz / s32 + au * eps) * (1.f + 1e-6f) + 4.f * kU * (au + 1.f);
-  const float hb = floorf(au) + 0.5f;
-  const bool near = valid && !full && (hb <= (float)qmax - 0.5f) && (fabsf(au - hb) <= tau_u);
+  // the interior boundary nearest |u| (0.5 .. qmax - 0.5)
+  const float hb = fminf(floorf(au) + 0.5f, (float)qmax - 0.5f);
+  const bool near = valid && !full && (fabsf(au - hb) <= tau_u);
   int q = (int)fminf(fmaxf(rintf(u), -(float)qmax), (float)qmax);
   __half s16 = __float2half_rn(s32);
 
   const unsigned vmask = __ballot_sync(kFull, valid);
   const unsigned nmask = full ? vmask : __ballot_sync(kFull, near);
-  if (full || s_unsure || nmask) {
+  const bool flagged = full || s_unsure || nmask;
+  bool decided = false;
+  if (flagged) {
     // The scale needs the exact maximum: recompute every component that could hold it.
     const bool cand = valid && (full || az + tz >= a32 - tzm);
-    unsigned todo = __ballot_sync(kFull, cand) | nmask;
-    const bool redone = (todo >> lane) & 1u;
+    const unsigned todo0 = __ballot_sync(kFull, cand) | nmask;
     if (lane == 0) {
       atomicAdd(nref, (unsigned)__popc(nmask));
       atomicAdd(nside, 1u);
     }
+    // First those components again in fp32 with short fma chains (a bound
+    // about 30 times tighter than the tensor-core one): that decides the
+    // scale's fp16 rounding and the near codes in most groups.
+    if (!full) {
+      float zm = z, tm = tz;
+      const float gm = mid_gamma(p.d_in);
+      for (unsigned f_m = todo0; f_m; f_m &= f_m - 1) {
+        const int f = __ffs(f_m) - 1;
+        const ff2 z2 =
+            dot_mid(c.xs, c.mean, p.Vt + ((int64_t)beta * p.r + first + f) * p.d_in, p.d_in, lane);
+        if (lane == f) {
+          zm = z2.hi + z2.lo;
+          tm = gm * c.nrm * vnorm[k] * (1.f + 1e-3f) + kU * fabsf(zm);
+        }
+      }
+      // the maximum is one of the candidates: a in [a_lo, a_hi], so
+      // s = max(a / qmax, 1e-8) in [s_lo, s_hi]
+      const float a_lo = warp_maxf(cand ? fabsf(zm) - tm : 0.f);
+      const float a_hi = warp_maxf(cand ? fabsf(zm) + tm : 0.f);
+      const float s_lo = a_lo / (float)qmax * (1.f - 4.f * kU);
+      const float s_hi = a_hi / (float)qmax * (1.f + 4.f * kU);
+      if (s_lo > 2e-8f && same_half(s_lo, s_hi)) {
+        // u = z / s against sm, the middle of the range: |s / sm - 1| <= e2
+        const float sm = 0.5f * (s_lo + s_hi);
+        const float e2 = (s_hi - s_lo) / (s_hi + s_lo) * (1.f + 1e-5f) + 4.f * kU;
+        bool bad = false;
+        int q2 = q;
+        if ((nmask >> lane) & 1u) {
+          const float u2 = zm / sm;
+          const float au2 = fabsf(u2);
+          const float tau2 = (tm / sm + au2 * e2) * (1.f + 2.f * e2) * (1.f + 1e-6f) +
+                             4.f * kU * (au2 + 1.f);
+          const float hb2 = fminf(floorf(au2) + 0.5f, (float)qmax - 0.5f);
+          bad = fabsf(au2 - hb2) <= tau2;
+          q2 = (int)fminf(fmaxf(rintf(u2), -(float)qmax), (float)qmax);
+        }
+        if (!__any_sync(kFull, bad)) {
+          q = q2;
+          s16 = __float2half_rn(s_lo);
+          decided = true;
+        }
+      }
+    }
+  }
+  if (flagged && !decided) {  // else in double-float, exactly
+    const bool cand = valid && (full || az + tz >= a32 - tzm);
+    unsigned todo = __ballot_sync(kFull, cand) | nmask;
+    const bool redone = (todo >> lane) & 1u;
     // double-float throughout (fp64 throughput is very low here)
     ff2 zmine{0.f, 0.f};
     while (todo) {
@@ -764,9 +865,10 @@ __device__ __forceinline__ unsigned append_int8_vals(const Params& p, const Appe
       uint32_t tb[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float u = __fmul_rn(v[i + e], inv);
-        const float t = __fadd_rn(u, kMagic);
-        any_near |= !(fabsf(__fsub_rn(u, __fsub_rn(t, kMagic))) <= 0.5f - 3e-5f);
+        // q = rint(v inv) of the exact product (within 127 2^-24 of 127 v / a)
+        const float t = __fmaf_rn(v[i + e], inv, kMagic);
+        const float q = __fsub_rn(t, kMagic);
+        any_near |= !(fabsf(__fmaf_rn(v[i + e], inv, -q)) <= 0.5f - 3e-5f);
         tb[e] = __float_as_uint(t);
       }
       packed[i >> 2] =
@@ -864,7 +966,7 @@ __global__ void __launch_bounds__(256) append_int8_vec(Params p, AppendArgs a) {
 // A thread reads back only what it copied: no barrier is needed.  ESZ: the
 // input element bytes (2 or 4).
 constexpr int kI8Stages = 4;
-template <int TPR, int ESZ>
+template <int TPR, int ESZ, bool F16>
 __global__ void __launch_bounds__(256, 3) append_int8_pipe(Params p, AppendArgs a) {
   constexpr int Q = kI8NV * ESZ / 16;  // 16-byte pieces of a thread's values
   constexpr bool IL = ESZ == 2;
@@ -880,18 +982,19 @@ __global__ void __launch_bounds__(256, 3) append_int8_pipe(Params p, AppendArgs 
   struct Pos {
     int64_t slot, t;
   };
-  auto advance = [&](Pos& q) {
+  auto advance = [&](Pos q) {
     q.slot += sq;
     q.t += st_rem;
     if (q.t >= a.T) {
       q.t -= a.T;
       ++q.slot;
     }
+    return q;
   };
   Pos pi{r0 / a.T, 0}, pp;
   pi.t = r0 - pi.slot * a.T;
   pp = pi;
-  auto issue = [&](const Pos& q, int st) {
+  auto issue = [&](const Pos q, int st) {
     if (q.slot < p.n_slots) {
       const int slot = (int)q.slot;
       const int b = slot / p.H, h = slot - b * p.H;
@@ -914,13 +1017,13 @@ __global__ void __launch_bounds__(256, 3) append_int8_pipe(Params p, AppendArgs 
 #pragma unroll
   for (int s0 = 0; s0 < kI8Stages - 1; ++s0) {
     issue(pi, s0);
-    advance(pi);
+    pi = advance(pi);
   }
   unsigned nref = 0, rows0 = 0;
   int64_t rb = (int64_t)blockIdx.x * RPB;  // the block's first row of the step
   for (int k = 0; rb < total; ++k, rb += step) {
     issue(pi, (k + kI8Stages - 1) % kI8Stages);
-    advance(pi);
+    pi = advance(pi);
     asm volatile("cp.async.wait_group %0;\n" ::"n"(kI8Stages - 1) : "memory");
     const int st = k % kI8Stages;
     float v[kI8NV];
@@ -937,12 +1040,12 @@ __global__ void __launch_bounds__(256, 3) append_int8_pipe(Params p, AppendArgs 
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const uint16_t lo = (uint16_t)(ww[e] & 0xffffu), hi = (uint16_t)(ww[e] >> 16);
-          if (p.in_dtype == KVC_F16) {
+          if (F16) {
             v[8 * q + 2 * e] = __half2float(__ushort_as_half(lo));
             v[8 * q + 2 * e + 1] = __half2float(__ushort_as_half(hi));
           } else {
-            v[8 * q + 2 * e] = __bfloat162float(__ushort_as_bfloat16(lo));
-            v[8 * q + 2 * e + 1] = __bfloat162float(__ushort_as_bfloat16(hi));
+            v[8 * q + 2 * e] = __uint_as_float(ww[e] << 16);
+            v[8 * q + 2 * e + 1] = __uint_as_float(ww[e] & 0xffff0000u);
           }
         }
       }
@@ -951,7 +1054,7 @@ __global__ void __launch_bounds__(256, 3) append_int8_pipe(Params p, AppendArgs 
     const int slot = valid ? (int)pp.slot : 0;
     nref += append_int8_vals<TPR, IL>(p, a, slot, valid ? pp.t : a.T, j, valid, v);
     rows0 += (valid && slot == 0 && j == 0) ? 1u : 0u;
-    advance(pp);
+    pp = advance(pp);
   }
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
   nref = __reduce_add_sync(kFull, nref);
@@ -1044,14 +1147,16 @@ cudaError_t launch_append_int8(const Params& p, const AppendArgs& a, cudaStream_
     const unsigned grid = (unsigned)std::min<int64_t>(steps, 3 * (int64_t)sm_count());
     const size_t smem = (size_t)kI8Stages * kI8NV * esz * 256;
     cudaError_t e = cudaSuccess;
-#define KVC_I8_PIPE(T, E)                                                                     \
-  e = cudaFuncSetAttribute(append_int8_pipe<T, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                           (int)smem);                                                         \
-  if (e == cudaSuccess) append_int8_pipe<T, E><<<grid, 256, smem, s>>>(p, a);
-    if (esz == 2) {
-      if (tpr == 2) { KVC_I8_PIPE(2, 2) } else if (tpr == 4) { KVC_I8_PIPE(4, 2) } else { KVC_I8_PIPE(8, 2) }
+#define KVC_I8_PIPE(T, E, H)                                                                 \
+  e = cudaFuncSetAttribute(append_int8_pipe<T, E, H>,                                          \
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);            \
+  if (e == cudaSuccess) append_int8_pipe<T, E, H><<<grid, 256, smem, s>>>(p, a);
+    if (esz == 2 && p.in_dtype == KVC_F16) {
+      if (tpr == 2) { KVC_I8_PIPE(2, 2, true) } else if (tpr == 4) { KVC_I8_PIPE(4, 2, true) } else { KVC_I8_PIPE(8, 2, true) }
+    } else if (esz == 2) {
+      if (tpr == 2) { KVC_I8_PIPE(2, 2, false) } else if (tpr == 4) { KVC_I8_PIPE(4, 2, false) } else { KVC_I8_PIPE(8, 2, false) }
     } else {
-      if (tpr == 2) { KVC_I8_PIPE(2, 4) } else if (tpr == 4) { KVC_I8_PIPE(4, 4) } else { KVC_I8_PIPE(8, 4) }
+      if (tpr == 2) { KVC_I8_PIPE(2, 4, false) } else if (tpr == 4) { KVC_I8_PIPE(4, 4, false) } else { KVC_I8_PIPE(8, 4, false) }
     }
 #undef KVC_I8_PIPE
     if (e != cudaSuccess) return e;

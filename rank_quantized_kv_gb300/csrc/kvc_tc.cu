@@ -443,8 +443,8 @@ __global__ void __launch_bounds__(kV3) append_tc_v3(const Params p, const Append
         const float tz = t.gamma * nxb * vn_s[k] + 4.f * kU * (fabsf(zc) + fabsf(ck));
         const float tau = tz * inv * (1.f + 1e-6f) + 4.f * kU * (fabsf(u) + 1.f);
         const int qmax = (1 << w) - 1;
-        const float hb = floorf(u) + 0.5f;
-        near = hb >= 0.5f && hb <= (float)qmax - 0.5f && fabsf(u - hb) <= tau;
+        const float hb = fminf(fmaxf(floorf(u) + 0.5f, 0.5f), (float)qmax - 0.5f);
+        near = fabsf(u - hb) <= tau;
         code = (int)fminf(fmaxf(rintf(u), 0.f), (float)qmax);
         uf = u;
         tf = tau;

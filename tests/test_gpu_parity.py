@@ -230,6 +230,51 @@ def test_group_tile_beyond_split_range(kvc, dtype):
     check_fetch(gl.fetch(), gl, rl)
 
 
+@pytest.mark.parametrize("dtype, path", [("f32", "generic"), ("f16", "auto"), ("f16", "generic"),
+                                         ("bf16", "auto")])
+def test_group_tiny_group_latents(kvc, dtype, path):
+    """Rows whose latents in one 32-component group are tiny against
+    ||x - mean|| (log-spread from 0 to 1e-2 of it): the group's maximum is at
+    or below a few times the projection's error bound, where the fp32 scale,
+    the maximum's own code and the codes next to the outer boundaries can all
+    be wrong.  Every code and fp16 scale against the oracle; the tensor-core
+    and CUDA-core projections store the same bytes."""
+    B, H, D, hpg, r, S = 1, 16, 128, 8, 64, 256
+    base = synth.group_spectral(B, H, 400, D, hpg, alpha=1.0, seed=7700, tensor=0, dtype="f32")
+    params = fit_group(base.double().numpy(), hpg, r)
+    rng = np.random.default_rng(7701)
+    d_in = hpg * D
+    x64 = np.zeros((B, H, S, D))
+    for g in range(H // hpg):
+        V = params["V"][g].astype(np.float64)
+        m = params["mean"][g].astype(np.float64)
+        c = rng.standard_normal((S, r)) * 0.3
+        qg = rng.integers(0, r // 32, size=S)  # the tiny group of each row
+        eps = np.concatenate([[0.0], 10.0 ** rng.uniform(-8, -2, size=S - 1)])
+        for t in range(S):
+            c[t, 32 * qg[t]:32 * qg[t] + 32] = eps[t] * rng.standard_normal(32)
+        w = rng.standard_normal((S, d_in))
+        w -= (w @ V) @ np.linalg.pinv(V)  # no component in the basis's span
+        w *= 1.0 / np.linalg.norm(w, axis=1, keepdims=True)
+        rows = m + c @ V.T + w
+        for hh in range(hpg):
+            x64[0, g * hpg + hh] = rows[:, hh * D:(hh + 1) * D]
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    x = torch.from_numpy(x64).to(tdt)
+    x64 = x.double().numpy()
+    gl, rl = _make(kvc, "group", B, H, D, params, dtype, S, path)
+    gl.append(x.to(_dev()))
+    assert gl.sync_status() == 0
+    rl.append(x64)
+    _all_slots_match(gl, rl, x64)
+    if dtype != "f32":
+        gg, _ = _make(kvc, "group", B, H, D, params, dtype, S, "generic" if path == "auto" else "auto")
+        gg.append(x.to(_dev()))
+        assert gg.sync_status() == 0
+        _same_store(gl, gg, rl.n_slots)
+    print(f"tiny group latents {dtype}/{path}: counters {gl.counters()}")
+
+
 @pytest.mark.parametrize("hpg, r, dtype", [(2, 20, "bf16"), (4, 128, "f16")])
 def test_group_tensor_core_ranks(kvc, hpg, r, dtype):
     """The tensor-core group projection at other ranks: r = 20 (N padded to 32,
