@@ -874,6 +874,20 @@ __device__ __forceinline__ unsigned append_int8_vals(const Params& p, const Appe
       packed[i >> 2] =
           __byte_perm(__byte_perm(tb[0], tb[1], 0x0040), __byte_perm(tb[2], tb[3], 0x0040), 0x5410);
     }
+    // the fast codes go out first; the rare re-decisions below overwrite
+    // single bytes of them (same thread, so in program order), which keeps
+    // the packed words out of the rare path's registers
+    uint8_t* dst = p.store + p.pay_off[slot] + (a.t_base + t) * p.D + (IL ? 8 * j : kI8NV * j);
+    if (IL) {
+#pragma unroll
+      for (int g = 0; g < kI8NV / 8; ++g)
+        reinterpret_cast<uint2*>(dst + 8 * TPR * g)[0] = make_uint2(packed[2 * g], packed[2 * g + 1]);
+    } else {
+#pragma unroll
+      for (int w = 0; w < kI8NV / 16; ++w)
+        reinterpret_cast<uint4*>(dst)[w] =
+            make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2], packed[4 * w + 3]);
+    }
     uint32_t flag = 0;
     if (any_near) {
 #pragma unroll
@@ -890,11 +904,11 @@ __device__ __forceinline__ unsigned append_int8_vals(const Params& p, const Appe
         float vi = 0.f;
 #pragma unroll
         for (int e = 0; e < kI8NV; ++e) vi = e == i ? v[e] : vi;  // no local-memory indexing
+        // the byte of value i: group i / 8 of the thread's groups when interleaved
+        uint8_t* bp = dst + (IL ? 8 * TPR * (i >> 3) + (i & 7) : i);
         const float u = vi * inv;
         if (!slow && u != u) {  // a NaN (or an infinity times 0): code 0
-#pragma unroll
-          for (int w = 0; w < kI8NV / 4; ++w)
-            if (w == (i >> 2)) packed[w] &= ~(0xffu << (8 * (i & 3)));
+          *bp = 0;
           continue;
         }
         ++nref;
@@ -906,24 +920,8 @@ __device__ __forceinline__ unsigned append_int8_vals(const Params& p, const Appe
         } else {  // an exact tie, fp32 input or a tiny row: as float64 decides it
           q = (float)fmin(fmax(rint((double)vi / s64), -127.0), 127.0);
         }
-        const uint32_t byte = (uint32_t)__float2int_rn(q) & 0xffu;
-#pragma unroll
-        for (int w = 0; w < kI8NV / 4; ++w)
-          if (w == (i >> 2))
-            packed[w] = (packed[w] & ~(0xffu << (8 * (i & 3)))) | (byte << (8 * (i & 3)));
+        *bp = (uint8_t)(__float2int_rn(q) & 0xff);
       }
-    }
-    if (IL) {
-      uint8_t* dst = p.store + p.pay_off[slot] + (a.t_base + t) * p.D + 8 * j;
-#pragma unroll
-      for (int g = 0; g < kI8NV / 8; ++g)
-        reinterpret_cast<uint2*>(dst + 8 * TPR * g)[0] = make_uint2(packed[2 * g], packed[2 * g + 1]);
-    } else {
-      uint8_t* dst = p.store + p.pay_off[slot] + (a.t_base + t) * p.D + kI8NV * j;
-#pragma unroll
-      for (int w = 0; w < kI8NV / 16; ++w)
-        reinterpret_cast<uint4*>(dst)[w] =
-            make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2], packed[4 * w + 3]);
     }
     if (j == 0) {
       const float s32 = am / 127.f;
