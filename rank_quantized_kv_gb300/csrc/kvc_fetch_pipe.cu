@@ -69,6 +69,7 @@ struct PipeArgs {
   int a_col0, a_cols;      // TMEM column of the first A buffer; columns per A buffer
   int n_stg, n_b;          // staging buffers, B buffers (1 when every slot shares a basis)
   int rs_bytes;            // bytes of one row stage
+  int quad;                // codebook: entries of the 4-code table (0: decode by pairs)
   int64_t S;
   int tiles_per_slot, total_tiles;
 };
@@ -165,6 +166,41 @@ __device__ __forceinline__ uint4 decode_codebook_pairs(uint2 b, int w, const uin
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// 4W bits at bit offset `off` of the words w (offsets fixed at compile time
+// once the caller's loops are unrolled).
+template <int W>
+__device__ __forceinline__ uint32_t quad_field(const uint32_t (&w)[W], int off) {
+  const int i = off >> 5, sh = off & 31;
+  const uint32_t x =
+      sh + 4 * W <= 32 ? w[i] >> sh : __funnelshift_r(w[i], w[i + 1 < W ? i + 1 : W - 1], sh);
+  return x & ((1u << (4 * W)) - 1u);
+}
+
+// Codebook rows of W-bit codes (W <= 3, one segment from byte 0): the codes
+// [k0, k0 + 32 nblk) of one token's row in blocks of 32 (W aligned words),
+// four codes per table lookup, each chunk of 8 written to TMEM as 4 columns.
+template <int W>
+__device__ __forceinline__ void decode_cb_quads(const unsigned char* row, bool live, int k0,
+                                                int nblk, const uint2* cb4, uint32_t a_tm) {
+  for (int b = 0; b < nblk; ++b) {
+    const int kb = k0 + 32 * b;
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(row + kb / 8 * W);
+    uint32_t w[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) w[i] = live ? src[i] : 0u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (live) {
+        const uint2 e0 = cb4[quad_field<W>(w, 4 * W * (2 * c))];
+        const uint2 e1 = cb4[quad_field<W>(w, 4 * W * (2 * c + 1))];
+        v = make_uint4(e0.x, e0.y, e1.x, e1.y);
+      }
+      tmem_st4(a_tm + (kb / 8 + c) * 4, v);  // chunk kb / 8 + c: K positions 8 (kb / 8 + c) ..
+    }
+  }
+}
+
 template <int MODE, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fetch_pipe_kernel(const Params p, const PipeArgs t, const __grid_constant__ CUtensorMap omap) {
@@ -201,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint16_t* cbh = reinterpret_cast<uint16_t*>(rs + (size_t)RS * t.rs_bytes);
   float* norm_ring = reinterpret_cast<float*>(cbh + 256);
   uint32_t* cb2 = reinterpret_cast<uint32_t*>(norm_ring + kNormRing * kTile);  // [256] pairs
+  uint2* cb4 = reinterpret_cast<uint2*>(cb2 + 256);  // [t.quad] four codes as two pairs
   float* mean_c = reinterpret_cast<float*>(rs + (size_t)RS * t.rs_bytes);  // [hpg][D]
   // a row stage: [0, 128) chunk table, then the packed rows, then the side words
   const int side_off = t.rs_bytes - (int)(((size_t)kTile * p.side_bytes + 16 + 15) & ~size_t(15));
@@ -227,6 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         cb2[j] = (uint32_t)__half_as_ushort(__float2half_rn(p.codebook[c0])) |
                  ((uint32_t)__half_as_ushort(__float2half_rn(p.codebook[c1])) << 16);
       }
+    const int wb = p.cb_bits, lm = p.cb_levels - 1;
+    for (int j = tid; j < t.quad; j += kThreads) {
+      uint32_t h[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        h[e] = __half_as_ushort(__float2half_rn(p.codebook[(j >> (e * wb)) & lm]));
+      cb4[j] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -399,6 +444,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool live = tt < n;
       const int rowoff = tt * P;
       const uint32_t a_tm = taddr0 + lane_base + t.a_col0 + a * t.a_cols;
+      if (MODE == KVC_MODE_CODEBOOK && t.quad) {
+        // thread c0 takes the codes [c0 K / 2, (c0 + 1) K / 2)
+        const unsigned char* row = rows + rowoff;
+        const int nq = K / 64;
+        if (p.cb_bits == 3) decode_cb_quads<3>(row, live, c0 * (K / 2), nq, cb4, a_tm);
+        else if (p.cb_bits == 2) decode_cb_quads<2>(row, live, c0 * (K / 2), nq, cb4, a_tm);
+        else decode_cb_quads<1>(row, live, c0 * (K / 2), nq, cb4, a_tm);
+      } else
       for (int cb = c0; cb < KC; cb += 8) {
         uint32_t ent[4];
         uint2 bits[4];
@@ -571,7 +624,7 @@ PipeKernel pipe_kernel_for(int mode, int out_dtype) {
 }  // namespace
 
 size_t fetch_pipe_smem(int mode, int D, int hpg, int K, int side_bytes, int pmax, int n_bases,
-                       int min_rs, FetchPipeShape* sh) {
+                       int min_rs, int cb_bits, FetchPipeShape* sh) {
   const size_t rows = ((size_t)kTile * pmax + 16 + 15) & ~size_t(15);
   const size_t side = ((size_t)kTile * side_bytes + 16 + 15) & ~size_t(15);
   FetchPipeShape z;
@@ -587,9 +640,16 @@ size_t fetch_pipe_smem(int mode, int D, int hpg, int K, int side_bytes, int pmax
   z.n_b = n_bases > 1 ? 2 : 1;
   z.n_stg = 2;
   z.n_rs = min_rs;
-  const size_t tail = mode == KVC_MODE_CODEBOOK ? 256 * 2 + (size_t)kNormRing * kTile * 4 + 256 * 4
-                      : mode == KVC_MODE_GROUP  ? (size_t)hpg * D * 4
-                                                : 0;
+  // codebook rows of at most 3-bit codes (one segment from byte 0, K = D a
+  // multiple of 64) decode four codes per lookup: a table of 2^(4 bits) pairs
+  // of half2 words
+  z.quad = mode == KVC_MODE_CODEBOOK && cb_bits >= 1 && cb_bits <= 3 && K == D && K % 64 == 0
+               ? 1 << (4 * cb_bits)
+               : 0;
+  const size_t tail = mode == KVC_MODE_CODEBOOK
+                          ? 256 * 2 + (size_t)kNormRing * kTile * 4 + 256 * 4 + (size_t)z.quad * 8
+                      : mode == KVC_MODE_GROUP ? (size_t)hpg * D * 4
+                                               : 0;
   auto total = [&](const FetchPipeShape& q) {
     return 1024 + (size_t)q.n_stg * (D / 64) * 16384 + (size_t)q.n_b * D * K * 2 +
            (size_t)q.n_rs * q.rs_bytes + tail;
@@ -623,7 +683,7 @@ cudaError_t launch_fetch_pipe(const TcPlan& plan, const Params& p, const FetchAr
   const FetchPipeShape& sh = plan.pipe;
   const PipeArgs t{plan.fetchB, plan.bias, plan.chunks32, plan.slotP, plan.fetch_K, plan.pipe_cols,
                    sh.n_acc, sh.n_a, sh.n_rs, sh.a_col0, sh.a_cols, sh.n_stg, sh.n_b, sh.rs_bytes,
-                   f.S, tiles, total};
+                   sh.quad, f.S, tiles, total};
   k<<<(unsigned)grid, kThreads, plan.pipe_smem, s>>>(p, t, map);
   ++*nk;
   return cudaGetLastError();

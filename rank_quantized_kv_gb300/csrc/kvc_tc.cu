@@ -908,7 +908,8 @@ kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t
     FetchPipeShape sh;
     // group mode streams the heads' slices of B through two buffers
     const size_t ps = fetch_pipe_smem(d.mode, D, d.heads_per_group, K, g.side_bytes, pmax,
-                                      grp ? 2 : nb, grp ? 2 : 3, &sh);
+                                      grp ? 2 : nb, grp ? 2 : 3,
+                                      d.mode == KVC_MODE_CODEBOOK ? d.cb_bits : 0, &sh);
     if (ps > 0) {
       plan.pipe_ready = plan.fetch_ready;
       int cols_alloc = 32;  // TMEM allocations are powers of two

@@ -21,6 +21,7 @@ struct FetchPipeShape {
   int n_stg = 0;     // output staging buffers
   int n_b = 0;       // B buffers
   int rs_bytes = 0;  // bytes of one row stage
+  int quad = 0;      // entries of the codebook's 4-code table (0: none)
 };
 
 // Ring sizes of the warp-specialised append (kvc_append_ws.cu).
@@ -118,7 +119,7 @@ cudaError_t launch_append_group_tc(const TcPlan& plan, const Params& p, const Ap
 // tensor map.  fetch_pipe_smem sizes its rings for D, K, the side bytes, the
 // largest packed row and the number of bases; 0 when they do not fit.
 size_t fetch_pipe_smem(int mode, int D, int hpg, int K, int side_bytes, int pmax, int n_bases,
-                       int min_rs, FetchPipeShape* sh);
+                       int min_rs, int cb_bits, FetchPipeShape* sh);
 cudaError_t launch_fetch_pipe(const TcPlan& plan, const Params& p, const FetchArgs& f,
                               const CUtensorMap& map, cudaStream_t s, int* nk);
 // Warp-specialised append (kvc_append_ws.cu): table bytes per basis, one

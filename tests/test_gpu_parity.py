@@ -351,6 +351,26 @@ def test_cfg4_keys_scaled(kvc, path):
     assert gl.nbytes()["payload"] == B * H * S * 48        # ceil(128 * 3 / 8)
 
 
+@pytest.mark.parametrize("D, bits", [(128, 1), (128, 2), (128, 4), (64, 3), (256, 3), (256, 2)])
+@pytest.mark.parametrize("path", PATHS)
+def test_codebook_widths_and_heads(kvc, D, bits, path):
+    """Codebook keys at 1, 2, 3 and 4 bits and head sizes 64, 128 and 256 (the
+    fetch decodes widths up to 3 four codes per lookup, 4 bits by pairs), with
+    a ragged last tile: codes and norms against the oracle, the fetch within
+    its tolerance of the oracle's decode of the GPU's rows."""
+    B, H, S = 2, 2, 300
+    x = synth.heavy_tailed_keys(B, H, S, D, seed=4200 + D + bits, dtype="f16")
+    x64 = x.double().numpy()
+    params = fit_codebook(D, bits=bits, seed=77 + bits)
+    gl, rl = _make(kvc, "codebook", B, H, D, params, "f16", S, path)
+    gl.append(x.to(_dev()))
+    assert gl.sync_status() == 0
+    rl.append(x64)
+    _all_slots_match(gl, rl, x64)
+    check_fetch(gl.fetch(), gl, rl)
+    assert gl.nbytes()["payload"] == B * H * S * (D * bits // 8)
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
 def test_cfg4_values_int8(kvc, dtype):
     B, H, S, D = 2, 8, 1000, 128
