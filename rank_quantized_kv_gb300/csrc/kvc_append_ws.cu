@@ -60,6 +60,7 @@ struct AppendWsArgs {
   int n_acc, n_x, n_b;      // accumulators, x stages, B buffers
   int x_stage, tab_bytes, pmax;
   int ks;                   // bytes per token row of the code staging (chunk-aligned)
+  int nq;                   // queue entries per quantiser group
   int vt_smem;              // each group keeps its basis' V^T in shared memory
   float inv_scale, gamma;
   int tiles_per_slot, total_tiles;
@@ -123,9 +124,10 @@ struct Ring {
 
 // Shared-memory scratch of one quantiser group: code staging, packed rows,
 // the re-decision queue and its aux values, partial norms, side words.
-__host__ __device__ constexpr size_t ws_group_bytes(int ks, int pmax) {
+// nq: queue entries (near codes waiting for their exact decision)
+__host__ __device__ constexpr size_t ws_group_bytes(int ks, int pmax, int nq) {
   return ((size_t)kTile * ks + (((size_t)kTile * pmax + 16 + 15) & ~size_t(15)) +
-          (size_t)kQueue * 12 + kNCB * kTile * 4 + kTile * 2 + 15) & ~size_t(15);
+          (size_t)nq * 12 + kNCB * kTile * 4 + kTile * 2 + 15) & ~size_t(15);
 }
 
 // Decide code k of token tt exactly (k == kNormEntry: the fp16 norm of a
@@ -369,7 +371,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
   unsigned char* xst = smem;                                        // XS x (x tile, table)
   unsigned char* Bs = xst + (size_t)XS * t.x_stage;                 // NB x (B, V^T)
   unsigned char* grp0 = Bs + NB * b_bytes;                          // QG x group scratch
-  float* vt0 = reinterpret_cast<float*>(grp0 + QG * ws_group_bytes(t.ks, t.pmax));  // QG x V^T
+  float* vt0 = reinterpret_cast<float*>(grp0 + QG * ws_group_bytes(t.ks, t.pmax, t.nq));  // QG x V^T
   float* mids_s = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(vt0) + QG * vt_bytes);
   float* cb_s = mids_s + 256;                                       // [256]
   __shared__ float mpad[9];  // codebooks of <= 8 levels: -inf, the midpoints, +inf
@@ -499,12 +501,12 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
     const int g = warp / kQWarps, wq = warp - g * kQWarps, qt = tid - g * kQThreads;
     const int quarter = wq & 3, cblk = wq >> 2, row = quarter * 32 + lane;
     const int qbar = kQBar + g;
-    unsigned char* gbase = grp0 + (size_t)g * ws_group_bytes(t.ks, t.pmax);
+    unsigned char* gbase = grp0 + (size_t)g * ws_group_bytes(t.ks, t.pmax, t.nq);
     unsigned char* codes_s = gbase;                                   // [128][ks] chunk-aligned
     unsigned char* out_s = codes_s + (size_t)kTile * t.ks;            // [128][P] packed rows
     uint32_t* queue = reinterpret_cast<uint32_t*>(out_s + ((kTile * t.pmax + 16 + 15) & ~15));
-    float2* aux = reinterpret_cast<float2*>(queue + kQueue);
-    float* nsq_s = reinterpret_cast<float*>(aux + kQueue);            // [2][128]
+    float2* aux = reinterpret_cast<float2*>(queue + t.nq);
+    float* nsq_s = reinterpret_cast<float*>(aux + t.nq);              // [2][128]
     __half* side_s = reinterpret_cast<__half*>(nsq_s + kNCB * kTile); // [128]
     unsigned& qcount = qcount_g[g];
     unsigned& nside = nside_g[g];
@@ -650,7 +652,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
               fast_codebook(p, t1, mids_s, mpad, m3, z[j], rnx, e_u, tiny, uf, tf, near);
             }
             const unsigned q = atomicAdd(&qcount, 1u);
-            if (q < kQueue) {
+            if (q < (unsigned)t.nq) {
               queue[q] = ((uint32_t)row << 16) | (uint32_t)k;
               aux[q] = make_float2(uf, tf);
             } else {
@@ -671,7 +673,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
         if (MODE == KVC_MODE_CODEBOOK && cblk == 0) {
           if (tiny || !same_half(nx * (1.f - eps_n), nx * (1.f + eps_n))) {
             const unsigned q = atomicAdd(&qcount, 1u);
-            if (q < kQueue) {
+            if (q < (unsigned)t.nq) {
               queue[q] = ((uint32_t)row << 16) | kNormEntry;
               aux[q] = make_float2(0.f, 0.f);
             } else {
@@ -687,7 +689,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       const unsigned nq = qcount;
       {  // two entries per warp at a time, sixteen lanes each
         constexpr int GL = 16, PER = 32 / GL;
-        const unsigned nqe = min(nq, (unsigned)kQueue);
+        const unsigned nqe = min(nq, (unsigned)t.nq);
         for (unsigned e0 = wq * PER; e0 < nqe; e0 += kQWarps * PER) {
           const unsigned e = e0 + lane / GL;
           const bool act = e < nqe;
@@ -891,8 +893,13 @@ int append_ws_table(const Geo& g, const kvc_layer_desc& d, int rpad, const doubl
 }
 
 size_t append_ws_plan(int D, int r, int rpad, int npieces, int pmax, int max_chunks, int n_bases,
-                      AppendWsShape* sh) {
+                      bool direct, AppendWsShape* sh) {
   AppendWsShape z;
+  // codebook rows are packed straight to the store (no staging of packed
+  // rows), and their tiles queue few near codes: a short queue (past its end
+  // a code is decided by its own thread) leaves room for a third x stage
+  z.pmax = direct ? 0 : pmax;
+  z.nq = direct ? 128 : kQueue;
   const int ncols = npieces * rpad;
   z.acc_stride = (ncols + 31) / 32 * 32;
   z.n_acc = std::min(kMaxTS, 512 / z.acc_stride);
@@ -907,7 +914,7 @@ size_t append_ws_plan(int D, int r, int rpad, int npieces, int pmax, int max_chu
   const size_t limit = 226 * 1024;
   for (int vt = 1; vt >= 0; --vt) {  // the groups' V^T copies where they fit
     const size_t fixed = 1024 + (size_t)z.n_b * ncols * D * 2 +
-                         (size_t)kQG * (ws_group_bytes(z.ks, pmax) + (vt ? (size_t)r * D * 4 : 0)) +
+                         (size_t)kQG * (ws_group_bytes(z.ks, z.pmax, z.nq) + (vt ? (size_t)r * D * 4 : 0)) +
                          2 * 256 * 4;
     for (int xs = kMaxXS; xs >= (vt ? 3 : 2); --xs)
       if (fixed + (size_t)xs * z.x_stage <= limit) {
@@ -932,7 +939,7 @@ cudaError_t launch_append_ws(const TcPlan& plan, const Params& p, const AppendAr
   const AppendWsShape& sh = plan.ws;
   const AppendWsArgs t{plan.appB,    plan.c64,     plan.wsTab,   plan.app_rpad,      plan.app_pieces,
                        sh.acc_stride, sh.cols,      sh.n_acc,     sh.n_x,             sh.n_b,
-                       sh.x_stage,    sh.tab_bytes, plan.ws_pmax, sh.ks,              sh.vt_smem,
+                       sh.x_stage,    sh.tab_bytes, sh.pmax,      sh.ks,   sh.nq,     sh.vt_smem,
                        plan.app_inv_scale, plan.app_gamma, tiles, total, wait_ns};
   k<<<(unsigned)grid, kThreadsWs, plan.ws_smem, s>>>(p, t, xmap, a);
   ++*nk;

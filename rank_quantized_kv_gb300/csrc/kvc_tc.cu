@@ -682,12 +682,13 @@ void prepare_append(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>&
                         ks, b, tab.data() + (size_t)b * tab_bytes) < 0)
       max_chunks = -1;
   AppendWsShape ws;
-  const size_t wsm = max_chunks > 0 ? append_ws_plan(D, r, rpad, npieces, pmax, max_chunks, nb, &ws) : 0;
+  const size_t wsm = max_chunks > 0 ? append_ws_plan(D, r, rpad, npieces, pmax, max_chunks, nb,
+                                                    d.mode == KVC_MODE_CODEBOOK, &ws)
+                                     : 0;
   if (wsm > 0 && plan.append_ready) {
     plan.oWsTab = put(image, tab.data(), tab.size());
     plan.ws = ws;
     plan.ws_smem = wsm;
-    plan.ws_pmax = pmax;
     plan.ws_ready = true;
   }
 }

@@ -34,6 +34,8 @@ struct AppendWsShape {
   int n_x = 0;         // x stages
   int n_b = 0;         // B buffers
   int ks = 0;          // bytes per token row of the chunk-aligned code staging
+  int pmax = 0;        // bytes per token row of the packed-row staging (0: none)
+  int nq = 0;          // queue entries per quantiser group
   int vt_smem = 0;     // V^T kept in shared memory beside B
 };
 
@@ -78,7 +80,6 @@ struct TcPlan {
   bool ws_ready = false;
   AppendWsShape ws;
   size_t ws_smem = 0;
-  int ws_pmax = 0;                   // largest packed row
   size_t oWsTab = 0;
   const unsigned char* wsTab = nullptr;  // [nb][tab_bytes] quantiser tables
 
@@ -130,6 +131,7 @@ int append_ws_table(const Geo& g, const kvc_layer_desc& d, int rpad, const doubl
                     double inv_scale, double gamma, int ks, int b,
                     unsigned char* out);  // returns the basis' pack chunks, -1 if over 32
 size_t append_ws_plan(int D, int r, int rpad, int npieces, int pmax, int max_chunks, int n_bases,
+                      bool direct,
                       AppendWsShape* sh);
 cudaError_t launch_append_ws(const TcPlan& plan, const Params& p, const AppendArgs& a,
                              const CUtensorMap& xmap, uint64_t wait_ns, cudaStream_t s, int* nk);
