@@ -529,10 +529,12 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 size_t attend_plan(int B, int Hq, int n_slots, int rep, int64_t S, int NCk, int Dv, int sms,
                    int extra, int* splits, int64_t* span) {
-  // enough CTAs for about four per SM, at least 128 tokens each (a multiple of
-  // 128 so that every warp's 32-token blocks start at a multiple of 32)
+  // enough CTAs for about twelve per SM (the main kernel is bound by load
+  // latency; more resident warps hide more of it), at least 128 tokens each (a
+  // multiple of 128 so that every warp's 32-token blocks start at a multiple
+  // of 32)
   const int64_t max_splits = std::max<int64_t>(1, (S + 127) / 128);
-  int64_t sp = std::min<int64_t>(max_splits, std::max<int64_t>(1, (4 * sms + n_slots - 1) / n_slots));
+  int64_t sp = std::min<int64_t>(max_splits, std::max<int64_t>(1, (12 * sms + n_slots - 1) / n_slots));
   int64_t sn = (S + sp - 1) / sp;
   sn = (sn + 127) / 128 * 128;
   sp = (S + sn - 1) / sn;

@@ -70,6 +70,7 @@ struct PipeArgs {
   int n_stg, n_b;          // staging buffers, B buffers (1 when every slot shares a basis)
   int rs_bytes;            // bytes of one row stage
   int quad;                // codebook: entries of the 4-code table (0: decode by pairs)
+  int uni_w, uni_chunks;   // uniform rows of one width from byte 0 (0: by the chunk table)
   int64_t S;
   int tiles_per_slot, total_tiles;
 };
@@ -451,6 +452,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.cb_bits == 3) decode_cb_quads<3>(row, live, c0 * (K / 2), nq, cb4, a_tm);
         else if (p.cb_bits == 2) decode_cb_quads<2>(row, live, c0 * (K / 2), nq, cb4, a_tm);
         else decode_cb_quads<1>(row, live, c0 * (K / 2), nq, cb4, a_tm);
+      } else if (MODE == KVC_MODE_UNIFORM && t.uni_w) {
+        // one width w: code chunk c is the w bytes at c w of the row; thread
+        // c0 takes half of the code chunks, c0 = 1 also the bias chunk (ones)
+        // and the zero chunks after it
+        const int w = t.uni_w, kcc = t.uni_chunks, half = (kcc + 1) / 2;
+        const unsigned char* row = rows + rowoff;
+        const int cend = c0 ? KC : half;
+        for (int c = c0 * half; c < cend; ++c) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (live && c < kcc) {
+            uint2 b = make_uint2(0u, 0u);
+            if (w == 8) b = *reinterpret_cast<const uint2*>(row + 8 * c);
+            else if (w == 4) b.x = *reinterpret_cast<const uint32_t*>(row + 4 * c);
+            else if (w == 2) b.x = *reinterpret_cast<const uint16_t*>(row + 2 * c);
+            else b.x = row[c];
+            v = decode_uniform(b, w);
+          } else if (live && c == kcc) {
+            v.x = 0x3C003C00u;  // (1, 1): the two bias columns of B
+          }
+          tmem_st4(a_tm + c * 4, v);
+        }
       } else
       for (int cb = c0; cb < KC; cb += 8) {
         uint32_t ent[4];
@@ -683,7 +705,7 @@ cudaError_t launch_fetch_pipe(const TcPlan& plan, const Params& p, const FetchAr
   const FetchPipeShape& sh = plan.pipe;
   const PipeArgs t{plan.fetchB, plan.bias, plan.chunks32, plan.slotP, plan.fetch_K, plan.pipe_cols,
                    sh.n_acc, sh.n_a, sh.n_rs, sh.a_col0, sh.a_cols, sh.n_stg, sh.n_b, sh.rs_bytes,
-                   sh.quad, f.S, tiles, total};
+                   sh.quad, sh.uni_w, sh.uni_chunks, f.S, tiles, total};
   k<<<(unsigned)grid, kThreads, plan.pipe_smem, s>>>(p, t, map);
   ++*nk;
   return cudaGetLastError();

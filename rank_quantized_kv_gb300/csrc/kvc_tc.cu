@@ -911,6 +911,24 @@ kvc_status tc_prepare(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t
     const size_t ps = fetch_pipe_smem(d.mode, D, d.heads_per_group, K, g.side_bytes, pmax,
                                       grp ? 2 : nb, grp ? 2 : 3,
                                       d.mode == KVC_MODE_CODEBOOK ? d.cb_bits : 0, &sh);
+    if (ps > 0 && d.mode == KVC_MODE_UNIFORM) {
+      // every basis one segment of one width w in {1, 2, 4, 8}, whole 8-code
+      // chunks from byte 0 and K position 0: chunk c is w bytes at c w
+      int w0 = -1, n0 = -1;
+      bool one = true;
+      for (int b = 0; b < nb && one; ++b) {
+        const int32_t* e = &g.seg[(size_t)b * kMaxSeg * 4];
+        for (int s2 = 1; s2 < kMaxSeg; ++s2) one = one && g.seg[((size_t)b * kMaxSeg + s2) * 4 + 3] == 0;
+        one = one && e[0] == 0 && e[3] > 0 && e[3] % 8 == 0 &&
+              (e[1] == 1 || e[1] == 2 || e[1] == 4 || e[1] == 8) && (w0 < 0 || (e[1] == w0 && e[3] == n0));
+        w0 = e[1];
+        n0 = e[3];
+      }
+      if (one && n0 / 8 < K / 8) {
+        sh.uni_w = w0;
+        sh.uni_chunks = n0 / 8;
+      }
+    }
     if (ps > 0) {
       plan.pipe_ready = plan.fetch_ready;
       int cols_alloc = 32;  // TMEM allocations are powers of two

@@ -439,6 +439,26 @@ def test_cfg5_points(kvc, B, S, r, bits):
     check_fetch(gl.fetch(), gl, rl)
 
 
+@pytest.mark.parametrize("r, bits", [(32, 1), (64, 2), (32, 4), (64, 8), (40, 4), (36, 2)])
+@pytest.mark.parametrize("path", PATHS)
+def test_uniform_one_width(kvc, r, bits, path):
+    """Every kept component at one width (the fetch decodes such rows chunk by
+    chunk from aligned loads when the rank is a multiple of 8; r = 36 keeps a
+    partial chunk and takes the chunk table), a ragged last tile; codes against
+    the oracle and the fetch within its tolerance."""
+    B, H, D, S = 2, 2, 128, 300
+    x = synth.kv_spectral(B, H, S, D, alpha=1.0, seed=5100 + r + bits, tensor=0, dtype="bf16")
+    x64 = x.double().numpy()
+    p = fit_uniform(x64, S, r, [bits], bits * r)
+    assert np.all(p["bits"] == bits)
+    gl, rl = _make(kvc, "uniform", B, H, D, p, "bf16", S, path)
+    gl.append(x.to(_dev()))
+    assert gl.sync_status() == 0
+    rl.append(x64)
+    _all_slots_match(gl, rl, x64)
+    check_fetch(gl.fetch(), gl, rl)
+
+
 @pytest.mark.parametrize("r,choices,budget", [(128, [0, 2, 4, 8], 384), (96, [0, 4, 8], 384)])
 def test_uniform_wide_rank_bf16(kvc, r, choices, budget):
     """bf16 input, one basis per (b, h), rank above 64: the basis' three 16-bit
