@@ -687,8 +687,10 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       }
       named_bar_sync(qbar, kQThreads);  // B2: fast-path codes and the queue complete
       const unsigned nq = qcount;
-      {  // two entries per warp at a time, sixteen lanes each
-        constexpr int GL = 16, PER = 32 / GL;
+      {  // entries per warp at a time: codebook tiles queue few (two of sixteen
+         // lanes each: shorter chains), uniform tiles about twenty (four of eight
+         // lanes each: one round)
+        constexpr int GL = MODE == KVC_MODE_UNIFORM ? 8 : 16, PER = 32 / GL;
         const unsigned nqe = min(nq, (unsigned)t.nq);
         for (unsigned e0 = wq * PER; e0 < nqe; e0 += kQWarps * PER) {
           const unsigned e = e0 + lane / GL;
