@@ -309,19 +309,23 @@ __device__ __forceinline__ void pack_codebook(int qt, int n, int D, const unsign
 // registers (+inf past the last) and a 3-step bisection finds the code and the
 // two bracketing midpoints at once.
 __device__ __forceinline__ int fast_codebook(const Params& p, float t1, const float* mids_s,
-                                             const float* mpad, float m3, float z, float rnx,
-                                             float e_u, bool tiny, float& u, float& tau,
-                                             bool& near) {
+                                             const float* mpad, float m3, const float (&mr)[7],
+                                             float z, float rnx, float e_u, bool tiny, float& u,
+                                             float& tau, bool& near) {
   const int L = p.cb_levels;
   u = z * rnx;  // rnx = 2^-s fl(1 / ||x||) (0 for a tiny ||x||): two roundings, as z 2^-s / ||x||
   int c = 0;
   float dmin;
   if (L <= 8) {
-    // mpad = [-inf, m_0 .. m_6, +inf] (+inf past the last midpoint): a 3-step
-    // bisection, then the bracketing midpoints mpad[c] < u <= mpad[c + 1]
-    c = u > m3 ? 4 : 0;
-    c += u > mpad[c + 2] ? 2 : 0;
-    c += u > mpad[c + 1] ? 1 : 0;
+    // a 3-step bisection over the midpoints held in registers (mr = m_0 ..
+    // m_6, +inf past the last: no dependent shared-memory loads), then the
+    // bracketing midpoints mpad[c] < u <= mpad[c + 1] (mpad = [-inf, m_0 ..
+    // m_6, +inf])
+    const bool b2 = u > m3;
+    const float ma = b2 ? mr[5] : mr[1];
+    const bool b1 = u > ma;
+    const float mb = b2 ? (b1 ? mr[6] : mr[4]) : (b1 ? mr[2] : mr[0]);
+    c = (b2 ? 4 : 0) + (b1 ? 2 : 0) + (u > mb ? 1 : 0);
     dmin = fminf(u - mpad[c], mpad[c + 1] - u);
   } else {
     int hi_i = L - 1;
@@ -518,6 +522,9 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
     const float eps_n = 0.5f * ((D + 2) * kU) / (1.f - (D + 2) * kU) + 2.f * kU;
     const float e_u = (eps_n * (1.f + 1e-6f) + 4.f * kU) * (1.f + 1e-6f);  // |u| term of tau
     const float m3 = MODE == KVC_MODE_CODEBOOK ? mpad[4] : 0.f;  // the first bisection step
+    float mr[7];  // the midpoints m_0 .. m_6 (+inf past the last) in registers
+#pragma unroll
+    for (int q = 0; q < 7; ++q) mr[q] = MODE == KVC_MODE_CODEBOOK ? mpad[q + 1] : 0.f;
     Ring rx(XS), rt(TS);
     for (int j = 0; j < g; ++j) { rx.next(); rt.next(); }
     for (int i = g; i < m; i += QG) {
@@ -630,7 +637,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
           bool near;
           const int code = MODE == KVC_MODE_UNIFORM
                                ? fast_uniform<false>(tb, k, qmax, z[j], nx, uf, tf, near)
-                               : fast_codebook(p, t1, mids_s, mpad, m3, z[j], rnx, e_u, tiny, uf,
+                               : fast_codebook(p, t1, mids_s, mpad, m3, mr, z[j], rnx, e_u, tiny, uf,
                                                tf, near);
           crow[pos] = (uint8_t)code;
           nmask |= (uint32_t)near << j;
@@ -649,7 +656,7 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
               fast_uniform<true>(tb, k, tb.qp[k].x, z[j], nx, uf, tf, near);
               if (!near) continue;  // an outer boundary: the clamped code is certain
             } else {
-              fast_codebook(p, t1, mids_s, mpad, m3, z[j], rnx, e_u, tiny, uf, tf, near);
+              fast_codebook(p, t1, mids_s, mpad, m3, mr, z[j], rnx, e_u, tiny, uf, tf, near);
             }
             const unsigned q = atomicAdd(&qcount, 1u);
             if (q < (unsigned)t.nq) {
