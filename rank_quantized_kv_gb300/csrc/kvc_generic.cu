@@ -1061,39 +1061,58 @@ __global__ void __launch_bounds__(256, 3) append_int8_pipe(Params p, AppendArgs 
   if ((tid & 31) == 0 && rows0) atomicAdd(&p.counters[2], (unsigned long long)rows0);
 }
 
-// Grid as append_int8_vec.
-template <int TPR>
+// Grid: x over blocks of R (256 / TPR) tokens, y over slots (strided when
+// there are more than 65535).  A thread takes R token rows 256 / TPR apart
+// (a warp's rows stay contiguous), with all R loads issued before any decode.
+template <int TPR, int R>
 __global__ void __launch_bounds__(256) fetch_int8_vec(Params p, FetchArgs f) {
+  constexpr int RPB = 256 / TPR;  // rows per block step
   const int j = (int)(threadIdx.x % TPR);
-  const int64_t t = (int64_t)blockIdx.x * (256 / TPR) + threadIdx.x / TPR;
-  if (t >= f.S) return;
-  for (int slot = blockIdx.y; slot < p.n_slots; slot += gridDim.y) {
-  const int b = slot / p.H, h = slot - b * p.H;
-  const uint2 q = *reinterpret_cast<const uint2*>(p.store + p.pay_off[slot] + t * p.D + 8 * j);
-  const __half sh = reinterpret_cast<const __half*>(p.store + p.side_off[slot])[t];
+  const int64_t t0 = (int64_t)blockIdx.x * RPB * R + threadIdx.x / TPR;
+  if (t0 >= f.S) return;
   // Code byte b + 128 placed in the low mantissa bits of fp16 1024 gives
   // 1024 + 128 + b exactly; subtracting 1152 leaves b as an fp16 integer.  No
   // int-to-float conversions.  b s is exact in fp32 (8 by 11 significant
   // bits), so one fp16 product rounds exactly as fp16(float(b) s) does.
-  const uint32_t w[2] = {q.x ^ 0x80808080u, q.y ^ 0x80808080u};
   const __half2 bias = __float2half2_rn(-1152.f);
-  uint32_t o[4];
+  for (int slot = blockIdx.y; slot < p.n_slots; slot += gridDim.y) {
+    const int b = slot / p.H, h = slot - b * p.H;
+    const uint8_t* pay = p.store + p.pay_off[slot];
+    const __half* side = reinterpret_cast<const __half*>(p.store + p.side_off[slot]);
+    uint2 q[R];
+    __half sh[R];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t hb = __byte_perm(w[i >> 1], 0x64646464u, (i & 1) ? 0x4342 : 0x4140);
-    const __half2 b2 = __hadd2(*reinterpret_cast<const __half2*>(&hb), bias);
-    if (p.out_dtype == KVC_F16) {
-      const __half2 hv = __hmul2(b2, __half2half2(sh));
-      o[i] = *reinterpret_cast<const uint32_t*>(&hv);
-    } else {
-      const float2 f = __half22float2(b2);
-      const float s = __half2float(sh);
-      const __nv_bfloat162 hv = __floats2bfloat162_rn(f.x * s, f.y * s);
-      o[i] = *reinterpret_cast<const uint32_t*>(&hv);
+    for (int r = 0; r < R; ++r) {
+      const int64_t t = t0 + (int64_t)r * RPB;
+      if (t < f.S) {
+        q[r] = *reinterpret_cast<const uint2*>(pay + t * p.D + 8 * j);
+        sh[r] = side[t];
+      }
     }
-  }
-  uint16_t* out = static_cast<uint16_t*>(f.out) + (((int64_t)b * p.H + h) * f.ld_s + t) * p.D + 8 * j;
-  *reinterpret_cast<uint4*>(out) = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int64_t t = t0 + (int64_t)r * RPB;
+      if (t >= f.S) break;
+      const uint32_t w[2] = {q[r].x ^ 0x80808080u, q[r].y ^ 0x80808080u};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t hb = __byte_perm(w[i >> 1], 0x64646464u, (i & 1) ? 0x4342 : 0x4140);
+        const __half2 b2 = __hadd2(*reinterpret_cast<const __half2*>(&hb), bias);
+        if (p.out_dtype == KVC_F16) {
+          const __half2 hv = __hmul2(b2, __half2half2(sh[r]));
+          o[i] = *reinterpret_cast<const uint32_t*>(&hv);
+        } else {
+          const float2 fv = __half22float2(b2);
+          const float s = __half2float(sh[r]);
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(fv.x * s, fv.y * s);
+          o[i] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+      }
+      uint16_t* out =
+          static_cast<uint16_t*>(f.out) + (((int64_t)b * p.H + h) * f.ld_s + t) * p.D + 8 * j;
+      *reinterpret_cast<uint4*>(out) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
 }
 
@@ -1177,11 +1196,14 @@ cudaError_t launch_fetch_int8(const Params& p, const FetchArgs& f, cudaStream_t 
   const bool vec = (p.D == 64 || p.D == 128 || p.D == 256) &&
                    reinterpret_cast<uintptr_t>(f.out) % 16 == 0;
   if (vec) {
+    constexpr int R = 4;  // token rows per thread
     const int tpr = p.D / 8;
-    const dim3 grid((unsigned)((f.S * tpr + 255) / 256), (unsigned)std::min(p.n_slots, 65535));
-    if (tpr == 8) fetch_int8_vec<8><<<grid, 256, 0, s>>>(p, f);
-    else if (tpr == 16) fetch_int8_vec<16><<<grid, 256, 0, s>>>(p, f);
-    else fetch_int8_vec<32><<<grid, 256, 0, s>>>(p, f);
+    const int64_t rows_per_block = (int64_t)(256 / tpr) * R;
+    const dim3 grid((unsigned)((f.S + rows_per_block - 1) / rows_per_block),
+                    (unsigned)std::min(p.n_slots, 65535));
+    if (tpr == 8) fetch_int8_vec<8, R><<<grid, 256, 0, s>>>(p, f);
+    else if (tpr == 16) fetch_int8_vec<16, R><<<grid, 256, 0, s>>>(p, f);
+    else fetch_int8_vec<32, R><<<grid, 256, 0, s>>>(p, f);
   } else {
     fetch_int8_kernel<<<(unsigned)((toks + kI8Warps - 1) / kI8Warps), kI8Warps * 32, 0, s>>>(p, f);
   }
