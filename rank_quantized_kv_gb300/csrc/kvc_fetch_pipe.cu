@@ -69,7 +69,7 @@ struct PipeArgs {
   int a_col0, a_cols;      // TMEM column of the first A buffer; columns per A buffer
   int n_stg, n_b;          // staging buffers, B buffers (1 when every slot shares a basis)
   int rs_bytes;            // bytes of one row stage
-  int quad;                // codebook: entries of the 4-code table (0: decode by pairs)
+  int cb_rep;              // codebook: 8-byte slots of the lane-replicated pair table (0: none)
   int uni_w, uni_chunks;   // uniform rows of one width from byte 0 (0: by the chunk table)
   int64_t S;
   int tiles_per_slot, total_tiles;
@@ -167,22 +167,23 @@ __device__ __forceinline__ uint4 decode_codebook_pairs(uint2 b, int w, const uin
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// 4W bits at bit offset `off` of the words w (offsets fixed at compile time
-// once the caller's loops are unrolled).
+// 2W bits at bit offset `off` of the words w (compile-time offsets).
 template <int W>
-__device__ __forceinline__ uint32_t quad_field(const uint32_t (&w)[W], int off) {
+__device__ __forceinline__ uint32_t pair_field(const uint32_t (&w)[W], int off) {
   const int i = off >> 5, sh = off & 31;
   const uint32_t x =
-      sh + 4 * W <= 32 ? w[i] >> sh : __funnelshift_r(w[i], w[i + 1 < W ? i + 1 : W - 1], sh);
-  return x & ((1u << (4 * W)) - 1u);
+      sh + 2 * W <= 32 ? w[i] >> sh : __funnelshift_r(w[i], w[i + 1 < W ? i + 1 : W - 1], sh);
+  return x & ((1u << (2 * W)) - 1u);
 }
 
 // Codebook rows of W-bit codes (W <= 3, one segment from byte 0): the codes
 // [k0, k0 + 32 nblk) of one token's row in blocks of 32 (W aligned words),
-// four codes per table lookup, each chunk of 8 written to TMEM as 4 columns.
+// two codes per lookup in a table of pairs replicated once per lane (lane l
+// reads column l: no bank conflicts), each chunk of 8 written to TMEM as 4
+// columns.
 template <int W>
-__device__ __forceinline__ void decode_cb_quads(const unsigned char* row, bool live, int k0,
-                                                int nblk, const uint2* cb4, uint32_t a_tm) {
+__device__ __forceinline__ void decode_cb_rows(const unsigned char* row, bool live, int k0,
+                                               int nblk, const uint32_t* cbr, uint32_t a_tm) {
   for (int b = 0; b < nblk; ++b) {
     const int kb = k0 + 32 * b;
     const uint32_t* src = reinterpret_cast<const uint32_t*>(row + kb / 8 * W);
@@ -193,9 +194,11 @@ __device__ __forceinline__ void decode_cb_quads(const unsigned char* row, bool l
     for (int c = 0; c < 4; ++c) {
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (live) {
-        const uint2 e0 = cb4[quad_field<W>(w, 4 * W * (2 * c))];
-        const uint2 e1 = cb4[quad_field<W>(w, 4 * W * (2 * c + 1))];
-        v = make_uint4(e0.x, e0.y, e1.x, e1.y);
+        const uint32_t* cl = cbr + (threadIdx.x & 31);
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = cl[pair_field<W>(w, W * (8 * c + 2 * i)) * 32];
+        v = make_uint4(o[0], o[1], o[2], o[3]);
       }
       tmem_st4(a_tm + (kb / 8 + c) * 4, v);  // chunk kb / 8 + c: K positions 8 (kb / 8 + c) ..
     }
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint16_t* cbh = reinterpret_cast<uint16_t*>(rs + (size_t)RS * t.rs_bytes);
   float* norm_ring = reinterpret_cast<float*>(cbh + 256);
   uint32_t* cb2 = reinterpret_cast<uint32_t*>(norm_ring + kNormRing * kTile);  // [256] pairs
-  uint2* cb4 = reinterpret_cast<uint2*>(cb2 + 256);  // [t.quad] four codes as two pairs
+  uint32_t* cbr = cb2 + 256;  // [L^2][32]: each pair of centroids once per lane
   float* mean_c = reinterpret_cast<float*>(rs + (size_t)RS * t.rs_bytes);  // [hpg][D]
   // a row stage: [0, 128) chunk table, then the packed rows, then the side words
   const int side_off = t.rs_bytes - (int)(((size_t)kTile * p.side_bytes + 16 + 15) & ~size_t(15));
@@ -266,12 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                  ((uint32_t)__half_as_ushort(__float2half_rn(p.codebook[c1])) << 16);
       }
     const int wb = p.cb_bits, lm = p.cb_levels - 1;
-    for (int j = tid; j < t.quad; j += kThreads) {
-      uint32_t h[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        h[e] = __half_as_ushort(__float2half_rn(p.codebook[(j >> (e * wb)) & lm]));
-      cb4[j] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    for (int j = tid; j < 2 * t.cb_rep; j += kThreads) {  // word j: pair j / 32
+      const int e = j >> 5;
+      cbr[j] = (uint32_t)__half_as_ushort(__float2half_rn(p.codebook[e & lm])) |
+               ((uint32_t)__half_as_ushort(__float2half_rn(p.codebook[(e >> wb) & lm])) << 16);
     }
   }
   tc_fence_before();
@@ -445,13 +446,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool live = tt < n;
       const int rowoff = tt * P;
       const uint32_t a_tm = taddr0 + lane_base + t.a_col0 + a * t.a_cols;
-      if (MODE == KVC_MODE_CODEBOOK && t.quad) {
+      if (MODE == KVC_MODE_CODEBOOK && t.cb_rep) {
         // thread c0 takes the codes [c0 K / 2, (c0 + 1) K / 2)
         const unsigned char* row = rows + rowoff;
         const int nq = K / 64;
-        if (p.cb_bits == 3) decode_cb_quads<3>(row, live, c0 * (K / 2), nq, cb4, a_tm);
-        else if (p.cb_bits == 2) decode_cb_quads<2>(row, live, c0 * (K / 2), nq, cb4, a_tm);
-        else decode_cb_quads<1>(row, live, c0 * (K / 2), nq, cb4, a_tm);
+        if (p.cb_bits == 3) decode_cb_rows<3>(row, live, c0 * (K / 2), nq, cbr, a_tm);
+        else if (p.cb_bits == 2) decode_cb_rows<2>(row, live, c0 * (K / 2), nq, cbr, a_tm);
+        else decode_cb_rows<1>(row, live, c0 * (K / 2), nq, cbr, a_tm);
       } else if (MODE == KVC_MODE_UNIFORM && t.uni_w) {
         // one width w: code chunk c is the w bytes at c w of the row; thread
         // c0 takes half of the code chunks, c0 = 1 also the bias chunk (ones)
@@ -663,13 +664,13 @@ size_t fetch_pipe_smem(int mode, int D, int hpg, int K, int side_bytes, int pmax
   z.n_stg = 2;
   z.n_rs = min_rs;
   // codebook rows of at most 3-bit codes (one segment from byte 0, K = D a
-  // multiple of 64) decode four codes per lookup: a table of 2^(4 bits) pairs
-  // of half2 words
-  z.quad = mode == KVC_MODE_CODEBOOK && cb_bits >= 1 && cb_bits <= 3 && K == D && K % 64 == 0
-               ? 1 << (4 * cb_bits)
-               : 0;
+  // multiple of 64) decode two codes per lookup from a pair table replicated
+  // once per lane: 2^(2 bits) pairs x 32 copies, in 8-byte slots
+  z.cb_rep = mode == KVC_MODE_CODEBOOK && cb_bits >= 1 && cb_bits <= 3 && K == D && K % 64 == 0
+                 ? (1 << (2 * cb_bits)) * 16
+                 : 0;
   const size_t tail = mode == KVC_MODE_CODEBOOK
-                          ? 256 * 2 + (size_t)kNormRing * kTile * 4 + 256 * 4 + (size_t)z.quad * 8
+                          ? 256 * 2 + (size_t)kNormRing * kTile * 4 + 256 * 4 + (size_t)z.cb_rep * 8
                       : mode == KVC_MODE_GROUP ? (size_t)hpg * D * 4
                                                : 0;
   auto total = [&](const FetchPipeShape& q) {
@@ -705,7 +706,7 @@ cudaError_t launch_fetch_pipe(const TcPlan& plan, const Params& p, const FetchAr
   const FetchPipeShape& sh = plan.pipe;
   const PipeArgs t{plan.fetchB, plan.bias, plan.chunks32, plan.slotP, plan.fetch_K, plan.pipe_cols,
                    sh.n_acc, sh.n_a, sh.n_rs, sh.a_col0, sh.a_cols, sh.n_stg, sh.n_b, sh.rs_bytes,
-                   sh.quad, sh.uni_w, sh.uni_chunks, f.S, tiles, total};
+                   sh.cb_rep, sh.uni_w, sh.uni_chunks, f.S, tiles, total};
   k<<<(unsigned)grid, kThreads, plan.pipe_smem, s>>>(p, t, map);
   ++*nk;
   return cudaGetLastError();

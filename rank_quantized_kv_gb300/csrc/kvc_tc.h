@@ -21,7 +21,7 @@ struct FetchPipeShape {
   int n_stg = 0;     // output staging buffers
   int n_b = 0;       // B buffers
   int rs_bytes = 0;  // bytes of one row stage
-  int quad = 0;      // entries of the codebook's 4-code table (0: none)
+  int cb_rep = 0;    // codebook: 8-byte slots of the lane-replicated pair table (0: none)
   int uni_w = 0;     // uniform rows of one width (1, 2, 4 or 8) from byte 0: the width
   int uni_chunks = 0;  // ... and their 8-code chunks (the bias chunk follows)
 };
