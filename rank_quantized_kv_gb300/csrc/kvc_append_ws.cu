@@ -626,8 +626,9 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
         for (int j = 0; j < SB; ++j) {
           const int k = cblk * CW + sb * SB + j;  // < rpad; components past r are not kept
           // position (not kept: the row's scratch byte) and qmax; a codebook's
-          // one segment keeps the components in order from position 0
-          int pos = k < r ? k : ks - 1, qmax = 0;
+          // one segment keeps the components in order from position 0, and its
+          // staging row holds rpad codes (k >= r lands past the packed ones)
+          int pos = MODE == KVC_MODE_CODEBOOK ? k : (k < r ? k : ks - 1), qmax = 0;
           if (MODE == KVC_MODE_UNIFORM) {
             const int2 qp = tb.qp[k];
             qmax = qp.x;
@@ -919,7 +920,9 @@ size_t append_ws_plan(int D, int r, int rpad, int npieces, int pmax, int max_chu
   z.tab_bytes = (int)append_ws_tab_bytes(rpad);
   z.x_stage = ((D / 64) * 16384 + z.tab_bytes + 1023) / 1024 * 1024;
   z.n_b = n_bases > 1 ? 2 : 1;
-  z.ks = max_chunks * 8 + 8;  // the extra 8 bytes spread the rows over the banks
+  // the extra 8 bytes spread the rows over the banks; a codebook row holds
+  // rpad codes (the components past r land beyond the packed ones)
+  z.ks = std::max(max_chunks * 8, direct ? rpad : 0) + 8;
   const size_t limit = 226 * 1024;
   for (int vt = 1; vt >= 0; --vt) {  // the groups' V^T copies where they fit
     const size_t fixed = 1024 + (size_t)z.n_b * ncols * D * 2 +

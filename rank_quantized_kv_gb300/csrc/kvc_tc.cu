@@ -676,7 +676,8 @@ void prepare_append(const kvc_layer_desc& d, const Geo& g, std::vector<uint8_t>&
   int max_chunks = 0;
   for (int b = 0; b < nb; ++b) max_chunks = std::max(max_chunks, append_ws_chunks(g, b));
   if (max_chunks > 32) max_chunks = -1;
-  const int ks = max_chunks * 8 + 8;  // the code staging row (append_ws_plan's)
+  // the code staging row (append_ws_plan's)
+  const int ks = std::max(max_chunks * 8, d.mode == KVC_MODE_CODEBOOK ? rpad : 0) + 8;
   for (int b = 0; b < nb && max_chunks > 0; ++b)
     if (append_ws_table(g, d, rpad, c64.data(), (double)plan.app_inv_scale, (double)plan.app_gamma,
                         ks, b, tab.data() + (size_t)b * tab_bytes) < 0)
