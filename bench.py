@@ -134,8 +134,8 @@ class ClockSampler:
 # removed whenever its kernel changes.  The roofline's "traffic" scales it to
 # the launch.
 TRAFFIC_PER_UNIT = {
-    # codebook append: 268.83 MB read + 39.72 MB written for 16 x 8 x 8192 token-heads
-    ("append", "codebook"): (268.83e6 + 39.72e6) / (16 * 8 * 8192),
+    # codebook append: 268.83 MB read + 39.68 MB written for 16 x 8 x 8192 token-heads
+    ("append", "codebook"): (268.83e6 + 39.68e6) / (16 * 8 * 8192),
 }
 
 
