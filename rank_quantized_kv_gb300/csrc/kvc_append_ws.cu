@@ -538,8 +538,6 @@ __global__ void __launch_bounds__(kThreadsWs, 1)
       const float t1 = MODE == KVC_MODE_CODEBOOK ? tb.q4[0].z : 0.f;  // the codebook bound's base
       const XHdr hd = hdr[s];
       const int n = hd.n;
-      // V^T for the re-decision: beside B (visible: the MMA waited for B before
-      // committing this tile's accumulator) or in global memory
       // V^T for the re-decision: the group's copy (refreshed when the basis
       // changes; B1 below publishes it) or global memory
       const float* Vt = p.Vt + (size_t)hd.beta * r * D;
