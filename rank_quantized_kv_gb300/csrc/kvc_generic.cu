@@ -962,8 +962,11 @@ __global__ void __launch_bounds__(256) append_int8_vec(Params p, AppendArgs a) {
 // one commit group per step) and waits for its oldest group with
 // cp.async.wait_group, so HBM sees kI8Stages - 1 rows per thread in flight.
 // A thread reads back only what it copied: no barrier is needed.  ESZ: the
-// input element bytes (2 or 4).
-constexpr int kI8Stages = 4;
+// input element bytes (2 or 4).  Two stages (one row ahead) measured faster
+// than three or four: three blocks of 256 threads per SM already keep far
+// more bytes in flight than HBM needs, and fewer blocks per SM with deeper
+// stages were slower still.
+constexpr int kI8Stages = 2;
 template <int TPR, int ESZ, bool F16>
 __global__ void __launch_bounds__(256, 3) append_int8_pipe(Params p, AppendArgs a) {
   constexpr int Q = kI8NV * ESZ / 16;  // 16-byte pieces of a thread's values
