@@ -857,19 +857,27 @@ __device__ __forceinline__ unsigned append_int8_vals(const Params& p, const Appe
     // Rounding by adding 1.5 2^23 (half to even for |u| < 2^22) leaves the
     // code in the low byte of the sum, two's complement, so four codes are
     // packed by byte permutes: no float-to-int conversions on this path.
+    // Two values at a time with the packed fp32 fma (each lane rounds as the
+    // scalar one): t = v inv + M, -q = M - t (exact: t lies within a factor
+    // 2 of M), and the remainder v inv - q for the near test.
     constexpr float kMagic = 12582912.f;
+    const float2 inv2 = make_float2(inv, inv), m2 = make_float2(kMagic, kMagic),
+                 neg2 = make_float2(-1.f, -1.f);
     uint32_t packed[kI8NV / 4];
     bool any_near = slow;  // a value within 3e-5 of a half, a NaN, or a tiny row
 #pragma unroll
     for (int i = 0; i < kI8NV; i += 4) {
       uint32_t tb[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int e = 0; e < 4; e += 2) {
         // q = rint(v inv) of the exact product (within 127 2^-24 of 127 v / a)
-        const float t = __fmaf_rn(v[i + e], inv, kMagic);
-        const float q = __fsub_rn(t, kMagic);
-        any_near |= !(fabsf(__fmaf_rn(v[i + e], inv, -q)) <= 0.5f - 3e-5f);
-        tb[e] = __float_as_uint(t);
+        const float2 vv = make_float2(v[i + e], v[i + e + 1]);
+        const float2 t = __ffma2_rn(vv, inv2, m2);
+        const float2 nq = __ffma2_rn(t, neg2, m2);
+        const float2 rm = __ffma2_rn(vv, inv2, nq);
+        any_near |= !(fabsf(rm.x) <= 0.5f - 3e-5f) || !(fabsf(rm.y) <= 0.5f - 3e-5f);
+        tb[e] = __float_as_uint(t.x);
+        tb[e + 1] = __float_as_uint(t.y);
       }
       packed[i >> 2] =
           __byte_perm(__byte_perm(tb[0], tb[1], 0x0040), __byte_perm(tb[2], tb[3], 0x0040), 0x5410);
