@@ -1,10 +1,11 @@
-"""CPU checks of the bench's roofline arithmetic.
+"""CPU checks of the bench's roofline arithmetic and of its clock record.
 
 The algorithmic bytes per token-head (packed row + side words + the 16-bit
 row the append reads or the fetch writes), the per-op fractions and the
 traffic constant, with stand-in layers that report the TurboQuant-style slot
 layouts: 3-bit codebook keys (48 B of codes and a 2 B fp16 norm per token-head)
-and int8 values (128 B of codes and a 2 B fp16 scale).
+and int8 values (128 B of codes and a 2 B fp16 scale).  The clock sampler's
+parser is fed canned nvidia-smi rows.
 """
 import pytest
 
@@ -58,3 +59,22 @@ def test_traffic_constant_is_near_the_algorithmic_bytes():
     # must move: below it only by the write-back still in L2 at capture end
     tr = bench.TRAFFIC_PER_UNIT[("append", "codebook")]
     assert 0.9 * 306 < tr < 1.02 * 306
+
+
+def test_clock_sampler_reads_median_max_and_reasons():
+    s = bench.ClockSampler(0)
+    s.f.write("0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+              "0, 1980, 2070, 1390.5, 0x4, Not Active, Not Active, Not Active, Active\n"
+              "0, 2070, 2070, 1200.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+              "garbage line\n")
+    c = s.stop()                     # no sampler process was started: parse only
+    assert c["samples"] == 3
+    assert c["sm_mhz"] == 2070.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_flags_thermal_slowdown():
+    s = bench.ClockSampler(0)
+    s.f.write("0, 1500, 2070, 1000.0, 0x40, Not Active, Active, Not Active, Not Active\n")
+    c = s.stop()
+    assert c["reasons"] == ["hw_thermal_slowdown"] and c["sm_mhz"] == 1500.0
